@@ -1,0 +1,182 @@
+/*
+ * sdpa.h — C ABI of a fused, memory-efficient scaled-dot-product attention
+ * forward pass for NVIDIA GB300 (sm_103a).
+ *
+ *   O   = softmax(scale * Q K^T + mask [+ sink column]) V
+ *   LSE = ln( sum_j exp(scale * q.k_j + mask_j) [+ exp(sink)] )
+ *
+ * The operation is the one named by the problem statement of MLX PR #964
+ * ("Metal shaders for memory efficient self attention on large sequences",
+ * the call mx.fast.scaled_dot_product_attention(queries, keys, values,
+ * scale=scale, mask=None)) widened by MLX PR #4459 ("Add D512 support to
+ * Metal vector attention": grouped-query heads, head_dim 512, per-head
+ * sinks, single-query decode through single-pass and two-pass vector
+ * kernels) and by the option set of the cuDNN graph built in mlx 0.30.7
+ * mlx/backend/cuda/scaled_dot_product_attention.cpp (build_sdpa_graph:
+ * attention scale, log-sum-exp statistics output, bottom-right causal mask,
+ * additive bias, sink token).  The score matrix is computed tile by tile with
+ * an online softmax (running max m and running sum l, rustytorch
+ * flash_attention.metal, forward kernel) and never written to device memory.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout: q is [B, Hq, Lq, D], k and v are [B, Hkv, Lk, D], o is
+ *    [B, Hq, Lq, D], all dense row-major ("contiguous"), element type
+ *    params->dtype.  lse is [B, Hq, Lq] float32, dense.  The query head h
+ *    reads key/value head floor(h / (Hq / Hkv)) (contiguous head groups).
+ *  - Pointers q, k, v, o, lse, mask, sinks and workspace are DEVICE pointers
+ *    owned by the caller; the library never allocates, frees or retains them.
+ *    Base pointers of q, k, v, o and mask must be 16-byte aligned; lse, sinks
+ *    4-byte aligned; workspace 256-byte aligned.
+ *  - sdpa_forward is asynchronous on `stream` (a cudaStream_t, passed as
+ *    void* so that this header needs no CUDA include; NULL = legacy default
+ *    stream).  It never synchronises the host.
+ *  - Argument and layout errors are detected on the host before any launch,
+ *    and nothing is written.  Launch failures are reported as SDPA_ERR_CUDA.
+ *    No C++ exception crosses this ABI.  Kernels never trap: a device-side
+ *    wait that gives up sets a device status word, read and cleared by
+ *    sdpa_device_status().
+ */
+#ifndef GB300_SDPA_H_
+#define GB300_SDPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SDPA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define SDPA_API __attribute__((visibility("default")))
+#else
+#define SDPA_API
+#endif
+
+typedef enum {
+  SDPA_F32 = 0,
+  SDPA_F16 = 1,
+  SDPA_BF16 = 2
+} sdpa_dtype_t;
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID_ARGUMENT = 1, /* null pointer, non-positive size, bad stride */
+  SDPA_ERR_UNSUPPORTED = 2,      /* valid problem outside the supported space */
+  SDPA_ERR_MISALIGNED = 3,       /* a base pointer breaks the alignment rule */
+  SDPA_ERR_WORKSPACE_TOO_SMALL = 4,
+  SDPA_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
+  SDPA_ERR_TIMEOUT = 6           /* a device-side wait gave up (status word) */
+} sdpa_status_t;
+
+/* Kernel paths.  The launcher picks one from the shape alone. */
+typedef enum {
+  SDPA_KERNEL_NONE = 0,
+  SDPA_KERNEL_PREFILL_TC = 1,   /* fp16/bf16, Lq > 1: TMA + tcgen05 + TMEM */
+  SDPA_KERNEL_PREFILL_F32 = 2,  /* fp32, Lq > 1: fp32 FMA tiles */
+  SDPA_KERNEL_DECODE_SPLITKV = 3, /* Lq == 1: split-KV vector pass + combine */
+  SDPA_KERNEL_NO_KEYS = 4        /* Lk == 0: writes o = 0 and the empty lse */
+} sdpa_kernel_t;
+
+/*
+ * Problem description.
+ *  batch, num_q_heads, num_kv_heads, seq_len_q, seq_len_kv, head_dim:
+ *      B, Hq, Hkv, Lq, Lk, D.  Hkv >= 1, the others >= 0, Hq % Hkv == 0,
+ *      D in {64, 128, 512}, Lq and Lk at most 2^30.  When B * Hq * Lq == 0
+ *      there is nothing to compute and the call returns SDPA_OK at once.
+ *      When Lk == 0 every row sees no key: o = 0 and lse = -inf (the sink
+ *      logit itself with sinks).
+ *  dtype: element type of q, k, v, o and mask.
+ *  scale: multiplies q.k before the mask is added; the caller passes it
+ *      explicitly (1/sqrt(D) for the usual choice).  Must be finite.
+ *  causal: nonzero = bottom-right aligned causal mask, key j is visible to
+ *      query i iff j <= i + (Lk - Lq) (the alignment of the cuDNN graph's
+ *      causal_mask_bottom_right; identical to "j <= i" when Lq == Lk).
+ *      Requires Lq <= Lk.
+ *  mask: NULL or an additive bias added to the scaled scores, element type
+ *      dtype, addressed as mask[b*s0 + h*s1 + i*s2 + j*s3] with
+ *      mask_stride = {s0, s1, s2, s3} in ELEMENTS; a stride of 0 broadcasts
+ *      that dimension; s3 must be 1.  -inf entries remove a key.  When both
+ *      mask and causal are given, both apply.
+ *  sinks: NULL or float32 [Hq]: one extra logit per query head that enters
+ *      the softmax denominator only (a key with a zero value row).  It is
+ *      not multiplied by scale and not masked.
+ */
+typedef struct {
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t seq_len_q;
+  int32_t seq_len_kv;
+  int32_t head_dim;
+  int32_t dtype;   /* sdpa_dtype_t */
+  float scale;
+  int32_t causal;
+  int32_t reserved0;
+  const void* mask;
+  int64_t mask_stride[4];
+  const float* sinks;
+} sdpa_params_t;
+
+/*
+ * sdpa_workspace_size — bytes of device workspace that sdpa_forward needs for
+ * this problem (split-KV partial outputs of the decode path; 0 when the
+ * chosen path needs none).  Pure host function; returns 0 for an invalid
+ * problem as well (sdpa_forward then reports the error).
+ */
+SDPA_API size_t sdpa_workspace_size(const sdpa_params_t* params);
+
+/*
+ * sdpa_select_kernel — the kernel path sdpa_forward would run for this
+ * problem, or SDPA_KERNEL_NONE with *status set when the problem is invalid
+ * or unsupported (SDPA_KERNEL_NONE with SDPA_OK: nothing to compute).  Pure
+ * host function (no CUDA call).  `status` may be NULL.
+ */
+SDPA_API sdpa_kernel_t sdpa_select_kernel(const sdpa_params_t* params, sdpa_status_t* status);
+
+/*
+ * sdpa_forward — compute o (and lse, when non-NULL) for the problem in
+ * `params` on `stream`.
+ *  q, k, v: inputs (device, read only).  o: output (device, written).
+ *  lse: NULL or float32 [B, Hq, Lq] output in natural-log units; a fully
+ *      masked row gives o = 0 and lse = -inf (lse = sink with sinks).
+ *  workspace / workspace_bytes: device scratch of at least
+ *      sdpa_workspace_size(params) bytes (NULL allowed when that is 0).  Its
+ *      contents need no initialisation and are overwritten; two calls that
+ *      overlap on the GPU must not share one workspace.
+ * Returns SDPA_OK once the work is enqueued.
+ */
+SDPA_API sdpa_status_t sdpa_forward(const sdpa_params_t* params,
+                           const void* q, const void* k, const void* v,
+                           void* o, float* lse,
+                           void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* sdpa_status_string — static, NUL-terminated text for a status code. */
+SDPA_API const char* sdpa_status_string(sdpa_status_t status);
+
+/*
+ * sdpa_device_status — synchronise `stream`, then read and clear the device
+ * status word that kernels set when one of their bounded waits gives up.
+ * Returns SDPA_OK, SDPA_ERR_TIMEOUT, or SDPA_ERR_CUDA if the synchronisation
+ * itself failed.  The status word is per device and shared by all streams.
+ */
+SDPA_API sdpa_status_t sdpa_device_status(void* stream);
+
+/*
+ * sdpa_debug_set_wait_limit_ns — test hook: upper bound in nanoseconds on
+ * every device-side barrier wait of later launches (default 2e9).  0
+ * restores the default.  Returns the previous value.
+ */
+SDPA_API uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns);
+
+/* sdpa_abi_version — SDPA_ABI_VERSION of the built library. */
+SDPA_API int sdpa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_SDPA_H_ */

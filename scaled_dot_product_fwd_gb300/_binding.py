@@ -1,0 +1,211 @@
+"""ctypes binding of the C ABI in include/sdpa.h (argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels of libsdpa_gb300.so;
+this module only checks tensor properties, fills ``sdpa_params_t``, hands
+device pointers and the current CUDA stream to the library, and turns status
+codes into exceptions.  There is no CPU path: if the library cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libsdpa_gb300.so")
+
+SDPA_F32, SDPA_F16, SDPA_BF16 = 0, 1, 2
+STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARGUMENT", 2: "SDPA_ERR_UNSUPPORTED",
+          3: "SDPA_ERR_MISALIGNED", 4: "SDPA_ERR_WORKSPACE_TOO_SMALL", 5: "SDPA_ERR_CUDA",
+          6: "SDPA_ERR_TIMEOUT"}
+KERNELS = {0: "none", 1: "prefill_tc", 2: "prefill_f32", 3: "decode_splitkv", 4: "no_keys"}
+
+# Every symbol include/sdpa.h declares.
+EXPORTS = ("sdpa_workspace_size", "sdpa_select_kernel", "sdpa_forward", "sdpa_status_string",
+           "sdpa_device_status", "sdpa_debug_set_wait_limit_ns", "sdpa_abi_version")
+
+
+class SdpaParams(ctypes.Structure):
+    """Mirror of sdpa_params_t."""
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("seq_len_q", ctypes.c_int32),
+                ("seq_len_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("causal", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("mask", ctypes.c_void_p), ("mask_stride", ctypes.c_int64 * 4),
+                ("sinks", ctypes.c_void_p)]
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__("%s%s" % (STATUS.get(status, str(status)), (": " + what) if what else ""))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load (once) and return the ctypes handle of libsdpa_gb300.so."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError("libsdpa_gb300.so is not built (run __graft_entry__.build())")
+            lib = ctypes.CDLL(path)
+            P = ctypes.POINTER(SdpaParams)
+            lib.sdpa_workspace_size.argtypes = [P]
+            lib.sdpa_workspace_size.restype = ctypes.c_size_t
+            lib.sdpa_select_kernel.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+            lib.sdpa_select_kernel.restype = ctypes.c_int
+            lib.sdpa_forward.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_size_t, ctypes.c_void_p]
+            lib.sdpa_forward.restype = ctypes.c_int
+            lib.sdpa_status_string.argtypes = [ctypes.c_int]
+            lib.sdpa_status_string.restype = ctypes.c_char_p
+            lib.sdpa_device_status.argtypes = [ctypes.c_void_p]
+            lib.sdpa_device_status.restype = ctypes.c_int
+            lib.sdpa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            lib.sdpa_debug_set_wait_limit_ns.restype = ctypes.c_uint64
+            lib.sdpa_abi_version.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def make_params(B, Hq, Hkv, Lq, Lk, D, dtype, scale, causal=False, mask_ptr=None,
+                mask_stride=(0, 0, 0, 1), sinks_ptr=None) -> SdpaParams:
+    p = SdpaParams()
+    p.batch, p.num_q_heads, p.num_kv_heads = int(B), int(Hq), int(Hkv)
+    p.seq_len_q, p.seq_len_kv, p.head_dim = int(Lq), int(Lk), int(D)
+    p.dtype = int(dtype)
+    p.scale = float(scale)
+    p.causal = 1 if causal else 0
+    p.reserved0 = 0
+    p.mask = mask_ptr
+    for i in range(4):
+        p.mask_stride[i] = int(mask_stride[i])
+    p.sinks = sinks_ptr
+    return p
+
+
+def sdpa_status_string(status: int) -> str:
+    return load_library().sdpa_status_string(int(status)).decode()
+
+
+def sdpa_select_kernel(params: SdpaParams):
+    """Returns (kernel name, status code) for a params struct."""
+    st = ctypes.c_int(0)
+    k = load_library().sdpa_select_kernel(ctypes.byref(params), ctypes.byref(st))
+    return KERNELS.get(k, str(k)), st.value
+
+
+def sdpa_workspace_size(params: SdpaParams) -> int:
+    return int(load_library().sdpa_workspace_size(ctypes.byref(params)))
+
+
+def sdpa_forward_raw(params: SdpaParams, q, k, v, o, lse, workspace, workspace_bytes, stream) -> int:
+    """Direct call of the C entry point with integer device addresses."""
+    pp = ctypes.byref(params) if params is not None else None
+    return int(load_library().sdpa_forward(pp, q, k, v, o, lse, workspace,
+                                           int(workspace_bytes), stream))
+
+
+def sdpa_device_status(stream=None) -> int:
+    return int(load_library().sdpa_device_status(stream))
+
+
+def sdpa_debug_set_wait_limit_ns(ns: int) -> int:
+    return int(load_library().sdpa_debug_set_wait_limit_ns(int(ns)))
+
+
+def sdpa_abi_version() -> int:
+    return int(load_library().sdpa_abi_version())
+
+
+# ----------------------------------------------------------------- torch layer
+_ws_cache = {}
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(t) -> int:
+    torch = _torch()
+    m = {torch.float32: SDPA_F32, torch.float16: SDPA_F16, torch.bfloat16: SDPA_BF16}
+    if t not in m:
+        raise TypeError("unsupported dtype %s" % t)
+    return m[t]
+
+
+def _workspace(nbytes: int, device):
+    torch = _torch()
+    key = (device.index, threading.get_ident())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=None,
+                 lse=None, return_lse=True, workspace=None, stream=None):
+    """O (and LSE) of softmax(scale * q k^T + mask [+ sinks]) v on the GPU.
+
+    q [B, Hq, Lq, D], k/v [B, Hkv, Lk, D]: contiguous CUDA tensors of one
+    dtype (float32, float16 or bfloat16).  mask: None or a tensor of q's dtype
+    broadcastable to [B, Hq, Lq, Lk] (additive).  sinks: None or float32 [Hq].
+    scale defaults to 1/sqrt(D).  Returns (o, lse) or o.
+    """
+    torch = _torch()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, L, D]")
+    for t in (q, k, v):
+        if not t.is_cuda:
+            raise ValueError("q, k, v must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    B, Hq, Lq, D = q.shape
+    _, Hkv, Lk, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dt = dtype_code(q.dtype)
+    mask_ptr, mstride = None, (0, 0, 0, 1)
+    if mask is not None:
+        if mask.dtype != q.dtype or mask.device != q.device:
+            raise TypeError("mask must have q's dtype and device")
+        mexp = mask.expand(B, Hq, Lq, Lk)
+        mstride = tuple(int(s) for s in mexp.stride())
+        if Lk == 1:
+            mstride = mstride[:3] + (1,)
+        mask_ptr = mexp.data_ptr()
+    sinks_ptr = None
+    if sinks is not None:
+        if sinks.dtype != torch.float32 or not sinks.is_cuda or sinks.numel() != Hq:
+            raise TypeError("sinks must be a float32 CUDA tensor with Hq elements")
+        sinks = sinks.contiguous()
+        sinks_ptr = sinks.data_ptr()
+    params = make_params(B, Hq, Hkv, Lq, Lk, D, dt, scale, causal, mask_ptr, mstride, sinks_ptr)
+    if out is None:
+        out = torch.empty((B, Hq, Lq, D), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    nbytes = sdpa_workspace_size(params)
+    if workspace is None and nbytes > 0:
+        workspace = _workspace(nbytes, q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    st = sdpa_forward_raw(params, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr() if lse is not None else None, ws_ptr, ws_bytes, stream)
+    if st != 0:
+        raise SdpaError(st, sdpa_status_string(st))
+    return (out, lse) if return_lse else out

@@ -1,0 +1,219 @@
+// decode_combine.cu — split-KV plan, the combine pass and the decode launch.
+//
+// The combine is the second pass of the two-pass vector attention of MLX PR
+// #4459 ("Add D512 support to Metal vector attention"): with split s holding
+// the normalised partial output O_s and the log2-domain log-sum-exp
+// lse_s of its key range,
+//     M   = max(max_s lse_s, sink * log2 e)
+//     L   = sum_s 2^(lse_s - M) + [sink] 2^(sink * log2 e - M)
+//     O   = sum_s 2^(lse_s - M) O_s / L,    LSE = (M + log2 L) ln 2.
+// The sink logit (mlx 0.30.7 scaled_dot_product_attention.cpp,
+// set_sink_token) enters only the denominator.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdlib.h>
+
+#include "decode.cuh"
+#include "internal.h"
+
+namespace gb300 {
+namespace dec {
+
+constexpr int kCombineThreads = 128;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct CombineArgs {
+  const float* ws_o;
+  const float* ws_lse;
+  void* o;
+  float* lse;
+  const float* sinks;
+  int Hq, num_splits, D;
+  int rows_per_head;  // query rows per (batch, head): 1 for decode
+};
+
+template <typename T>
+struct St;
+template <>
+struct St<float> {
+  static __device__ __forceinline__ float c(float x) { return x; }
+};
+template <>
+struct St<__half> {
+  static __device__ __forceinline__ __half c(float x) { return __float2half_rn(x); }
+};
+template <>
+struct St<__nv_bfloat16> {
+  static __device__ __forceinline__ __nv_bfloat16 c(float x) { return __float2bfloat16_rn(x); }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const CombineArgs a) {
+  const size_t row = blockIdx.x;  // (b * Hq + hq) * rows_per_head + i
+  const int hq = static_cast<int>((row / a.rows_per_head) % a.Hq);
+  const int S = a.num_splits;
+  const float* ls = a.ws_lse + row * S;
+  float M = -INFINITY;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, ls[s]);
+  float sk = -INFINITY;
+  if (a.sinks) {
+    sk = a.sinks[hq] * kLog2e;
+    M = fmaxf(M, sk);
+  }
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < S; ++s) L += ex2(ls[s] - M);
+    if (a.sinks) L += ex2(sk - M);
+  }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  T* orow = static_cast<T*>(a.o) + row * a.D;
+  const float* wo = a.ws_o + row * S * a.D;
+  for (int d = threadIdx.x; d < a.D; d += kCombineThreads) {
+    float acc = 0.f;
+    if (L > 0.f)
+      for (int s = 0; s < S; ++s) acc = fmaf(ex2(ls[s] - M), wo[static_cast<size_t>(s) * a.D + d], acc);
+    orow[d] = St<T>::c(acc * inv);
+  }
+  if (threadIdx.x == 0 && a.lse) a.lse[row] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
+}
+
+}  // namespace dec
+
+static sdpa_status_t launch_combine(int dtype, const dec::CombineArgs& c, unsigned nrows,
+                                    cudaStream_t stream);
+
+namespace {
+int elem_bytes(int dtype) { return dtype == SDPA_F32 ? 4 : 2; }
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+}  // namespace
+
+bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
+  const int es = elem_bytes(p.dtype);
+  const int D = p.head_dim;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  const int hg_max = (D == 512) ? 4 : 8;
+  int hg = 1;
+  while (hg < G && hg < hg_max) hg <<= 1;
+  const int groups = (G + hg - 1) / hg;
+  const int kb = dec::keys_per_warp(es, D, hg);
+  const int tk = dec::kConsumerWarps * kb;
+  const int stage_bytes = 2 * tk * D * es;
+  int stages = 110000 / stage_bytes;
+  if (stages < 2) stages = 2;
+  if (stages > 4) stages = 4;
+  const size_t smem = static_cast<size_t>(stages) * stage_bytes + 4096;
+  int per_sm = static_cast<int>(232448 / (smem + 1024));
+  if (per_sm < 1) per_sm = 1;
+  if (per_sm > 2) per_sm = 2;
+  if (D == 512) per_sm = 1;  // register-bound at D = 512
+  const long long units = static_cast<long long>(p.batch) * p.num_kv_heads * groups;
+  const int ntiles = (p.seq_len_kv + tk - 1) / tk;
+  const long long slots = static_cast<long long>(num_sms > 0 ? num_sms : 152) * per_sm;
+  int best = 1;
+  long long best_cost = -1;
+  const int max_s = ntiles < 1024 ? ntiles : 1024;
+  for (int s = 1; s <= max_s; ++s) {
+    const long long tiles_per = (ntiles + s - 1) / s;
+    const long long waves = (units * s + slots - 1) / slots;
+    const long long cost = waves * (tiles_per + 2);  // 2 tiles of fixed cost per CTA
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  if (const char* env = getenv("GB300_SDPA_DECODE_SPLITS")) {  // test override
+    const int f = atoi(env);
+    if (f >= 1) best = f < ntiles ? f : ntiles;
+  }
+  const int tiles_per = (ntiles + best - 1) / best;
+  const int split_keys = tiles_per * tk;
+  const int splits = (p.seq_len_kv + split_keys - 1) / split_keys;
+  out->head_group = hg;
+  out->num_groups = groups;
+  out->tile_keys = tk;
+  out->num_splits = splits;
+  out->split_keys = split_keys;
+  out->stages = stages;
+  const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * splits;
+  out->workspace = align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
+  return true;
+}
+
+sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
+                            const void* k, const void* v, void* o, float* lse, void* workspace,
+                            const LaunchEnv& env) {
+  const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * plan.num_splits;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                           align256(rows * p.head_dim * sizeof(float)));
+  dec::SplitArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.Hq = p.num_q_heads;
+  a.Hkv = p.num_kv_heads;
+  a.G = p.num_q_heads / p.num_kv_heads;
+  a.Lk = p.seq_len_kv;
+  a.num_groups = plan.num_groups;
+  a.num_splits = plan.num_splits;
+  a.split_keys = plan.split_keys;
+  a.stages = plan.stages;
+  a.sl2 = p.scale * dec::kLog2e;
+  a.mask = p.mask;
+  a.ms0 = p.mask_stride[0];
+  a.ms1 = p.mask_stride[1];
+  a.ws_o = ws_o;
+  a.ws_lse = ws_lse;
+  a.status = env.status;
+  a.wait_ns = env.wait_limit_ns;
+  const char* drop = getenv("GB300_SDPA_DEBUG_DROP_LAST_TILE");
+  a.debug_drop_last = (drop && drop[0] == '1') ? 1 : 0;
+  sdpa_status_t st;
+  switch (p.dtype) {
+    case SDPA_F32: st = dec::launch_split_f32(a, p.head_dim, plan.head_group, p.batch, env.stream); break;
+    case SDPA_F16: st = dec::launch_split_f16(a, p.head_dim, plan.head_group, p.batch, env.stream); break;
+    case SDPA_BF16: st = dec::launch_split_bf16(a, p.head_dim, plan.head_group, p.batch, env.stream); break;
+    default: return SDPA_ERR_UNSUPPORTED;
+  }
+  if (st != SDPA_OK) return st;
+  dec::CombineArgs c;
+  c.ws_o = ws_o;
+  c.ws_lse = ws_lse;
+  c.o = o;
+  c.lse = lse;
+  c.sinks = p.sinks;
+  c.Hq = p.num_q_heads;
+  c.num_splits = plan.num_splits;
+  c.D = p.head_dim;
+  c.rows_per_head = 1;
+  return launch_combine(p.dtype, c, static_cast<unsigned>(p.batch) * p.num_q_heads, env.stream);
+}
+
+sdpa_status_t launch_no_keys(const sdpa_params_t& p, void* o, float* lse, const LaunchEnv& env) {
+  dec::CombineArgs c;
+  c.ws_o = nullptr;
+  c.ws_lse = nullptr;
+  c.o = o;
+  c.lse = lse;
+  c.sinks = p.sinks;
+  c.Hq = p.num_q_heads;
+  c.num_splits = 0;
+  c.D = p.head_dim;
+  c.rows_per_head = p.seq_len_q;
+  const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q;
+  if (rows > 0x7fffffffu) return SDPA_ERR_UNSUPPORTED;
+  return launch_combine(p.dtype, c, static_cast<unsigned>(rows), env.stream);
+}
+
+static sdpa_status_t launch_combine(int dtype, const dec::CombineArgs& c, unsigned nrows,
+                                    cudaStream_t stream) {
+  const dim3 grid(nrows);
+  switch (dtype) {
+    case SDPA_F32: dec::decode_combine_kernel<float><<<grid, dec::kCombineThreads, 0, stream>>>(c); break;
+    case SDPA_F16: dec::decode_combine_kernel<__half><<<grid, dec::kCombineThreads, 0, stream>>>(c); break;
+    default: dec::decode_combine_kernel<__nv_bfloat16><<<grid, dec::kCombineThreads, 0, stream>>>(c); break;
+  }
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+}  // namespace gb300

@@ -1,0 +1,45 @@
+// internal.h — host-side interface between the C ABI (sdpa_api.cu) and the
+// kernel launchers (one .cu per kernel family).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "sdpa.h"
+
+namespace gb300 {
+
+// What every launcher needs besides the problem: where kernels report a
+// timed-out wait, the wait bound, and the device's SM count.
+struct LaunchEnv {
+  int* status;          // device status word
+  uint64_t wait_limit_ns;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+// Split-KV decode plan (pure function of the problem and the SM count).
+struct DecodePlan {
+  int head_group;   // query heads handled by one CTA (power of two)
+  int num_groups;   // ceil(G / head_group)
+  int tile_keys;    // keys per shared-memory tile
+  int num_splits;   // key-range splits per (batch, kv head, head group)
+  int split_keys;   // keys per split (multiple of tile_keys)
+  int stages;       // shared-memory ring stages
+  size_t workspace; // bytes of partial results
+};
+
+bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);
+
+sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const void* k,
+                                const void* v, void* o, float* lse, const LaunchEnv& env);
+sdpa_status_t launch_prefill_f32(const sdpa_params_t& p, const void* q, const void* k,
+                                 const void* v, void* o, float* lse, const LaunchEnv& env);
+// Lk == 0: o = 0, lse = -inf (or the sink) for every row.
+sdpa_status_t launch_no_keys(const sdpa_params_t& p, void* o, float* lse, const LaunchEnv& env);
+sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
+                            const void* k, const void* v, void* o, float* lse, void* workspace,
+                            const LaunchEnv& env);
+
+}  // namespace gb300

@@ -1,0 +1,500 @@
+// prefill_tc.cu — fused attention forward for fp16/bf16, head_dim 64/128,
+// on the 5th-generation tensor cores of sm_103a.
+//
+// The computation is the tiled online-softmax forward of the rustytorch
+// flash_attention.metal page (forward kernel: per key tile, row max, running
+// max m and sum l, accumulator rescale by exp(m_old - m_new), final O / l
+// and LSE = m + log l), with the options of the MLX pages (causal block
+// skipping, bounds masking of the ragged key tail, additive mask, per-head
+// sinks in the denominator, grouped-query head mapping).
+//
+// GB300 design (not the page's): one CTA owns NQ = 2 query tiles of 128 rows
+// that share every K/V tile.  Warp roles:
+//   warps 0-7  softmax: warpgroup t owns query tile t, one thread per row
+//              (TMEM lane); it also rescales O in TMEM and writes the output;
+//   warp 8     TMA producer: Q tiles once, then K_j, V_j into a ring of
+//              shared-memory buffers (128-byte swizzle);
+//   warp 9     MMA issuer: one thread issues tcgen05.mma,
+//              S_t = Q_t K_j^T (A, B from shared memory, fp32 in TMEM) and
+//              O_t += P_t V_j (P from TMEM, written there by the softmax
+//              warps over the columns of S_t; V from shared memory).
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  The issue order
+// S_0,j+1 right after PV_0,j lets softmax of one tile overlap the MMAs of
+// the other.  The O rescale is lazy: a row's reference max moves only when
+// the new max exceeds it by more than 8 (log2 units), so P stays <= 2^8.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tensor_map.h"
+
+namespace gb300 {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;  // keys per K/V tile
+constexpr int NQ = 2;    // query tiles per CTA
+constexpr int kSoftmaxWarps = 4 * NQ;
+constexpr int kLoadWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct Cfg {
+  static constexpr int CB = D / 64;           // 128-byte column blocks per row
+  static constexpr int TILE = BM * D * 2;     // bytes of one 128-row fp16/bf16 tile
+  static constexpr int NS = (D == 64) ? 8 : 4;  // K/V ring buffers (K_j, V_j alternate)
+  static constexpr int Q_OFF = 0;
+  static constexpr int RING_OFF = NQ * TILE;
+  static constexpr int BAR_OFF = RING_OFF + NS * TILE;
+  // q_full, full[NS], empty[NS], s_full[NQ], p_full[NQ], o_done[NQ], drain
+  static constexpr int NBARS = 1 + 2 * NS + 3 * NQ + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t s_col(int t) { return static_cast<uint32_t>(t * BN); }
+  static constexpr uint32_t o_col(int t) { return static_cast<uint32_t>(NQ * BN + t * D); }
+  static_assert(NQ * BN + NQ * D <= 512, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct PrefillArgs {
+  int Hq, Hkv, G, Lq, Lk;
+  int num_qblocks;
+  float sl2;  // scale * log2(e)
+  int causal;
+  const void* mask;
+  long long ms0, ms1, ms2;  // mask element strides (last stride is 1)
+  const float* sinks;
+  void* o;
+  float* lse;
+  int* status;
+  unsigned long long wait_ns;
+};
+
+template <bool BF16>
+struct Elem;
+template <>
+struct Elem<true> {
+  using T = __nv_bfloat16;
+  static __device__ __forceinline__ float to_f(T x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+template <>
+struct Elem<false> {
+  using T = __half;
+  static __device__ __forceinline__ float to_f(T x) { return __half2float(x); }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+
+// Wait for a phase ignoring the abort flag (used only to drain in-flight
+// asynchronous work before the CTA exits); bounded by limit_ns.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) break;
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const PrefillArgs a) {
+  using C = Cfg<D>;
+  using E = Elem<BF16>;
+  using T = typename E::T;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment of the shared-memory window (128-byte swizzle atoms).
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sQ = smem + C::Q_OFF;
+  uint8_t* sRing = smem + C::RING_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* full = bars + 1;
+  uint64_t* empty = full + C::NS;
+  uint64_t* s_full = empty + C::NS;
+  uint64_t* p_full = s_full + NQ;
+  uint64_t* o_done = p_full + NQ;
+  uint64_t* drain = o_done + NQ;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: (query block, head, batch); causal: heaviest blocks first
+  const int qb = a.causal ? (a.num_qblocks - 1 - static_cast<int>(blockIdx.x))
+                          : static_cast<int>(blockIdx.x);
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int m0 = qb * (BM * NQ);
+  const int nt = min(NQ, (a.Lq - m0 + BM - 1) / BM);  // active query tiles (>= 1)
+  const int kvh = h / a.G;
+  const int nkv_all = (a.Lk + BN - 1) / BN;
+  int nkv[NQ];
+  int nmax = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    int n = 0;
+    if (t < nt) {
+      const int last_row = min(m0 + t * BM + BM - 1, a.Lq - 1);
+      if (a.causal) {
+        const int lim = last_row + (a.Lk - a.Lq);  // last key visible to the tile
+        n = lim < 0 ? 0 : min(nkv_all, lim / BN + 1);
+      } else {
+        n = nkv_all;
+      }
+    }
+    nkv[t] = n;
+    nmax = max(nmax, n);
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int t = 0; t < NQ; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{a.wait_ns, abort_flag, a.status};
+  int last_use[C::NS];  // producer: last fill of each ring buffer (-1: none)
+#pragma unroll
+  for (int s = 0; s < C::NS; ++s) last_use[s] = -1;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nt * C::TILE));
+      for (int t = 0; t < nt; ++t)
+        for (int cb = 0; cb < C::CB; ++cb)
+          tma_load_3d(sQ + t * C::TILE + cb * BM * 128, &tmQ, q_full, cb * 64, m0 + t * BM,
+                      b * a.Hq + h);
+      for (int idx = 0; idx < 2 * nmax; ++idx) {
+        const int s = idx % C::NS;
+        const int use = idx / C::NS;
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, wc)) break;
+        mbar_arrive_expect_tx(&full[s], C::TILE);
+        const CUtensorMap* map = (idx & 1) ? &tmV : &tmK;
+        const int j = idx >> 1;
+        for (int cb = 0; cb < C::CB; ++cb)
+          tma_load_3d(sRing + s * C::TILE + cb * BN * 128, map, &full[s], cb * 64, j * BN,
+                      b * a.Hkv + kvh);
+        last_use[s] = use;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
+      constexpr uint32_t idO = idesc_f16(BF16, BM, D, false, true);
+      const uint32_t q_addr = smem_addr(sQ);
+      const uint32_t ring_addr = smem_addr(sRing);
+      auto kbuf = [](int j) { return (2 * j) % C::NS; };
+      auto kpar = [](int j) { return static_cast<uint32_t>(((2 * j) / C::NS) & 1); };
+      auto vbuf = [](int j) { return (2 * j + 1) % C::NS; };
+      auto vpar = [](int j) { return static_cast<uint32_t>(((2 * j + 1) / C::NS) & 1); };
+      // S_t = Q_t K_j^T: both operands K-major, 128-byte swizzle; a K step of
+      // 16 elements is 32 bytes inside a 128-byte row, 4 steps per column block.
+      auto issue_s = [&](int t, int j) {
+        const uint32_t qa = q_addr + t * C::TILE;
+        const uint32_t ka = ring_addr + kbuf(j) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          mma_f16_ss(tmem + C::s_col(t), sdesc(qa + off, 16, 1024, kSwizzle128B),
+                     sdesc(ka + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V_j: P (128 x 128, K-major) from TMEM columns of S_t,
+      // 2 elements per column; V MN-major: 64-wide column blocks BN*128
+      // bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t va = ring_addr + vbuf(j) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          mma_f16_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
+                     sdesc(va + kk * 16 * 128, BN * 128, 1024, kSwizzle128B), idO,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, wc);
+      if (ok) {
+        for (int t = 0; t < nt; ++t)
+          if (nkv[t] == 0) mma_commit(&o_done[t]);
+        if (nmax > 0) {
+          ok = mbar_wait(&full[kbuf(0)], kpar(0), wc);
+          if (ok) {
+            tc_fence_after();
+            for (int t = 0; t < nt; ++t)
+              if (nkv[t] > 0) {
+                issue_s(t, 0);
+                mma_commit(&s_full[t]);
+              }
+            mma_commit(&empty[kbuf(0)]);
+          }
+        }
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        ok = mbar_wait(&full[vbuf(j)], vpar(j), wc);
+        if (!ok) break;
+        tc_fence_after();
+        bool kwaited = false;
+        for (int t = 0; t < nt && ok; ++t) {
+          if (j >= nkv[t]) continue;
+          ok = mbar_wait(&p_full[t], j & 1, wc);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < nkv[t]) {
+            if (!kwaited) {
+              ok = mbar_wait(&full[kbuf(j + 1)], kpar(j + 1), wc);
+              if (!ok) break;
+              tc_fence_after();
+              kwaited = true;
+            }
+            issue_s(t, j + 1);
+            mma_commit(&s_full[t]);
+          } else {
+            mma_commit(&o_done[t]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&empty[vbuf(j)]);
+        if (kwaited) mma_commit(&empty[kbuf(j + 1)]);
+      }
+      // every MMA issued by this thread completes before TMEM is freed
+      mma_commit(drain);
+      drain_wait(drain, 0, kDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int t = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;  // row inside the tile = TMEM lane
+    const int qi = m0 + t * BM + r;        // query row
+    const bool row_ok = qi < a.Lq;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::s_col(t);
+    const uint32_t tO = tmem + lane_off + C::o_col(t);
+    // last key visible to this row (bounds and causal)
+    int limit = a.Lk - 1;
+    if (a.causal) limit = min(limit, qi + (a.Lk - a.Lq));
+    const T* mrow = nullptr;
+    if (a.mask && row_ok)
+      mrow = static_cast<const T*>(a.mask) + b * a.ms0 + h * a.ms1 + qi * a.ms2;
+    float m = -INFINITY;  // reference max (log2 units)
+    float l = 0.f;        // running sum relative to m
+    bool ok = true;
+    if (t < nt) {
+      for (int j = 0; j < nkv[t]; ++j) {
+        ok = mbar_wait(&s_full[t], j & 1, wc);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+        tmem_wait_ld();
+        const int kv0 = j * BN;
+        float x[BN];
+#pragma unroll
+        for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(s[i]) * a.sl2;
+        if (mrow) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i)
+            if (kv0 + i < a.Lk) x[i] += E::to_f(mrow[kv0 + i]) * kLog2e;
+        }
+        if (kv0 + BN - 1 > limit) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i)
+            if (kv0 + i > limit) x[i] = -INFINITY;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < BN; ++i) mx = fmaxf(mx, x[i]);
+        float alpha = 1.f;
+        const bool resc = mx > m + kRescaleThreshold;  // true on the first visible tile
+        if (resc) {
+          alpha = ex2(m - mx);  // 0 when m = -inf
+          m = mx;
+        }
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        float rs = 0.f;
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int i = 0; i < BN / 2; ++i) {
+          const float p0 = ex2(x[2 * i] - mu);
+          const float p1 = ex2(x[2 * i + 1] - mu);
+          rs += p0 + p1;
+          pk[i] = E::pack(p0, p1);
+        }
+        l = l * alpha + rs;
+        // O_t holds the sum through PV_{t,j-1} (complete: the commit behind
+        // s_full tracks every earlier MMA); rescale rows whose max moved.
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ob[32];
+            tmem_ld32(tO + c * 32, ob);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ob[i] = __float_as_uint(__uint_as_float(ob[i]) * alpha);
+            tmem_st32(tO + c * 32, ob);
+          }
+        }
+        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+      }
+      if (ok) ok = mbar_wait(&o_done[t], 0, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        // sink logit joins the denominator only (value row 0)
+        float oscale = 1.f;
+        if (a.sinks) {
+          const float sk = a.sinks[h] * kLog2e;
+          const float mn = fmaxf(m, sk);
+          oscale = ex2(m - mn);
+          l = l * oscale + ex2(sk - mn);
+          m = mn;
+        }
+        const float inv = (l > 0.f) ? oscale / l : 0.f;
+        T* orow = static_cast<T*>(a.o) + ((static_cast<size_t>(b) * a.Hq + h) * a.Lq + qi) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ob[32];
+          tmem_ld32(tO + c * 32, ob);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float v0 = (inv == 0.f) ? 0.f : __uint_as_float(ob[2 * i]) * inv;
+            const float v1 = (inv == 0.f) ? 0.f : __uint_as_float(ob[2 * i + 1]) * inv;
+            w[i] = E::pack(v0, v1);
+          }
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+        if (row_ok && a.lse) {
+          a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.Lq + qi] =
+              (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (warp == kLoadWarp && lane == 0 && *abort_flag) {
+    // a role gave up: every copy the producer issued lands before the CTA exits
+    drain_wait(q_full, 0, kDrainNs);
+    for (int s = 0; s < C::NS; ++s)
+      if (last_use[s] >= 0) drain_wait(&full[s], last_use[s] & 1, kDrainNs);
+  }
+}
+
+template <int D, bool BF16>
+sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, const void* v,
+                          void* o, float* lse, const LaunchEnv& env) {
+  using C = Cfg<D>;
+  const CUtensorMapDataType dt =
+      BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap tq, tk, tv;
+  // [B*H, L, D] viewed innermost-first; box 64 x 128 rows, 128-byte swizzle.
+  if (!encode_tiled_3d(&tq, dt, q, D, p.seq_len_q, static_cast<uint64_t>(p.batch) * p.num_q_heads,
+                       2, 64, BM) ||
+      !encode_tiled_3d(&tk, dt, k, D, p.seq_len_kv,
+                       static_cast<uint64_t>(p.batch) * p.num_kv_heads, 2, 64, BN) ||
+      !encode_tiled_3d(&tv, dt, v, D, p.seq_len_kv,
+                       static_cast<uint64_t>(p.batch) * p.num_kv_heads, 2, 64, BN))
+    return SDPA_ERR_CUDA;
+  PrefillArgs a;
+  a.Hq = p.num_q_heads;
+  a.Hkv = p.num_kv_heads;
+  a.G = p.num_q_heads / p.num_kv_heads;
+  a.Lq = p.seq_len_q;
+  a.Lk = p.seq_len_kv;
+  a.num_qblocks = (p.seq_len_q + BM * NQ - 1) / (BM * NQ);
+  a.sl2 = p.scale * kLog2e;
+  a.causal = p.causal ? 1 : 0;
+  a.mask = p.mask;
+  a.ms0 = p.mask_stride[0];
+  a.ms1 = p.mask_stride[1];
+  a.ms2 = p.mask_stride[2];
+  a.sinks = p.sinks;
+  a.o = o;
+  a.lse = lse;
+  a.status = env.status;
+  a.wait_ns = env.wait_limit_ns;
+  auto kern = prefill_tc_kernel<D, BF16>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+      cudaSuccess)
+    return SDPA_ERR_CUDA;
+  dim3 grid(a.num_qblocks, p.num_q_heads, p.batch);
+  kern<<<grid, kThreads, C::SMEM, env.stream>>>(tq, tk, tv, a);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+}  // namespace
+
+sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const void* k,
+                                const void* v, void* o, float* lse, const LaunchEnv& env) {
+  const bool bf16 = p.dtype == SDPA_BF16;
+  if (p.head_dim == 64)
+    return bf16 ? launch_impl<64, true>(p, q, k, v, o, lse, env)
+                : launch_impl<64, false>(p, q, k, v, o, lse, env);
+  if (p.head_dim == 128)
+    return bf16 ? launch_impl<128, true>(p, q, k, v, o, lse, env)
+                : launch_impl<128, false>(p, q, k, v, o, lse, env);
+  return SDPA_ERR_UNSUPPORTED;
+}
+
+}  // namespace gb300

@@ -1,0 +1,197 @@
+// sdpa_api.cu — the C ABI declared in include/sdpa.h: argument validation,
+// kernel selection by shape, workspace sizing, error mapping and the device
+// status word.
+//
+// Selection follows the dispatch role of mlx 0.30.7
+// scaled_dot_product_attention.cpp (ScaledDotProductAttention::eval_gpu
+// chooses between a fused graph and the sdpa_vector kernel) without any
+// fallback: a single query row (Lq = 1) takes the split-KV vector path of MLX
+// PR #4459, every other shape takes the fused prefill kernel for its dtype,
+// and anything else is reported as unsupported (the force_fused admission
+// check of the same PR raises instead of falling back).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+#include "sdpa.h"
+
+namespace {
+
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::mutex g_dev_mutex;
+int* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Host-only checks of the problem description (no CUDA call).
+sdpa_status_t validate_problem(const sdpa_params_t* p) {
+  if (!p) return SDPA_ERR_INVALID_ARGUMENT;
+  if (p->batch < 0 || p->num_q_heads < 0 || p->num_kv_heads < 1 || p->seq_len_q < 0 ||
+      p->seq_len_kv < 0 || p->head_dim < 1)
+    return SDPA_ERR_INVALID_ARGUMENT;
+  if (p->num_q_heads % p->num_kv_heads != 0) return SDPA_ERR_INVALID_ARGUMENT;
+  if (p->dtype != SDPA_F32 && p->dtype != SDPA_F16 && p->dtype != SDPA_BF16)
+    return SDPA_ERR_INVALID_ARGUMENT;
+  if (!isfinite(p->scale)) return SDPA_ERR_INVALID_ARGUMENT;
+  if (p->seq_len_q > (1 << 30) || p->seq_len_kv > (1 << 30)) return SDPA_ERR_UNSUPPORTED;
+  if (p->mask) {
+    for (int i = 0; i < 4; ++i)
+      if (p->mask_stride[i] < 0) return SDPA_ERR_INVALID_ARGUMENT;
+    if (p->mask_stride[3] != 1) return SDPA_ERR_INVALID_ARGUMENT;
+  }
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 512) return SDPA_ERR_UNSUPPORTED;
+  // cuDNN's bottom-right causal mask is undefined for Tq > Tkv (mlx 0.30.7
+  // supports_sdpa_cudnn); the same rule holds here.
+  if (p->causal && p->seq_len_q > p->seq_len_kv) return SDPA_ERR_UNSUPPORTED;
+  // head_dim 512 is served for single-query decode only.
+  if (p->head_dim == 512 && p->seq_len_q > 1) return SDPA_ERR_UNSUPPORTED;
+  return SDPA_OK;
+}
+
+bool nothing_to_do(const sdpa_params_t* p) {
+  return static_cast<int64_t>(p->batch) * p->num_q_heads * p->seq_len_q == 0;
+}
+
+sdpa_kernel_t pick(const sdpa_params_t* p) {
+  if (nothing_to_do(p)) return SDPA_KERNEL_NONE;
+  if (p->seq_len_kv == 0) return SDPA_KERNEL_NO_KEYS;
+  if (p->seq_len_q == 1) return SDPA_KERNEL_DECODE_SPLITKV;
+  return p->dtype == SDPA_F32 ? SDPA_KERNEL_PREFILL_F32 : SDPA_KERNEL_PREFILL_TC;
+}
+
+// Per-device state: address of the status word and the SM count.
+bool device_state(int* dev_out, int** status, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_dev_mutex);
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return false;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return false;
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+    g_num_sms[dev] = sms;
+  }
+  if (dev_out) *dev_out = dev;
+  if (status) *status = g_status_ptr[dev];
+  if (num_sms) *num_sms = g_num_sms[dev];
+  return true;
+}
+
+int current_num_sms() {
+  int sms = 0;
+  if (!device_state(nullptr, nullptr, &sms)) {
+    cudaGetLastError();  // no device: plan for a full GB300
+    return 152;
+  }
+  return sms;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sdpa_abi_version(void) { return SDPA_ABI_VERSION; }
+
+const char* sdpa_status_string(sdpa_status_t s) {
+  switch (s) {
+    case SDPA_OK: return "ok";
+    case SDPA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case SDPA_ERR_UNSUPPORTED: return "unsupported problem";
+    case SDPA_ERR_MISALIGNED: return "misaligned pointer";
+    case SDPA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case SDPA_ERR_CUDA: return "CUDA error";
+    case SDPA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+sdpa_kernel_t sdpa_select_kernel(const sdpa_params_t* params, sdpa_status_t* status) {
+  const sdpa_status_t st = validate_problem(params);
+  if (status) *status = st;
+  return st == SDPA_OK ? pick(params) : SDPA_KERNEL_NONE;
+}
+
+size_t sdpa_workspace_size(const sdpa_params_t* params) {
+  if (validate_problem(params) != SDPA_OK) return 0;
+  if (pick(params) != SDPA_KERNEL_DECODE_SPLITKV) return 0;
+  gb300::DecodePlan plan;
+  if (!gb300::decode_plan(*params, current_num_sms(), &plan)) return 0;
+  return plan.workspace;
+}
+
+uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns);
+}
+
+sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k, const void* v,
+                           void* o, float* lse, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  sdpa_status_t st = validate_problem(p);
+  if (st != SDPA_OK) return st;
+  if (nothing_to_do(p)) return SDPA_OK;
+  // k and v may be empty (NULL) when there are no keys
+  if (!q || !o || (p->seq_len_kv > 0 && (!k || !v))) return SDPA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return SDPA_ERR_MISALIGNED;
+  if (p->mask && !aligned(p->mask, 16)) return SDPA_ERR_MISALIGNED;
+  if (lse && !aligned(lse, 4)) return SDPA_ERR_MISALIGNED;
+  if (p->sinks && !aligned(p->sinks, 4)) return SDPA_ERR_MISALIGNED;
+  const sdpa_kernel_t kern = pick(p);
+  // the decode workspace is checked before any launch-side CUDA call
+  gb300::DecodePlan plan{};
+  if (kern == SDPA_KERNEL_DECODE_SPLITKV) {
+    if (!gb300::decode_plan(*p, current_num_sms(), &plan)) return SDPA_ERR_UNSUPPORTED;
+    if (plan.workspace > 0) {
+      if (!workspace || workspace_bytes < plan.workspace) return SDPA_ERR_WORKSPACE_TOO_SMALL;
+      if (!aligned(workspace, 256)) return SDPA_ERR_MISALIGNED;
+    }
+  }
+  int* status = nullptr;
+  int num_sms = 0;
+  if (!device_state(nullptr, &status, &num_sms)) return SDPA_ERR_CUDA;
+  gb300::LaunchEnv env;
+  env.status = status;
+  env.wait_limit_ns = g_wait_ns.load();
+  env.num_sms = num_sms;
+  env.stream = static_cast<cudaStream_t>(stream);
+  switch (kern) {
+    case SDPA_KERNEL_PREFILL_TC:
+      return gb300::launch_prefill_tc(*p, q, k, v, o, lse, env);
+    case SDPA_KERNEL_PREFILL_F32:
+      return gb300::launch_prefill_f32(*p, q, k, v, o, lse, env);
+    case SDPA_KERNEL_DECODE_SPLITKV:
+      return gb300::launch_decode(*p, plan, q, k, v, o, lse, workspace, env);
+    case SDPA_KERNEL_NO_KEYS:
+      return gb300::launch_no_keys(*p, o, lse, env);
+    default:
+      return SDPA_ERR_UNSUPPORTED;
+  }
+}
+
+sdpa_status_t sdpa_device_status(void* stream) {
+  int* status = nullptr;
+  if (!device_state(nullptr, &status, nullptr)) return SDPA_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SDPA_ERR_CUDA;
+  int val = 0;
+  if (cudaMemcpy(&val, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  if (val != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+  }
+  return val == 0 ? SDPA_OK : static_cast<sdpa_status_t>(val);
+}
+
+}  // extern "C"

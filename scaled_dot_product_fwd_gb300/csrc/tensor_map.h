@@ -1,0 +1,17 @@
+// tensor_map.h — encoding of TMA tensor maps through the driver entry point
+// obtained from the runtime (no link-time dependency on libcuda).
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace gb300 {
+
+// 3-D tiled map over a dense [planes, rows, inner] tensor (inner contiguous)
+// with a box of box_inner x box_rows x 1 and 128-byte swizzle; out-of-range
+// elements read as zero.  Returns false if the driver rejects the map.
+bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                     uint64_t inner, uint64_t rows, uint64_t planes, uint32_t elem_bytes,
+                     uint32_t box_inner, uint32_t box_rows);
+
+}  // namespace gb300

@@ -1,0 +1,141 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports
+every symbol include/sdpa.h declares, and rejects bad problems before any
+CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import scaled_dot_product_fwd_gb300 as S
+from scaled_dot_product_fwd_gb300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdpa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    assert declared_functions() == sorted(B.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(sdpa_lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", S.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    syms = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    for name in declared_functions():
+        assert name in syms, name
+        assert getattr(sdpa_lib, name) is not None
+    # nothing else leaks out of the library
+    assert not [s for s in syms if s.startswith("_ZN5gb300")]
+
+
+def test_params_struct_layout():
+    assert ctypes.sizeof(B.SdpaParams) == 88
+    assert B.SdpaParams.mask.offset == 40
+    assert B.SdpaParams.mask_stride.offset == 48
+    assert B.SdpaParams.sinks.offset == 80
+
+
+def test_abi_version_and_status_strings(sdpa_lib):
+    assert S.sdpa_abi_version() == 1
+    assert S.sdpa_status_string(0) == "ok"
+    assert S.sdpa_status_string(2) == "unsupported problem"
+    assert S.sdpa_status_string(99) == "unknown status"
+
+
+def P(**kw):
+    d = dict(B=1, Hq=4, Hkv=2, Lq=16, Lk=32, D=64, dtype=S.SDPA_BF16, scale=0.125)
+    d.update(kw)
+    causal = d.pop("causal", False)
+    return S.make_params(d["B"], d["Hq"], d["Hkv"], d["Lq"], d["Lk"], d["D"], d["dtype"],
+                         d["scale"], causal, d.get("mask"), d.get("ms", (0, 0, 0, 1)),
+                         d.get("sinks"))
+
+
+@pytest.mark.parametrize("kw,kernel", [
+    (dict(), "prefill_tc"),
+    (dict(dtype=S.SDPA_F16, D=128), "prefill_tc"),
+    (dict(dtype=S.SDPA_F32), "prefill_f32"),
+    (dict(Lq=1), "decode_splitkv"),
+    (dict(Lq=1, D=512, dtype=S.SDPA_F32), "decode_splitkv"),
+    (dict(Lk=0), "no_keys"),
+    (dict(Lq=1, Lk=0, D=512), "no_keys"),
+    (dict(B=0), "none"),
+    (dict(Lq=0), "none"),
+    (dict(Hq=0), "none"),
+])
+def test_select_kernel(sdpa_lib, kw, kernel):
+    name, st = S.sdpa_select_kernel(P(**kw))
+    assert (name, st) == (kernel, 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=3, Hkv=2), 1),
+    (dict(Hkv=0), 1),
+    (dict(B=-1), 1),
+    (dict(Lk=-2), 1),
+    (dict(dtype=7), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(D=96), 2),
+    (dict(D=256), 2),
+    (dict(D=512, Lq=2), 2),
+    (dict(Lq=64, Lk=32, causal=True), 2),
+    (dict(Lq=(1 << 30) + 1), 2),
+    (dict(mask=16, ms=(0, 0, 32, 2)), 1),
+    (dict(mask=16, ms=(-1, 0, 32, 1)), 1),
+])
+def test_invalid_problems_rejected(sdpa_lib, kw, status):
+    p = P(**kw)
+    name, st = S.sdpa_select_kernel(p)
+    assert (name, st) == ("none", status)
+    assert S.sdpa_workspace_size(p) == 0
+    # sdpa_forward returns the same status before touching CUDA
+    assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, None, 0, None) == status
+
+
+def test_null_and_misaligned_pointers_rejected(sdpa_lib):
+    p = P()
+    assert S.sdpa_forward_raw(p, None, 256, 256, 256, None, None, 0, None) == 1
+    assert S.sdpa_forward_raw(p, 256, None, 256, 256, None, None, 0, None) == 1
+    assert S.sdpa_forward_raw(p, 256, 256, 256, None, None, None, 0, None) == 1
+    assert S.sdpa_forward_raw(None, 256, 256, 256, 256, None, None, 0, None) == 1
+    assert S.sdpa_forward_raw(p, 264, 256, 256, 256, None, None, 0, None) == 3
+    assert S.sdpa_forward_raw(p, 256, 256, 256, 258, None, None, 0, None) == 3
+    assert S.sdpa_forward_raw(p, 256, 256, 256, 256, 258, None, 0, None) == 3
+    pm = P(mask=8)
+    assert S.sdpa_forward_raw(pm, 256, 256, 256, 256, None, None, 0, None) == 3
+    ps = P(sinks=2)
+    assert S.sdpa_forward_raw(ps, 256, 256, 256, 256, None, None, 0, None) == 3
+
+
+def test_nothing_to_compute_is_ok_without_pointers(sdpa_lib):
+    for kw in (dict(B=0), dict(Lq=0), dict(Hq=0)):
+        assert S.sdpa_forward_raw(P(**kw), None, None, None, None, None, None, 0, None) == 0
+
+
+def test_decode_workspace_size_and_check(sdpa_lib):
+    p = P(Lq=1, Lk=32768, B=8, Hq=32, Hkv=8, D=128)
+    ws = S.sdpa_workspace_size(p)
+    assert ws > 0 and ws % 256 == 0
+    # bounded by B*Hq*splits*(D+1) floats with at most 1024 splits
+    assert ws <= 8 * 32 * 1024 * 129 * 4 + 512
+    # too small a workspace is refused before any launch
+    assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, 256, ws - 1, None) == 4
+    assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, None, 0, None) == 4
+    # prefill needs none
+    assert S.sdpa_workspace_size(P()) == 0
+
+
+def test_python_binding_rejects_cpu_tensors(sdpa_lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        S.sdpa_forward(q, q, q)

@@ -1,0 +1,243 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded inputs.
+
+Bars (from the method's statement of accuracy): max |dO| <= 1e-4 for fp32 and
+<= 2e-2 for fp16/bf16, mean |dO| <= 2e-3, |dLSE| <= 1e-3 on finite entries;
+non-finite LSE entries (fully masked rows) must match exactly and O must be
+exactly 0 there.  Small cases compare every element; the full-size workloads
+compare sampled rows (every row of a few (b, h) pairs' ragged tails plus
+seeded random rows) that the oracle evaluates one by one.
+"""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+from scaled_dot_product_fwd_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"float32": 1e-4, "float16": 2e-2, "bfloat16": 2e-2}
+MEAN_TOL = 2e-3
+LSE_TOL = 1e-3
+
+
+def to_dev(t, torch):
+    return None if t is None else t.to("cuda")
+
+
+def run_gpu(torch, w, inp):
+    import scaled_dot_product_fwd_gb300 as S
+    q, k, v = (to_dev(inp[x], torch) for x in ("q", "k", "v"))
+    o, lse = S.sdpa_forward(q, k, v, scale=w.scale, causal=w.causal,
+                            mask=to_dev(inp["mask"], torch), sinks=to_dev(inp["sinks"], torch))
+    torch.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    return o.cpu(), lse.cpu()
+
+
+def oracle_rows(w, inp, rows):
+    f = W.as_float64
+    mask = None if inp["mask"] is None else f(inp["mask"])
+    sinks = None if inp["sinks"] is None else f(inp["sinks"])
+    return O.sdpa(f(inp["q"]), f(inp["k"]), f(inp["v"]), w.scale, w.causal, mask, sinks,
+                  rows=rows)
+
+
+def compare(w, o_gpu, lse_gpu, o_ref, lse_ref, rows):
+    D = w.D
+    og = W.as_float64(o_gpu).reshape(-1, D)
+    lg = lse_gpu.double().numpy().reshape(-1)
+    if rows is not None:
+        og, lg = og[rows], lg[rows]
+    o_ref = o_ref.reshape(-1, D)
+    lse_ref = lse_ref.reshape(-1)
+    assert np.all(np.isfinite(og)), "non-finite output"
+    err = np.abs(og - o_ref)
+    tol = TOL[w.dtype]
+    assert err.max() <= tol, "max |dO| %.3g > %.3g" % (err.max(), tol)
+    assert err.mean() <= MEAN_TOL, "mean |dO| %.3g" % err.mean()
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lg), fin), "LSE finiteness differs"
+    assert np.array_equal(lg[~fin], lse_ref[~fin])
+    assert np.all(og[~fin] == 0)
+    if fin.any():
+        lerr = np.abs(lg[fin] - lse_ref[fin]).max()
+        assert lerr <= LSE_TOL, "max |dLSE| %.3g" % lerr
+    return err.max()
+
+
+def check(torch, w, rows=None):
+    inp = W.make_inputs(w)
+    o_gpu, lse_gpu = run_gpu(torch, w, inp)
+    o_ref, lse_ref = oracle_rows(w, inp, rows)
+    return compare(w, o_gpu, lse_gpu, o_ref, lse_ref, rows)
+
+
+def sample_rows(w, n_random=400, tail=160, seed=7):
+    """Rows of a few (b, h) pairs' first and last query rows plus random rows."""
+    rng = np.random.default_rng(seed)
+    total = w.B * w.Hq * w.Lq
+    picks = []
+    for (b, h) in {(0, 0), (w.B - 1, w.Hq - 1), (0, w.Hq // 2)}:
+        base = (b * w.Hq + h) * w.Lq
+        picks += [base + i for i in range(min(w.Lq, 8))]
+        picks += [base + i for i in range(max(0, w.Lq - tail), w.Lq)]
+    picks += list(rng.integers(0, total, size=n_random))
+    return np.unique(np.array(picks, dtype=np.int64))
+
+
+def wl(B, Hq, Hkv, Lq, Lk, D, dtype, **kw):
+    name = "case_%d_%d_%d_%d_%d_%d_%s" % (B, Hq, Hkv, Lq, Lk, D, dtype)
+    return W.Workload(name, B, Hq, Hkv, Lq, Lk, D, dtype, **kw)
+
+
+# ------------------------------------------------------------ named workloads
+def test_tiny_full(cuda):
+    check(cuda, W.TINY)
+
+
+@pytest.mark.parametrize("w", [W.DIT_F16, W.DIT_F32], ids=lambda w: w.name)
+def test_dit_sampled(cuda, w):
+    check(cuda, w, sample_rows(w))
+
+
+def test_causal_gqa_sampled(cuda):
+    check(cuda, W.CAUSAL_GQA, sample_rows(W.CAUSAL_GQA, n_random=300, tail=130))
+
+
+@pytest.mark.parametrize("key", sorted(W.DECODE_D512), ids=lambda k: W.DECODE_D512[k].name)
+def test_decode_d512_full(cuda, key):
+    check(cuda, W.DECODE_D512[key])
+
+
+def test_decode_long_full(cuda):
+    check(cuda, W.DECODE_LONG)
+
+
+# ---------------------------------------------------- small shapes, all rows
+PREFILL_SHAPES = [(2, 4, 2, 300, 333), (1, 2, 1, 129, 129), (1, 3, 3, 7, 200), (1, 1, 1, 2, 1),
+                  (1, 2, 2, 256, 256), (2, 8, 1, 97, 1000), (1, 2, 1, 513, 520)]
+
+
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_prefill_small(cuda, dtype, D, causal, shape):
+    B, Hq, Hkv, Lq, Lk = shape
+    if causal and Lq > Lk:
+        pytest.skip("causal needs Lq <= Lk")
+    check(cuda, wl(B, Hq, Hkv, Lq, Lk, D, dtype, causal=causal))
+
+
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("mask", ["full", "row", "key"])
+@pytest.mark.parametrize("sinks", [False, True])
+@pytest.mark.parametrize("Lq", [1, 150])
+def test_mask_and_sinks(cuda, dtype, mask, sinks, Lq):
+    D = 128
+    check(cuda, wl(2, 4, 2, Lq, 300, D, dtype, mask=mask, sinks=sinks, causal=(Lq > 1)))
+
+
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("Lq", [1, 140])
+def test_large_sinks(cuda, dtype, Lq):
+    check(cuda, wl(1, 8, 2, Lq, 257, 64, dtype, sinks=True, sink_scale=10.0))
+
+
+@pytest.mark.parametrize("dtype", ["float16", "float32"])
+@pytest.mark.parametrize("Lq", [1, 70])
+@pytest.mark.parametrize("sinks", [False, True])
+def test_fully_masked_rows(cuda, dtype, Lq, sinks):
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    w = wl(1, 2, 1, Lq, 90, 64, dtype, sinks=sinks)
+    inp = W.make_inputs(w)
+    m = torch.zeros((1, 2, Lq, 90), dtype=inp["q"].dtype)
+    m[:, :, ::3, :] = float("-inf")  # every third row sees nothing
+    inp["mask"] = m
+    o_gpu, lse_gpu = run_gpu(torch, w, inp)
+    o_ref, lse_ref = oracle_rows(w, inp, None)
+    compare(w, o_gpu, lse_gpu, o_ref, lse_ref, None)
+    assert S.sdpa_device_status() == 0
+
+
+# ----------------------------------------------------------------- decode sweep
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("D", [64, 128, 512])
+@pytest.mark.parametrize("G", [1, 3, 4, 8, 16])
+@pytest.mark.parametrize("Lk", [1, 7, 1000, 4097])
+def test_decode_sweep(cuda, dtype, D, G, Lk):
+    Hkv = 2
+    check(cuda, wl(2, Hkv * G, Hkv, 1, Lk, D, dtype, sinks=(Lk % 2 == 1)))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 64])
+def test_decode_forced_splits(cuda, splits, monkeypatch):
+    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", str(splits))
+    check(cuda, wl(1, 8, 1, 1, 3001, 128, "bfloat16", sinks=True))
+
+
+# ----------------------------------------------------------------- edge cases
+@pytest.mark.parametrize("Lq", [1, 5])
+@pytest.mark.parametrize("sinks", [False, True])
+def test_no_keys(cuda, Lq, sinks):
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    q = torch.randn(2, 4, Lq, 64, device="cuda", dtype=torch.float16)
+    k = torch.empty(2, 2, 0, 64, device="cuda", dtype=torch.float16)
+    s = torch.tensor([0.5, -1.0, 2.0, 0.0], device="cuda") if sinks else None
+    o, lse = S.sdpa_forward(q, k, k, sinks=s)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0)
+    if sinks:
+        assert torch.equal(lse, s.view(1, 4, 1).expand(2, 4, Lq).contiguous())
+    else:
+        assert torch.all(torch.isneginf(lse))
+
+
+def test_empty_batch_is_noop(cuda):
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    q = torch.empty(0, 4, 10, 64, device="cuda", dtype=torch.bfloat16)
+    k = torch.empty(0, 2, 10, 64, device="cuda", dtype=torch.bfloat16)
+    o, lse = S.sdpa_forward(q, k, k)
+    assert o.shape == (0, 4, 10, 64)
+
+
+def test_long_causal_prefill_sampled(cuda):
+    w = wl(1, 2, 1, 32768, 32768, 128, "bfloat16", causal=True)
+    check(cuda, w, sample_rows(w, n_random=120, tail=40))
+
+
+def test_long_decode_sampled(cuda):
+    w = wl(1, 8, 1, 1, 1 << 20, 128, "float16")
+    check(cuda, w)
+
+
+def test_bottom_right_causal_lq_lt_lk(cuda):
+    check(cuda, wl(1, 4, 2, 200, 1000, 128, "bfloat16", causal=True))
+
+
+def test_wait_timeout_reports_status(cuda, monkeypatch):
+    """A device wait that runs out sets the status word; the context stays
+    usable.  The failure is made on the host: the decode producer is told to
+    drop its last copy, so the consumers' bounded wait on it expires."""
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    w = wl(1, 4, 1, 1, 640, 128, "bfloat16")
+    inp = W.make_inputs(w)
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", "1")
+    monkeypatch.setenv("GB300_SDPA_DEBUG_DROP_LAST_TILE", "1")
+    old = S.sdpa_debug_set_wait_limit_ns(50_000_000)
+    try:
+        S.sdpa_forward(q, k, v)
+        assert S.sdpa_device_status() == 6  # SDPA_ERR_TIMEOUT
+    finally:
+        S.sdpa_debug_set_wait_limit_ns(old)
+        monkeypatch.delenv("GB300_SDPA_DEBUG_DROP_LAST_TILE")
+    assert S.sdpa_device_status() == 0  # cleared by the read
+    check(torch, w)  # the context still works
