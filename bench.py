@@ -1,0 +1,392 @@
+"""Benchmark of the fused SDPA forward on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}]
+
+A step is one sdpa_forward call (the whole hot path) on the diffusion-
+transformer self-attention workload of MLX PR #964 (B=2, H=38, Lq=Lk=4250,
+D=64, fp16, scale 1/8, no mask; seeded N(0,1) inputs).  The value is the
+algorithmic attention throughput, 4*D FLOPs per visible (query, key) pair,
+over the K timed steps, timed with CUDA events on the launching stream.  The
+inputs rotate over three copies (372 MB > 2 x L2) so that no step starts
+with its inputs in L2.  With N > 1 (torchrun) every rank runs the same
+workload on its own GPU (replicas; weak scaling) and the slowest rank's time
+counts.
+
+Besides the headline line the JSON carries: `e2e` (the same metric through
+the C ABI with host buffers: pinned host->device copy of q, k, v and
+device->host copy of o and lse inside the timed region), `roofline` of the
+prefill kernel against the measured peak, `clocks` sampled during the timed
+region, `cpu_baseline` (the float64 oracle on this host's cores over a
+bounded sample of the same workload) and `secondary` measurements of the
+other workloads (causal GQA prefill, fp32 prefill, both decode workloads).
+
+`--impl reference` times the float64 CPU oracle as it stands (there is no
+reference implementation to install: the pages carry no code for this path)
+on the same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SDPA TFLOP/s (prefill) & KV-read GB/s (decode), % of GB300 roofline, 1 GPU"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "scaled_dot_product_fwd_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(name, files, launch_units=None):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    summary is missing or the kernel source changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", name + ".json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash(files):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------ GPU arm
+def gpu_inputs(torch, w, copies, device):
+    from scaled_dot_product_fwd_gb300 import workloads as W
+    base = W.make_inputs(w)
+    sets = []
+    for c in range(copies):
+        sets.append({k: (None if t is None else t.to(device)) for k, t in base.items()})
+    return base, sets
+
+
+def time_device(torch, fn, nsets, steps, warmup, stream):
+    """fn(i) launches step i (input set i % nsets); seconds of `steps` calls."""
+    for i in range(warmup):
+        fn(i % nsets)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        fn(i % nsets)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop) / 1e3  # seconds
+
+
+def run_workload(torch, S, w, steps, warmup, device, stream, copies=None):
+    """Device-timed seconds for `steps` calls on rotating input copies."""
+    es = 4 if w.dtype == "float32" else 2
+    per = (w.B * w.Hq * w.Lq * w.D + 2 * w.B * w.Hkv * w.Lk * w.D) * es
+    if copies is None:
+        copies = min(64, max(1, -(-2 * L2_BYTES // max(per, 1))))
+    _, sets = gpu_inputs(torch, w, copies, device)
+    Bq, Hq, Lq, D = sets[0]["q"].shape
+    outs = [torch.empty_like(s["q"]) for s in sets]
+    lses = [torch.empty((Bq, Hq, Lq), dtype=torch.float32, device=device) for s in sets]
+
+    def fn(i):
+        s = sets[i]
+        S.sdpa_forward(s["q"], s["k"], s["v"], scale=w.scale, causal=w.causal,
+                       sinks=s["sinks"], out=outs[i], lse=lses[i])
+
+    secs = time_device(torch, fn, len(sets), steps, warmup, stream)
+    if S.sdpa_device_status() != 0:
+        raise RuntimeError("device status set during %s" % w.name)
+    return secs, copies, per
+
+
+def run_e2e(torch, S, w, steps, warmup, device, stream):
+    """Same metric with host buffers: H2D of q, k, v and D2H of o, lse per step."""
+    from scaled_dot_product_fwd_gb300 import workloads as W
+    host = W.make_inputs(w)
+    hq, hk, hv = (host[k].pin_memory() for k in ("q", "k", "v"))
+    dq, dk, dv = (torch.empty_like(t, device=device) for t in (hq, hk, hv))
+    B, Hq, Lq, D = hq.shape
+    do = torch.empty_like(dq)
+    dl = torch.empty((B, Hq, Lq), dtype=torch.float32, device=device)
+    ho = torch.empty_like(hq).pin_memory()
+    hl = torch.empty((B, Hq, Lq), dtype=torch.float32).pin_memory()
+
+    def step(_):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        S.sdpa_forward(dq, dk, dv, scale=w.scale, causal=w.causal, out=do, lse=dl)
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+
+    secs = time_device(torch, step, 1, steps, warmup, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return secs, h2d, d2h
+
+
+def cpu_baseline(w, target_s=12.0):
+    """The float64 oracle on this host's cores over a bounded row sample."""
+    import numpy as np
+
+    from oracle import oracle as orc
+    from scaled_dot_product_fwd_gb300 import workloads as W
+    inp = W.make_inputs(w)
+    f = W.as_float64
+    q, k, v = f(inp["q"]), f(inp["k"]), f(inp["v"])
+    total = w.B * w.Hq * w.Lq
+    rng = np.random.default_rng(3)
+    flops_row = w.flops() / total
+    n, done, elapsed = 256, 0, 0.0
+    while elapsed < target_s and n <= total:
+        rows = rng.integers(0, total, size=n)
+        t0 = time.perf_counter()
+        orc.sdpa(q, k, v, w.scale, w.causal, rows=rows)
+        dt = time.perf_counter() - t0
+        done += n
+        elapsed += dt
+        n = min(total, int(n * max(2.0, 1.5 * (target_s - elapsed) / max(dt, 1e-3))))
+    rate = done * flops_row / elapsed
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": "%d random query rows of %s (all keys each), %.1f s" % (done, w.name, elapsed)}
+
+
+def secondary(torch, S, device, stream, peaks):
+    """Other workloads, device-timed (for context; not the headline)."""
+    from scaled_dot_product_fwd_gb300 import workloads as W
+    out = {}
+    for w, steps in ((W.CAUSAL_GQA, 100), (W.DIT_F32, 20)):
+        secs, copies, _ = run_workload(torch, S, w, steps, 3, device, stream)
+        t = w.flops() * steps / secs / 1e12
+        out[w.name] = {"value": round(t, 2), "unit": "TFLOP/s", "ms_per_call": secs / steps * 1e3,
+                       "frac_of_bf16_peak": round(t / peaks["bf16_tflops"], 4)}
+    for w, steps in ((W.DECODE_LONG, 200), (W.DECODE_D512[(1, "bfloat16", False)], 500),
+                     (W.DECODE_D512[(1, "float16", True)], 500)):
+        secs, copies, _ = run_workload(torch, S, w, steps, 5, device, stream)
+        g = w.kv_bytes() * steps / secs / 1e9
+        out[w.name] = {"value": round(g, 1), "unit": "GB/s", "us_per_call": secs / steps * 1e6,
+                       "frac_of_hbm": round(g / peaks["hbm_gbs"], 4),
+                       "input_copies": copies}
+    return out
+
+
+def gb300_arm(args):
+    import torch
+
+    import scaled_dot_product_fwd_gb300 as S
+    from scaled_dot_product_fwd_gb300 import workloads as W
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+    S.load_library()
+    peaks, peak_kind = load_peaks()
+    w = W.NAMED[args.workload]
+    stream = torch.cuda.current_stream(device)
+
+    # --- timed region: K steps, device time, max over ranks
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        secs, copies, per = run_workload(torch, S, w, args.steps, args.warmup, device, stream)
+    if dist is not None:
+        t = torch.tensor([secs], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = float(t.item())
+        dist.barrier()
+    flops = w.flops()
+    value = flops * args.steps * world / secs / 1e12
+    per_launch = secs / args.steps
+    achieved = flops / per_launch / 1e12
+    e2e_secs, h2d, d2h = run_e2e(torch, S, w, max(3, args.steps // 10), args.warmup, device, stream)
+    e2e_value = flops * max(3, args.steps // 10) * world / e2e_secs / 1e12
+    traffic = profile_traffic("prefill_tc_" + w.name, ["prefill_tc.cu", "ptx.cuh"])
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"float16": "f16", "bfloat16": "bf16", "float32": "f32"}[w.dtype],
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq,
+                   "Lk": w.Lk, "D": w.D, "causal": w.causal,
+                   "flops_per_step": flops,
+                   "l2": "inputs rotate over %d copies (%d MB > 2 x L2)" % (
+                       copies, copies * per // 10**6),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": traffic, "peak_source": peak_kind + " (bf16 dense, burst)",
+                     "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)},
+        "clocks": clk.summary(),
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+    }
+    if rank == 0 and not args.no_secondary:
+        result["secondary"] = secondary(torch, S, device, stream, peaks)
+    if rank == 0 and not args.no_cpu and world == 1:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def reference_arm(args):
+    world, rank, local = dist_setup(args)
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+    from scaled_dot_product_fwd_gb300 import workloads as W
+    import numpy as np
+    orc.build()
+    w = W.NAMED[args.workload]
+    inp = W.make_inputs(w)
+    f = W.as_float64
+    q, k, v = f(inp["q"]), f(inp["k"]), f(inp["v"])
+    total = w.B * w.Hq * w.Lq
+    flops_row = w.flops() / total
+    rng = np.random.default_rng(5)
+    # size one step so that warmup + steps take about a minute
+    t0 = time.perf_counter()
+    orc.sdpa(q, k, v, w.scale, w.causal, rows=rng.integers(0, total, size=128))
+    per_row = (time.perf_counter() - t0) / 128
+    rows = int(max(1, min(total, 60.0 / max(args.steps + args.warmup, 1) / per_row)))
+    for _ in range(args.warmup):
+        orc.sdpa(q, k, v, w.scale, w.causal, rows=rng.integers(0, total, size=rows))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.sdpa(q, k, v, w.scale, w.causal, rows=rng.integers(0, total, size=rows))
+    secs = time.perf_counter() - t0
+    value = rows * flops_row * args.steps / secs / 1e12
+    sample = "%d random query rows of %s per step (all keys each)" % (rows, w.name)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq,
+                   "Lk": w.Lk, "D": w.D, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": orc.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="dit_b2_h38_l4250_d64_f16")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gb300_arm(args)
+
+
+if __name__ == "__main__":
+    main()
