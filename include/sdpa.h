@@ -175,6 +175,36 @@ SDPA_API uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns);
 /* sdpa_abi_version — SDPA_ABI_VERSION of the built library. */
 SDPA_API int sdpa_abi_version(void);
 
+/*
+ * sdpa_forward_decode_noalloc — single-query decode (Lq == 1) without a
+ * caller workspace.  The pages have no counterpart: this entry point exists
+ * for callers that cannot call cudaMalloc or pass device scratch where they
+ * run attention (a stream being captured into a CUDA graph may not
+ * allocate, cudaMalloc can synchronise the device, and some hosts own every
+ * device byte through their own pool and have none to spare for a library).
+ *
+ * Same problem description, inputs, outputs, stream and errors as
+ * sdpa_forward, restricted to problems that sdpa_select_kernel maps to
+ * SDPA_KERNEL_DECODE_SPLITKV (others: SDPA_ERR_UNSUPPORTED; nothing to
+ * compute: SDPA_OK).  The split-KV partial results go to one static device
+ * array of SDPA_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the
+ * library holds until exit; a problem whose partial results do not fit
+ * (about B * Hq * splits * (D + 1) * 4 bytes) returns
+ * SDPA_ERR_WORKSPACE_TOO_SMALL before any launch.  Nothing is allocated.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address (cudaGetSymbolAddress) and caches it: make that
+ *    first call before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents; calls whose kernels overlap on the GPU race on it, so the
+ *    caller must order them (one stream, or events).  Nothing in it needs to
+ *    start at zero: each call writes every partial result before reading it.
+ */
+#define SDPA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+SDPA_API sdpa_status_t sdpa_forward_decode_noalloc(const sdpa_params_t* params,
+                                                   const void* q, const void* k,
+                                                   const void* v, void* o, float* lse,
+                                                   void* stream);
+
 #ifdef __cplusplus
 }
 #endif

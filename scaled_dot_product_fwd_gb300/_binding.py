@@ -24,7 +24,8 @@ KERNELS = {0: "none", 1: "prefill_tc", 2: "prefill_f32", 3: "decode_splitkv", 4:
 
 # Every symbol include/sdpa.h declares.
 EXPORTS = ("sdpa_workspace_size", "sdpa_select_kernel", "sdpa_forward", "sdpa_status_string",
-           "sdpa_device_status", "sdpa_debug_set_wait_limit_ns", "sdpa_abi_version")
+           "sdpa_device_status", "sdpa_debug_set_wait_limit_ns", "sdpa_abi_version",
+           "sdpa_forward_decode_noalloc")
 
 
 class SdpaParams(ctypes.Structure):
@@ -72,6 +73,8 @@ def load_library(path: str = LIB_PATH):
             lib.sdpa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             lib.sdpa_debug_set_wait_limit_ns.restype = ctypes.c_uint64
             lib.sdpa_abi_version.restype = ctypes.c_int
+            lib.sdpa_forward_decode_noalloc.argtypes = [P] + [ctypes.c_void_p] * 6
+            lib.sdpa_forward_decode_noalloc.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -112,6 +115,13 @@ def sdpa_forward_raw(params: SdpaParams, q, k, v, o, lse, workspace, workspace_b
     pp = ctypes.byref(params) if params is not None else None
     return int(load_library().sdpa_forward(pp, q, k, v, o, lse, workspace,
                                            int(workspace_bytes), stream))
+
+
+def sdpa_forward_decode_noalloc_raw(params: SdpaParams, q, k, v, o, lse, stream) -> int:
+    """Direct call of the allocation-free decode entry point (integer device
+    addresses; partial results in the library's static device scratch)."""
+    pp = ctypes.byref(params) if params is not None else None
+    return int(load_library().sdpa_forward_decode_noalloc(pp, q, k, v, o, lse, stream))
 
 
 def sdpa_device_status(stream=None) -> int:

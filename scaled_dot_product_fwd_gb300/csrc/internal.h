@@ -32,6 +32,11 @@ struct DecodePlan {
 
 bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);
 
+// Device status word of the current device (nullptr if there is no device)
+// and the current bound on device-side waits; both owned by sdpa_api.cu.
+int* status_word_current_device();
+uint64_t current_wait_limit_ns();
+
 sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const void* k,
                                 const void* v, void* o, float* lse, const LaunchEnv& env);
 sdpa_status_t launch_prefill_f32(const sdpa_params_t& p, const void* q, const void* k,

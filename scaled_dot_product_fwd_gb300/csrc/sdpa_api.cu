@@ -99,6 +99,17 @@ int current_num_sms() {
 
 }  // namespace
 
+namespace gb300 {
+
+int* status_word_current_device() {
+  int* status = nullptr;
+  return device_state(nullptr, &status, nullptr) ? status : nullptr;
+}
+
+uint64_t current_wait_limit_ns() { return g_wait_ns.load(); }
+
+}  // namespace gb300
+
 extern "C" {
 
 int sdpa_abi_version(void) { return SDPA_ABI_VERSION; }
