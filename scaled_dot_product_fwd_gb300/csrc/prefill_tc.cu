@@ -17,8 +17,10 @@
 //   warp 9     MMA issuer: one thread issues tcgen05.mma,
 //              S_t = Q_t K_j^T (A, B from shared memory, fp32 in TMEM) and
 //              O_t += P_t V_j (P from TMEM, written there by the softmax
-//              warps over the columns of S_t; V from shared memory).
-// TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  The issue order
+//              warps over the columns of S_t; V from shared memory);
+//   warps 10-11 idle (complete the control warpgroup).
+// Each ring stage holds K_j and V_j (one full and one empty barrier per
+// step).  TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  The issue order
 // S_0,j+1 right after PV_0,j lets softmax of one tile overlap the MMAs of
 // the other.  The O rescale is lazy: a row's reference max moves only when
 // the new max exceeds it by more than 8 (log2 units), so P stays <= 2^8.
@@ -40,7 +42,11 @@ constexpr int NQ = 2;    // query tiles per CTA
 constexpr int kSoftmaxWarps = 4 * NQ;
 constexpr int kLoadWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+// warps 8-11 form the control warpgroup (producer, MMA issuer, two idle
+// warps); it gives registers to the softmax warpgroups with setmaxnreg.
+constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
+constexpr uint32_t kSoftmaxRegs = 224;
+constexpr uint32_t kControlRegs = 56;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -49,10 +55,11 @@ template <int D>
 struct Cfg {
   static constexpr int CB = D / 64;           // 128-byte column blocks per row
   static constexpr int TILE = BM * D * 2;     // bytes of one 128-row fp16/bf16 tile
-  static constexpr int NS = (D == 64) ? 8 : 4;  // K/V ring buffers (K_j, V_j alternate)
+  static constexpr int NS = (D == 64) ? 4 : 2;  // ring stages, each K_j then V_j
+  static constexpr int STAGE = 2 * TILE;
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = NQ * TILE;
-  static constexpr int BAR_OFF = RING_OFF + NS * TILE;
+  static constexpr int BAR_OFF = RING_OFF + NS * STAGE;
   // q_full, full[NS], empty[NS], s_full[NQ], p_full[NQ], o_done[NQ], drain
   static constexpr int NBARS = 1 + 2 * NS + 3 * NQ + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
@@ -98,6 +105,94 @@ struct Elem<false> {
     return *reinterpret_cast<uint32_t*>(&v);
   }
 };
+
+// ---------------------------------------------------------------- softmax math
+// Pairs of fp32 values in one 64-bit register for the packed f32x2 FMA/add.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x for a pair x in [-125, 128) on the FMA pipe.  x = n + f with n the
+// nearest integer (added to 1.5 * 2^23, whose low mantissa bits then hold n)
+// and f in [-1/2, 1/2]; 2^f from a degree-3 polynomial fitted for this
+// kernel (minimax in relative error on [-1/2, 1/2], max 7.5e-5, below the
+// rounding of the fp16/bf16 P it feeds); 2^n enters as n << 23 added to the
+// exponent field.  The caller clamps x below at -125 so the field stays >= 1.
+__device__ __forceinline__ void exp2_poly_pair(uint64_t X, float& r0, float& r1) {
+  constexpr uint64_t kMagic = 0x4b4000004b400000ull;     // 1.5 * 2^23 (pair)
+  constexpr uint64_t kNegMagic = 0xcb400000cb400000ull;  // -1.5 * 2^23
+  constexpr uint64_t kNeg1 = 0xbf800000bf800000ull;      // -1
+  constexpr uint64_t kC0 = 0x3f7ffb493f7ffb49ull;        // 0.99992806
+  constexpr uint64_t kC1 = 0x3f31798d3f31798dull;        // 0.69326097
+  constexpr uint64_t kC2 = 0x3e786f0d3e786f0dull;        // 0.24261113
+  constexpr uint64_t kC3 = 0x3d61fbb03d61fbb0ull;        // 0.05517167
+  const uint64_t NP = f2_add(X, kMagic);
+  const uint64_t N = f2_add(NP, kNegMagic);
+  const uint64_t F = f2_fma(N, kNeg1, X);
+  uint64_t P = f2_fma(kC3, F, kC2);
+  P = f2_fma(P, F, kC1);
+  P = f2_fma(P, F, kC0);
+  float p0, p1, n0, n1;
+  f2_unpack(P, p0, p1);
+  f2_unpack(NP, n0, n1);
+  r0 = __int_as_float(__float_as_int(p0) + (__float_as_int(n0) << 23));
+  r1 = __int_as_float(__float_as_int(p1) + (__float_as_int(n1) << 23));
+}
+
+// Pairs (bit i of the mask = pair index mod 8) whose exponentials go to the
+// FMA pipe instead of the MUFU unit.
+#ifndef SDPA_POLY_PAIRS_MASK
+#define SDPA_POLY_PAIRS_MASK 0x00
+#endif
+
+// p_i = 2^(s_i * sl2 - m) for one row of raw scores, packed to fp16/bf16
+// pairs; rs receives the fp32 sum of the p_i.
+template <bool BF16, int N>
+__device__ __forceinline__ void softmax_pairs(const uint32_t (&s)[N], float sl2, float m,
+                                              uint32_t (&pk)[N / 2], float& rs) {
+  const uint64_t SL = f2_pack(sl2, sl2);
+  const uint64_t NM = f2_pack(-m, -m);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const uint64_t X = f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                              SL, NM);
+    float x0, x1, p0, p1;
+    f2_unpack(X, x0, x1);
+    if ((SDPA_POLY_PAIRS_MASK >> (i & 7)) & 1) {
+      exp2_poly_pair(f2_pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f)), p0, p1);
+    } else {
+      p0 = ex2(x0);
+      p1 = ex2(x1);
+    }
+    acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+    pk[i] = Elem<BF16>::pack(p0, p1);
+  }
+  const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+  float t0, t1;
+  f2_unpack(t, t0, t1);
+  rs = t0 + t1;
+}
 
 // Wait for a phase ignoring the abort flag (used only to drain in-flight
 // asynchronous work before the CTA exits); bounded by limit_ns.
@@ -191,6 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int s = 0; s < C::NS; ++s) last_use[s] = -1;
 
+  // launch: 384 threads x 168 registers; the control warpgroup drops to 56
+  // and the softmax warpgroups rise to 224 (256*224 + 128*56 = 384*168).
+  if (warp >= kSoftmaxWarps) {
+    setmaxnreg_dec<kControlRegs>();
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -202,75 +301,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cb = 0; cb < C::CB; ++cb)
           tma_load_3d(sQ + t * C::TILE + cb * BM * 128, &tmQ, q_full, cb * 64, m0 + t * BM,
                       b * a.Hq + h);
-      for (int idx = 0; idx < 2 * nmax; ++idx) {
-        const int s = idx % C::NS;
-        const int use = idx / C::NS;
+      for (int j = 0; j < nmax; ++j) {
+        const int s = j % C::NS;
+        const int use = j / C::NS;
         if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, wc)) break;
-        mbar_arrive_expect_tx(&full[s], C::TILE);
-        const CUtensorMap* map = (idx & 1) ? &tmV : &tmK;
-        const int j = idx >> 1;
-        for (int cb = 0; cb < C::CB; ++cb)
-          tma_load_3d(sRing + s * C::TILE + cb * BN * 128, map, &full[s], cb * 64, j * BN,
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        uint8_t* st = sRing + s * C::STAGE;
+        for (int cb = 0; cb < C::CB; ++cb) {
+          tma_load_3d(st + cb * BN * 128, &tmK, &full[s], cb * 64, j * BN, b * a.Hkv + kvh);
+          tma_load_3d(st + C::TILE + cb * BN * 128, &tmV, &full[s], cb * 64, j * BN,
                       b * a.Hkv + kvh);
+        }
         last_use[s] = use;
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
+    // One thread issues every MMA in a fixed order, PV_0,j S_0,j+1 PV_1,j
+    // S_1,j+1, so each tile's next scores are ready as early as possible.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
       constexpr uint32_t idO = idesc_f16(BF16, BM, D, false, true);
-      const uint32_t q_addr = smem_addr(sQ);
-      const uint32_t ring_addr = smem_addr(sRing);
-      auto kbuf = [](int j) { return (2 * j) % C::NS; };
-      auto kpar = [](int j) { return static_cast<uint32_t>(((2 * j) / C::NS) & 1); };
-      auto vbuf = [](int j) { return (2 * j + 1) % C::NS; };
-      auto vpar = [](int j) { return static_cast<uint32_t>(((2 * j + 1) / C::NS) & 1); };
+      // descriptors of Q_0 and ring buffer 0; other tiles, buffers and K
+      // steps are offsets of the 16-byte-granular start-address field
+      const uint64_t q_desc = sdesc(smem_addr(sQ), 16, 1024, kSwizzle128B);
+      const uint64_t k_desc0 = sdesc(smem_addr(sRing), 16, 1024, kSwizzle128B);
+      const uint64_t v_desc0 = sdesc(smem_addr(sRing), BN * 128, 1024, kSwizzle128B);
+      auto stage = [](int j) { return j % C::NS; };
+      auto spar = [](int j) { return static_cast<uint32_t>((j / C::NS) & 1); };
       // S_t = Q_t K_j^T: both operands K-major, 128-byte swizzle; a K step of
       // 16 elements is 32 bytes inside a 128-byte row, 4 steps per column block.
       auto issue_s = [&](int t, int j) {
-        const uint32_t qa = q_addr + t * C::TILE;
-        const uint32_t ka = ring_addr + kbuf(j) * C::TILE;
+        const uint64_t qd = q_desc + static_cast<uint64_t>((t * C::TILE) >> 4);
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>((stage(j) * C::STAGE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          mma_f16_ss(tmem + C::s_col(t), sdesc(qa + off, 16, 1024, kSwizzle128B),
-                     sdesc(ka + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+          mma_f16_ss(tmem + C::s_col(t), qd + off, kd + off, idS, kk > 0 ? 1u : 0u);
         }
       };
       // O_t += P_t V_j: P (128 x 128, K-major) from TMEM columns of S_t,
       // 2 elements per column; V MN-major: 64-wide column blocks BN*128
       // bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).
       auto issue_pv = [&](int t, int j) {
-        const uint32_t va = ring_addr + vbuf(j) * C::TILE;
+        const uint64_t vd =
+            v_desc0 + static_cast<uint64_t>((stage(j) * C::STAGE + C::TILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
+        for (int kk = 0; kk < BN / 16; ++kk)
           mma_f16_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                     sdesc(va + kk * 16 * 128, BN * 128, 1024, kSwizzle128B), idO,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-        }
+                     vd + ((kk * 16 * 128) >> 4), idO, (j > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(q_full, 0, wc);
       if (ok) {
         for (int t = 0; t < nt; ++t)
           if (nkv[t] == 0) mma_commit(&o_done[t]);
         if (nmax > 0) {
-          ok = mbar_wait(&full[kbuf(0)], kpar(0), wc);
+          ok = mbar_wait(&full[stage(0)], spar(0), wc);
           if (ok) {
-            tc_fence_after();
             for (int t = 0; t < nt; ++t)
               if (nkv[t] > 0) {
                 issue_s(t, 0);
                 mma_commit(&s_full[t]);
               }
-            mma_commit(&empty[kbuf(0)]);
           }
         }
       }
       for (int j = 0; ok && j < nmax; ++j) {
-        ok = mbar_wait(&full[vbuf(j)], vpar(j), wc);
-        if (!ok) break;
-        tc_fence_after();
         bool kwaited = false;
         for (int t = 0; t < nt && ok; ++t) {
           if (j >= nkv[t]) continue;
@@ -280,9 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(t, j);
           if (j + 1 < nkv[t]) {
             if (!kwaited) {
-              ok = mbar_wait(&full[kbuf(j + 1)], kpar(j + 1), wc);
+              ok = mbar_wait(&full[stage(j + 1)], spar(j + 1), wc);
               if (!ok) break;
-              tc_fence_after();
               kwaited = true;
             }
             issue_s(t, j + 1);
@@ -292,15 +387,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(&empty[vbuf(j)]);
-        if (kwaited) mma_commit(&empty[kbuf(j + 1)]);
+        // stage j (K_j read by S_t,j, V_j by PV_t,j) is free once these land
+        mma_commit(&empty[stage(j)]);
       }
       // every MMA issued by this thread completes before TMEM is freed
       mma_commit(drain);
       drain_wait(drain, 0, kDrainNs);
     }
     __syncwarp();
+  }
   } else {
+    setmaxnreg_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------- softmax
     const int t = warp >> 2;
     const int r = (warp & 3) * 32 + lane;  // row inside the tile = TMEM lane
@@ -318,6 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY;  // reference max (log2 units)
     float l = 0.f;        // running sum relative to m
     bool ok = true;
+    // interior tiles take the fused path when the scores need no mask and
+    // the scale is positive (max of raw scores = max of scaled scores)
+    const bool fast_ok = (a.sl2 > 0.f) && (a.mask == nullptr);
     if (t < nt) {
       for (int j = 0; j < nkv[t]; ++j) {
         ok = mbar_wait(&s_full[t], j & 1, wc);
@@ -332,38 +432,68 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
         tmem_wait_ld();
         const int kv0 = j * BN;
-        float x[BN];
-#pragma unroll
-        for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(s[i]) * a.sl2;
-        if (mrow) {
-#pragma unroll
-          for (int i = 0; i < BN; ++i)
-            if (kv0 + i < a.Lk) x[i] += E::to_f(mrow[kv0 + i]) * kLog2e;
-        }
-        if (kv0 + BN - 1 > limit) {
-#pragma unroll
-          for (int i = 0; i < BN; ++i)
-            if (kv0 + i > limit) x[i] = -INFINITY;
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < BN; ++i) mx = fmaxf(mx, x[i]);
         float alpha = 1.f;
-        const bool resc = mx > m + kRescaleThreshold;  // true on the first visible tile
-        if (resc) {
-          alpha = ex2(m - mx);  // 0 when m = -inf
-          m = mx;
-        }
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        float rs = 0.f;
+        bool resc;
+        float rs;
         uint32_t pk[BN / 2];
+        if (fast_ok && kv0 + BN - 1 <= limit) {
+          // Interior tile, positive scale, no mask: max of the raw scores,
+          // then p = 2^(s * scale*log2e - m) with the scale folded into one
+          // packed FMA per pair.
+          float mr[8];
 #pragma unroll
-        for (int i = 0; i < BN / 2; ++i) {
-          const float p0 = ex2(x[2 * i] - mu);
-          const float p1 = ex2(x[2 * i + 1] - mu);
-          rs += p0 + p1;
-          pk[i] = E::pack(p0, p1);
+          for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
+#pragma unroll
+          for (int i = 8; i < BN; i += 16)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
+          const float mx = fmaxf(fmax3(mr[0], mr[1], mr[2]),
+                                 fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7]))) *
+                           a.sl2;
+          resc = mx > m + kRescaleThreshold;
+          if (resc) {
+            alpha = ex2(m - mx);
+            m = mx;
+          }
+          softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
+        } else {
+          float x[BN];
+#pragma unroll
+          for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(s[i]) * a.sl2;
+          if (mrow) {
+#pragma unroll
+            for (int i = 0; i < BN; ++i)
+              if (kv0 + i < a.Lk) x[i] += E::to_f(mrow[kv0 + i]) * kLog2e;
+          }
+          if (kv0 + BN - 1 > limit) {
+#pragma unroll
+            for (int i = 0; i < BN; ++i)
+              if (kv0 + i > limit) x[i] = -INFINITY;
+          }
+          float mr[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+          for (int i = 4; i < BN; i += 8)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) mr[c] = fmax3(mr[c], x[i + 2 * c], x[i + 2 * c + 1]);
+          const float mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+          resc = mx > m + kRescaleThreshold;  // true on the first visible tile
+          if (resc) {
+            alpha = ex2(m - mx);  // 0 when m = -inf
+            m = mx;
+          }
+          const float mu = (m == -INFINITY) ? 0.f : m;
+          float rp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < BN / 2; ++i) {
+            const float p0 = ex2(x[2 * i] - mu);
+            const float p1 = ex2(x[2 * i + 1] - mu);
+            rp[i & 3] += p0 + p1;
+            pk[i] = E::pack(p0, p1);
+          }
+          rs = (rp[0] + rp[1]) + (rp[2] + rp[3]);
         }
+        __syncwarp();
         l = l * alpha + rs;
         // O_t holds the sum through PV_{t,j-1} (complete: the commit behind
         // s_full tracks every earlier MMA); rescale rows whose max moved.
