@@ -384,6 +384,7 @@ sdpa_status_t launch_split(const SplitArgs& a, int batch, cudaStream_t stream) {
   using C = SplitCfg<T, D, HG, KB>;
   auto kern = decode_split_kernel<T, D, HG, KB>;
   const size_t smem = C::smem_bytes(a.stages);
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return SDPA_ERR_CUDA;

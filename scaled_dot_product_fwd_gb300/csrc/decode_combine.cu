@@ -47,32 +47,72 @@ struct St<__nv_bfloat16> {
   static __device__ __forceinline__ __nv_bfloat16 c(float x) { return __float2bfloat16_rn(x); }
 };
 
+constexpr int kMaxSplits = 1024;  // upper bound of the split plan
+
+// Block-wide max / sum over the 128 threads (4 warps).
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, w) : v + w;
+  }
+  __syncthreads();  // red is reused by consecutive reductions
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = red[0];
+#pragma unroll
+  for (int i = 1; i < kCombineThreads / 32; ++i) v = is_max ? fmaxf(v, red[i]) : v + red[i];
+  return v;
+}
+
+// One block per output row: the split weights 2^(lse_s - M) go to shared
+// memory once, then each thread sums its float4 columns over the splits with
+// the loads of several splits in flight.
 template <typename T>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const CombineArgs a) {
+  __shared__ float w[kMaxSplits];
+  __shared__ float red[kCombineThreads / 32];
   const size_t row = blockIdx.x;  // (b * Hq + hq) * rows_per_head + i
   const int hq = static_cast<int>((row / a.rows_per_head) % a.Hq);
   const int S = a.num_splits;
   const float* ls = a.ws_lse + row * S;
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, ls[s]);
+  for (int s = threadIdx.x; s < S; s += kCombineThreads) M = fmaxf(M, ls[s]);
+  M = block_reduce(M, true, red);
   float sk = -INFINITY;
   if (a.sinks) {
     sk = a.sinks[hq] * kLog2e;
     M = fmaxf(M, sk);
   }
   float L = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) L += ex2(ls[s] - M);
-    if (a.sinks) L += ex2(sk - M);
+  for (int s = threadIdx.x; s < S; s += kCombineThreads) {
+    const float e = (M == -INFINITY) ? 0.f : ex2(ls[s] - M);
+    w[s] = e;
+    L += e;
   }
+  L = block_reduce(L, false, red);  // its barriers also publish w[]
+  if (a.sinks && M != -INFINITY) L += ex2(sk - M);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
   T* orow = static_cast<T*>(a.o) + row * a.D;
-  const float* wo = a.ws_o + row * S * a.D;
-  for (int d = threadIdx.x; d < a.D; d += kCombineThreads) {
-    float acc = 0.f;
-    if (L > 0.f)
-      for (int s = 0; s < S; ++s) acc = fmaf(ex2(ls[s] - M), wo[static_cast<size_t>(s) * a.D + d], acc);
-    orow[d] = St<T>::c(acc * inv);
+  const float4* wo = reinterpret_cast<const float4*>(a.ws_o + row * S * a.D);
+  const int D4 = a.D / 4;
+  for (int c = threadIdx.x; c < D4; c += kCombineThreads) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (L > 0.f) {
+#pragma unroll 8
+      for (int s = 0; s < S; ++s) {
+        const float4 v = wo[static_cast<size_t>(s) * D4 + c];
+        const float ws = w[s];
+        acc.x = fmaf(ws, v.x, acc.x);
+        acc.y = fmaf(ws, v.y, acc.y);
+        acc.z = fmaf(ws, v.z, acc.z);
+        acc.w = fmaf(ws, v.w, acc.w);
+      }
+    }
+    orow[4 * c + 0] = St<T>::c(acc.x * inv);
+    orow[4 * c + 1] = St<T>::c(acc.y * inv);
+    orow[4 * c + 2] = St<T>::c(acc.z * inv);
+    orow[4 * c + 3] = St<T>::c(acc.w * inv);
   }
   if (threadIdx.x == 0 && a.lse) a.lse[row] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
@@ -123,7 +163,7 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   }
   if (const char* env = getenv("GB300_SDPA_DECODE_SPLITS")) {  // test override
     const int f = atoi(env);
-    if (f >= 1) best = f < ntiles ? f : ntiles;
+    if (f >= 1) best = f < max_s ? f : max_s;
   }
   const int tiles_per = (ntiles + best - 1) / best;
   const int split_keys = tiles_per * tk;
@@ -208,6 +248,18 @@ sdpa_status_t launch_no_keys(const sdpa_params_t& p, void* o, float* lse, const 
 static sdpa_status_t launch_combine(int dtype, const dec::CombineArgs& c, unsigned nrows,
                                     cudaStream_t stream) {
   const dim3 grid(nrows);
+  // Same shared-memory carveout as the split pass and the prefill kernels, so
+  // alternating launches do not reconfigure the SM's L1/shared split.
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    cudaFuncSetAttribute(dec::decode_combine_kernel<float>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaFuncSetAttribute(dec::decode_combine_kernel<__half>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaFuncSetAttribute(dec::decode_combine_kernel<__nv_bfloat16>,
+                         cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    carveout_set = true;
+  }
   switch (dtype) {
     case SDPA_F32: dec::decode_combine_kernel<float><<<grid, dec::kCombineThreads, 0, stream>>>(c); break;
     case SDPA_F16: dec::decode_combine_kernel<__half><<<grid, dec::kCombineThreads, 0, stream>>>(c); break;
