@@ -209,6 +209,14 @@ def run_e2e(torch, S, w, steps, warmup, device, stream):
     return secs, h2d, d2h
 
 
+def work_per_row(w, total_rows):
+    """Work of one query row in the workload's metric: FLOPs (prefill,
+    TFLOP/s) or its share of the K/V bytes read once (decode, GB/s)."""
+    if w.Lq == 1:
+        return w.kv_bytes() / total_rows, 1e9, "GB/s"
+    return w.flops() / total_rows, 1e12, "TFLOP/s"
+
+
 def cpu_baseline(w, target_s=12.0):
     """The float64 oracle on this host's cores over a bounded row sample."""
     import numpy as np
@@ -220,7 +228,7 @@ def cpu_baseline(w, target_s=12.0):
     q, k, v = f(inp["q"]), f(inp["k"]), f(inp["v"])
     total = w.B * w.Hq * w.Lq
     rng = np.random.default_rng(3)
-    flops_row = w.flops() / total
+    work_row, scale, unit = work_per_row(w, total)
     n, done, elapsed = 256, 0, 0.0
     while elapsed < target_s and n <= total:
         rows = rng.integers(0, total, size=n)
@@ -230,8 +238,8 @@ def cpu_baseline(w, target_s=12.0):
         done += n
         elapsed += dt
         n = min(total, int(n * max(2.0, 1.5 * (target_s - elapsed) / max(dt, 1e-3))))
-    rate = done * flops_row / elapsed
-    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": orc.num_threads(),
+    rate = done * work_row / elapsed
+    return {"value": rate / scale, "unit": unit, "cores": orc.num_threads(),
             "kind": "oracle",
             "sample": "%d random query rows of %s (all keys each), %.1f s" % (done, w.name, elapsed)}
 
@@ -289,14 +297,29 @@ def gb300_arm(args):
         secs = float(t.item())
         dist.barrier()
     flops = w.flops()
-    value = flops * args.steps * world / secs / 1e12
     per_launch = secs / args.steps
-    achieved = flops / per_launch / 1e12
-    e2e_secs, h2d, d2h = run_e2e(torch, S, w, max(3, args.steps // 10), args.warmup, device, stream)
-    e2e_value = flops * max(3, args.steps // 10) * world / e2e_secs / 1e12
-    traffic = profile_traffic("prefill_tc_" + w.name, ["prefill_tc.cu", "ptx.cuh"])
+    e2e_steps = max(3, args.steps // 10)
+    e2e_secs, h2d, d2h = run_e2e(torch, S, w, e2e_steps, args.warmup, device, stream)
+    if w.Lq == 1:
+        # decode: KV-read GB/s, HBM roofline of the split-KV pass (its launch
+        # and the combine's together: one step)
+        work, unit, scale = w.kv_bytes(), "GB/s", 1e9
+        bound, peak, peak_name = "hbm", peaks["hbm_gbs"], " (HBM copy)"
+        sustained = peaks["hbm_gbs"]
+        traffic = profile_traffic("decode_split_" + w.name, ["decode.cuh", "decode_combine.cu"])
+        launches = 2 * args.steps
+    else:
+        work, unit, scale = flops, "TFLOP/s", 1e12
+        bound, peak, peak_name = "tensor", peaks["bf16_tflops"], " (bf16 dense, burst)"
+        sustained = peaks["bf16_tflops_sustained"]
+        kfile = "prefill_f32.cu" if w.dtype == "float32" else "prefill_tc.cu"
+        traffic = profile_traffic(kfile[:-3] + "_" + w.name, [kfile, "ptx.cuh"])
+        launches = args.steps
+    value = work * args.steps * world / secs / scale
+    achieved = work / per_launch / scale
+    e2e_value = work * e2e_steps * world / e2e_secs / scale
     result = {
-        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"float16": "f16", "bfloat16": "bf16", "float32": "f32"}[w.dtype],
@@ -307,14 +330,14 @@ def gb300_arm(args):
                    "l2": "inputs rotate over %d copies (%d MB > 2 x L2)" % (
                        copies, copies * per // 10**6),
                    "parallelism": "replicas" if world > 1 else "single"},
-        "gpu_launches": args.steps,
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": traffic, "peak_source": peak_kind + " (bf16 dense, burst)",
-                     "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)},
+        "gpu_launches": launches,
+        "roofline": {"bound": bound, "achieved": round(achieved, 2),
+                     "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_source": peak_kind + peak_name,
+                     "frac_of_sustained": round(achieved / sustained, 4)},
         "clocks": clk.summary(),
-        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
     }
     if rank == 0 and not args.no_secondary:
@@ -341,7 +364,7 @@ def reference_arm(args):
     f = W.as_float64
     q, k, v = f(inp["q"]), f(inp["k"]), f(inp["v"])
     total = w.B * w.Hq * w.Lq
-    flops_row = w.flops() / total
+    work_row, scale, unit = work_per_row(w, total)
     rng = np.random.default_rng(5)
     # size one step so that warmup + steps take about a minute
     t0 = time.perf_counter()
@@ -354,18 +377,18 @@ def reference_arm(args):
     for _ in range(args.steps):
         orc.sdpa(q, k, v, w.scale, w.causal, rows=rng.integers(0, total, size=rows))
     secs = time.perf_counter() - t0
-    value = rows * flops_row * args.steps / secs / 1e12
+    value = rows * work_row * args.steps / secs / scale
     sample = "%d random query rows of %s per step (all keys each)" % (rows, w.name)
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq,
                    "Lk": w.Lk, "D": w.D, "causal": w.causal},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": orc.num_threads(),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": orc.num_threads(),
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
 
