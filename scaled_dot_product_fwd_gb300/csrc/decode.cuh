@@ -9,14 +9,15 @@
 //  - Warp 8 (producer) streams the split's K and V rows, which are contiguous
 //    in [B, Hkv, Lk, D], into a ring of shared-memory stages with 1-D bulk
 //    copies (cp.async.bulk, completion counted on an mbarrier).
-//  - Warps 0-7 (consumers) each take KB keys of every stage.  A lane owns
-//    D/32 elements of a row (16-byte pieces where the row is long enough, so
-//    a warp reads one row with conflict-free, coalesced shared-memory loads),
-//    keeps the HG query rows of its head group in registers, and forms
-//    HG x KB partial dot products.  One butterfly reduce-scatter over the 32
-//    lanes turns them into complete scores (one per lane, or replicated), a
-//    group xor-shuffle gives the per-head tile max, and the probabilities
-//    and rescale factors are broadcast through a small per-warp buffer.
+//  - Warps 0-7 (consumers) each take KB keys of every stage.  A lane owns a
+//    16-byte piece (or more) of a key row, so a D=128 bf16 row spans 16
+//    lanes and one warp-wide load covers two keys; shared-memory reads are
+//    coalesced and conflict-free.  The HG query rows of the head group stay
+//    in registers as fp32 pairs; dot products and the V accumulation use the
+//    packed f32x2 FMA.  A butterfly reduce-scatter over the lanes of a row
+//    turns the HG x (KB / rows-per-load) partial sums into complete scores,
+//    a shuffle max gives the per-head tile max, and probabilities and rescale
+//    factors are broadcast through a small per-warp buffer.
 //  - At the end the 8 warps' (m, l, acc) states are merged in shared memory
 //    and the split writes its normalised partial output and its log2-domain
 //    log-sum-exp to the workspace.  The combine kernel merges the splits.
@@ -72,34 +73,81 @@ struct Ld<__nv_bfloat16> {
   static __device__ __forceinline__ float f(__nv_bfloat16 x) { return __bfloat162float(x); }
 };
 
-// Load PIECE consecutive elements (4, 8 or 16 bytes) and widen to fp32.
-template <typename T, int PIECE>
-__device__ __forceinline__ void load_piece(const T* p, float* out) {
-  constexpr int BYTES = PIECE * static_cast<int>(sizeof(T));
-  static_assert(BYTES == 4 || BYTES == 8 || BYTES == 16, "piece size");
-  T tmp[PIECE];
-  if constexpr (BYTES == 16) {
-    *reinterpret_cast<uint4*>(tmp) = *reinterpret_cast<const uint4*>(p);
-  } else if constexpr (BYTES == 8) {
-    *reinterpret_cast<uint2*>(tmp) = *reinterpret_cast<const uint2*>(p);
-  } else {
-    *reinterpret_cast<uint32_t*>(tmp) = *reinterpret_cast<const uint32_t*>(p);
-  }
-#pragma unroll
-  for (int i = 0; i < PIECE; ++i) out[i] = Ld<T>::f(tmp[i]);
+// Pairs of fp32 values in one 64-bit register for the packed f32x2 ops.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float f2_sum(uint64_t r) {
+  float a, b;
+  f2_split(r, a, b);
+  return a + b;
 }
 
-// Butterfly reduce-scatter of NV (power of two <= 32) values over the warp:
-// afterwards lane l holds the full sum of value index l >> (5 - log2 NV).
-template <int NV>
-__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
-  constexpr int LOG = (NV >= 32) ? 5 : (NV >= 16) ? 4 : (NV >= 8) ? 3 : (NV >= 4) ? 2 : (NV >= 2) ? 1 : 0;
-  static_assert((1 << LOG) == NV, "NV must be a power of two <= 32");
+// 16 bytes of T widened exactly to fp32 pairs (element 2i in the low half).
+template <typename T>
+struct Widen;
+template <>
+struct Widen<__nv_bfloat16> {
+  static constexpr int CE = 8;
+  static __device__ __forceinline__ void pairs(uint4 w, uint64_t* p) {
+    p[0] = f2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+    p[1] = f2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    p[2] = f2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
+    p[3] = f2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+  }
+};
+template <>
+struct Widen<__half> {
+  static constexpr int CE = 8;
+  static __device__ __forceinline__ uint64_t one(uint32_t x) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x));
+    return f2(f.x, f.y);
+  }
+  static __device__ __forceinline__ void pairs(uint4 w, uint64_t* p) {
+    p[0] = one(w.x);
+    p[1] = one(w.y);
+    p[2] = one(w.z);
+    p[3] = one(w.w);
+  }
+};
+template <>
+struct Widen<float> {
+  static constexpr int CE = 4;
+  static __device__ __forceinline__ void pairs(uint4 w, uint64_t* p) {
+    p[0] = f2(__uint_as_float(w.x), __uint_as_float(w.y));
+    p[1] = f2(__uint_as_float(w.z), __uint_as_float(w.w));
+  }
+};
+
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Butterfly reduce-scatter of NV (power of two) values over the LR lanes of
+// a row group (lanes differing in their low log2(LR) bits): afterwards lane
+// position c holds the full sum of value index c >> (log2 LR - log2 NV).
+template <int NV, int LR>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int c) {
+  constexpr int LOG = ilog2(NV);
+  static_assert((1 << LOG) == NV && NV <= LR, "NV must be a power of two <= LR");
 #pragma unroll
   for (int lev = 0; lev < LOG; ++lev) {
     const int n = NV >> lev;
-    const int msk = 16 >> lev;
-    const bool upper = (lane & msk) != 0;
+    const int msk = (LR / 2) >> lev;
+    const bool upper = (c & msk) != 0;
 #pragma unroll
     for (int i = 0; i < n / 2; ++i) {
       const float send = upper ? v[i] : v[i + n / 2];
@@ -108,38 +156,45 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
     }
   }
 #pragma unroll
-  for (int msk = 16 >> LOG; msk >= 1; msk >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], msk);
+  for (int msk = (LR / 2) >> LOG; msk >= 1; msk >>= 1)
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], msk);
   return v[0];
 }
 
 template <typename T, int D, int HG, int KB>
 struct SplitCfg {
-  static constexpr int EPL = D / 32;                          // elements per lane
-  static constexpr int CE = 16 / static_cast<int>(sizeof(T));  // elements per 16 bytes
-  static constexpr int PIECE = EPL < CE ? EPL : CE;
-  static constexpr int NPIECE = EPL / PIECE;
-  static constexpr int NV = HG * KB;
-  static constexpr int TK = kConsumerWarps * KB;               // keys per stage
+  static constexpr int CE = Widen<T>::CE;                     // elements per 16 bytes
+  static constexpr int EPL = (D / 32 > CE) ? D / 32 : CE;    // elements per lane and row
+  static constexpr int LR = D / EPL;                          // lanes per key row
+  static constexpr int RPW = 32 / LR;                         // key rows per warp-wide load
+  static constexpr int NPIECE = EPL / CE;                     // 16-byte pieces per lane and row
+  static constexpr int NP2 = EPL / 2;                         // fp32 pairs per lane and row
+  static constexpr int LPB = KB / RPW;                        // loads per lane per batch
+  static constexpr int NVL = HG * LPB;                        // partial sums per lane
+  static constexpr int LOG_LR = ilog2(LR);
+  static constexpr int VSHIFT = LOG_LR - ilog2(NVL);          // value index = c >> VSHIFT
+  static constexpr int HBIT = VSHIFT + ilog2(LPB);            // head index = c >> HBIT
+  static constexpr int TK = kConsumerWarps * KB;              // keys per stage
   static constexpr int TILE_BYTES = TK * D * static_cast<int>(sizeof(T));
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int LOG_NV = (NV >= 32) ? 5 : (NV >= 16) ? 4 : (NV >= 8) ? 3 : (NV >= 4) ? 2 : (NV >= 2) ? 1 : 0;
-  static constexpr int HLANES = 32 / HG;                       // lanes per head after the scatter
-  static constexpr int VLANES = 32 / NV;                       // lanes per value
-  // per-warp broadcast buffer: NV probabilities + HG rescale factors
-  static constexpr int PB_FLOATS = NV + HG;
+  // per-warp broadcast buffer: (p, p) pairs per (head, key), then HG factors
+  static constexpr int PB_WORDS = 2 * HG * KB + ((HG + 1) & ~1);
   static constexpr int COMBINE_BYTES = kConsumerWarps * HG * (D + 2) * 4;
-  static_assert(NV <= 32, "too many partial sums per lane");
+  static_assert(LR * EPL == D && RPW * LR == 32, "lane layout");
+  static_assert(KB % RPW == 0 && NVL <= LR, "batch layout");
   static_assert((TILE_BYTES % 16) == 0, "bulk copy granularity");
   static size_t smem_bytes(int stages) {
     size_t ring = static_cast<size_t>(stages) * STAGE_BYTES;
     if (ring < static_cast<size_t>(COMBINE_BYTES)) ring = COMBINE_BYTES;
-    return 128 /*align*/ + ring + kConsumerWarps * PB_FLOATS * 4 + 2 * 8 * 8 /*bars*/ + 16;
+    return 128 /*align*/ + ring + kConsumerWarps * PB_WORDS * 4 + 2 * 8 * 8 /*bars*/ + 16;
   }
 };
 
 template <typename T, int D, int HG, int KB>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs a) {
+__global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
+    decode_split_kernel(const SplitArgs a) {
   using C = SplitCfg<T, D, HG, KB>;
+  using Wd = Widen<T>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((128u - (raw_addr & 127u)) & 127u);
@@ -148,7 +203,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
   size_t ring_bytes = static_cast<size_t>(NS) * C::STAGE_BYTES;
   if (ring_bytes < static_cast<size_t>(C::COMBINE_BYTES)) ring_bytes = C::COMBINE_BYTES;
   float* pbuf = reinterpret_cast<float*>(smem + ring_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + kConsumerWarps * C::PB_FLOATS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + kConsumerWarps * C::PB_WORDS);
   uint64_t* empty = full + 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + 8);
 
@@ -212,28 +267,22 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
   }
 
   // -------------------------------------------------------------- consumers
-  const int vidx = lane >> (5 - C::LOG_NV);  // value index held after the scatter
-  const int hl = vidx / KB;                  // its head inside the group
-  const int kl = vidx % KB;                  // its key inside the warp's batch
-  float qv[HG][C::EPL];
-  bool head_ok[HG];
+  const int r = lane / C::LR;          // key row inside a warp-wide load
+  const int c = lane % C::LR;          // lane position inside the row
+  const int vi = c >> C::VSHIFT;       // value held after the reduce-scatter
+  const int hl = vi / C::LPB;          // its head inside the group
+  const int kl = (vi % C::LPB) * C::RPW + r;  // its key inside the warp batch
+  uint64_t q2[HG][C::NP2];
 #pragma unroll
   for (int hh = 0; hh < HG; ++hh) {
     const int gh = grp * HG + hh;
-    head_ok[hh] = gh < a.G;
     const int hq = kvh * a.G + gh;
     const T* qrow = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + hq) * D;
 #pragma unroll
     for (int pi = 0; pi < C::NPIECE; ++pi) {
-      float tmp[C::PIECE];
-      if (head_ok[hh]) {
-        load_piece<T, C::PIECE>(qrow + (pi * 32 + lane) * C::PIECE, tmp);
-      } else {
-#pragma unroll
-        for (int i = 0; i < C::PIECE; ++i) tmp[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < C::PIECE; ++i) qv[hh][pi * C::PIECE + i] = tmp[i];
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (gh < a.G) w = *reinterpret_cast<const uint4*>(qrow + (pi * C::LR + c) * C::CE);
+      Wd::pairs(w, &q2[hh][pi * (C::CE / 2)]);
     }
   }
   const int my_hq = kvh * a.G + grp * HG + hl;
@@ -241,16 +290,18 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
   const T* mrow = nullptr;
   if (a.mask && my_head_ok) mrow = static_cast<const T*>(a.mask) + b * a.ms0 + my_hq * a.ms1;
 
-  float acc[HG][C::EPL];
+  uint64_t acc2[HG][C::NP2];
   float lsum[HG];
 #pragma unroll
   for (int hh = 0; hh < HG; ++hh) {
     lsum[hh] = 0.f;
 #pragma unroll
-    for (int e = 0; e < C::EPL; ++e) acc[hh][e] = 0.f;
+    for (int e = 0; e < C::NP2; ++e) acc2[hh][e] = 0ull;
   }
   float m_own = -INFINITY;  // running max of head hl (log2 units)
-  float* pb = pbuf + warp * C::PB_FLOATS;
+  float* pb = pbuf + warp * C::PB_WORDS;
+  uint64_t* pb2 = reinterpret_cast<uint64_t*>(pb);  // (p, p) per (head, key)
+  float* pba = pb + 2 * HG * KB;                    // rescale factor per head
   bool ok = true;
 
   for (int t = 0; t < ntiles; ++t) {
@@ -265,27 +316,27 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
     const T* Vs = reinterpret_cast<const T*>(st + C::TILE_BYTES) + warp * KB * D;
     const int key0 = key_begin + t * C::TK + warp * KB;  // key of kk = 0
 
-    float part[C::NV];
+    float part[C::NVL];
 #pragma unroll
-    for (int kk = 0; kk < KB; ++kk) {
-      float kf[C::EPL];
-      if (key0 + kk < key_end) {
+    for (int i = 0; i < C::LPB; ++i) {
+      const int kk = i * C::RPW + r;
+      uint64_t k2[C::NP2];
 #pragma unroll
-        for (int pi = 0; pi < C::NPIECE; ++pi)
-          load_piece<T, C::PIECE>(Ks + kk * D + (pi * 32 + lane) * C::PIECE, kf + pi * C::PIECE);
-      } else {
-#pragma unroll
-        for (int e = 0; e < C::EPL; ++e) kf[e] = 0.f;
+      for (int pi = 0; pi < C::NPIECE; ++pi) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (key0 + kk < key_end)  // rows past the split were not loaded
+          w = *reinterpret_cast<const uint4*>(Ks + kk * D + (pi * C::LR + c) * C::CE);
+        Wd::pairs(w, &k2[pi * (C::CE / 2)]);
       }
 #pragma unroll
       for (int hh = 0; hh < HG; ++hh) {
-        float d0 = 0.f;
+        uint64_t d2 = 0ull;
 #pragma unroll
-        for (int e = 0; e < C::EPL; ++e) d0 = fmaf(qv[hh][e], kf[e], d0);
-        part[hh * KB + kk] = d0;
+        for (int e = 0; e < C::NP2; ++e) d2 = f2_fma(q2[hh][e], k2[e], d2);
+        part[hh * C::LPB + i] = f2_sum(d2);
       }
     }
-    const float sc = reduce_scatter<C::NV>(part, lane);
+    const float sc = reduce_scatter<C::NVL, C::LR>(part, c);
     const int key = key0 + kl;
     float x = sc * a.sl2;
     if (key >= key_end) {
@@ -293,47 +344,65 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
     } else if (mrow) {
       x += Ld<T>::f(mrow[key]) * kLog2e;
     }
+    // tile max of head hl: lanes differing below HBIT or in the row bits
     float tmax = x;
 #pragma unroll
-    for (int off = 1; off < C::HLANES; off <<= 1)
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+    for (int bit = 0; bit < 5; ++bit)
+      if (bit < C::HBIT || bit >= C::LOG_LR)
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1 << bit));
     const float m_new = fmaxf(m_own, tmax);
     const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_own - m_new);
     const float p = (x == -INFINITY) ? 0.f : ex2(x - m_new);
     m_own = m_new;
-    if ((lane & (C::VLANES - 1)) == 0) pb[vidx] = p;
-    if ((lane & (C::HLANES - 1)) == 0) pb[C::NV + hl] = alpha;
+    if ((c & ((1 << C::VSHIFT) - 1)) == 0) pb2[hl * KB + kl] = f2(p, p);
+    if (r == 0 && (c & ((1 << C::HBIT) - 1)) == 0) pba[hl] = alpha;
     __syncwarp();
-    float pv[C::NV], al[HG];
-#pragma unroll
-    for (int i = 0; i < C::NV; ++i) pv[i] = pb[i];
-#pragma unroll
-    for (int hh = 0; hh < HG; ++hh) al[hh] = pb[C::NV + hh];
 #pragma unroll
     for (int hh = 0; hh < HG; ++hh) {
-      float ssum = 0.f;
+      const float al = pba[hh];
+      lsum[hh] *= al;
+      const uint64_t al2 = f2(al, al);
 #pragma unroll
-      for (int kk = 0; kk < KB; ++kk) ssum += pv[hh * KB + kk];
-      lsum[hh] = lsum[hh] * al[hh] + ssum;
-#pragma unroll
-      for (int e = 0; e < C::EPL; ++e) acc[hh][e] *= al[hh];
+      for (int e = 0; e < C::NP2; ++e) acc2[hh][e] = f2_mul(acc2[hh][e], al2);
     }
 #pragma unroll
-    for (int kk = 0; kk < KB; ++kk) {
-      if (key0 + kk >= key_end) continue;  // rows past the split were not loaded
-      float vf[C::EPL];
+    for (int i = 0; i < C::LPB; ++i) {
+      const int kk = i * C::RPW + r;
+      if (key0 + kk >= key_end) continue;  // rows past the split were not loaded (p = 0)
+      uint64_t v2[C::NP2];
 #pragma unroll
       for (int pi = 0; pi < C::NPIECE; ++pi)
-        load_piece<T, C::PIECE>(Vs + kk * D + (pi * 32 + lane) * C::PIECE, vf + pi * C::PIECE);
+        Wd::pairs(*reinterpret_cast<const uint4*>(Vs + kk * D + (pi * C::LR + c) * C::CE),
+                  &v2[pi * (C::CE / 2)]);
 #pragma unroll
       for (int hh = 0; hh < HG; ++hh) {
-        const float w = pv[hh * KB + kk];
+        const uint64_t pp = pb2[hh * KB + kk];
+        float p0, p1;
+        f2_split(pp, p0, p1);
+        lsum[hh] += p0;
 #pragma unroll
-        for (int e = 0; e < C::EPL; ++e) acc[hh][e] = fmaf(w, vf[e], acc[hh][e]);
+        for (int e = 0; e < C::NP2; ++e) acc2[hh][e] = f2_fma(pp, v2[e], acc2[hh][e]);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // ---- fold the row groups of the warp together (same heads, other keys)
+#pragma unroll
+  for (int bit = C::LOG_LR; bit < 5; ++bit) {
+#pragma unroll
+    for (int hh = 0; hh < HG; ++hh) {
+      lsum[hh] += __shfl_xor_sync(0xffffffffu, lsum[hh], 1 << bit);
+#pragma unroll
+      for (int e = 0; e < C::NP2; ++e) {
+        float a0, a1;
+        f2_split(acc2[hh][e], a0, a1);
+        a0 += __shfl_xor_sync(0xffffffffu, a0, 1 << bit);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, 1 << bit);
+        acc2[hh][e] = f2(a0, a1);
+      }
+    }
   }
 
   // ---- merge the warps' states (the ring is idle: every copy was consumed)
@@ -342,17 +411,24 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
   float* wl = wm + kConsumerWarps * HG;             // [warps][HG]
   float* wacc = wl + kConsumerWarps * HG;           // [warps][HG][D]
   if (ok) {
-    if ((lane & (C::HLANES - 1)) == 0) wm[warp * HG + hl] = m_own;
+    if (r == 0 && (c & ((1 << C::HBIT) - 1)) == 0) wm[warp * HG + hl] = m_own;
     if (lane == 0)
 #pragma unroll
       for (int hh = 0; hh < HG; ++hh) wl[warp * HG + hh] = lsum[hh];
+    if (r == 0) {
 #pragma unroll
-    for (int hh = 0; hh < HG; ++hh)
+      for (int hh = 0; hh < HG; ++hh)
 #pragma unroll
-      for (int pi = 0; pi < C::NPIECE; ++pi)
+        for (int pi = 0; pi < C::NPIECE; ++pi)
 #pragma unroll
-        for (int i = 0; i < C::PIECE; ++i)
-          wacc[(warp * HG + hh) * D + (pi * 32 + lane) * C::PIECE + i] = acc[hh][pi * C::PIECE + i];
+          for (int j = 0; j < C::CE / 2; ++j) {
+            float a0, a1;
+            f2_split(acc2[hh][pi * (C::CE / 2) + j], a0, a1);
+            float* dst = wacc + (warp * HG + hh) * D + (pi * C::LR + c) * C::CE + 2 * j;
+            dst[0] = a0;
+            dst[1] = a1;
+          }
+    }
   }
   named_bar_sync(2, kConsumerWarps * 32);
   if (*abort_flag) return;

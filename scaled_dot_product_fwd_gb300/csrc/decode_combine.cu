@@ -145,7 +145,7 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   int per_sm = static_cast<int>(232448 / (smem + 1024));
   if (per_sm < 1) per_sm = 1;
   if (per_sm > 2) per_sm = 2;
-  if (D == 512) per_sm = 1;  // register-bound at D = 512
+  if (D == 512 || hg == 8) per_sm = 1;  // register-bound (one CTA per SM)
   const long long units = static_cast<long long>(p.batch) * p.num_kv_heads * groups;
   const int ntiles = (p.seq_len_kv + tk - 1) / tk;
   const long long slots = static_cast<long long>(num_sms > 0 ? num_sms : 152) * per_sm;
