@@ -23,7 +23,8 @@
 // step).  TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  The issue order
 // S_0,j+1 right after PV_0,j lets softmax of one tile overlap the MMAs of
 // the other.  The O rescale is lazy: a row's reference max moves only when
-// the new max exceeds it by more than 8 (log2 units), so P stays <= 2^8.
+// the new max exceeds it (by more than 8 in log2 units on masked tiles, or
+// so far that a row sum passes 2^15 on interior tiles), so P stays <= 2^15.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -49,7 +50,8 @@ constexpr uint32_t kSoftmaxRegs = 224;
 constexpr uint32_t kControlRegs = 56;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRescaleThreshold = 8.0f;  // log2 units (masked path)
+constexpr float kFusedSumLimit = 32768.0f;  // 2^15: bound on p (fused path)
 
 template <int D>
 struct Cfg {
@@ -437,26 +439,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rs;
         uint32_t pk[BN / 2];
         if (fast_ok && kv0 + BN - 1 <= limit) {
-          // Interior tile, positive scale, no mask: max of the raw scores,
-          // then p = 2^(s * scale*log2e - m) with the scale folded into one
-          // packed FMA per pair.
-          float mr[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
-#pragma unroll
-          for (int i = 8; i < BN; i += 16)
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
-          const float mx = fmaxf(fmax3(mr[0], mr[1], mr[2]),
-                                 fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7]))) *
-                           a.sl2;
-          resc = mx > m + kRescaleThreshold;
-          if (resc) {
-            alpha = ex2(m - mx);
-            m = mx;
+          // Interior tile, positive scale, no mask: p = 2^(s * scale*log2e
+          // - m) with the scale folded into one packed FMA per pair, taken
+          // against the current reference max m without looking for the
+          // tile max.  Every p is at most the row sum, so a sum <= 2^15
+          // proves all p <= 2^15 (exact range in fp16 and bf16); only a row
+          // whose sum exceeds it (its max grew) or the first tile (m = -inf)
+          // finds the tile max of the raw scores and repeats.
+          resc = !(m > -INFINITY);
+          if (!resc) {
+            softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
+            resc = !(rs <= kFusedSumLimit);  // also true for inf or nan
           }
-          softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
+          if (resc) {
+            float mr[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
+#pragma unroll
+            for (int i = 8; i < BN; i += 16)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]),
+                              __uint_as_float(s[i + 2 * c + 1]));
+            const float mx = fmaxf(fmax3(mr[0], mr[1], mr[2]),
+                                   fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7]))) *
+                             a.sl2;
+            alpha = ex2(m - mx);  // 0 when m = -inf
+            m = mx;
+            softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
+          }
         } else {
           float x[BN];
 #pragma unroll
