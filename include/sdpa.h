@@ -77,7 +77,9 @@ typedef enum {
   SDPA_KERNEL_PREFILL_TC = 1,   /* fp16/bf16, Lq > 1: TMA + tcgen05 + TMEM */
   SDPA_KERNEL_PREFILL_F32 = 2,  /* fp32, Lq > 1: fp32 FMA tiles */
   SDPA_KERNEL_DECODE_SPLITKV = 3, /* Lq == 1: split-KV vector pass + combine */
-  SDPA_KERNEL_NO_KEYS = 4        /* Lk == 0: writes o = 0 and the empty lse */
+  SDPA_KERNEL_NO_KEYS = 4,       /* Lk == 0: writes o = 0 and the empty lse */
+  SDPA_KERNEL_PREFILL_TC_F32 = 5 /* fp32, D = 64, Lq > 1: bf16 hi/lo splits on
+                                    tcgen05 (three products per step) */
 } sdpa_kernel_t;
 
 /*
@@ -122,8 +124,9 @@ typedef struct {
 
 /*
  * sdpa_workspace_size — bytes of device workspace that sdpa_forward needs for
- * this problem (split-KV partial outputs of the decode path; 0 when the
- * chosen path needs none).  Pure host function; returns 0 for an invalid
+ * this problem (split-KV partial outputs of the decode path; the bf16 hi/lo
+ * copies of q, k and v of the fp32 tensor-core prefill; 0 when the chosen
+ * path needs none).  Pure host function; returns 0 for an invalid
  * problem as well (sdpa_forward then reports the error).
  */
 SDPA_API size_t sdpa_workspace_size(const sdpa_params_t* params);

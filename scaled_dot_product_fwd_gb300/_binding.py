@@ -20,7 +20,8 @@ SDPA_F32, SDPA_F16, SDPA_BF16 = 0, 1, 2
 STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARGUMENT", 2: "SDPA_ERR_UNSUPPORTED",
           3: "SDPA_ERR_MISALIGNED", 4: "SDPA_ERR_WORKSPACE_TOO_SMALL", 5: "SDPA_ERR_CUDA",
           6: "SDPA_ERR_TIMEOUT"}
-KERNELS = {0: "none", 1: "prefill_tc", 2: "prefill_f32", 3: "decode_splitkv", 4: "no_keys"}
+KERNELS = {0: "none", 1: "prefill_tc", 2: "prefill_f32", 3: "decode_splitkv", 4: "no_keys",
+           5: "prefill_tc_f32"}
 
 # Every symbol include/sdpa.h declares.
 EXPORTS = ("sdpa_workspace_size", "sdpa_select_kernel", "sdpa_forward", "sdpa_status_string",

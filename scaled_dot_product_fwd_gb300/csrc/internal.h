@@ -39,6 +39,12 @@ uint64_t current_wait_limit_ns();
 
 sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const void* k,
                                 const void* v, void* o, float* lse, const LaunchEnv& env);
+// fp32 inputs, D = 64: split into bf16 hi/lo parts in the workspace, then the
+// tensor-core kernel with three products per MMA step.
+size_t prefill_x3_workspace(const sdpa_params_t& p);
+sdpa_status_t launch_prefill_x3(const sdpa_params_t& p, const void* q, const void* k,
+                                const void* v, void* o, float* lse, void* workspace,
+                                const LaunchEnv& env);
 sdpa_status_t launch_prefill_f32(const sdpa_params_t& p, const void* q, const void* k,
                                  const void* v, void* o, float* lse, const LaunchEnv& env);
 // Lk == 0: o = 0, lse = -inf (or the sink) for every row.

@@ -30,6 +30,8 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "tensor_map.h"
@@ -53,14 +55,22 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units (masked path)
 constexpr float kFusedSumLimit = 32768.0f;  // 2^15: bound on p (fused path)
 
-template <int D>
+// X3: fp32 inputs given as bf16 hi + lo splits (x = hi + lo + O(2^-16 x));
+// S = Q_hi K_hi^T + Q_hi K_lo^T + Q_lo K_hi^T and O += P_hi V_hi + P_hi V_lo
+// + P_lo V_hi, each product on the bf16 tensor path with fp32 accumulation.
+template <int D, bool X3 = false>
 struct Cfg {
   static constexpr int CB = D / 64;           // 128-byte column blocks per row
   static constexpr int TILE = BM * D * 2;     // bytes of one 128-row fp16/bf16 tile
-  static constexpr int NS = (D == 64) ? 4 : 2;  // ring stages, each K_j then V_j
-  static constexpr int STAGE = 2 * TILE;
+  static constexpr int QT = X3 ? 2 : 1;       // tiles per query tile (hi, lo)
+  static constexpr int KVT = X3 ? 4 : 2;      // tiles per stage: K (hi, lo), V (hi, lo)
+  static constexpr int NS = X3 ? 2 : ((D == 64) ? 4 : 2);  // ring stages
+  static constexpr int STAGE = KVT * TILE;
+  static constexpr int K_LO = TILE;                  // offsets inside a stage
+  static constexpr int V_OFF = (X3 ? 2 : 1) * TILE;
+  static constexpr int V_LO = 3 * TILE;
   static constexpr int Q_OFF = 0;
-  static constexpr int RING_OFF = NQ * TILE;
+  static constexpr int RING_OFF = NQ * QT * TILE;
   static constexpr int BAR_OFF = RING_OFF + NS * STAGE;
   // q_full, full[NS], empty[NS], s_full[NQ], p_full[NQ], o_done[NQ], drain
   static constexpr int NBARS = 1 + 2 * NS + 3 * NQ + 1;
@@ -107,6 +117,10 @@ struct Elem<false> {
     return *reinterpret_cast<uint32_t*>(&v);
   }
 };
+
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 // ---------------------------------------------------------------- softmax math
 // Pairs of fp32 values in one 64-bit register for the packed f32x2 FMA/add.
@@ -169,9 +183,11 @@ __device__ __forceinline__ void exp2_poly_pair(uint64_t X, float& r0, float& r1)
 
 // p_i = 2^(s_i * sl2 - m) for one row of raw scores, packed to fp16/bf16
 // pairs; rs receives the fp32 sum of the p_i.
-template <bool BF16, int N>
+// With X3, pk2 receives the bf16 residuals p - bf16(p) (P_lo).
+template <bool BF16, int N, bool X3 = false>
 __device__ __forceinline__ void softmax_pairs(const uint32_t (&s)[N], float sl2, float m,
-                                              uint32_t (&pk)[N / 2], float& rs) {
+                                              uint32_t (&pk)[N / 2], float& rs,
+                                              uint32_t* pk2 = nullptr) {
   const uint64_t SL = f2_pack(sl2, sl2);
   const uint64_t NM = f2_pack(-m, -m);
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -189,6 +205,11 @@ __device__ __forceinline__ void softmax_pairs(const uint32_t (&s)[N], float sl2,
     }
     acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
     pk[i] = Elem<BF16>::pack(p0, p1);
+    if constexpr (X3) {
+      const float h0 = __uint_as_float(pk[i] << 16);
+      const float h1 = __uint_as_float(pk[i] & 0xffff0000u);
+      pk2[i] = Elem<true>::pack(p0 - h0, p1 - h1);
+    }
   }
   const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
   float t0, t1;
@@ -205,14 +226,18 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool X3>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const PrefillArgs a) {
-  using C = Cfg<D>;
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmQ2,
+                      const __grid_constant__ CUtensorMap tmK2,
+                      const __grid_constant__ CUtensorMap tmV2, const PrefillArgs a) {
+  using C = Cfg<D, X3>;
   using E = Elem<BF16>;
-  using T = typename E::T;
+  // element type of the output and of the mask: the caller's dtype (fp32 in X3)
+  using T = std::conditional_t<X3, float, typename E::T>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment of the shared-memory window (128-byte swizzle atoms).
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -298,21 +323,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nt * C::TILE));
+      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nt * C::QT * C::TILE));
       for (int t = 0; t < nt; ++t)
-        for (int cb = 0; cb < C::CB; ++cb)
-          tma_load_3d(sQ + t * C::TILE + cb * BM * 128, &tmQ, q_full, cb * 64, m0 + t * BM,
-                      b * a.Hq + h);
+        for (int cb = 0; cb < C::CB; ++cb) {
+          tma_load_3d(sQ + t * C::QT * C::TILE + cb * BM * 128, &tmQ, q_full, cb * 64,
+                      m0 + t * BM, b * a.Hq + h);
+          if constexpr (X3)
+            tma_load_3d(sQ + (t * C::QT + 1) * C::TILE + cb * BM * 128, &tmQ2, q_full,
+                        cb * 64, m0 + t * BM, b * a.Hq + h);
+        }
       for (int j = 0; j < nmax; ++j) {
         const int s = j % C::NS;
         const int use = j / C::NS;
         if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, wc)) break;
         mbar_arrive_expect_tx(&full[s], C::STAGE);
         uint8_t* st = sRing + s * C::STAGE;
+        const int kvz = b * a.Hkv + kvh;
         for (int cb = 0; cb < C::CB; ++cb) {
-          tma_load_3d(st + cb * BN * 128, &tmK, &full[s], cb * 64, j * BN, b * a.Hkv + kvh);
-          tma_load_3d(st + C::TILE + cb * BN * 128, &tmV, &full[s], cb * 64, j * BN,
-                      b * a.Hkv + kvh);
+          tma_load_3d(st + cb * BN * 128, &tmK, &full[s], cb * 64, j * BN, kvz);
+          tma_load_3d(st + C::V_OFF + cb * BN * 128, &tmV, &full[s], cb * 64, j * BN, kvz);
+          if constexpr (X3) {
+            tma_load_3d(st + C::K_LO + cb * BN * 128, &tmK2, &full[s], cb * 64, j * BN, kvz);
+            tma_load_3d(st + C::V_LO + cb * BN * 128, &tmV2, &full[s], cb * 64, j * BN, kvz);
+          }
         }
         last_use[s] = use;
       }
@@ -334,24 +367,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_t = Q_t K_j^T: both operands K-major, 128-byte swizzle; a K step of
       // 16 elements is 32 bytes inside a 128-byte row, 4 steps per column block.
       auto issue_s = [&](int t, int j) {
-        const uint64_t qd = q_desc + static_cast<uint64_t>((t * C::TILE) >> 4);
+        const uint64_t qd = q_desc + static_cast<uint64_t>((t * C::QT * C::TILE) >> 4);
         const uint64_t kd = k_desc0 + static_cast<uint64_t>((stage(j) * C::STAGE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
           mma_f16_ss(tmem + C::s_col(t), qd + off, kd + off, idS, kk > 0 ? 1u : 0u);
+          if constexpr (X3) {  // Q_hi K_lo^T + Q_lo K_hi^T
+            mma_f16_ss(tmem + C::s_col(t), qd + off, kd + (C::K_LO >> 4) + off, idS, 1u);
+            mma_f16_ss(tmem + C::s_col(t), qd + (C::TILE >> 4) + off, kd + off, idS, 1u);
+          }
         }
       };
       // O_t += P_t V_j: P (128 x 128, K-major) from TMEM columns of S_t,
       // 2 elements per column; V MN-major: 64-wide column blocks BN*128
-      // bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).
+      // bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).  In X3, P_hi
+      // sits in the first 64 columns of S_t and P_lo in the next 64.
       auto issue_pv = [&](int t, int j) {
         const uint64_t vd =
-            v_desc0 + static_cast<uint64_t>((stage(j) * C::STAGE + C::TILE) >> 4);
+            v_desc0 + static_cast<uint64_t>((stage(j) * C::STAGE + C::V_OFF) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_f16_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                     vd + ((kk * 16 * 128) >> 4), idO, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint32_t voff = (kk * 16 * 128) >> 4;
+          mma_f16_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, vd + voff, idO,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (X3) {  // P_hi V_lo + P_lo V_hi
+            mma_f16_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
+                       vd + ((C::V_LO - C::V_OFF) >> 4) + voff, idO, 1u);
+            mma_f16_ts(tmem + C::o_col(t), tmem + C::s_col(t) + BN / 2 + kk * 8, vd + voff,
+                       idO, 1u);
+          }
+        }
       };
       bool ok = mbar_wait(q_full, 0, wc);
       if (ok) {
@@ -438,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool resc;
         float rs;
         uint32_t pk[BN / 2];
+        uint32_t pk2[X3 ? BN / 2 : 1];  // P_lo (X3)
         if (fast_ok && kv0 + BN - 1 <= limit) {
           // Interior tile, positive scale, no mask: p = 2^(s * scale*log2e
           // - m) with the scale folded into one packed FMA per pair, taken
@@ -448,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // finds the tile max of the raw scores and repeats.
           resc = !(m > -INFINITY);
           if (!resc) {
-            softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
+            softmax_pairs<BF16, BN, X3>(s, a.sl2, m, pk, rs, pk2);
             resc = !(rs <= kFusedSumLimit);  // also true for inf or nan
           }
           if (resc) {
@@ -466,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              a.sl2;
             alpha = ex2(m - mx);  // 0 when m = -inf
             m = mx;
-            softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
+            softmax_pairs<BF16, BN, X3>(s, a.sl2, m, pk, rs, pk2);
           }
         } else {
           float x[BN];
@@ -475,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (mrow) {
 #pragma unroll
             for (int i = 0; i < BN; ++i)
-              if (kv0 + i < a.Lk) x[i] += E::to_f(mrow[kv0 + i]) * kLog2e;
+              if (kv0 + i < a.Lk) x[i] += to_float(mrow[kv0 + i]) * kLog2e;
           }
           if (kv0 + BN - 1 > limit) {
 #pragma unroll
@@ -501,6 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = ex2(x[2 * i + 1] - mu);
             rp[i & 3] += p0 + p1;
             pk[i] = E::pack(p0, p1);
+            if constexpr (X3) {
+              const float h0 = __uint_as_float(pk[i] << 16);
+              const float h1 = __uint_as_float(pk[i] & 0xffff0000u);
+              pk2[i] = Elem<true>::pack(p0 - h0, p1 - h1);
+            }
           }
           rs = (rp[0] + rp[1]) + (rp[2] + rp[3]);
         }
@@ -521,6 +573,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
         tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        if constexpr (X3) {
+          tmem_st32(tS + BN / 2, *reinterpret_cast<uint32_t(*)[32]>(&pk2[0]));
+          tmem_st32(tS + BN / 2 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk2[32]));
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[t]);
@@ -545,18 +601,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ob[32];
           tmem_ld32(tO + c * 32, ob);
           tmem_wait_ld();
-          uint32_t w[16];
+          if constexpr (X3) {  // fp32 output
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float v0 = (inv == 0.f) ? 0.f : __uint_as_float(ob[2 * i]) * inv;
-            const float v1 = (inv == 0.f) ? 0.f : __uint_as_float(ob[2 * i + 1]) * inv;
-            w[i] = E::pack(v0, v1);
-          }
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+            for (int i = 0; i < 32; ++i)
+              ob[i] = __float_as_uint((inv == 0.f) ? 0.f : __uint_as_float(ob[i]) * inv);
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+            }
+          } else {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float v0 = (inv == 0.f) ? 0.f : __uint_as_float(ob[2 * i]) * inv;
+              const float v1 = (inv == 0.f) ? 0.f : __uint_as_float(ob[2 * i + 1]) * inv;
+              w[i] = E::pack(v0, v1);
+            }
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
           }
         }
         if (row_ok && a.lse) {
@@ -582,21 +650,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool BF16>
+// Split of fp32 inputs into bf16 hi and lo parts (x = hi + lo + O(2^-16 |x|)),
+// for up to three tensors in one launch (n4 = elements / 4 of each).
+struct SplitJob {
+  const float* x[3];
+  __nv_bfloat16* hi[3];
+  __nv_bfloat16* lo[3];
+  size_t n4[3];
+};
+
+__global__ void __launch_bounds__(256) split_bf16_kernel(const SplitJob job) {
+  for (int s = 0; s < 3; ++s) {
+    const float4* x = reinterpret_cast<const float4*>(job.x[s]);
+    uint2* hi = reinterpret_cast<uint2*>(job.hi[s]);
+    uint2* lo = reinterpret_cast<uint2*>(job.lo[s]);
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < job.n4[s];
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+      const float4 v = x[i];
+      const uint32_t h01 = Elem<true>::pack(v.x, v.y);
+      const uint32_t h23 = Elem<true>::pack(v.z, v.w);
+      const uint32_t l01 = Elem<true>::pack(v.x - __uint_as_float(h01 << 16),
+                                            v.y - __uint_as_float(h01 & 0xffff0000u));
+      const uint32_t l23 = Elem<true>::pack(v.z - __uint_as_float(h23 << 16),
+                                            v.w - __uint_as_float(h23 & 0xffff0000u));
+      hi[i] = make_uint2(h01, h23);
+      lo[i] = make_uint2(l01, l23);
+    }
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+template <int D, bool BF16, bool X3>
 sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, const void* v,
-                          void* o, float* lse, const LaunchEnv& env) {
-  using C = Cfg<D>;
+                          const void* q2, const void* k2, const void* v2, void* o, float* lse,
+                          const LaunchEnv& env) {
+  using C = Cfg<D, X3>;
   const CUtensorMapDataType dt =
       BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap tq, tk, tv;
+  const uint64_t qz = static_cast<uint64_t>(p.batch) * p.num_q_heads;
+  const uint64_t kz = static_cast<uint64_t>(p.batch) * p.num_kv_heads;
+  CUtensorMap tq, tk, tv, tq2, tk2, tv2;
   // [B*H, L, D] viewed innermost-first; box 64 x 128 rows, 128-byte swizzle.
-  if (!encode_tiled_3d(&tq, dt, q, D, p.seq_len_q, static_cast<uint64_t>(p.batch) * p.num_q_heads,
-                       2, 64, BM) ||
-      !encode_tiled_3d(&tk, dt, k, D, p.seq_len_kv,
-                       static_cast<uint64_t>(p.batch) * p.num_kv_heads, 2, 64, BN) ||
-      !encode_tiled_3d(&tv, dt, v, D, p.seq_len_kv,
-                       static_cast<uint64_t>(p.batch) * p.num_kv_heads, 2, 64, BN))
+  if (!encode_tiled_3d(&tq, dt, q, D, p.seq_len_q, qz, 2, 64, BM) ||
+      !encode_tiled_3d(&tk, dt, k, D, p.seq_len_kv, kz, 2, 64, BN) ||
+      !encode_tiled_3d(&tv, dt, v, D, p.seq_len_kv, kz, 2, 64, BN))
     return SDPA_ERR_CUDA;
+  if (X3) {
+    if (!encode_tiled_3d(&tq2, dt, q2, D, p.seq_len_q, qz, 2, 64, BM) ||
+        !encode_tiled_3d(&tk2, dt, k2, D, p.seq_len_kv, kz, 2, 64, BN) ||
+        !encode_tiled_3d(&tv2, dt, v2, D, p.seq_len_kv, kz, 2, 64, BN))
+      return SDPA_ERR_CUDA;
+  } else {
+    tq2 = tq;
+    tk2 = tk;
+    tv2 = tv;
+  }
   PrefillArgs a;
   a.Hq = p.num_q_heads;
   a.Hkv = p.num_kv_heads;
@@ -615,12 +724,12 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   a.lse = lse;
   a.status = env.status;
   a.wait_ns = env.wait_limit_ns;
-  auto kern = prefill_tc_kernel<D, BF16>;
+  auto kern = prefill_tc_kernel<D, BF16, X3>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return SDPA_ERR_CUDA;
   dim3 grid(a.num_qblocks, p.num_q_heads, p.batch);
-  kern<<<grid, kThreads, C::SMEM, env.stream>>>(tq, tk, tv, a);
+  kern<<<grid, kThreads, C::SMEM, env.stream>>>(tq, tk, tv, tq2, tk2, tv2, a);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
@@ -630,12 +739,51 @@ sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const voi
                                 const void* v, void* o, float* lse, const LaunchEnv& env) {
   const bool bf16 = p.dtype == SDPA_BF16;
   if (p.head_dim == 64)
-    return bf16 ? launch_impl<64, true>(p, q, k, v, o, lse, env)
-                : launch_impl<64, false>(p, q, k, v, o, lse, env);
+    return bf16 ? launch_impl<64, true, false>(p, q, k, v, q, k, v, o, lse, env)
+                : launch_impl<64, false, false>(p, q, k, v, q, k, v, o, lse, env);
   if (p.head_dim == 128)
-    return bf16 ? launch_impl<128, true>(p, q, k, v, o, lse, env)
-                : launch_impl<128, false>(p, q, k, v, o, lse, env);
+    return bf16 ? launch_impl<128, true, false>(p, q, k, v, q, k, v, o, lse, env)
+                : launch_impl<128, false, false>(p, q, k, v, q, k, v, o, lse, env);
   return SDPA_ERR_UNSUPPORTED;
+}
+
+size_t prefill_x3_workspace(const sdpa_params_t& p) {
+  const size_t nq = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * p.head_dim;
+  const size_t nk = static_cast<size_t>(p.batch) * p.num_kv_heads * p.seq_len_kv * p.head_dim;
+  return 2 * align256(nq * 2) + 4 * align256(nk * 2);
+}
+
+sdpa_status_t launch_prefill_x3(const sdpa_params_t& p, const void* q, const void* k,
+                                const void* v, void* o, float* lse, void* workspace,
+                                const LaunchEnv& env) {
+  if (p.head_dim != 64) return SDPA_ERR_UNSUPPORTED;
+  const size_t nq = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * p.head_dim;
+  const size_t nk = static_cast<size_t>(p.batch) * p.num_kv_heads * p.seq_len_kv * p.head_dim;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* qh = reinterpret_cast<__nv_bfloat16*>(w);
+  __nv_bfloat16* ql = reinterpret_cast<__nv_bfloat16*>(w + align256(nq * 2));
+  __nv_bfloat16* kh = reinterpret_cast<__nv_bfloat16*>(w + 2 * align256(nq * 2));
+  __nv_bfloat16* kl = reinterpret_cast<__nv_bfloat16*>(w + 2 * align256(nq * 2) + align256(nk * 2));
+  __nv_bfloat16* vh =
+      reinterpret_cast<__nv_bfloat16*>(w + 2 * align256(nq * 2) + 2 * align256(nk * 2));
+  __nv_bfloat16* vl =
+      reinterpret_cast<__nv_bfloat16*>(w + 2 * align256(nq * 2) + 3 * align256(nk * 2));
+  SplitJob job;
+  job.x[0] = static_cast<const float*>(q);
+  job.x[1] = static_cast<const float*>(k);
+  job.x[2] = static_cast<const float*>(v);
+  job.hi[0] = qh;
+  job.lo[0] = ql;
+  job.hi[1] = kh;
+  job.lo[1] = kl;
+  job.hi[2] = vh;
+  job.lo[2] = vl;
+  job.n4[0] = nq / 4;
+  job.n4[1] = nk / 4;
+  job.n4[2] = nk / 4;
+  split_bf16_kernel<<<env.num_sms * 8, 256, 0, env.stream>>>(job);
+  if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
+  return launch_impl<64, true, true>(p, qh, kh, vh, ql, kl, vl, o, lse, env);
 }
 
 }  // namespace gb300

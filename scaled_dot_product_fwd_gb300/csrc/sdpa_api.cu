@@ -65,7 +65,9 @@ sdpa_kernel_t pick(const sdpa_params_t* p) {
   if (nothing_to_do(p)) return SDPA_KERNEL_NONE;
   if (p->seq_len_kv == 0) return SDPA_KERNEL_NO_KEYS;
   if (p->seq_len_q == 1) return SDPA_KERNEL_DECODE_SPLITKV;
-  return p->dtype == SDPA_F32 ? SDPA_KERNEL_PREFILL_F32 : SDPA_KERNEL_PREFILL_TC;
+  if (p->dtype == SDPA_F32)
+    return p->head_dim == 64 ? SDPA_KERNEL_PREFILL_TC_F32 : SDPA_KERNEL_PREFILL_F32;
+  return SDPA_KERNEL_PREFILL_TC;
 }
 
 // Per-device state: address of the status word and the SM count.
@@ -135,6 +137,7 @@ sdpa_kernel_t sdpa_select_kernel(const sdpa_params_t* params, sdpa_status_t* sta
 
 size_t sdpa_workspace_size(const sdpa_params_t* params) {
   if (validate_problem(params) != SDPA_OK) return 0;
+  if (pick(params) == SDPA_KERNEL_PREFILL_TC_F32) return gb300::prefill_x3_workspace(*params);
   if (pick(params) != SDPA_KERNEL_DECODE_SPLITKV) return 0;
   gb300::DecodePlan plan;
   if (!gb300::decode_plan(*params, current_num_sms(), &plan)) return 0;
@@ -168,6 +171,11 @@ sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k,
       if (!aligned(workspace, 256)) return SDPA_ERR_MISALIGNED;
     }
   }
+  if (kern == SDPA_KERNEL_PREFILL_TC_F32) {
+    if (!workspace || workspace_bytes < gb300::prefill_x3_workspace(*p))
+      return SDPA_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 256)) return SDPA_ERR_MISALIGNED;
+  }
   int* status = nullptr;
   int num_sms = 0;
   if (!device_state(nullptr, &status, &num_sms)) return SDPA_ERR_CUDA;
@@ -181,6 +189,8 @@ sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k,
       return gb300::launch_prefill_tc(*p, q, k, v, o, lse, env);
     case SDPA_KERNEL_PREFILL_F32:
       return gb300::launch_prefill_f32(*p, q, k, v, o, lse, env);
+    case SDPA_KERNEL_PREFILL_TC_F32:
+      return gb300::launch_prefill_x3(*p, q, k, v, o, lse, workspace, env);
     case SDPA_KERNEL_DECODE_SPLITKV:
       return gb300::launch_decode(*p, plan, q, k, v, o, lse, workspace, env);
     case SDPA_KERNEL_NO_KEYS:

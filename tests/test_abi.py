@@ -62,7 +62,8 @@ def P(**kw):
 @pytest.mark.parametrize("kw,kernel", [
     (dict(), "prefill_tc"),
     (dict(dtype=S.SDPA_F16, D=128), "prefill_tc"),
-    (dict(dtype=S.SDPA_F32), "prefill_f32"),
+    (dict(dtype=S.SDPA_F32), "prefill_tc_f32"),
+    (dict(dtype=S.SDPA_F32, D=128), "prefill_f32"),
     (dict(Lq=1), "decode_splitkv"),
     (dict(Lq=1, D=512, dtype=S.SDPA_F32), "decode_splitkv"),
     (dict(Lk=0), "no_keys"),
@@ -130,8 +131,12 @@ def test_decode_workspace_size_and_check(sdpa_lib):
     # too small a workspace is refused before any launch
     assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, 256, ws - 1, None) == 4
     assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, None, 0, None) == 4
-    # prefill needs none
+    # the fp16/bf16 prefill needs none
     assert S.sdpa_workspace_size(P()) == 0
+    # the fp32 tensor-core prefill keeps bf16 hi/lo copies of q, k and v
+    pf = P(dtype=S.SDPA_F32, B=1, Hq=4, Hkv=2, Lq=16, Lk=32, D=64)
+    assert S.sdpa_workspace_size(pf) == 2 * 2 * 4 * 16 * 64 // 256 * 256 + 4 * 2 * 2 * 32 * 64
+    assert S.sdpa_forward_raw(pf, 256, 256, 256, 256, None, None, 0, None) == 4
 
 
 def test_python_binding_rejects_cpu_tensors(sdpa_lib):
