@@ -485,7 +485,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rs;
         uint32_t pk[BN / 2];
         uint32_t pk2[X3 ? BN / 2 : 1];  // P_lo (X3)
-        if (fast_ok && kv0 + BN - 1 <= limit) {
+        const bool fast = fast_ok && kv0 + BN - 1 <= limit;
+        if constexpr (X3) {
+          // bf16 hi/lo P: computed half a row at a time and stored to TMEM
+          // as soon as each half exists, so that the 128 scores plus one
+          // half of P_hi and P_lo are the most that is live at once.  The
+          // scores are used raw with p = 2^(s * scale*log2e - m) on the
+          // fused path, and as scaled, masked x = s * scale*log2e + bias
+          // (rewritten in place) with p = 2^(x - m) elsewhere.
+          float mul = a.sl2;
+          if (!fast) {
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+              float x = __uint_as_float(s[i]) * a.sl2;
+              if (mrow && kv0 + i < a.Lk) x += to_float(mrow[kv0 + i]) * kLog2e;
+              if (kv0 + i > limit) x = -INFINITY;
+              s[i] = __float_as_uint(x);
+            }
+            mul = 1.f;
+          }
+          // fused rows with a reference max skip the tile max, others take it
+          bool need_max = !fast || !(m > -INFINITY);
+          resc = false;
+          for (int pass = 0; pass < 2; ++pass) {
+            if (need_max) {
+              float mr[8];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
+#pragma unroll
+              for (int i = 8; i < BN; i += 16)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]),
+                                __uint_as_float(s[i + 2 * c + 1]));
+              const float mx = fmaxf(fmax3(mr[0], mr[1], mr[2]),
+                                     fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7]))) *
+                               mul;
+              // the fused path always moves to the tile max; the general
+              // path only when it grew by more than the threshold
+              if (fast || mx > m + kRescaleThreshold) {
+                alpha = ex2(m - mx);  // 0 when m = -inf
+                m = mx;
+                resc = true;
+              }
+            }
+            const float mu = (m == -INFINITY) ? 0.f : m;
+            float rs0, rs1;
+            softmax_pairs<BF16, BN / 2, true>(*reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[0]),
+                                             mul, mu, *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[0]),
+                                             rs0, &pk2[0]);
+            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(tS + BN / 2, *reinterpret_cast<uint32_t(*)[32]>(&pk2[0]));
+            softmax_pairs<BF16, BN / 2, true>(*reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[BN / 2]),
+                                             mul, mu, *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[BN / 4]),
+                                             rs1, &pk2[BN / 4]);
+            tmem_st32(tS + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk[BN / 4]));
+            tmem_st32(tS + BN / 2 + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk2[BN / 4]));
+            rs = rs0 + rs1;
+            // a fused row whose sum exceeds 2^15 (its max grew) takes the
+            // tile max and the warp computes the tile again; the second
+            // pass cannot fail (every p <= 1)
+            const bool redo = fast && !need_max && !(rs <= kFusedSumLimit);
+            if (!__any_sync(0xffffffffu, redo)) break;
+            need_max = redo;
+          }
+        } else if (fast) {
           // Interior tile, positive scale, no mask: p = 2^(s * scale*log2e
           // - m) with the scale folded into one packed FMA per pair, taken
           // against the current reference max m without looking for the
@@ -495,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // finds the tile max of the raw scores and repeats.
           resc = !(m > -INFINITY);
           if (!resc) {
-            softmax_pairs<BF16, BN, X3>(s, a.sl2, m, pk, rs, pk2);
+            softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
             resc = !(rs <= kFusedSumLimit);  // also true for inf or nan
           }
           if (resc) {
@@ -513,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              a.sl2;
             alpha = ex2(m - mx);  // 0 when m = -inf
             m = mx;
-            softmax_pairs<BF16, BN, X3>(s, a.sl2, m, pk, rs, pk2);
+            softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
           }
         } else {
           float x[BN];
@@ -548,11 +612,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = ex2(x[2 * i + 1] - mu);
             rp[i & 3] += p0 + p1;
             pk[i] = E::pack(p0, p1);
-            if constexpr (X3) {
-              const float h0 = __uint_as_float(pk[i] << 16);
-              const float h1 = __uint_as_float(pk[i] & 0xffff0000u);
-              pk2[i] = Elem<true>::pack(p0 - h0, p1 - h1);
-            }
           }
           rs = (rp[0] + rp[1]) + (rp[2] + rp[3]);
         }
@@ -571,11 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tO + c * 32, ob);
           }
         }
-        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-        if constexpr (X3) {
-          tmem_st32(tS + BN / 2, *reinterpret_cast<uint32_t(*)[32]>(&pk2[0]));
-          tmem_st32(tS + BN / 2 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk2[32]));
+        if constexpr (!X3) {
+          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         }
         tmem_wait_st();
         tc_fence_before();
