@@ -14,17 +14,22 @@
 //              (TMEM lane); it also rescales O in TMEM and writes the output;
 //   warp 8     TMA producer: Q tiles once, then K_j, V_j into a ring of
 //              shared-memory buffers (128-byte swizzle);
-//   warp 9     MMA issuer: one thread issues tcgen05.mma,
+//   warp 9     MMA issuer: one elected lane issues tcgen05.mma,
 //              S_t = Q_t K_j^T (A, B from shared memory, fp32 in TMEM) and
 //              O_t += P_t V_j (P from TMEM, written there by the softmax
-//              warps over the columns of S_t; V from shared memory);
-//   warps 10-11 idle (complete the control warpgroup).
+//              warps; V from shared memory), while the whole warp runs the
+//              loop in step and meets the other roles only at named
+//              barriers (no shared-memory access between MMAs);
+//   warp 10    stage helper: waits for each K/V stage to land and passes
+//              it to the MMA issuer;
+//   warp 11    idle (completes the control warpgroup).
 // Each ring stage holds K_j and V_j (one full and one empty barrier per
-// step).  TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  The issue order
-// S_0,j+1 right after PV_0,j lets softmax of one tile overlap the MMAs of
-// the other.  The O rescale is lazy: a row's reference max moves only when
-// the new max exceeds it (by more than 8 in log2 units on masked tiles, or
-// so far that a row sum passes 2^15 on interior tiles), so P stays <= 2^15.
+// step).  TMEM (512 columns): S_0 | S_1 | O_0 | O_1, with P written over
+// the columns of S_t.  The issue order S_0,j+1 right after PV_0,j lets
+// softmax of one tile overlap the MMAs of the other.  The O rescale is
+// lazy: a row's reference max moves only when the new max exceeds it (by
+// more than 8 in log2 units on masked tiles, or so far that a row sum passes
+// 2^15 on interior tiles), so P stays <= 2^15.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -50,6 +55,10 @@ constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
 constexpr uint32_t kSoftmaxRegs = 224;
 constexpr uint32_t kControlRegs = 56;
+// named barriers: kBarP + t (softmax warps of tile t with the MMA warp),
+// kBarK (stage helper with the MMA warp)
+constexpr uint32_t kBarP = 1;
+constexpr uint32_t kBarK = kBarP + NQ;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units (masked path)
@@ -72,14 +81,14 @@ struct Cfg {
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = NQ * QT * TILE;
   static constexpr int BAR_OFF = RING_OFF + NS * STAGE;
-  // q_full, full[NS], empty[NS], s_full[NQ], p_full[NQ], o_done[NQ], drain
-  static constexpr int NBARS = 1 + 2 * NS + 3 * NQ + 1;
+  // q_full, full[NS], empty[NS], s_full[NQ], o_done[NQ], drain
+  static constexpr int NBARS = 1 + 2 * NS + 2 * NQ + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t s_col(int t) { return static_cast<uint32_t>(t * BN); }
   static constexpr uint32_t o_col(int t) { return static_cast<uint32_t>(NQ * BN + t * D); }
-  static_assert(NQ * BN + NQ * D <= 512, "TMEM budget");
+  static_assert(o_col(NQ - 1) + D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -217,6 +226,7 @@ __device__ __forceinline__ void softmax_pairs(const uint32_t (&s)[N], float sl2,
   rs = t0 + t1;
 }
 
+
 // Wait for a phase ignoring the abort flag (used only to drain in-flight
 // asynchronous work before the CTA exits); bounded by limit_ns.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -249,8 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = bars + 1;
   uint64_t* empty = full + C::NS;
   uint64_t* s_full = empty + C::NS;
-  uint64_t* p_full = s_full + NQ;
-  uint64_t* o_done = p_full + NQ;
+  uint64_t* o_done = s_full + NQ;
   uint64_t* drain = o_done + NQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
@@ -293,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < NQ; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 128);
       mbar_init(&o_done[t], 1);
     }
     mbar_init(drain, 1);
@@ -352,97 +360,123 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    // One thread issues every MMA in a fixed order, PV_0,j S_0,j+1 PV_1,j
-    // S_1,j+1, so each tile's next scores are ready as early as possible.
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
-      constexpr uint32_t idO = idesc_f16(BF16, BM, D, false, true);
-      // descriptors of Q_0 and ring buffer 0; other tiles, buffers and K
-      // steps are offsets of the 16-byte-granular start-address field
-      const uint64_t q_desc = sdesc(smem_addr(sQ), 16, 1024, kSwizzle128B);
-      const uint64_t k_desc0 = sdesc(smem_addr(sRing), 16, 1024, kSwizzle128B);
-      const uint64_t v_desc0 = sdesc(smem_addr(sRing), BN * 128, 1024, kSwizzle128B);
-      auto stage = [](int j) { return j % C::NS; };
-      auto spar = [](int j) { return static_cast<uint32_t>((j / C::NS) & 1); };
-      // S_t = Q_t K_j^T: both operands K-major, 128-byte swizzle; a K step of
-      // 16 elements is 32 bytes inside a 128-byte row, 4 steps per column block.
-      auto issue_s = [&](int t, int j) {
-        const uint64_t qd = q_desc + static_cast<uint64_t>((t * C::QT * C::TILE) >> 4);
-        const uint64_t kd = k_desc0 + static_cast<uint64_t>((stage(j) * C::STAGE) >> 4);
+    // The whole warp runs the issue loop in step; one lane, picked by
+    // elect.sync inside each instruction, issues, so the warp never branches
+    // around it.  The loop touches no shared memory: the softmax warps of
+    // tile t hand P_t over through named barrier kBarP + t and the stage
+    // helper reports each K/V stage that has landed through kBarK (an
+    // mbarrier poll, a local-memory spill or a warp reconvergence here holds
+    // the issuing thread until the MMAs in flight drain).  Fixed order:
+    // PV_0,j S_0,j+1 PV_1,j S_1,j+1, so each tile's next scores are ready as
+    // early as possible.
+    const uint32_t lead = lane == 0 ? 1u : 0u;
+    constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
+    constexpr uint32_t idO = idesc_f16(BF16, BM, D, false, true);
+    // Descriptors of Q_0 and ring buffer 0.  Other tiles, buffers and K
+    // steps differ only in the start-address field (bits 0-13, 16-byte
+    // units) of the low word, so the loop adds 32-bit offsets to the low
+    // words and pairs them with the fixed high words.
+    const uint64_t q_desc = sdesc(smem_addr(sQ), 16, 1024, kSwizzle128B);
+    const uint64_t k_desc = sdesc(smem_addr(sRing), 16, 1024, kSwizzle128B);
+    const uint64_t v_desc = sdesc(smem_addr(sRing), BN * 128, 1024, kSwizzle128B);
+    const uint32_t qk_hi = static_cast<uint32_t>(q_desc >> 32);
+    const uint32_t v_hi = static_cast<uint32_t>(v_desc >> 32);
+    const uint32_t q_lo = static_cast<uint32_t>(q_desc);
+    const uint32_t k_lo = static_cast<uint32_t>(k_desc);
+    const uint32_t v_lo = static_cast<uint32_t>(v_desc);
+    auto qk = [&](uint32_t lo) { return (static_cast<uint64_t>(qk_hi) << 32) | lo; };
+    auto vv = [&](uint32_t lo) { return (static_cast<uint64_t>(v_hi) << 32) | lo; };
+    auto stage = [](int j) { return j % C::NS; };
+    auto spar = [](int j) { return static_cast<uint32_t>((j / C::NS) & 1); };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, wc));
+    if (nmax > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(&full[stage(0)], spar(0), wc));
+    // after a failed wait the loop still meets every named barrier, without
+    // issuing anything
+    const uint32_t go = ok ? 1u : 0u;
+    // S_t = Q_t K_j^T: both operands K-major, 128-byte swizzle; a K step of
+    // 16 elements is 32 bytes inside a 128-byte row, 4 steps per column block.
+    auto issue_s = [&](int t, int j) {
+      const uint32_t qd = q_lo + static_cast<uint32_t>((t * C::QT * C::TILE) >> 4);
+      const uint32_t kd = k_lo + static_cast<uint32_t>((stage(j) * C::STAGE) >> 4);
+      const uint32_t dS = tmem + C::s_col(t);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
-          mma_f16_ss(tmem + C::s_col(t), qd + off, kd + off, idS, kk > 0 ? 1u : 0u);
-          if constexpr (X3) {  // Q_hi K_lo^T + Q_lo K_hi^T
-            mma_f16_ss(tmem + C::s_col(t), qd + off, kd + (C::K_LO >> 4) + off, idS, 1u);
-            mma_f16_ss(tmem + C::s_col(t), qd + (C::TILE >> 4) + off, kd + off, idS, 1u);
-          }
-        }
-      };
-      // O_t += P_t V_j: P (128 x 128, K-major) from TMEM columns of S_t,
-      // 2 elements per column; V MN-major: 64-wide column blocks BN*128
-      // bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).  In X3, P_hi
-      // sits in the first 64 columns of S_t and P_lo in the next 64.
-      auto issue_pv = [&](int t, int j) {
-        const uint64_t vd =
-            v_desc0 + static_cast<uint64_t>((stage(j) * C::STAGE + C::V_OFF) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t voff = (kk * 16 * 128) >> 4;
-          mma_f16_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, vd + voff, idO,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-          if constexpr (X3) {  // P_hi V_lo + P_lo V_hi
-            mma_f16_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                       vd + ((C::V_LO - C::V_OFF) >> 4) + voff, idO, 1u);
-            mma_f16_ts(tmem + C::o_col(t), tmem + C::s_col(t) + BN / 2 + kk * 8, vd + voff,
-                       idO, 1u);
-          }
-        }
-      };
-      bool ok = mbar_wait(q_full, 0, wc);
-      if (ok) {
-        for (int t = 0; t < nt; ++t)
-          if (nkv[t] == 0) mma_commit(&o_done[t]);
-        if (nmax > 0) {
-          ok = mbar_wait(&full[stage(0)], spar(0), wc);
-          if (ok) {
-            for (int t = 0; t < nt; ++t)
-              if (nkv[t] > 0) {
-                issue_s(t, 0);
-                mma_commit(&s_full[t]);
-              }
-          }
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+        mma_f16_ss_elect(dS, qk(qd + off), qk(kd + off), idS, kk > 0 ? 1u : 0u, go);
+        if constexpr (X3) {  // Q_hi K_lo^T + Q_lo K_hi^T
+          mma_f16_ss_elect(dS, qk(qd + off), qk(kd + (C::K_LO >> 4) + off), idS, 1u, go);
+          mma_f16_ss_elect(dS, qk(qd + (C::TILE >> 4) + off), qk(kd + off), idS, 1u, go);
         }
       }
-      for (int j = 0; ok && j < nmax; ++j) {
-        bool kwaited = false;
-        for (int t = 0; t < nt && ok; ++t) {
-          if (j >= nkv[t]) continue;
-          ok = mbar_wait(&p_full[t], j & 1, wc);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, j);
-          if (j + 1 < nkv[t]) {
-            if (!kwaited) {
-              ok = mbar_wait(&full[stage(j + 1)], spar(j + 1), wc);
-              if (!ok) break;
-              kwaited = true;
-            }
-            issue_s(t, j + 1);
-            mma_commit(&s_full[t]);
-          } else {
-            mma_commit(&o_done[t]);
-          }
+    };
+    // O_t += P_t V_j: P (128 x 128, K-major) from TMEM columns of S_t,
+    // 2 elements per column; V MN-major: 64-wide column blocks BN*128 bytes
+    // apart (LBO), 8-key groups 1024 bytes apart (SBO).  In X3, P_hi sits in
+    // the first 64 columns of S_t and P_lo in the next 64.
+    auto issue_pv = [&](int t, int j) {
+      const uint32_t vd = v_lo + static_cast<uint32_t>((stage(j) * C::STAGE + C::V_OFF) >> 4);
+      const uint32_t dO = tmem + C::o_col(t);
+      const uint32_t aP = tmem + C::s_col(t);
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        const uint32_t voff = (kk * 16 * 128) >> 4;
+        mma_f16_ts_elect(dO, aP + kk * 8, vv(vd + voff), idO, (j > 0 || kk > 0) ? 1u : 0u, go);
+        if constexpr (X3) {  // P_hi V_lo + P_lo V_hi
+          mma_f16_ts_elect(dO, aP + kk * 8, vv(vd + ((C::V_LO - C::V_OFF) >> 4) + voff), idO, 1u,
+                           go);
+          mma_f16_ts_elect(dO, aP + BN / 2 + kk * 8, vv(vd + voff), idO, 1u, go);
         }
-        if (!ok) break;
-        // stage j (K_j read by S_t,j, V_j by PV_t,j) is free once these land
-        mma_commit(&empty[stage(j)]);
       }
-      // every MMA issued by this thread completes before TMEM is freed
-      mma_commit(drain);
-      drain_wait(drain, 0, kDrainNs);
+    };
+    for (int t = 0; t < nt; ++t) {
+      if (nkv[t] == 0) {
+        mma_commit_elect(&o_done[t], go);
+      } else {
+        issue_s(t, 0);
+        mma_commit_elect(&s_full[t], go);
+      }
     }
+    for (int j = 0; j < nmax; ++j) {
+      bool kwaited = false;
+      // stage j+1 has landed (the helper saw it); once per step
+      auto wait_stage = [&]() {
+        if (!kwaited) {
+          named_bar_sync(kBarK, 64);
+          kwaited = true;
+        }
+      };
+      for (int t = 0; t < nt; ++t) {
+        if (j >= nkv[t]) continue;
+        // P_t,j is in TMEM (4 softmax warps and this one meet)
+        named_bar_sync(kBarP + t, 32 * 5);
+        tc_fence_after();
+        issue_pv(t, j);
+        if (j + 1 < nkv[t]) {
+          wait_stage();
+          issue_s(t, j + 1);
+          mma_commit_elect(&s_full[t], go);
+        } else {
+          mma_commit_elect(&o_done[t], go);
+        }
+      }
+      // stage j (K_j read by S_t,j, V_j by PV_t,j) is free once these land
+      mma_commit_elect(&empty[stage(j)], go);
+    }
+    // every MMA issued by this warp completes before TMEM is freed
+    mma_commit_elect(drain, go);
+    if (go && lead) drain_wait(drain, 0, kDrainNs);
     __syncwarp();
+  } else if (warp == kMmaWarp + 1) {
+    // -------------------------------------------------------- stage helper
+    // Waits for K/V stage j+1 of every step that reads one and hands it to
+    // the MMA issuer through kBarK (same count of meetings on both sides,
+    // also after a failed wait).
+    bool ok = true;
+    for (int j = 0; j + 1 < nmax; ++j) {
+      const int s = (j + 1) % C::NS;
+      ok = ok && mbar_wait(&full[s], static_cast<uint32_t>(((j + 1) / C::NS) & 1), wc);
+      named_bar_sync(kBarK, 64);
+    }
   }
   } else {
     setmaxnreg_inc<kSoftmaxRegs>();
@@ -468,47 +502,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool fast_ok = (a.sl2 > 0.f) && (a.mask == nullptr);
     if (t < nt) {
       for (int j = 0; j < nkv[t]; ++j) {
-        ok = mbar_wait(&s_full[t], j & 1, wc);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t s[BN];
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[t], j & 1, wc));
+        if (ok) {
+          tc_fence_after();
+          uint32_t s[BN];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-          tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-        tmem_wait_ld();
-        const int kv0 = j * BN;
-        float alpha = 1.f;
-        bool resc;
-        float rs;
-        uint32_t pk[BN / 2];
-        uint32_t pk2[X3 ? BN / 2 : 1];  // P_lo (X3)
-        const bool fast = fast_ok && kv0 + BN - 1 <= limit;
-        if constexpr (X3) {
-          // bf16 hi/lo P: computed half a row at a time and stored to TMEM
-          // as soon as each half exists, so that the 128 scores plus one
-          // half of P_hi and P_lo are the most that is live at once.  The
-          // scores are used raw with p = 2^(s * scale*log2e - m) on the
-          // fused path, and as scaled, masked x = s * scale*log2e + bias
-          // (rewritten in place) with p = 2^(x - m) elsewhere.
-          float mul = a.sl2;
-          if (!fast) {
+          for (int c = 0; c < BN / 32; ++c)
+            tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+          tmem_wait_ld();
+          const int kv0 = j * BN;
+          float alpha = 1.f;
+          bool resc;
+          float rs;
+          uint32_t pk[BN / 2];
+          uint32_t pk2[X3 ? BN / 2 : 1];  // P_lo (X3)
+          const bool fast = fast_ok && kv0 + BN - 1 <= limit;
+          if constexpr (X3) {
+            // bf16 hi/lo P: computed half a row at a time and stored to TMEM
+            // as soon as each half exists, so that the 128 scores plus one
+            // half of P_hi and P_lo are the most that is live at once.  The
+            // scores are used raw with p = 2^(s * scale*log2e - m) on the
+            // fused path, and as scaled, masked x = s * scale*log2e + bias
+            // (rewritten in place) with p = 2^(x - m) elsewhere.
+            float mul = a.sl2;
+            if (!fast) {
 #pragma unroll
-            for (int i = 0; i < BN; ++i) {
-              float x = __uint_as_float(s[i]) * a.sl2;
-              if (mrow && kv0 + i < a.Lk) x += to_float(mrow[kv0 + i]) * kLog2e;
-              if (kv0 + i > limit) x = -INFINITY;
-              s[i] = __float_as_uint(x);
+              for (int i = 0; i < BN; ++i) {
+                float x = __uint_as_float(s[i]) * a.sl2;
+                if (mrow && kv0 + i < a.Lk) x += to_float(mrow[kv0 + i]) * kLog2e;
+                if (kv0 + i > limit) x = -INFINITY;
+                s[i] = __float_as_uint(x);
+              }
+              mul = 1.f;
             }
-            mul = 1.f;
-          }
-          // fused rows with a reference max skip the tile max, others take it
-          bool need_max = !fast || !(m > -INFINITY);
-          resc = false;
-          for (int pass = 0; pass < 2; ++pass) {
-            if (need_max) {
+            // fused rows with a reference max skip the tile max, others take it
+            bool need_max = !fast || !(m > -INFINITY);
+            resc = false;
+            for (int pass = 0; pass < 2; ++pass) {
+              if (need_max) {
+                float mr[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
+#pragma unroll
+                for (int i = 8; i < BN; i += 16)
+#pragma unroll
+                  for (int c = 0; c < 8; ++c)
+                    mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]),
+                                  __uint_as_float(s[i + 2 * c + 1]));
+                const float mx = fmaxf(fmax3(mr[0], mr[1], mr[2]),
+                                       fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7]))) *
+                                 mul;
+                // the fused path always moves to the tile max; the general
+                // path only when it grew by more than the threshold
+                if (fast || mx > m + kRescaleThreshold) {
+                  alpha = ex2(m - mx);  // 0 when m = -inf
+                  m = mx;
+                  resc = true;
+                }
+              }
+              const float mu = (m == -INFINITY) ? 0.f : m;
+              float rs0, rs1;
+              softmax_pairs<BF16, BN / 2, true>(*reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[0]),
+                                               mul, mu, *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[0]),
+                                               rs0, &pk2[0]);
+              tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+              tmem_st32(tS + BN / 2, *reinterpret_cast<uint32_t(*)[32]>(&pk2[0]));
+              softmax_pairs<BF16, BN / 2, true>(*reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[BN / 2]),
+                                               mul, mu, *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[BN / 4]),
+                                               rs1, &pk2[BN / 4]);
+              tmem_st32(tS + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk[BN / 4]));
+              tmem_st32(tS + BN / 2 + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk2[BN / 4]));
+              rs = rs0 + rs1;
+              // a fused row whose sum exceeds 2^15 (its max grew) takes the
+              // tile max and the warp computes the tile again; the second
+              // pass cannot fail (every p <= 1)
+              const bool redo = fast && !need_max && !(rs <= kFusedSumLimit);
+              if (!__any_sync(0xffffffffu, redo)) break;
+              need_max = redo;
+            }
+          } else if (fast) {
+            // Interior tile, positive scale, no mask: p = 2^(s * scale*log2e
+            // - m) with the scale folded into one packed FMA per pair, taken
+            // against the current reference max m without looking for the
+            // tile max.  Every p is at most the row sum, so a sum <= 2^15
+            // proves all p <= 2^15 (exact range in fp16 and bf16); only a row
+            // whose sum exceeds it (its max grew) or the first tile (m = -inf)
+            // finds the tile max of the raw scores and repeats.
+            resc = !(m > -INFINITY);
+            if (!resc) {
+              softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
+              resc = !(rs <= kFusedSumLimit);  // also true for inf or nan
+            }
+            if (resc) {
               float mr[8];
 #pragma unroll
               for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
@@ -520,123 +605,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 __uint_as_float(s[i + 2 * c + 1]));
               const float mx = fmaxf(fmax3(mr[0], mr[1], mr[2]),
                                      fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7]))) *
-                               mul;
-              // the fused path always moves to the tile max; the general
-              // path only when it grew by more than the threshold
-              if (fast || mx > m + kRescaleThreshold) {
-                alpha = ex2(m - mx);  // 0 when m = -inf
-                m = mx;
-                resc = true;
-              }
+                               a.sl2;
+              alpha = ex2(m - mx);  // 0 when m = -inf
+              m = mx;
+              softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
+            }
+          } else {
+            float x[BN];
+#pragma unroll
+            for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(s[i]) * a.sl2;
+            if (mrow) {
+#pragma unroll
+              for (int i = 0; i < BN; ++i)
+                if (kv0 + i < a.Lk) x[i] += to_float(mrow[kv0 + i]) * kLog2e;
+            }
+            if (kv0 + BN - 1 > limit) {
+#pragma unroll
+              for (int i = 0; i < BN; ++i)
+                if (kv0 + i > limit) x[i] = -INFINITY;
+            }
+            float mr[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+            for (int i = 4; i < BN; i += 8)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) mr[c] = fmax3(mr[c], x[i + 2 * c], x[i + 2 * c + 1]);
+            const float mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+            resc = mx > m + kRescaleThreshold;  // true on the first visible tile
+            if (resc) {
+              alpha = ex2(m - mx);  // 0 when m = -inf
+              m = mx;
             }
             const float mu = (m == -INFINITY) ? 0.f : m;
-            float rs0, rs1;
-            softmax_pairs<BF16, BN / 2, true>(*reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[0]),
-                                             mul, mu, *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[0]),
-                                             rs0, &pk2[0]);
+            float rp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < BN / 2; ++i) {
+              const float p0 = ex2(x[2 * i] - mu);
+              const float p1 = ex2(x[2 * i + 1] - mu);
+              rp[i & 3] += p0 + p1;
+              pk[i] = E::pack(p0, p1);
+            }
+            rs = (rp[0] + rp[1]) + (rp[2] + rp[3]);
+          }
+          __syncwarp();
+          l = l * alpha + rs;
+          // O_t holds the sum through PV_{t,j-1} (complete: the commit behind
+          // s_full tracks every earlier MMA); rescale rows whose max moved.
+          if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ob[32];
+              tmem_ld32(tO + c * 32, ob);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ob[i] = __float_as_uint(__uint_as_float(ob[i]) * alpha);
+              tmem_st32(tO + c * 32, ob);
+            }
+          }
+          if constexpr (!X3) {
             tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(tS + BN / 2, *reinterpret_cast<uint32_t(*)[32]>(&pk2[0]));
-            softmax_pairs<BF16, BN / 2, true>(*reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[BN / 2]),
-                                             mul, mu, *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[BN / 4]),
-                                             rs1, &pk2[BN / 4]);
-            tmem_st32(tS + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk[BN / 4]));
-            tmem_st32(tS + BN / 2 + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk2[BN / 4]));
-            rs = rs0 + rs1;
-            // a fused row whose sum exceeds 2^15 (its max grew) takes the
-            // tile max and the warp computes the tile again; the second
-            // pass cannot fail (every p <= 1)
-            const bool redo = fast && !need_max && !(rs <= kFusedSumLimit);
-            if (!__any_sync(0xffffffffu, redo)) break;
-            need_max = redo;
+            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
           }
-        } else if (fast) {
-          // Interior tile, positive scale, no mask: p = 2^(s * scale*log2e
-          // - m) with the scale folded into one packed FMA per pair, taken
-          // against the current reference max m without looking for the
-          // tile max.  Every p is at most the row sum, so a sum <= 2^15
-          // proves all p <= 2^15 (exact range in fp16 and bf16); only a row
-          // whose sum exceeds it (its max grew) or the first tile (m = -inf)
-          // finds the tile max of the raw scores and repeats.
-          resc = !(m > -INFINITY);
-          if (!resc) {
-            softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
-            resc = !(rs <= kFusedSumLimit);  // also true for inf or nan
-          }
-          if (resc) {
-            float mr[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
-#pragma unroll
-            for (int i = 8; i < BN; i += 16)
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]),
-                              __uint_as_float(s[i + 2 * c + 1]));
-            const float mx = fmaxf(fmax3(mr[0], mr[1], mr[2]),
-                                   fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7]))) *
-                             a.sl2;
-            alpha = ex2(m - mx);  // 0 when m = -inf
-            m = mx;
-            softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
-          }
-        } else {
-          float x[BN];
-#pragma unroll
-          for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(s[i]) * a.sl2;
-          if (mrow) {
-#pragma unroll
-            for (int i = 0; i < BN; ++i)
-              if (kv0 + i < a.Lk) x[i] += to_float(mrow[kv0 + i]) * kLog2e;
-          }
-          if (kv0 + BN - 1 > limit) {
-#pragma unroll
-            for (int i = 0; i < BN; ++i)
-              if (kv0 + i > limit) x[i] = -INFINITY;
-          }
-          float mr[4] = {x[0], x[1], x[2], x[3]};
-#pragma unroll
-          for (int i = 4; i < BN; i += 8)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) mr[c] = fmax3(mr[c], x[i + 2 * c], x[i + 2 * c + 1]);
-          const float mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
-          resc = mx > m + kRescaleThreshold;  // true on the first visible tile
-          if (resc) {
-            alpha = ex2(m - mx);  // 0 when m = -inf
-            m = mx;
-          }
-          const float mu = (m == -INFINITY) ? 0.f : m;
-          float rp[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < BN / 2; ++i) {
-            const float p0 = ex2(x[2 * i] - mu);
-            const float p1 = ex2(x[2 * i + 1] - mu);
-            rp[i & 3] += p0 + p1;
-            pk[i] = E::pack(p0, p1);
-          }
-          rs = (rp[0] + rp[1]) + (rp[2] + rp[3]);
+          tmem_wait_st();
+          tc_fence_before();
         }
-        __syncwarp();
-        l = l * alpha + rs;
-        // O_t holds the sum through PV_{t,j-1} (complete: the commit behind
-        // s_full tracks every earlier MMA); rescale rows whose max moved.
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ob[32];
-            tmem_ld32(tO + c * 32, ob);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ob[i] = __float_as_uint(__uint_as_float(ob[i]) * alpha);
-            tmem_st32(tO + c * 32, ob);
-          }
-        }
-        if constexpr (!X3) {
-          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&p_full[t]);
+        // hand P_t,j to the MMA warp; met every step, also after a failed wait
+        named_bar_sync(kBarP + t, 32 * 5);
       }
       if (ok) ok = mbar_wait(&o_done[t], 0, wc);
       ok = __all_sync(0xffffffffu, ok);

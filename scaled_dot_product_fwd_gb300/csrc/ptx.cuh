@@ -173,6 +173,47 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// Forms of the three above for a warp that runs the issue loop in step: one
+// lane, picked by elect.sync inside the asm, issues when `ok` (the same in
+// every lane) is nonzero, so the warp never branches around the instruction.
+__device__ __forceinline__ void mma_f16_ss_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate, uint32_t ok) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, o;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 o, %5, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "and.pred e, e, o;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(ok)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate, uint32_t ok) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, o;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 o, %5, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "and.pred e, e, o;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(ok)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar, uint32_t ok) {
+  asm volatile(
+      "{\n\t.reg .pred e, o;\n\t"
+      "setp.ne.b32 o, %1, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "and.pred e, e, o;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+          smem_addr(bar)),
+      "r"(ok)
+      : "memory");
+}
+
 // 32 lanes x 32 columns of 32-bit words: thread t of the warp receives
 // row (lane quarter base + t), columns [col, col + 32).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -257,6 +298,8 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Named barrier (whole warps; every participant must reach it the same number
+// of times: it has no time limit).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
