@@ -20,7 +20,14 @@
 //    factors are broadcast through a small per-warp buffer.
 //  - At the end the 8 warps' (m, l, acc) states are merged in shared memory
 //    and the split writes its normalised partial output and its log2-domain
-//    log-sum-exp to the workspace.  The combine kernel merges the splits.
+//    log-sum-exp to the workspace; the combine kernel merges the splits.
+//  - When the splits of a head group fit one thread-block cluster (2, 4, 8
+//    or 16 CTAs that divide D), the launcher makes them one, and the merge
+//    happens inside it instead: each CTA keeps its partial in shared memory,
+//    and after a cluster barrier CTA r reads every partial's lse and its
+//    slice of D columns through distributed shared memory, applies the same
+//    weights as the combine kernel, and writes that slice of O (CTA 0 also
+//    writes the LSE).  No workspace traffic and no second launch.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -51,6 +58,12 @@ struct SplitArgs {
   long long ms0, ms1;  // batch and head strides of the mask (row 0, key stride 1)
   float* ws_o;    // [B, Hq, num_splits, D], normalised partial outputs
   float* ws_lse;  // [B, Hq, num_splits], log2-domain log-sum-exp
+  // in-cluster merge (set by the launcher): output, LSE and sinks
+  void* o;
+  float* lse;
+  const float* sinks;
+  int cluster;      // 1: the num_splits CTAs of a head group form one cluster
+  int cluster_ok;   // 0: the caller asks for the two-pass form
   int* status;
   unsigned long long wait_ns;
   // Failure-detection test hook: when set, the producer does not issue the
@@ -72,6 +85,44 @@ template <>
 struct Ld<__nv_bfloat16> {
   static __device__ __forceinline__ float f(__nv_bfloat16 x) { return __bfloat162float(x); }
 };
+
+// fp32 -> storage type, round to nearest even.
+template <typename T>
+struct StoreAs;
+template <>
+struct StoreAs<float> {
+  static __device__ __forceinline__ float c(float x) { return x; }
+};
+template <>
+struct StoreAs<__half> {
+  static __device__ __forceinline__ __half c(float x) { return __float2half_rn(x); }
+};
+template <>
+struct StoreAs<__nv_bfloat16> {
+  static __device__ __forceinline__ __nv_bfloat16 c(float x) { return __float2bfloat16_rn(x); }
+};
+
+// Thread-block cluster helpers: barrier over every thread of the cluster
+// (exited threads count as arrived), this CTA's rank, and a 32-bit load from
+// the shared memory of another CTA of the cluster at the address that
+// corresponds to `local` in this one.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+constexpr int kMaxClusterSplits = 16;
 
 // Pairs of fp32 values in one 64-bit register for the packed f32x2 ops.
 __device__ __forceinline__ uint64_t f2(float a, float b) {
@@ -180,12 +231,16 @@ struct SplitCfg {
   // per-warp broadcast buffer: (p, p) pairs per (head, key), then HG factors
   static constexpr int PB_WORDS = 2 * HG * KB + ((HG + 1) & ~1);
   static constexpr int COMBINE_BYTES = kConsumerWarps * HG * (D + 2) * 4;
+  // in-cluster merge, after the warps' states: partial O [HG][D], lse [HG],
+  // split weights [HG][16], 1/L [HG]
+  static constexpr int MERGE_BYTES =
+      COMBINE_BYTES + (HG * D + HG + HG * kMaxClusterSplits + HG) * 4;
   static_assert(LR * EPL == D && RPW * LR == 32, "lane layout");
   static_assert(KB % RPW == 0 && NVL <= LR, "batch layout");
   static_assert((TILE_BYTES % 16) == 0, "bulk copy granularity");
   static size_t smem_bytes(int stages) {
     size_t ring = static_cast<size_t>(stages) * STAGE_BYTES;
-    if (ring < static_cast<size_t>(COMBINE_BYTES)) ring = COMBINE_BYTES;
+    if (ring < static_cast<size_t>(MERGE_BYTES)) ring = MERGE_BYTES;
     return 128 /*align*/ + ring + kConsumerWarps * PB_WORDS * 4 + 2 * 8 * 8 /*bars*/ + 16;
   }
 };
@@ -201,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   const int NS = a.stages;
   uint8_t* ring = smem;
   size_t ring_bytes = static_cast<size_t>(NS) * C::STAGE_BYTES;
-  if (ring_bytes < static_cast<size_t>(C::COMBINE_BYTES)) ring_bytes = C::COMBINE_BYTES;
+  if (ring_bytes < static_cast<size_t>(C::MERGE_BYTES)) ring_bytes = C::MERGE_BYTES;
   float* pbuf = reinterpret_cast<float*>(smem + ring_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + kConsumerWarps * C::PB_WORDS);
   uint64_t* empty = full + 8;
@@ -431,10 +486,10 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
     }
   }
   named_bar_sync(2, kConsumerWarps * 32);
-  if (*abort_flag) return;
-  for (int e = threadIdx.x; e < HG * D; e += kConsumerWarps * 32) {
-    const int hh = e / D, d = e % D;
-    if (grp * HG + hh >= a.G) continue;
+  const bool aborted = *abort_flag != 0;
+  // this split's state of head hh: normalised partial output at column d
+  // and the log2-domain log-sum-exp
+  auto split_state = [&](int hh, int d, float& o_out, float& lse_out) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wm[w * HG + hh]);
@@ -447,16 +502,101 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
         O = fmaf(wacc[(w * HG + hh) * D + d], f, O);
       }
     }
-    const int hq = kvh * a.G + grp * HG + hh;
-    const size_t row = (static_cast<size_t>(b) * a.Hq + hq) * a.num_splits + split;
-    a.ws_o[row * D + d] = (L > 0.f) ? O / L : 0.f;
-    if (d == 0) a.ws_lse[row] = (L > 0.f) ? M + __log2f(L) : -INFINITY;
+    o_out = (L > 0.f) ? O / L : 0.f;
+    lse_out = (L > 0.f) ? M + __log2f(L) : -INFINITY;
+  };
+  if (!a.cluster) {
+    if (aborted) return;
+    for (int e = threadIdx.x; e < HG * D; e += kConsumerWarps * 32) {
+      const int hh = e / D, d = e % D;
+      if (grp * HG + hh >= a.G) continue;
+      float ov, lv;
+      split_state(hh, d, ov, lv);
+      const int hq = kvh * a.G + grp * HG + hh;
+      const size_t row = (static_cast<size_t>(b) * a.Hq + hq) * a.num_splits + split;
+      a.ws_o[row * D + d] = ov;
+      if (d == 0) a.ws_lse[row] = lv;
+    }
+    return;
   }
+
+  // ---- splits merged inside the cluster.  Every consumer thread meets both
+  // cluster barriers, also after a failed wait (the results are then not
+  // used: the status word reports the timeout), so that no CTA leaves while
+  // another still reads its shared memory.
+  float* cpo = wacc + kConsumerWarps * HG * D;  // [HG][D] partial output
+  float* cpl = cpo + HG * D;                    // [HG] lse (log2)
+  float* wts = cpl + HG;                        // [HG][kMaxClusterSplits]
+  float* hinv = wts + HG * kMaxClusterSplits;   // [HG] 1 / L
+  for (int e = threadIdx.x; e < HG * D; e += kConsumerWarps * 32) {
+    const int hh = e / D, d = e % D;
+    float ov = 0.f, lv = -INFINITY;
+    if (!aborted && grp * HG + hh < a.G) split_state(hh, d, ov, lv);
+    cpo[e] = ov;
+    if (d == 0) cpl[hh] = lv;
+  }
+  cluster_sync_all();
+  const int S = a.num_splits;
+  const uint32_t rank = cluster_rank();
+  if (threadIdx.x < HG) {
+    // weights 2^(lse_s - M) of the splits, and the sink in the denominator
+    const int hh = threadIdx.x;
+    const int gh = grp * HG + hh;
+    const int hq = kvh * a.G + gh;
+    // all remote loads in flight before any is used
+    float lq[kMaxClusterSplits];
+#pragma unroll
+    for (int q = 0; q < kMaxClusterSplits; ++q)
+      if (q < S) lq[q] = ld_cluster(cpl + hh, static_cast<uint32_t>(q));
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kMaxClusterSplits; ++q)
+      if (q < S) {
+        wts[hh * kMaxClusterSplits + q] = lq[q];
+        M = fmaxf(M, lq[q]);
+      }
+    float sk = -INFINITY;
+    if (a.sinks && gh < a.G) {
+      sk = a.sinks[hq] * kLog2e;
+      M = fmaxf(M, sk);
+    }
+    float L = 0.f;
+    for (int q = 0; q < S; ++q) {
+      const float w = (M == -INFINITY) ? 0.f : ex2(wts[hh * kMaxClusterSplits + q] - M);
+      wts[hh * kMaxClusterSplits + q] = w;
+      L += w;
+    }
+    if (a.sinks && M != -INFINITY) L += ex2(sk - M);
+    hinv[hh] = (L > 0.f) ? 1.f / L : 0.f;
+    if (rank == 0 && a.lse && gh < a.G && !aborted)
+      a.lse[static_cast<size_t>(b) * a.Hq + hq] =
+          (L > 0.f) ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
+  }
+  named_bar_sync(3, kConsumerWarps * 32);
+  const int dpr = D / S;  // output columns of this CTA
+  for (int e = threadIdx.x; e < HG * dpr; e += kConsumerWarps * 32) {
+    const int hh = e / dpr;
+    const int d = static_cast<int>(rank) * dpr + e % dpr;
+    const int gh = grp * HG + hh;
+    if (gh >= a.G || aborted) continue;
+    float pv[kMaxClusterSplits];  // all remote loads in flight first
+#pragma unroll
+    for (int q = 0; q < kMaxClusterSplits; ++q)
+      if (q < S) pv[q] = ld_cluster(cpo + hh * D + d, static_cast<uint32_t>(q));
+    float acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxClusterSplits; ++q)
+      if (q < S) acc = fmaf(wts[hh * kMaxClusterSplits + q], pv[q], acc);
+    const int hq = kvh * a.G + gh;
+    static_cast<T*>(a.o)[(static_cast<size_t>(b) * a.Hq + hq) * D + d] = StoreAs<T>::c(acc * hinv[hh]);
+  }
+  cluster_sync_all();
 }
 
-// Host-side launch of one instantiation.
+// Host-side launch of one instantiation.  *merged tells the caller whether
+// the splits were merged inside a cluster (no combine pass needed).
 template <typename T, int D, int HG, int KB>
-sdpa_status_t launch_split(const SplitArgs& a, int batch, cudaStream_t stream) {
+sdpa_status_t launch_split(SplitArgs a, int batch, cudaStream_t stream, bool* merged) {
   using C = SplitCfg<T, D, HG, KB>;
   auto kern = decode_split_kernel<T, D, HG, KB>;
   const size_t smem = C::smem_bytes(a.stages);
@@ -465,6 +605,39 @@ sdpa_status_t launch_split(const SplitArgs& a, int batch, cudaStream_t stream) {
                            static_cast<int>(smem)) != cudaSuccess)
     return SDPA_ERR_CUDA;
   dim3 grid(a.num_splits, a.Hkv * a.num_groups, batch);
+  *merged = false;
+  const int S = a.num_splits;
+  if (a.cluster_ok && S >= 2 && S <= kMaxClusterSplits && (S & (S - 1)) == 0 && D % S == 0) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // whether such a cluster can be resident at all (once per cluster size)
+    static int fits[5] = {0, 0, 0, 0, 0};  // 0 unknown, 1 yes, -1 no
+    int li = 0;
+    while ((1 << li) < S) ++li;
+    if (fits[li] == 0) {
+      if (S > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      int n = 0;
+      fits[li] = (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) ? 1 : -1;
+      cudaGetLastError();
+    }
+    if (fits[li] > 0) {
+      a.cluster = 1;
+      if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return SDPA_ERR_CUDA;
+      *merged = true;
+      return SDPA_OK;
+    }
+  }
+  a.cluster = 0;
   kern<<<grid, kThreads, smem, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
@@ -480,38 +653,43 @@ __host__ __device__ constexpr int keys_per_warp(int elem_bytes, int D, int HG) {
 }
 
 template <typename T, int D, int HG>
-sdpa_status_t launch_split_hg(const SplitArgs& a, int batch, cudaStream_t stream) {
+sdpa_status_t launch_split_hg(const SplitArgs& a, int batch, cudaStream_t stream, bool* merged) {
   constexpr int KB = keys_per_warp(static_cast<int>(sizeof(T)), D, HG);
-  return launch_split<T, D, HG, KB>(a, batch, stream);
+  return launch_split<T, D, HG, KB>(a, batch, stream, merged);
 }
 
 template <typename T, int D>
-sdpa_status_t launch_split_d(const SplitArgs& a, int hg, int batch, cudaStream_t stream) {
+sdpa_status_t launch_split_d(const SplitArgs& a, int hg, int batch, cudaStream_t stream,
+                             bool* merged) {
   switch (hg) {
-    case 1: return launch_split_hg<T, D, 1>(a, batch, stream);
-    case 2: return launch_split_hg<T, D, 2>(a, batch, stream);
-    case 4: return launch_split_hg<T, D, 4>(a, batch, stream);
+    case 1: return launch_split_hg<T, D, 1>(a, batch, stream, merged);
+    case 2: return launch_split_hg<T, D, 2>(a, batch, stream, merged);
+    case 4: return launch_split_hg<T, D, 4>(a, batch, stream, merged);
     case 8:
-      if constexpr (D <= 128) return launch_split_hg<T, D, 8>(a, batch, stream);
+      if constexpr (D <= 128) return launch_split_hg<T, D, 8>(a, batch, stream, merged);
       return SDPA_ERR_UNSUPPORTED;
     default: return SDPA_ERR_UNSUPPORTED;
   }
 }
 
 template <typename T>
-sdpa_status_t launch_split_t(const SplitArgs& a, int D, int hg, int batch, cudaStream_t stream) {
+sdpa_status_t launch_split_t(const SplitArgs& a, int D, int hg, int batch, cudaStream_t stream,
+                             bool* merged) {
   switch (D) {
-    case 64: return launch_split_d<T, 64>(a, hg, batch, stream);
-    case 128: return launch_split_d<T, 128>(a, hg, batch, stream);
-    case 512: return launch_split_d<T, 512>(a, hg, batch, stream);
+    case 64: return launch_split_d<T, 64>(a, hg, batch, stream, merged);
+    case 128: return launch_split_d<T, 128>(a, hg, batch, stream, merged);
+    case 512: return launch_split_d<T, 512>(a, hg, batch, stream, merged);
     default: return SDPA_ERR_UNSUPPORTED;
   }
 }
 
 // Per-dtype entry points (one translation unit each).
-sdpa_status_t launch_split_f32(const SplitArgs& a, int D, int hg, int batch, cudaStream_t s);
-sdpa_status_t launch_split_f16(const SplitArgs& a, int D, int hg, int batch, cudaStream_t s);
-sdpa_status_t launch_split_bf16(const SplitArgs& a, int D, int hg, int batch, cudaStream_t s);
+sdpa_status_t launch_split_f32(const SplitArgs& a, int D, int hg, int batch, cudaStream_t s,
+                              bool* merged);
+sdpa_status_t launch_split_f16(const SplitArgs& a, int D, int hg, int batch, cudaStream_t s,
+                              bool* merged);
+sdpa_status_t launch_split_bf16(const SplitArgs& a, int D, int hg, int batch, cudaStream_t s,
+                              bool* merged);
 
 }  // namespace dec
 }  // namespace gb300

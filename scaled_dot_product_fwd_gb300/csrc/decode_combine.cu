@@ -32,21 +32,6 @@ struct CombineArgs {
   int rows_per_head;  // query rows per (batch, head): 1 for decode
 };
 
-template <typename T>
-struct St;
-template <>
-struct St<float> {
-  static __device__ __forceinline__ float c(float x) { return x; }
-};
-template <>
-struct St<__half> {
-  static __device__ __forceinline__ __half c(float x) { return __float2half_rn(x); }
-};
-template <>
-struct St<__nv_bfloat16> {
-  static __device__ __forceinline__ __nv_bfloat16 c(float x) { return __float2bfloat16_rn(x); }
-};
-
 constexpr int kMaxSplits = 1024;  // upper bound of the split plan
 
 // Block-wide max / sum over the 128 threads (4 warps).
@@ -109,10 +94,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
         acc.w = fmaf(ws, v.w, acc.w);
       }
     }
-    orow[4 * c + 0] = St<T>::c(acc.x * inv);
-    orow[4 * c + 1] = St<T>::c(acc.y * inv);
-    orow[4 * c + 2] = St<T>::c(acc.z * inv);
-    orow[4 * c + 3] = St<T>::c(acc.w * inv);
+    orow[4 * c + 0] = StoreAs<T>::c(acc.x * inv);
+    orow[4 * c + 1] = StoreAs<T>::c(acc.y * inv);
+    orow[4 * c + 2] = StoreAs<T>::c(acc.z * inv);
+    orow[4 * c + 3] = StoreAs<T>::c(acc.w * inv);
   }
   if (threadIdx.x == 0 && a.lse) a.lse[row] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
@@ -161,9 +146,33 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
       best = s;
     }
   }
+  // The two-pass form pays a second launch and a workspace round trip.  A
+  // split count of 2..16 dividing D lets the splits of each head group form
+  // one thread-block cluster that merges them itself, when all the plan's
+  // clusters are resident at once.  Clusters of C CTAs resident per GPU at
+  // one CTA per SM, measured on a 152-SM GB300: 76, 36, 15 and 7 for
+  // C = 2, 4, 8, 16 (scaled by the SM count and by CTAs per SM here).
+  constexpr long long kCombineCost = 3;  // in tile units
+  best_cost += kCombineCost;
+  bool cluster = false;
+  const long long nsm = num_sms > 0 ? num_sms : 152;
+  for (int c = 2; c <= 16 && c <= max_s; c <<= 1) {
+    if (D % c != 0) continue;
+    const long long per_c = c == 2 ? 76 : c == 4 ? 36 : c == 8 ? 15 : 7;
+    if (units > per_c * nsm / 152 * per_sm) continue;
+    const long long cost = (ntiles + c - 1) / c + 2;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = c;
+      cluster = true;
+    }
+  }
   if (const char* env = getenv("GB300_SDPA_DECODE_SPLITS")) {  // test override
     const int f = atoi(env);
-    if (f >= 1) best = f < max_s ? f : max_s;
+    if (f >= 1) {
+      best = f < max_s ? f : max_s;
+      cluster = best >= 2 && best <= 16 && (best & (best - 1)) == 0 && D % best == 0;
+    }
   }
   const int tiles_per = (ntiles + best - 1) / best;
   const int split_keys = tiles_per * tk;
@@ -174,6 +183,7 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   out->num_splits = splits;
   out->split_keys = split_keys;
   out->stages = stages;
+  out->cluster = cluster;  // the launcher checks the final split count
   const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * splits;
   out->workspace = align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
   return true;
@@ -204,18 +214,26 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   a.ms1 = p.mask_stride[1];
   a.ws_o = ws_o;
   a.ws_lse = ws_lse;
+  a.o = o;
+  a.lse = lse;
+  a.sinks = p.sinks;
+  a.cluster = 0;
+  const char* clu = getenv("GB300_SDPA_DECODE_CLUSTER");  // test override: 0 = two passes
+  a.cluster_ok = (plan.cluster && !(clu && clu[0] == '0')) ? 1 : 0;
   a.status = env.status;
   a.wait_ns = env.wait_limit_ns;
   const char* drop = getenv("GB300_SDPA_DEBUG_DROP_LAST_TILE");
   a.debug_drop_last = (drop && drop[0] == '1') ? 1 : 0;
   sdpa_status_t st;
+  bool merged = false;
+  const int D = p.head_dim, hg = plan.head_group;
   switch (p.dtype) {
-    case SDPA_F32: st = dec::launch_split_f32(a, p.head_dim, plan.head_group, p.batch, env.stream); break;
-    case SDPA_F16: st = dec::launch_split_f16(a, p.head_dim, plan.head_group, p.batch, env.stream); break;
-    case SDPA_BF16: st = dec::launch_split_bf16(a, p.head_dim, plan.head_group, p.batch, env.stream); break;
+    case SDPA_F32: st = dec::launch_split_f32(a, D, hg, p.batch, env.stream, &merged); break;
+    case SDPA_F16: st = dec::launch_split_f16(a, D, hg, p.batch, env.stream, &merged); break;
+    case SDPA_BF16: st = dec::launch_split_bf16(a, D, hg, p.batch, env.stream, &merged); break;
     default: return SDPA_ERR_UNSUPPORTED;
   }
-  if (st != SDPA_OK) return st;
+  if (st != SDPA_OK || merged) return st;
   dec::CombineArgs c;
   c.ws_o = ws_o;
   c.ws_lse = ws_lse;

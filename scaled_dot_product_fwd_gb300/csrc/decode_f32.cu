@@ -4,8 +4,9 @@
 namespace gb300 {
 namespace dec {
 
-sdpa_status_t launch_split_f32(const SplitArgs& a, int D, int hg, int batch, cudaStream_t s) {
-  return launch_split_t<float>(a, D, hg, batch, s);
+sdpa_status_t launch_split_f32(const SplitArgs& a, int D, int hg, int batch, cudaStream_t s,
+                              bool* merged) {
+  return launch_split_t<float>(a, D, hg, batch, s, merged);
 }
 
 }  // namespace dec

@@ -27,7 +27,9 @@ struct DecodePlan {
   int num_splits;   // key-range splits per (batch, kv head, head group)
   int split_keys;   // keys per split (multiple of tile_keys)
   int stages;       // shared-memory ring stages
-  size_t workspace; // bytes of partial results
+  bool cluster;     // merge the splits inside a thread-block cluster when it
+                    // can be resident (else the combine pass does)
+  size_t workspace; // bytes of partial results (also reserved for clusters)
 };
 
 bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);

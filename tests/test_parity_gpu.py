@@ -174,10 +174,35 @@ def test_decode_sweep(cuda, dtype, D, G, Lk):
     check(cuda, wl(2, Hkv * G, Hkv, 1, Lk, D, dtype, sinks=(Lk % 2 == 1)))
 
 
-@pytest.mark.parametrize("splits", [1, 2, 5, 64])
-def test_decode_forced_splits(cuda, splits, monkeypatch):
+@pytest.mark.parametrize("cluster", ["1", "0"])
+@pytest.mark.parametrize("splits", [1, 2, 4, 5, 8, 16, 64])
+def test_decode_forced_splits(cuda, splits, cluster, monkeypatch):
+    """Split counts that a thread-block cluster merges (2, 4, 8, 16) and ones
+    that go through the combine kernel; cluster "0" forces the two-pass form."""
     monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", str(splits))
+    monkeypatch.setenv("GB300_SDPA_DECODE_CLUSTER", cluster)
     check(cuda, wl(1, 8, 1, 1, 3001, 128, "bfloat16", sinks=True))
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+@pytest.mark.parametrize("splits", [2, 16])
+def test_decode_d512_cluster_merge_matches_two_pass(cuda, dtype, splits, monkeypatch):
+    """The in-cluster merge and the combine kernel give the same result on the
+    head_dim 512 GQA-8 shape with sinks (both against the oracle too)."""
+    import torch
+    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", str(splits))
+    w = wl(2, 32, 4, 1, 1024, 512, dtype, sinks=True)
+    inp = W.make_inputs(w)
+    outs = []
+    for cl in ("1", "0"):
+        monkeypatch.setenv("GB300_SDPA_DECODE_CLUSTER", cl)
+        outs.append(run_gpu(torch, w, inp))
+    o_ref, lse_ref = oracle_rows(w, inp, None)
+    for o_gpu, lse_gpu in outs:
+        compare(w, o_gpu, lse_gpu, o_ref, lse_ref, None)
+    tol = 1e-6 if dtype == "float32" else 1e-2
+    assert float((outs[0][0].float() - outs[1][0].float()).abs().max()) <= tol
+    assert float((outs[0][1] - outs[1][1]).abs().max()) <= 1e-5
 
 
 # ----------------------------------------------------------------- edge cases
