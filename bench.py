@@ -295,7 +295,11 @@ def secondary(torch, S, device, stream, peaks):
         t = w.flops() * steps / secs / 1e12
         out[w.name] = {"value": round(t, 2), "unit": "TFLOP/s", "ms_per_call": secs / steps * 1e3,
                        "frac_of_bf16_peak": round(t / peaks["bf16_tflops"], 4)}
-    # decode calls are microseconds long: timed as a CUDA graph of 20 calls
+    # microsecond-long calls are timed as a CUDA graph of 20 calls
+    per_call, copies = run_workload_graph(torch, S, W.TINY, 20, 25, device, copies=4)
+    out[W.TINY.name] = {"value": round(W.TINY.flops() / per_call / 1e12, 3), "unit": "TFLOP/s",
+                        "us_per_call": round(per_call * 1e6, 2), "input_copies": copies,
+                        "timing": "CUDA graph of 20 calls, replayed"}
     for w, reps in ((W.DECODE_LONG, 10), (W.DECODE_D512[(1, "bfloat16", False)], 25),
                     (W.DECODE_D512[(2, "bfloat16", False)], 25),
                     (W.DECODE_D512[(1, "float16", True)], 25),
