@@ -144,3 +144,20 @@ def test_python_binding_rejects_cpu_tensors(sdpa_lib):
     q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         S.sdpa_forward(q, q, q)
+
+
+def test_host_entry_rejects_unpinned_inputs(sdpa_lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        S.sdpa_forward_host(q, q, q)
+
+
+@pytest.mark.parametrize("nb,hkv,chunks", [(1, 1, 8), (2, 38, 8), (2, 38, 3), (3, 4, 1), (1, 5, 64)])
+def test_host_entry_pieces_cover_every_head_once(nb, hkv, chunks):
+    pieces = B._host_chunks(nb, hkv, chunks)
+    seen = [(b, h) for b, h0, h1 in pieces for h in range(h0, h1)]
+    assert sorted(seen) == [(b, h) for b in range(nb) for h in range(hkv)]
+    assert all(0 <= h0 < h1 <= hkv for _, h0, h1 in pieces)
+    # every batch in about chunks / nb pieces
+    assert len(pieces) == nb * min(hkv, -(-chunks // nb))

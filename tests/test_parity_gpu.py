@@ -266,3 +266,47 @@ def test_wait_timeout_reports_status(cuda, monkeypatch):
         monkeypatch.delenv("GB300_SDPA_DEBUG_DROP_LAST_TILE")
     assert S.sdpa_device_status() == 0  # cleared by the read
     check(torch, w)  # the context still works
+
+
+# ------------------------------------------------------ host-buffer entry point
+@pytest.mark.parametrize("case", ["f16_mha", "bf16_gqa_causal_sinks", "f32_hilo"])
+def test_host_entry_matches_device_entry(cuda, case):
+    """sdpa_forward_host (pinned host buffers, pieces on several streams) gives
+    the same bytes as sdpa_forward on device buffers: every (b, h) is computed
+    by the same kernel either way (the fp32 case also checks that the two
+    compute streams do not share a workspace)."""
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    w = {"f16_mha": wl(2, 6, 6, 300, 300, 64, "float16"),
+         "bf16_gqa_causal_sinks": wl(2, 8, 2, 200, 333, 128, "bfloat16", causal=True, sinks=True),
+         "f32_hilo": wl(1, 6, 6, 257, 257, 64, "float32")}[case]
+    inp = W.make_inputs(w)
+    q, k, v = (inp[x].pin_memory() for x in ("q", "k", "v"))
+    s = None if inp["sinks"] is None else inp["sinks"].cuda()
+    o_d, l_d = S.sdpa_forward(q.cuda(), k.cuda(), v.cuda(), scale=w.scale, causal=w.causal, sinks=s)
+    torch.cuda.synchronize()
+    o_h = torch.empty_like(q).pin_memory()
+    l_h = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
+    # first call: eager run plus graph capture; second: graph replay; third: no graph
+    for graph in (True, True, False):
+        o_h.zero_()
+        l_h.zero_()
+        S.sdpa_forward_host(q, k, v, scale=w.scale, causal=w.causal, sinks=s, out=o_h, lse=l_h,
+                            chunks=5, graph=graph)
+        torch.cuda.synchronize()
+        assert S.sdpa_device_status() == 0
+        assert torch.equal(o_h, o_d.cpu())
+        assert torch.equal(l_h, l_d.cpu())
+
+
+def test_host_entry_decode_against_oracle(cuda):
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    w = wl(2, 32, 4, 1, 1024, 512, "bfloat16", sinks=True)
+    inp = W.make_inputs(w)
+    q, k, v = (inp[x].pin_memory() for x in ("q", "k", "v"))
+    o_h, l_h = S.sdpa_forward_host(q, k, v, scale=w.scale, sinks=inp["sinks"].cuda(), chunks=4)
+    torch.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    o_ref, lse_ref = oracle_rows(w, inp, None)
+    compare(w, o_h, l_h, o_ref, lse_ref, None)
