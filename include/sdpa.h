@@ -71,14 +71,17 @@ typedef enum {
   SDPA_ERR_TIMEOUT = 6           /* a device-side wait gave up (status word) */
 } sdpa_status_t;
 
-/* Kernel paths.  The launcher picks one from the shape alone. */
+/* Kernel paths.  The launcher picks one from the shape alone: one query row
+ * per head (decode), or a few (up to 2 at D = 64/128, up to 8 at D = 512),
+ * take the split-KV vector path, where the rows of a kv head share its K/V
+ * stream; longer query sequences take the prefill kernels. */
 typedef enum {
   SDPA_KERNEL_NONE = 0,
-  SDPA_KERNEL_PREFILL_TC = 1,   /* fp16/bf16, Lq > 1: TMA + tcgen05 + TMEM */
-  SDPA_KERNEL_PREFILL_F32 = 2,  /* fp32, Lq > 1: fp32 FMA tiles */
-  SDPA_KERNEL_DECODE_SPLITKV = 3, /* Lq == 1: split-KV vector pass + combine */
+  SDPA_KERNEL_PREFILL_TC = 1,   /* fp16/bf16, Lq > 2: TMA + tcgen05 + TMEM */
+  SDPA_KERNEL_PREFILL_F32 = 2,  /* fp32, D = 128, Lq > 2: fp32 FMA tiles */
+  SDPA_KERNEL_DECODE_SPLITKV = 3, /* small Lq: split-KV vector pass + merge */
   SDPA_KERNEL_NO_KEYS = 4,       /* Lk == 0: writes o = 0 and the empty lse */
-  SDPA_KERNEL_PREFILL_TC_F32 = 5 /* fp32, D = 64, Lq > 1: bf16 hi/lo splits on
+  SDPA_KERNEL_PREFILL_TC_F32 = 5 /* fp32, D = 64, Lq > 2: bf16 hi/lo splits on
                                     tcgen05 (three products per step) */
 } sdpa_kernel_t;
 
@@ -86,7 +89,7 @@ typedef enum {
  * Problem description.
  *  batch, num_q_heads, num_kv_heads, seq_len_q, seq_len_kv, head_dim:
  *      B, Hq, Hkv, Lq, Lk, D.  Hkv >= 1, the others >= 0, Hq % Hkv == 0,
- *      D in {64, 128, 512}, Lq and Lk at most 2^30.  When B * Hq * Lq == 0
+ *      D in {64, 128, 512} (512: Lq <= 8 only), Lq and Lk at most 2^30.  When B * Hq * Lq == 0
  *      there is nothing to compute and the call returns SDPA_OK at once.
  *      When Lk == 0 every row sees no key: o = 0 and lse = -inf (the sink
  *      logit itself with sinks).
@@ -179,7 +182,7 @@ SDPA_API uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns);
 SDPA_API int sdpa_abi_version(void);
 
 /*
- * sdpa_forward_decode_noalloc — single-query decode (Lq == 1) without a
+ * sdpa_forward_decode_noalloc — the vector path (decode) without a
  * caller workspace.  The pages have no counterpart: this entry point exists
  * for callers that cannot call cudaMalloc or pass device scratch where they
  * run attention (a stream being captured into a CUDA graph may not
@@ -192,7 +195,7 @@ SDPA_API int sdpa_abi_version(void);
  * compute: SDPA_OK).  The split-KV partial results go to one static device
  * array of SDPA_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the
  * library holds until exit; a problem whose partial results do not fit
- * (about B * Hq * splits * (D + 1) * 4 bytes) returns
+ * (about B * Hq * Lq * splits * (D + 1) * 4 bytes) returns
  * SDPA_ERR_WORKSPACE_TOO_SMALL before any launch.  Nothing is allocated.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address (cudaGetSymbolAddress) and caches it: make that

@@ -1,4 +1,6 @@
-// decode.cuh — single-query (Lq = 1) attention: split-KV vector pass.
+// decode.cuh — single-query (Lq = 1) and few-query (Lq <= 8) attention:
+// split-KV vector pass.  The G x Lq query rows of a kv head form its head
+// groups, so they all share one K/V stream.
 //
 // MLX PR #4459 ("Add D512 support to Metal vector attention") serves
 // single-token decode with a single-pass and a two-pass vector kernel: the
@@ -49,13 +51,15 @@ struct SplitArgs {
   const void* k;
   const void* v;
   int Hq, Hkv, G, Lk;
-  int num_groups;   // query-head groups per kv head
+  int Lq;           // query rows per head (1 for decode, up to 8 for multi-query)
+  int causal;       // bottom-right: key j visible to row i iff j <= i + Lk - Lq
+  int num_groups;   // groups of HG query rows per kv head (rows: G heads x Lq)
   int num_splits;
   int split_keys;
   int stages;
   float sl2;  // scale * log2(e)
   const void* mask;
-  long long ms0, ms1;  // batch and head strides of the mask (row 0, key stride 1)
+  long long ms0, ms1, ms2;  // batch, head and row strides of the mask (key stride 1)
   float* ws_o;    // [B, Hq, num_splits, D], normalised partial outputs
   float* ws_lse;  // [B, Hq, num_splits], log2-domain log-sum-exp
   // in-cluster merge (set by the launcher): output, LSE and sinks
@@ -327,23 +331,35 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   const int vi = c >> C::VSHIFT;       // value held after the reduce-scatter
   const int hl = vi / C::LPB;          // its head inside the group
   const int kl = (vi % C::LPB) * C::RPW + r;  // its key inside the warp batch
+  // The group's HG rows are (query head, query row) pairs of this kv head:
+  // row rr of the kv head is head kvh * G + rr / Lq, query row rr % Lq.
+  const int R = a.G * a.Lq;  // rows per kv head
+  auto row_index = [&](int rr) {  // global query row [b, hq, qi]
+    const int hq = kvh * a.G + rr / a.Lq;
+    return (static_cast<size_t>(b) * a.Hq + hq) * a.Lq + rr % a.Lq;
+  };
   uint64_t q2[HG][C::NP2];
 #pragma unroll
   for (int hh = 0; hh < HG; ++hh) {
-    const int gh = grp * HG + hh;
-    const int hq = kvh * a.G + gh;
-    const T* qrow = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + hq) * D;
+    const int rr = grp * HG + hh;
+    const T* qrow = static_cast<const T*>(a.q) + row_index(rr < R ? rr : 0) * D;
 #pragma unroll
     for (int pi = 0; pi < C::NPIECE; ++pi) {
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (gh < a.G) w = *reinterpret_cast<const uint4*>(qrow + (pi * C::LR + c) * C::CE);
+      if (rr < R) w = *reinterpret_cast<const uint4*>(qrow + (pi * C::LR + c) * C::CE);
       Wd::pairs(w, &q2[hh][pi * (C::CE / 2)]);
     }
   }
-  const int my_hq = kvh * a.G + grp * HG + hl;
-  const bool my_head_ok = grp * HG + hl < a.G;
+  const int my_rr = grp * HG + hl;
+  const bool my_head_ok = my_rr < R;
+  const int my_hq = kvh * a.G + (my_head_ok ? my_rr / a.Lq : 0);
+  const int my_qi = my_head_ok ? my_rr % a.Lq : 0;
+  // last key this lane's row sees (bounds, and the causal rule)
+  int my_limit = a.Lk - 1;
+  if (a.causal) my_limit = min(my_limit, my_qi + (a.Lk - a.Lq));
   const T* mrow = nullptr;
-  if (a.mask && my_head_ok) mrow = static_cast<const T*>(a.mask) + b * a.ms0 + my_hq * a.ms1;
+  if (a.mask && my_head_ok)
+    mrow = static_cast<const T*>(a.mask) + b * a.ms0 + my_hq * a.ms1 + my_qi * a.ms2;
 
   uint64_t acc2[HG][C::NP2];
   float lsum[HG];
@@ -394,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
     const float sc = reduce_scatter<C::NVL, C::LR>(part, c);
     const int key = key0 + kl;
     float x = sc * a.sl2;
-    if (key >= key_end) {
+    if (key >= key_end || key > my_limit) {
       x = -INFINITY;
     } else if (mrow) {
       x += Ld<T>::f(mrow[key]) * kLog2e;
@@ -509,11 +525,10 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
     if (aborted) return;
     for (int e = threadIdx.x; e < HG * D; e += kConsumerWarps * 32) {
       const int hh = e / D, d = e % D;
-      if (grp * HG + hh >= a.G) continue;
+      if (grp * HG + hh >= R) continue;
       float ov, lv;
       split_state(hh, d, ov, lv);
-      const int hq = kvh * a.G + grp * HG + hh;
-      const size_t row = (static_cast<size_t>(b) * a.Hq + hq) * a.num_splits + split;
+      const size_t row = row_index(grp * HG + hh) * a.num_splits + split;
       a.ws_o[row * D + d] = ov;
       if (d == 0) a.ws_lse[row] = lv;
     }
@@ -531,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   for (int e = threadIdx.x; e < HG * D; e += kConsumerWarps * 32) {
     const int hh = e / D, d = e % D;
     float ov = 0.f, lv = -INFINITY;
-    if (!aborted && grp * HG + hh < a.G) split_state(hh, d, ov, lv);
+    if (!aborted && grp * HG + hh < R) split_state(hh, d, ov, lv);
     cpo[e] = ov;
     if (d == 0) cpl[hh] = lv;
   }
@@ -541,8 +556,9 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   if (threadIdx.x < HG) {
     // weights 2^(lse_s - M) of the splits, and the sink in the denominator
     const int hh = threadIdx.x;
-    const int gh = grp * HG + hh;
-    const int hq = kvh * a.G + gh;
+    const int rr = grp * HG + hh;
+    const bool valid = rr < R;
+    const int hq = kvh * a.G + (valid ? rr / a.Lq : 0);
     // all remote loads in flight before any is used
     float lq[kMaxClusterSplits];
 #pragma unroll
@@ -556,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
         M = fmaxf(M, lq[q]);
       }
     float sk = -INFINITY;
-    if (a.sinks && gh < a.G) {
+    if (a.sinks && valid) {
       sk = a.sinks[hq] * kLog2e;
       M = fmaxf(M, sk);
     }
@@ -568,8 +584,8 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
     }
     if (a.sinks && M != -INFINITY) L += ex2(sk - M);
     hinv[hh] = (L > 0.f) ? 1.f / L : 0.f;
-    if (rank == 0 && a.lse && gh < a.G && !aborted)
-      a.lse[static_cast<size_t>(b) * a.Hq + hq] =
+    if (rank == 0 && a.lse && valid && !aborted)
+      a.lse[row_index(rr)] =
           (L > 0.f) ? (M + __log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
   named_bar_sync(3, kConsumerWarps * 32);
@@ -577,8 +593,8 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   for (int e = threadIdx.x; e < HG * dpr; e += kConsumerWarps * 32) {
     const int hh = e / dpr;
     const int d = static_cast<int>(rank) * dpr + e % dpr;
-    const int gh = grp * HG + hh;
-    if (gh >= a.G || aborted) continue;
+    const int rr = grp * HG + hh;
+    if (rr >= R || aborted) continue;
     float pv[kMaxClusterSplits];  // all remote loads in flight first
 #pragma unroll
     for (int q = 0; q < kMaxClusterSplits; ++q)
@@ -587,8 +603,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
 #pragma unroll
     for (int q = 0; q < kMaxClusterSplits; ++q)
       if (q < S) acc = fmaf(wts[hh * kMaxClusterSplits + q], pv[q], acc);
-    const int hq = kvh * a.G + gh;
-    static_cast<T*>(a.o)[(static_cast<size_t>(b) * a.Hq + hq) * D + d] = StoreAs<T>::c(acc * hinv[hh]);
+    static_cast<T*>(a.o)[row_index(rr) * D + d] = StoreAs<T>::c(acc * hinv[hh]);
   }
   cluster_sync_all();
 }

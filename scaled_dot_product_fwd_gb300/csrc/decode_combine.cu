@@ -115,7 +115,8 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   const int es = elem_bytes(p.dtype);
   const int D = p.head_dim;
-  const int G = p.num_q_heads / p.num_kv_heads;
+  // rows per kv head: its G query heads times Lq query rows
+  const int G = p.num_q_heads / p.num_kv_heads * p.seq_len_q;
   const int hg_max = (D == 512) ? 4 : 8;
   int hg = 1;
   while (hg < G && hg < hg_max) hg <<= 1;
@@ -184,7 +185,7 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   out->split_keys = split_keys;
   out->stages = stages;
   out->cluster = cluster;  // the launcher checks the final split count
-  const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * splits;
+  const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * splits;
   out->workspace = align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
   return true;
 }
@@ -192,7 +193,8 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
 sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
                             const void* k, const void* v, void* o, float* lse, void* workspace,
                             const LaunchEnv& env) {
-  const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * plan.num_splits;
+  const size_t rows =
+      static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * plan.num_splits;
   float* ws_o = static_cast<float*>(workspace);
   float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                            align256(rows * p.head_dim * sizeof(float)));
@@ -204,6 +206,8 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   a.Hkv = p.num_kv_heads;
   a.G = p.num_q_heads / p.num_kv_heads;
   a.Lk = p.seq_len_kv;
+  a.Lq = p.seq_len_q;
+  a.causal = p.causal ? 1 : 0;
   a.num_groups = plan.num_groups;
   a.num_splits = plan.num_splits;
   a.split_keys = plan.split_keys;
@@ -212,6 +216,7 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   a.mask = p.mask;
   a.ms0 = p.mask_stride[0];
   a.ms1 = p.mask_stride[1];
+  a.ms2 = p.mask_stride[2];
   a.ws_o = ws_o;
   a.ws_lse = ws_lse;
   a.o = o;
@@ -243,8 +248,9 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   c.Hq = p.num_q_heads;
   c.num_splits = plan.num_splits;
   c.D = p.head_dim;
-  c.rows_per_head = 1;
-  return launch_combine(p.dtype, c, static_cast<unsigned>(p.batch) * p.num_q_heads, env.stream);
+  c.rows_per_head = p.seq_len_q;
+  return launch_combine(p.dtype, c,
+                        static_cast<unsigned>(p.batch) * p.num_q_heads * p.seq_len_q, env.stream);
 }
 
 sdpa_status_t launch_no_keys(const sdpa_params_t& p, void* o, float* lse, const LaunchEnv& env) {

@@ -1,4 +1,4 @@
-// decode_static.cu — allocation-free variant of the single-query (Lq == 1)
+// decode_static.cu — allocation-free variant of the vector (Lq <= 8)
 // split-KV decode: sdpa_forward_decode_noalloc.
 //
 // Who needs it: callers that cannot call cudaMalloc (or hand the library a

@@ -5,10 +5,13 @@
 // Selection follows the dispatch role of mlx 0.30.7
 // scaled_dot_product_attention.cpp (ScaledDotProductAttention::eval_gpu
 // chooses between a fused graph and the sdpa_vector kernel) without any
-// fallback: a single query row (Lq = 1) takes the split-KV vector path of MLX
-// PR #4459, every other shape takes the fused prefill kernel for its dtype,
-// and anything else is reported as unsupported (the force_fused admission
-// check of the same PR raises instead of falling back).
+// fallback: a single query row (Lq = 1), or a few (the rows of a kv head then
+// share its K/V stream: up to 2 at D = 64/128, where the tensor-core tiles
+// are ahead from 4 rows on, measured on GB300; up to 8 at D = 512, which has
+// no prefill kernel), takes the split-KV vector path of MLX PR #4459, every
+// other shape takes the fused prefill kernel for its dtype, and anything else
+// is reported as unsupported (the force_fused admission check of the same PR
+// raises instead of falling back).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -24,6 +27,8 @@ namespace {
 __device__ int g_status_word;
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxDecodeRows = 8;     // query rows per head of the vector path, D = 512
+constexpr int kMaxDecodeRowsTc = 2;   // the same where a tensor-core prefill exists
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::mutex g_dev_mutex;
@@ -52,8 +57,8 @@ sdpa_status_t validate_problem(const sdpa_params_t* p) {
   // cuDNN's bottom-right causal mask is undefined for Tq > Tkv (mlx 0.30.7
   // supports_sdpa_cudnn); the same rule holds here.
   if (p->causal && p->seq_len_q > p->seq_len_kv) return SDPA_ERR_UNSUPPORTED;
-  // head_dim 512 is served for single-query decode only.
-  if (p->head_dim == 512 && p->seq_len_q > 1) return SDPA_ERR_UNSUPPORTED;
+  // head_dim 512 is served by the vector path only (up to 8 query rows).
+  if (p->head_dim == 512 && p->seq_len_q > kMaxDecodeRows) return SDPA_ERR_UNSUPPORTED;
   return SDPA_OK;
 }
 
@@ -64,7 +69,8 @@ bool nothing_to_do(const sdpa_params_t* p) {
 sdpa_kernel_t pick(const sdpa_params_t* p) {
   if (nothing_to_do(p)) return SDPA_KERNEL_NONE;
   if (p->seq_len_kv == 0) return SDPA_KERNEL_NO_KEYS;
-  if (p->seq_len_q == 1) return SDPA_KERNEL_DECODE_SPLITKV;
+  if (p->seq_len_q <= (p->head_dim == 512 ? kMaxDecodeRows : kMaxDecodeRowsTc))
+    return SDPA_KERNEL_DECODE_SPLITKV;
   if (p->dtype == SDPA_F32)
     return p->head_dim == 64 ? SDPA_KERNEL_PREFILL_TC_F32 : SDPA_KERNEL_PREFILL_F32;
   return SDPA_KERNEL_PREFILL_TC;

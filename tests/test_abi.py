@@ -66,6 +66,10 @@ def P(**kw):
     (dict(dtype=S.SDPA_F32, D=128), "prefill_f32"),
     (dict(Lq=1), "decode_splitkv"),
     (dict(Lq=1, D=512, dtype=S.SDPA_F32), "decode_splitkv"),
+    (dict(Lq=2), "decode_splitkv"),
+    (dict(Lq=3), "prefill_tc"),
+    (dict(Lq=8, D=512, causal=True), "decode_splitkv"),
+    (dict(Lq=3, dtype=S.SDPA_F32), "prefill_tc_f32"),
     (dict(Lk=0), "no_keys"),
     (dict(Lq=1, Lk=0, D=512), "no_keys"),
     (dict(B=0), "none"),
@@ -87,7 +91,7 @@ def test_select_kernel(sdpa_lib, kw, kernel):
     (dict(scale=float("inf")), 1),
     (dict(D=96), 2),
     (dict(D=256), 2),
-    (dict(D=512, Lq=2), 2),
+    (dict(D=512, Lq=9), 2),
     (dict(Lq=64, Lk=32, causal=True), 2),
     (dict(Lq=(1 << 30) + 1), 2),
     (dict(mask=16, ms=(0, 0, 32, 2)), 1),

@@ -310,3 +310,42 @@ def test_host_entry_decode_against_oracle(cuda):
     assert S.sdpa_device_status() == 0
     o_ref, lse_ref = oracle_rows(w, inp, None)
     compare(w, o_h, l_h, o_ref, lse_ref, None)
+
+
+# ------------------------------------------------ few-query rows (Lq 2..8)
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("D", [64, 128, 512])
+@pytest.mark.parametrize("G,Lq", [(1, 2), (4, 2), (4, 3), (8, 8), (16, 4)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_query_vector_path(cuda, dtype, D, G, Lq, causal):
+    """A few query rows per head: the vector path (2 rows at D = 64/128, up to
+    8 at D = 512; the G x Lq rows of a kv head share its K/V stream) or the
+    prefill tiles for the rest; bottom-right causal rule per row."""
+    Hkv = 2
+    check(cuda, wl(2, Hkv * G, Hkv, Lq, 777, D, dtype, causal=causal, sinks=(G % 2 == 0)))
+
+
+@pytest.mark.parametrize("dtype", ["float16", "float32"])
+@pytest.mark.parametrize("mask", ["full", "row", "key"])
+def test_multi_query_mask(cuda, dtype, mask):
+    check(cuda, wl(2, 8, 2, 2, 300, 128, dtype, mask=mask, sinks=True, causal=True))
+    check(cuda, wl(2, 8, 2, 5, 300, 512, dtype, mask=mask, sinks=True, causal=True))
+
+
+def test_multi_query_fully_masked_rows(cuda):
+    import torch
+    w = wl(1, 4, 2, 6, 90, 512, "bfloat16", sinks=True)
+    inp = W.make_inputs(w)
+    m = torch.zeros((1, 4, 6, 90), dtype=inp["q"].dtype)
+    m[:, :, ::3, :] = float("-inf")  # every third row sees nothing
+    inp["mask"] = m
+    o_gpu, lse_gpu = run_gpu(torch, w, inp)
+    o_ref, lse_ref = oracle_rows(w, inp, None)
+    compare(w, o_gpu, lse_gpu, o_ref, lse_ref, None)
+
+
+@pytest.mark.parametrize("splits", [2, 16])
+def test_multi_query_forced_splits(cuda, splits, monkeypatch):
+    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", str(splits))
+    check(cuda, wl(1, 16, 2, 2, 3001, 128, "bfloat16", causal=True, sinks=True))
+    check(cuda, wl(1, 8, 1, 6, 3001, 512, "bfloat16", causal=True, sinks=True))
