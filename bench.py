@@ -136,6 +136,22 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(dist, secs, device):
+    """The slowest rank's time (every rank gets it); `dist` None = one rank."""
+    if dist is None:
+        return secs
+    import torch
+    t = torch.tensor([float(secs)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_step, steps, world, secs, scale):
+    """Throughput of the whole job: every rank runs `steps` steps of the same
+    work (replicas, weak scaling); `secs` is the slowest rank's time."""
+    return work_per_step * steps * world / secs / scale
+
+
 # ------------------------------------------------------------------ GPU arm
 def gpu_inputs(torch, w, copies, device):
     from scaled_dot_product_fwd_gb300 import workloads as W
@@ -178,9 +194,10 @@ def run_workload(torch, S, w, steps, warmup, device, stream, copies=None):
                        sinks=s["sinks"], out=outs[i], lse=lses[i])
 
     secs = time_device(torch, fn, len(sets), steps, warmup, stream)
+    launches = S.sdpa_last_launch_count()  # kernels per call, from the library
     if S.sdpa_device_status() != 0:
         raise RuntimeError("device status set during %s" % w.name)
-    return secs, copies, per
+    return secs, copies, per, launches
 
 
 def run_workload_graph(torch, S, w, calls, reps, device, copies=None):
@@ -289,7 +306,7 @@ def secondary(torch, S, device, stream, peaks):
     from scaled_dot_product_fwd_gb300 import workloads as W
     out = {}
     for w, steps in ((W.CAUSAL_GQA, 100), (W.DIT_F32, 20)):
-        secs, copies, _ = run_workload(torch, S, w, steps, 3, device, stream)
+        secs, copies, _, _ = run_workload(torch, S, w, steps, 3, device, stream)
         t = w.flops() * steps / secs / 1e12
         out[w.name] = {"value": round(t, 2), "unit": "TFLOP/s", "ms_per_call": secs / steps * 1e3,
                        "frac_of_bf16_peak": round(t / peaks["bf16_tflops"], 4)}
@@ -337,11 +354,10 @@ def gb300_arm(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        secs, copies, per = run_workload(torch, S, w, args.steps, args.warmup, device, stream)
+        secs, copies, per, per_call_launches = run_workload(torch, S, w, args.steps, args.warmup,
+                                                            device, stream)
+    secs = max_over_ranks(dist, secs, device)
     if dist is not None:
-        t = torch.tensor([secs], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
         dist.barrier()
     flops = w.flops()
     per_launch = secs / args.steps
@@ -354,17 +370,17 @@ def gb300_arm(args):
         bound, peak, peak_name = "hbm", peaks["hbm_gbs"], " (HBM copy)"
         sustained = peaks["hbm_gbs"]
         traffic = profile_traffic("decode_split_" + w.name, ["decode.cuh", "decode_combine.cu"])
-        launches = 2 * args.steps
     else:
         work, unit, scale = flops, "TFLOP/s", 1e12
         bound, peak, peak_name = "tensor", peaks["bf16_tflops"], " (bf16 dense, burst)"
         sustained = peaks["bf16_tflops_sustained"]
         kfile = "prefill_f32.cu" if w.dtype == "float32" else "prefill_tc.cu"
         traffic = profile_traffic(kfile[:-3] + "_" + w.name, [kfile, "ptx.cuh"])
-        launches = args.steps
-    value = work * args.steps * world / secs / scale
+    launches = per_call_launches * args.steps
+    value = whole_job_rate(work, args.steps, world, secs, scale)
     achieved = work / per_launch / scale
-    e2e_value = work * e2e_steps * world / e2e_secs / scale
+    e2e_secs = max_over_ranks(dist, e2e_secs, device)
+    e2e_value = whole_job_rate(work, e2e_steps, world, e2e_secs, scale)
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 5),

@@ -182,6 +182,16 @@ SDPA_API uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns);
 SDPA_API int sdpa_abi_version(void);
 
 /*
+ * sdpa_last_launch_count — number of kernels that the calling thread's last
+ * sdpa_forward or sdpa_forward_decode_noalloc call enqueued (0 if it
+ * returned an error or had nothing to compute): 1 for the prefill kernels
+ * and for a decode whose splits merge inside a thread-block cluster, 2 for
+ * the fp32 hi/lo prefill (split, then prefill) and the two-pass decode.
+ * Host function, no CUDA call.
+ */
+SDPA_API int sdpa_last_launch_count(void);
+
+/*
  * sdpa_forward_decode_noalloc — the vector path (decode) without a
  * caller workspace.  The pages have no counterpart: this entry point exists
  * for callers that cannot call cudaMalloc or pass device scratch where they

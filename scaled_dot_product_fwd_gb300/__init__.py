@@ -10,12 +10,14 @@ The work runs in the CUDA kernels of ``libsdpa_gb300.so`` (C ABI in
 from ._binding import (EXPORTS, KERNELS, LIB_PATH, SDPA_BF16, SDPA_F16, SDPA_F32, STATUS,
                        SdpaError, SdpaParams, dtype_code, load_library, make_params,
                        sdpa_abi_version, sdpa_debug_set_wait_limit_ns, sdpa_device_status,
+                       sdpa_last_launch_count,
                        sdpa_forward, sdpa_forward_host, sdpa_forward_raw, sdpa_select_kernel,
                        sdpa_status_string,
                        sdpa_workspace_size)
 
 __all__ = ["sdpa_forward", "sdpa_forward_host", "sdpa_forward_raw", "sdpa_workspace_size", "sdpa_select_kernel",
            "sdpa_status_string", "sdpa_device_status", "sdpa_debug_set_wait_limit_ns",
-           "sdpa_abi_version", "make_params", "SdpaParams", "SdpaError", "load_library",
+           "sdpa_abi_version", "sdpa_last_launch_count", "make_params", "SdpaParams", "SdpaError",
+           "load_library",
            "EXPORTS", "KERNELS", "STATUS", "LIB_PATH", "SDPA_F32", "SDPA_F16", "SDPA_BF16",
            "dtype_code"]

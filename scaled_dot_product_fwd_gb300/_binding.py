@@ -26,7 +26,7 @@ KERNELS = {0: "none", 1: "prefill_tc", 2: "prefill_f32", 3: "decode_splitkv", 4:
 # Every symbol include/sdpa.h declares.
 EXPORTS = ("sdpa_workspace_size", "sdpa_select_kernel", "sdpa_forward", "sdpa_status_string",
            "sdpa_device_status", "sdpa_debug_set_wait_limit_ns", "sdpa_abi_version",
-           "sdpa_forward_decode_noalloc")
+           "sdpa_forward_decode_noalloc", "sdpa_last_launch_count")
 
 
 class SdpaParams(ctypes.Structure):
@@ -74,6 +74,7 @@ def load_library(path: str = LIB_PATH):
             lib.sdpa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             lib.sdpa_debug_set_wait_limit_ns.restype = ctypes.c_uint64
             lib.sdpa_abi_version.restype = ctypes.c_int
+            lib.sdpa_last_launch_count.restype = ctypes.c_int
             lib.sdpa_forward_decode_noalloc.argtypes = [P] + [ctypes.c_void_p] * 6
             lib.sdpa_forward_decode_noalloc.restype = ctypes.c_int
             _lib = lib
@@ -135,6 +136,11 @@ def sdpa_debug_set_wait_limit_ns(ns: int) -> int:
 
 def sdpa_abi_version() -> int:
     return int(load_library().sdpa_abi_version())
+
+
+def sdpa_last_launch_count() -> int:
+    """Kernels enqueued by this thread's last sdpa_forward call (C ABI)."""
+    return int(load_library().sdpa_last_launch_count())
 
 
 # ----------------------------------------------------------------- torch layer

@@ -238,7 +238,11 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
     case SDPA_BF16: st = dec::launch_split_bf16(a, D, hg, p.batch, env.stream, &merged); break;
     default: return SDPA_ERR_UNSUPPORTED;
   }
-  if (st != SDPA_OK || merged) return st;
+  if (st != SDPA_OK) return st;
+  if (merged) {
+    set_last_launches(1);
+    return SDPA_OK;
+  }
   dec::CombineArgs c;
   c.ws_o = ws_o;
   c.ws_lse = ws_lse;
@@ -249,8 +253,10 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   c.num_splits = plan.num_splits;
   c.D = p.head_dim;
   c.rows_per_head = p.seq_len_q;
-  return launch_combine(p.dtype, c,
-                        static_cast<unsigned>(p.batch) * p.num_q_heads * p.seq_len_q, env.stream);
+  st = launch_combine(p.dtype, c, static_cast<unsigned>(p.batch) * p.num_q_heads * p.seq_len_q,
+                      env.stream);
+  if (st == SDPA_OK) set_last_launches(2);
+  return st;
 }
 
 sdpa_status_t launch_no_keys(const sdpa_params_t& p, void* o, float* lse, const LaunchEnv& env) {

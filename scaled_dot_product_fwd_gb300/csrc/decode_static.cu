@@ -71,6 +71,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 extern "C" sdpa_status_t sdpa_forward_decode_noalloc(const sdpa_params_t* p, const void* q,
                                                      const void* k, const void* v, void* o,
                                                      float* lse, void* stream) {
+  gb300::set_last_launches(0);
   sdpa_status_t st = SDPA_OK;
   const sdpa_kernel_t kern = sdpa_select_kernel(p, &st);
   if (st != SDPA_OK) return st;

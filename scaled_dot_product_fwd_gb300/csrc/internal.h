@@ -38,6 +38,8 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);
 // and the current bound on device-side waits; both owned by sdpa_api.cu.
 int* status_word_current_device();
 uint64_t current_wait_limit_ns();
+// Kernels enqueued by the calling thread's last call (sdpa_last_launch_count).
+void set_last_launches(int n);
 
 sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const void* k,
                                 const void* v, void* o, float* lse, const LaunchEnv& env);

@@ -31,6 +31,7 @@ constexpr int kMaxDecodeRows = 8;     // query rows per head of the vector path,
 constexpr int kMaxDecodeRowsTc = 2;   // the same where a tensor-core prefill exists
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+thread_local int g_last_launches = 0;
 std::mutex g_dev_mutex;
 int* g_status_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
@@ -116,6 +117,8 @@ int* status_word_current_device() {
 
 uint64_t current_wait_limit_ns() { return g_wait_ns.load(); }
 
+void set_last_launches(int n) { g_last_launches = n; }
+
 }  // namespace gb300
 
 extern "C" {
@@ -150,6 +153,8 @@ size_t sdpa_workspace_size(const sdpa_params_t* params) {
   return plan.workspace;
 }
 
+int sdpa_last_launch_count(void) { return g_last_launches; }
+
 uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns) {
   return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns);
 }
@@ -157,6 +162,7 @@ uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns) {
 sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k, const void* v,
                            void* o, float* lse, void* workspace, size_t workspace_bytes,
                            void* stream) {
+  g_last_launches = 0;
   sdpa_status_t st = validate_problem(p);
   if (st != SDPA_OK) return st;
   if (nothing_to_do(p)) return SDPA_OK;
@@ -192,15 +198,23 @@ sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k,
   env.stream = static_cast<cudaStream_t>(stream);
   switch (kern) {
     case SDPA_KERNEL_PREFILL_TC:
-      return gb300::launch_prefill_tc(*p, q, k, v, o, lse, env);
+      st = gb300::launch_prefill_tc(*p, q, k, v, o, lse, env);
+      if (st == SDPA_OK) g_last_launches = 1;
+      return st;
     case SDPA_KERNEL_PREFILL_F32:
-      return gb300::launch_prefill_f32(*p, q, k, v, o, lse, env);
-    case SDPA_KERNEL_PREFILL_TC_F32:
-      return gb300::launch_prefill_x3(*p, q, k, v, o, lse, workspace, env);
-    case SDPA_KERNEL_DECODE_SPLITKV:
+      st = gb300::launch_prefill_f32(*p, q, k, v, o, lse, env);
+      if (st == SDPA_OK) g_last_launches = 1;
+      return st;
+    case SDPA_KERNEL_PREFILL_TC_F32:  // hi/lo split, then the prefill kernel
+      st = gb300::launch_prefill_x3(*p, q, k, v, o, lse, workspace, env);
+      if (st == SDPA_OK) g_last_launches = 2;
+      return st;
+    case SDPA_KERNEL_DECODE_SPLITKV:  // sets the count itself (1 or 2 kernels)
       return gb300::launch_decode(*p, plan, q, k, v, o, lse, workspace, env);
     case SDPA_KERNEL_NO_KEYS:
-      return gb300::launch_no_keys(*p, o, lse, env);
+      st = gb300::launch_no_keys(*p, o, lse, env);
+      if (st == SDPA_OK) g_last_launches = 1;
+      return st;
     default:
       return SDPA_ERR_UNSUPPORTED;
   }

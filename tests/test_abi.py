@@ -43,6 +43,11 @@ def test_params_struct_layout():
     assert B.SdpaParams.sinks.offset == 80
 
 
+def test_launch_count_is_zero_after_a_rejected_call(sdpa_lib):
+    assert S.sdpa_forward_raw(P(D=96), 256, 256, 256, 256, None, None, 0, None) == 2
+    assert S.sdpa_last_launch_count() == 0
+
+
 def test_abi_version_and_status_strings(sdpa_lib):
     assert S.sdpa_abi_version() == 1
     assert S.sdpa_status_string(0) == "ok"

@@ -349,3 +349,33 @@ def test_multi_query_forced_splits(cuda, splits, monkeypatch):
     monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", str(splits))
     check(cuda, wl(1, 16, 2, 2, 3001, 128, "bfloat16", causal=True, sinks=True))
     check(cuda, wl(1, 8, 1, 6, 3001, 512, "bfloat16", causal=True, sinks=True))
+
+
+def test_launch_count_reports_kernels_per_call(cuda, monkeypatch):
+    """sdpa_last_launch_count: 1 for prefill, 2 for the fp32 hi/lo prefill
+    (split + prefill), 1 or 2 for decode (in-cluster merge or combine pass),
+    1 for no keys, 0 after an error or an empty problem."""
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+
+    def run(w, **kw):
+        inp = W.make_inputs(w)
+        q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+        S.sdpa_forward(q, k, v, scale=w.scale, causal=w.causal, **kw)
+        torch.cuda.synchronize()
+        return S.sdpa_last_launch_count()
+
+    assert run(wl(1, 2, 2, 300, 300, 64, "float16")) == 1
+    assert run(wl(1, 2, 2, 300, 300, 64, "float32")) == 2
+    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", "4")
+    assert run(wl(1, 8, 1, 1, 4096, 128, "bfloat16")) == 1  # 4 CTAs per cluster
+    monkeypatch.setenv("GB300_SDPA_DECODE_CLUSTER", "0")
+    assert run(wl(1, 8, 1, 1, 4096, 128, "bfloat16")) == 2
+    monkeypatch.delenv("GB300_SDPA_DECODE_CLUSTER")
+    monkeypatch.delenv("GB300_SDPA_DECODE_SPLITS")
+    q = torch.zeros(1, 2, 4, 64, device="cuda", dtype=torch.float16)
+    kk = torch.zeros(1, 2, 0, 64, device="cuda", dtype=torch.float16)
+    S.sdpa_forward(q, kk, kk)
+    assert S.sdpa_last_launch_count() == 1
+    S.sdpa_forward(q[:0], q[:0], q[:0])
+    assert S.sdpa_last_launch_count() == 0
