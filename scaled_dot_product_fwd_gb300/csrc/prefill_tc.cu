@@ -50,8 +50,9 @@ constexpr int NQ = 2;    // query tiles per CTA
 constexpr int kSoftmaxWarps = 4 * NQ;
 constexpr int kLoadWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
-// warps 8-11 form the control warpgroup (producer, MMA issuer, two idle
-// warps); it gives registers to the softmax warpgroups with setmaxnreg.
+// warps 8-11 form the control warpgroup (producer, MMA issuer, stage
+// helper, one idle warp); it gives registers to the softmax warpgroups with
+// setmaxnreg (launch: 384 x 168 = 256 x 224 + 128 x 56).
 constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
 constexpr uint32_t kSoftmaxRegs = 224;
 constexpr uint32_t kControlRegs = 56;
@@ -561,15 +562,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
               const float mu = (m == -INFINITY) ? 0.f : m;
+              if (pass > 0) tmem_wait_st();  // the first pass's P is overwritten
               float rs0, rs1;
-              softmax_pairs<BF16, BN / 2, true>(*reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[0]),
-                                               mul, mu, *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[0]),
-                                               rs0, &pk2[0]);
+              softmax_pairs<BF16, BN / 2, true>(
+                  *reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[0]), mul, mu,
+                  *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[0]), rs0, &pk2[0]);
               tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
               tmem_st32(tS + BN / 2, *reinterpret_cast<uint32_t(*)[32]>(&pk2[0]));
-              softmax_pairs<BF16, BN / 2, true>(*reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[BN / 2]),
-                                               mul, mu, *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[BN / 4]),
-                                               rs1, &pk2[BN / 4]);
+              softmax_pairs<BF16, BN / 2, true>(
+                  *reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[BN / 2]), mul, mu,
+                  *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[BN / 4]), rs1, &pk2[BN / 4]);
               tmem_st32(tS + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk[BN / 4]));
               tmem_st32(tS + BN / 2 + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk2[BN / 4]));
               rs = rs0 + rs1;
@@ -815,6 +817,18 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   a.status = env.status;
   a.wait_ns = env.wait_limit_ns;
   auto kern = prefill_tc_kernel<D, BF16, X3>;
+  // The setmaxnreg split must fit the registers the kernel is launched with
+  // (an increase beyond them would wait forever): check the compiled count
+  // once per instantiation.
+  static int regs_ok = 0;  // 0 unknown, 1 fits, -1 does not
+  if (regs_ok == 0) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SDPA_ERR_CUDA;
+    const long alloc = static_cast<long>((fa.numRegs + 7) & ~7) * kThreads;
+    const long need = 32L * (kSoftmaxWarps * static_cast<long>(kSoftmaxRegs) + 4L * kControlRegs);
+    regs_ok = alloc >= need ? 1 : -1;
+  }
+  if (regs_ok < 0) return SDPA_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return SDPA_ERR_CUDA;
