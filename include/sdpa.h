@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define SDPA_ABI_VERSION 1
+#define SDPA_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define SDPA_API __attribute__((visibility("default")))
@@ -108,6 +108,21 @@ typedef enum {
  *  sinks: NULL or float32 [Hq]: one extra logit per query head that enters
  *      the softmax denominator only (a key with a zero value row).  It is
  *      not multiplied by scale and not masked.
+ *  kv_capacity: 0, or the number of rows per (batch, kv head) that k and v
+ *      hold (>= seq_len_kv): k and v are then [B, Hkv, kv_capacity, D], a
+ *      fixed-capacity KV cache of which rows [0, seq_len_kv) are used (the
+ *      rest is never read into a result).  0 means kv_capacity = seq_len_kv.
+ *  seq_lens_q, seq_lens_kv: NULL, or DEVICE int32 [B] arrays of per-batch
+ *      lengths (padding masks): batch b uses query rows [0, seq_lens_q[b])
+ *      and keys [0, seq_lens_kv[b]) (values are clamped to [0, seq_len_q]
+ *      and [0, seq_len_kv]); query rows at or past its length see no key
+ *      (o = 0, lse = -inf or the sink), and the bottom-right causal rule
+ *      uses the batch's own lengths: key j visible to query i iff
+ *      j <= i + (seq_lens_kv[b] - seq_lens_q[b]).  Both arrays must stay
+ *      valid until the call's kernels have run.  The prefill kernels load
+ *      whole key tiles, so v rows [seq_lens_kv[b], seq_len_kv) meet zero
+ *      weights there and must hold finite values (rows past seq_len_kv are
+ *      never read).
  */
 typedef struct {
   int32_t batch;
@@ -123,6 +138,10 @@ typedef struct {
   const void* mask;
   int64_t mask_stride[4];
   const float* sinks;
+  int32_t kv_capacity;          /* ABI 2 */
+  int32_t reserved1;
+  const int32_t* seq_lens_q;    /* ABI 2 */
+  const int32_t* seq_lens_kv;   /* ABI 2 */
 } sdpa_params_t;
 
 /*

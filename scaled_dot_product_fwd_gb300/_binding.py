@@ -37,7 +37,9 @@ class SdpaParams(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("causal", ctypes.c_int32), ("reserved0", ctypes.c_int32),
                 ("mask", ctypes.c_void_p), ("mask_stride", ctypes.c_int64 * 4),
-                ("sinks", ctypes.c_void_p)]
+                ("sinks", ctypes.c_void_p), ("kv_capacity", ctypes.c_int32),
+                ("reserved1", ctypes.c_int32), ("seq_lens_q", ctypes.c_void_p),
+                ("seq_lens_kv", ctypes.c_void_p)]
 
 
 class SdpaError(RuntimeError):
@@ -82,7 +84,8 @@ def load_library(path: str = LIB_PATH):
 
 
 def make_params(B, Hq, Hkv, Lq, Lk, D, dtype, scale, causal=False, mask_ptr=None,
-                mask_stride=(0, 0, 0, 1), sinks_ptr=None) -> SdpaParams:
+                mask_stride=(0, 0, 0, 1), sinks_ptr=None, kv_capacity=0, seq_lens_q_ptr=None,
+                seq_lens_kv_ptr=None) -> SdpaParams:
     p = SdpaParams()
     p.batch, p.num_q_heads, p.num_kv_heads = int(B), int(Hq), int(Hkv)
     p.seq_len_q, p.seq_len_kv, p.head_dim = int(Lq), int(Lk), int(D)
@@ -94,6 +97,10 @@ def make_params(B, Hq, Hkv, Lq, Lk, D, dtype, scale, causal=False, mask_ptr=None
     for i in range(4):
         p.mask_stride[i] = int(mask_stride[i])
     p.sinks = sinks_ptr
+    p.kv_capacity = int(kv_capacity)
+    p.reserved1 = 0
+    p.seq_lens_q = seq_lens_q_ptr
+    p.seq_lens_kv = seq_lens_kv_ptr
     return p
 
 
@@ -171,13 +178,18 @@ def _workspace(nbytes: int, device):
 
 
 def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=None,
-                 lse=None, return_lse=True, workspace=None, stream=None):
+                 lse=None, return_lse=True, workspace=None, stream=None, kv_len=None,
+                 seq_lens_q=None, seq_lens_kv=None):
     """O (and LSE) of softmax(scale * q k^T + mask [+ sinks]) v on the GPU.
 
-    q [B, Hq, Lq, D], k/v [B, Hkv, Lk, D]: contiguous CUDA tensors of one
-    dtype (float32, float16 or bfloat16).  mask: None or a tensor of q's dtype
-    broadcastable to [B, Hq, Lq, Lk] (additive).  sinks: None or float32 [Hq].
-    scale defaults to 1/sqrt(D).  Returns (o, lse) or o.
+    q [B, Hq, Lq, D], k/v [B, Hkv, C, D]: contiguous CUDA tensors of one
+    dtype (float32, float16 or bfloat16).  The keys are rows [0, Lk) of k and
+    v, Lk = kv_len (default C: with kv_len < C, k and v are a fixed-capacity
+    KV cache).  mask: None or a tensor of q's dtype broadcastable to
+    [B, Hq, Lq, Lk] (additive).  sinks: None or float32 [Hq].  seq_lens_q,
+    seq_lens_kv: None or int32 CUDA tensors [B] of per-batch lengths (padding
+    masks; rows past a batch's query length see no key).  scale defaults to
+    1/sqrt(D).  Returns (o, lse) or o.
     """
     torch = _torch()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -190,7 +202,21 @@ def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=N
     if q.dtype != k.dtype or q.dtype != v.dtype:
         raise TypeError("q, k, v must share a dtype")
     B, Hq, Lq, D = q.shape
-    _, Hkv, Lk, _ = k.shape
+    _, Hkv, cap, _ = k.shape
+    if v.shape != k.shape:
+        raise ValueError("k and v must have one shape")
+    Lk = cap if kv_len is None else int(kv_len)
+    if Lk < 0 or Lk > cap:
+        raise ValueError("kv_len must be within [0, k.shape[2]]")
+    lens = []
+    for t in (seq_lens_q, seq_lens_kv):
+        if t is not None:
+            if t.dtype != torch.int32 or not t.is_cuda or t.numel() != B or not t.is_contiguous():
+                raise TypeError("seq_lens_q / seq_lens_kv must be contiguous int32 CUDA "
+                                "tensors with B elements")
+            lens.append(t.data_ptr())
+        else:
+            lens.append(None)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     dt = dtype_code(q.dtype)
@@ -209,7 +235,9 @@ def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=N
             raise TypeError("sinks must be a float32 CUDA tensor with Hq elements")
         sinks = sinks.contiguous()
         sinks_ptr = sinks.data_ptr()
-    params = make_params(B, Hq, Hkv, Lq, Lk, D, dt, scale, causal, mask_ptr, mstride, sinks_ptr)
+    params = make_params(B, Hq, Hkv, Lq, Lk, D, dt, scale, causal, mask_ptr, mstride, sinks_ptr,
+                         kv_capacity=cap if cap != Lk else 0, seq_lens_q_ptr=lens[0],
+                         seq_lens_kv_ptr=lens[1])
     if out is None:
         out = torch.empty((B, Hq, Lq, D), dtype=q.dtype, device=q.device)
     if lse is None and return_lse:

@@ -53,6 +53,9 @@ struct SplitArgs {
   int Hq, Hkv, G, Lk;
   int Lq;           // query rows per head (1 for decode, up to 8 for multi-query)
   int causal;       // bottom-right: key j visible to row i iff j <= i + Lk - Lq
+  int kv_cap;       // rows per (batch, kv head) in k and v (>= Lk)
+  const int* seq_lens_q;   // nullptr or per-batch valid query rows
+  const int* seq_lens_kv;  // nullptr or per-batch valid keys
   int num_groups;   // groups of HG query rows per kv head (rows: G heads x Lq)
   int num_splits;
   int split_keys;
@@ -272,8 +275,11 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   const int kvh = blockIdx.y / a.num_groups;
   const int grp = blockIdx.y % a.num_groups;
   const int b = blockIdx.z;
+  // this batch's lengths (padding masks), clamped to the call's maxima
+  const int Lkb = a.seq_lens_kv ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
+  const int Lqb = a.seq_lens_q ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
   const int key_begin = split * a.split_keys;
-  const int key_end = min(a.Lk, key_begin + a.split_keys);
+  const int key_end = min(Lkb, key_begin + a.split_keys);
   const int nkeys = max(0, key_end - key_begin);
   const int ntiles = (nkeys + C::TK - 1) / C::TK;
 
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   __syncthreads();
   const WaitCtl wc{a.wait_ns, abort_flag, a.status};
 
-  const size_t kv_row0 = (static_cast<size_t>(b) * a.Hkv + kvh) * a.Lk;
+  const size_t kv_row0 = (static_cast<size_t>(b) * a.Hkv + kvh) * a.kv_cap;
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     int last_use[8];  // last fill of each stage (-1: none)
@@ -355,8 +361,9 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   const int my_hq = kvh * a.G + (my_head_ok ? my_rr / a.Lq : 0);
   const int my_qi = my_head_ok ? my_rr % a.Lq : 0;
   // last key this lane's row sees (bounds, and the causal rule)
-  int my_limit = a.Lk - 1;
-  if (a.causal) my_limit = min(my_limit, my_qi + (a.Lk - a.Lq));
+  int my_limit = Lkb - 1;
+  if (a.causal) my_limit = min(my_limit, my_qi + (Lkb - Lqb));
+  if (my_qi >= Lqb) my_limit = -1;  // a padding row sees no key
   const T* mrow = nullptr;
   if (a.mask && my_head_ok)
     mrow = static_cast<const T*>(a.mask) + b * a.ms0 + my_hq * a.ms1 + my_qi * a.ms2;

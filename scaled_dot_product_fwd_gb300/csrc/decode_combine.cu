@@ -207,6 +207,9 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   a.G = p.num_q_heads / p.num_kv_heads;
   a.Lk = p.seq_len_kv;
   a.Lq = p.seq_len_q;
+  a.kv_cap = p.kv_capacity > 0 ? p.kv_capacity : p.seq_len_kv;
+  a.seq_lens_q = p.seq_lens_q;
+  a.seq_lens_kv = p.seq_lens_kv;
   a.causal = p.causal ? 1 : 0;
   a.num_groups = plan.num_groups;
   a.num_splits = plan.num_splits;

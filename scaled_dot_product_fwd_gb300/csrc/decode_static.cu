@@ -83,6 +83,9 @@ extern "C" sdpa_status_t sdpa_forward_decode_noalloc(const sdpa_params_t* p, con
   if (p->mask && !aligned(p->mask, 16)) return SDPA_ERR_MISALIGNED;
   if (lse && !aligned(lse, 4)) return SDPA_ERR_MISALIGNED;
   if (p->sinks && !aligned(p->sinks, 4)) return SDPA_ERR_MISALIGNED;
+  if ((p->seq_lens_q && !aligned(p->seq_lens_q, 4)) ||
+      (p->seq_lens_kv && !aligned(p->seq_lens_kv, 4)))
+    return SDPA_ERR_MISALIGNED;
   void* scratch = nullptr;
   int num_sms = 0;
   st = setup_device(&scratch, &num_sms);

@@ -38,6 +38,9 @@ struct F32Args {
   const float* mask;
   long long ms0, ms1, ms2;
   const float* sinks;
+  int kv_cap;              // rows per (batch, kv head) in k and v (>= Lk)
+  const int* seq_lens_q;   // nullptr or per-batch valid query rows
+  const int* seq_lens_kv;  // nullptr or per-batch valid keys
 };
 
 template <int D>
@@ -68,8 +71,11 @@ __global__ void __launch_bounds__(kF32Threads) prefill_f32_kernel(const F32Args 
   const int kvh = h / a.G;
   const int q0 = qb * FBM;
   const float* qbase = a.q + ((static_cast<size_t>(b) * a.Hq + h) * a.Lq) * D;
-  const float* kbase = a.k + ((static_cast<size_t>(b) * a.Hkv + kvh) * a.Lk) * D;
-  const float* vbase = a.v + ((static_cast<size_t>(b) * a.Hkv + kvh) * a.Lk) * D;
+  const float* kbase = a.k + ((static_cast<size_t>(b) * a.Hkv + kvh) * a.kv_cap) * D;
+  const float* vbase = a.v + ((static_cast<size_t>(b) * a.Hkv + kvh) * a.kv_cap) * D;
+  // this batch's lengths (padding masks), clamped to the call's maxima
+  const int Lkb = a.seq_lens_kv ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
+  const int Lqb = a.seq_lens_q ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
 
   // Q tile (rows beyond Lq read as zero)
   for (int e = tid; e < FBM * D / 4; e += kF32Threads) {
@@ -84,14 +90,15 @@ __global__ void __launch_bounds__(kF32Threads) prefill_f32_kernel(const F32Args 
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     qrow[i] = q0 + ty * 4 + i;
-    limit[i] = a.Lk - 1;
-    if (a.causal) limit[i] = min(limit[i], qrow[i] + (a.Lk - a.Lq));
+    limit[i] = Lkb - 1;
+    if (a.causal) limit[i] = min(limit[i], qrow[i] + (Lkb - Lqb));
+    if (qrow[i] >= Lqb) limit[i] = -1;  // a padding row sees no key
     mrow[i] = (a.mask && qrow[i] < a.Lq) ? a.mask + b * a.ms0 + h * a.ms1 + qrow[i] * a.ms2
                                           : nullptr;
   }
   // keys needed by the block: up to the last visible key of its last row
-  int kend = a.Lk;
-  if (a.causal) kend = min(a.Lk, min(q0 + FBM, a.Lq) - 1 + (a.Lk - a.Lq) + 1);
+  int kend = q0 < Lqb ? Lkb : 0;
+  if (a.causal) kend = min(kend, min(q0 + FBM, Lqb) - 1 + (Lkb - Lqb) + 1);
   const int ntiles = kend > 0 ? (kend + FBN - 1) / FBN : 0;
 
   constexpr int OC = D / 64;  // float4 column groups per thread in O
@@ -115,7 +122,7 @@ __global__ void __launch_bounds__(kF32Threads) prefill_f32_kernel(const F32Args 
     for (int e = tid; e < FBN * D / 4; e += kF32Threads) {
       const int r = e / (D / 4), c4 = e % (D / 4);
       float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-      if (k0 + r < a.Lk) {
+      if (k0 + r < Lkb) {  // keys past the batch's length are never read
         kv = reinterpret_cast<const float4*>(kbase + static_cast<size_t>(k0 + r) * D)[c4];
         vv = reinterpret_cast<const float4*>(vbase + static_cast<size_t>(k0 + r) * D)[c4];
       }
@@ -261,6 +268,9 @@ sdpa_status_t launch_f32_impl(const sdpa_params_t& p, const void* q, const void*
   a.ms1 = p.mask_stride[1];
   a.ms2 = p.mask_stride[2];
   a.sinks = p.sinks;
+  a.kv_cap = p.kv_capacity > 0 ? p.kv_capacity : p.seq_len_kv;
+  a.seq_lens_q = p.seq_lens_q;
+  a.seq_lens_kv = p.seq_lens_kv;
   auto kern = prefill_f32_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            F32Cfg<D>::SMEM) != cudaSuccess)

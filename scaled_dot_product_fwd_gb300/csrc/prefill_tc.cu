@@ -105,6 +105,8 @@ struct PrefillArgs {
   float* lse;
   int* status;
   unsigned long long wait_ns;
+  const int* seq_lens_q;   // nullptr or per-batch valid query rows
+  const int* seq_lens_kv;  // nullptr or per-batch valid keys
 };
 
 template <bool BF16>
@@ -276,16 +278,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m0 = qb * (BM * NQ);
   const int nt = min(NQ, (a.Lq - m0 + BM - 1) / BM);  // active query tiles (>= 1)
   const int kvh = h / a.G;
-  const int nkv_all = (a.Lk + BN - 1) / BN;
+  // this batch's lengths (padding masks), clamped to the call's maxima; rows
+  // at or past Lqb see no key
+  const int Lkb = a.seq_lens_kv ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
+  const int Lqb = a.seq_lens_q ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
+  const int nkv_all = (Lkb + BN - 1) / BN;
   int nkv[NQ];
   int nmax = 0;
 #pragma unroll
   for (int t = 0; t < NQ; ++t) {
     int n = 0;
-    if (t < nt) {
-      const int last_row = min(m0 + t * BM + BM - 1, a.Lq - 1);
+    const int last_row = min(m0 + t * BM + BM - 1, Lqb - 1);  // last row that sees keys
+    if (t < nt && last_row >= m0 + t * BM) {
       if (a.causal) {
-        const int lim = last_row + (a.Lk - a.Lq);  // last key visible to the tile
+        const int lim = last_row + (Lkb - Lqb);  // last key visible to the tile
         n = lim < 0 ? 0 : min(nkv_all, lim / BN + 1);
       } else {
         n = nkv_all;
@@ -490,8 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + C::s_col(t);
     const uint32_t tO = tmem + lane_off + C::o_col(t);
     // last key visible to this row (bounds and causal)
-    int limit = a.Lk - 1;
-    if (a.causal) limit = min(limit, qi + (a.Lk - a.Lq));
+    int limit = Lkb - 1;
+    if (a.causal) limit = min(limit, qi + (Lkb - Lqb));
+    if (qi >= Lqb) limit = -1;  // a padding row sees no key
     const T* mrow = nullptr;
     if (a.mask && row_ok)
       mrow = static_cast<const T*>(a.mask) + b * a.ms0 + h * a.ms1 + qi * a.ms2;
@@ -743,12 +750,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Split of fp32 inputs into bf16 hi and lo parts (x = hi + lo + O(2^-16 |x|)),
-// for up to three tensors in one launch (n4 = elements / 4 of each).
+// for up to three tensors in one launch.  Tensor s has n4[s] float4 groups
+// in its compact output, planes of plane4[s] groups that start src_plane4[s]
+// groups apart in the input (a KV cache keeps more rows than it uses).
 struct SplitJob {
   const float* x[3];
   __nv_bfloat16* hi[3];
   __nv_bfloat16* lo[3];
   size_t n4[3];
+  size_t plane4[3];
+  size_t src_plane4[3];
 };
 
 __global__ void __launch_bounds__(256) split_bf16_kernel(const SplitJob job) {
@@ -758,7 +769,8 @@ __global__ void __launch_bounds__(256) split_bf16_kernel(const SplitJob job) {
     uint2* lo = reinterpret_cast<uint2*>(job.lo[s]);
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < job.n4[s];
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-      const float4 v = x[i];
+      const size_t plane = i / job.plane4[s];
+      const float4 v = x[plane * job.src_plane4[s] + (i - plane * job.plane4[s])];
       const uint32_t h01 = Elem<true>::pack(v.x, v.y);
       const uint32_t h23 = Elem<true>::pack(v.z, v.w);
       const uint32_t l01 = Elem<true>::pack(v.x - __uint_as_float(h01 << 16),
@@ -773,25 +785,29 @@ __global__ void __launch_bounds__(256) split_bf16_kernel(const SplitJob job) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// kv_plane_rows: rows per (batch, kv head) in k, v, k2, v2 as passed here
 template <int D, bool BF16, bool X3>
 sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, const void* v,
                           const void* q2, const void* k2, const void* v2, void* o, float* lse,
-                          const LaunchEnv& env) {
+                          uint64_t kv_plane_rows, const LaunchEnv& env) {
   using C = Cfg<D, X3>;
   const CUtensorMapDataType dt =
       BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const uint64_t qz = static_cast<uint64_t>(p.batch) * p.num_q_heads;
   const uint64_t kz = static_cast<uint64_t>(p.batch) * p.num_kv_heads;
+  // k, v rows per (batch, kv head) may exceed seq_len_kv (a KV cache); the
+  // maps stop at seq_len_kv, so rows past it read as zero and are never loaded
+  const uint64_t cap = kv_plane_rows;
   CUtensorMap tq, tk, tv, tq2, tk2, tv2;
   // [B*H, L, D] viewed innermost-first; box 64 x 128 rows, 128-byte swizzle.
   if (!encode_tiled_3d(&tq, dt, q, D, p.seq_len_q, qz, 2, 64, BM) ||
-      !encode_tiled_3d(&tk, dt, k, D, p.seq_len_kv, kz, 2, 64, BN) ||
-      !encode_tiled_3d(&tv, dt, v, D, p.seq_len_kv, kz, 2, 64, BN))
+      !encode_tiled_3d(&tk, dt, k, D, p.seq_len_kv, kz, 2, 64, BN, cap) ||
+      !encode_tiled_3d(&tv, dt, v, D, p.seq_len_kv, kz, 2, 64, BN, cap))
     return SDPA_ERR_CUDA;
   if (X3) {
     if (!encode_tiled_3d(&tq2, dt, q2, D, p.seq_len_q, qz, 2, 64, BM) ||
-        !encode_tiled_3d(&tk2, dt, k2, D, p.seq_len_kv, kz, 2, 64, BN) ||
-        !encode_tiled_3d(&tv2, dt, v2, D, p.seq_len_kv, kz, 2, 64, BN))
+        !encode_tiled_3d(&tk2, dt, k2, D, p.seq_len_kv, kz, 2, 64, BN, cap) ||
+        !encode_tiled_3d(&tv2, dt, v2, D, p.seq_len_kv, kz, 2, 64, BN, cap))
       return SDPA_ERR_CUDA;
   } else {
     tq2 = tq;
@@ -816,6 +832,8 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   a.lse = lse;
   a.status = env.status;
   a.wait_ns = env.wait_limit_ns;
+  a.seq_lens_q = p.seq_lens_q;
+  a.seq_lens_kv = p.seq_lens_kv;
   auto kern = prefill_tc_kernel<D, BF16, X3>;
   // The setmaxnreg split must fit the registers the kernel is launched with
   // (an increase beyond them would wait forever): check the compiled count
@@ -842,12 +860,13 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
 sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const void* k,
                                 const void* v, void* o, float* lse, const LaunchEnv& env) {
   const bool bf16 = p.dtype == SDPA_BF16;
+  const uint64_t cap = p.kv_capacity > 0 ? p.kv_capacity : p.seq_len_kv;
   if (p.head_dim == 64)
-    return bf16 ? launch_impl<64, true, false>(p, q, k, v, q, k, v, o, lse, env)
-                : launch_impl<64, false, false>(p, q, k, v, q, k, v, o, lse, env);
+    return bf16 ? launch_impl<64, true, false>(p, q, k, v, q, k, v, o, lse, cap, env)
+                : launch_impl<64, false, false>(p, q, k, v, q, k, v, o, lse, cap, env);
   if (p.head_dim == 128)
-    return bf16 ? launch_impl<128, true, false>(p, q, k, v, q, k, v, o, lse, env)
-                : launch_impl<128, false, false>(p, q, k, v, q, k, v, o, lse, env);
+    return bf16 ? launch_impl<128, true, false>(p, q, k, v, q, k, v, o, lse, cap, env)
+                : launch_impl<128, false, false>(p, q, k, v, q, k, v, o, lse, cap, env);
   return SDPA_ERR_UNSUPPORTED;
 }
 
@@ -862,7 +881,9 @@ sdpa_status_t launch_prefill_x3(const sdpa_params_t& p, const void* q, const voi
                                 const LaunchEnv& env) {
   if (p.head_dim != 64) return SDPA_ERR_UNSUPPORTED;
   const size_t nq = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * p.head_dim;
+  // compact hi/lo copies of the used rows [0, seq_len_kv) of k and v
   const size_t nk = static_cast<size_t>(p.batch) * p.num_kv_heads * p.seq_len_kv * p.head_dim;
+  const size_t cap = p.kv_capacity > 0 ? p.kv_capacity : p.seq_len_kv;
   uint8_t* w = static_cast<uint8_t*>(workspace);
   __nv_bfloat16* qh = reinterpret_cast<__nv_bfloat16*>(w);
   __nv_bfloat16* ql = reinterpret_cast<__nv_bfloat16*>(w + align256(nq * 2));
@@ -885,9 +906,13 @@ sdpa_status_t launch_prefill_x3(const sdpa_params_t& p, const void* q, const voi
   job.n4[0] = nq / 4;
   job.n4[1] = nk / 4;
   job.n4[2] = nk / 4;
+  job.plane4[0] = job.src_plane4[0] = nq / 4;  // q is dense
+  job.plane4[1] = job.plane4[2] = static_cast<size_t>(p.seq_len_kv) * p.head_dim / 4;
+  job.src_plane4[1] = job.src_plane4[2] = cap * p.head_dim / 4;
+  if (nk == 0) job.plane4[1] = job.plane4[2] = 1;  // no keys: nothing to split
   split_bf16_kernel<<<env.num_sms * 8, 256, 0, env.stream>>>(job);
   if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
-  return launch_impl<64, true, true>(p, qh, kh, vh, ql, kl, vl, o, lse, env);
+  return launch_impl<64, true, true>(p, qh, kh, vh, ql, kl, vl, o, lse, p.seq_len_kv, env);
 }
 
 }  // namespace gb300

@@ -54,6 +54,8 @@ sdpa_status_t validate_problem(const sdpa_params_t* p) {
       if (p->mask_stride[i] < 0) return SDPA_ERR_INVALID_ARGUMENT;
     if (p->mask_stride[3] != 1) return SDPA_ERR_INVALID_ARGUMENT;
   }
+  if (p->kv_capacity < 0 || (p->kv_capacity > 0 && p->kv_capacity < p->seq_len_kv))
+    return SDPA_ERR_INVALID_ARGUMENT;
   if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 512) return SDPA_ERR_UNSUPPORTED;
   // cuDNN's bottom-right causal mask is undefined for Tq > Tkv (mlx 0.30.7
   // supports_sdpa_cudnn); the same rule holds here.
@@ -173,6 +175,9 @@ sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k,
   if (p->mask && !aligned(p->mask, 16)) return SDPA_ERR_MISALIGNED;
   if (lse && !aligned(lse, 4)) return SDPA_ERR_MISALIGNED;
   if (p->sinks && !aligned(p->sinks, 4)) return SDPA_ERR_MISALIGNED;
+  if ((p->seq_lens_q && !aligned(p->seq_lens_q, 4)) ||
+      (p->seq_lens_kv && !aligned(p->seq_lens_kv, 4)))
+    return SDPA_ERR_MISALIGNED;
   const sdpa_kernel_t kern = pick(p);
   // the decode workspace is checked before any launch-side CUDA call
   gb300::DecodePlan plan{};

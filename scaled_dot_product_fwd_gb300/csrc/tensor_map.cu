@@ -24,11 +24,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                      uint64_t inner, uint64_t rows, uint64_t planes, uint32_t elem_bytes,
-                     uint32_t box_inner, uint32_t box_rows) {
+                     uint32_t box_inner, uint32_t box_rows, uint64_t plane_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
+  if (plane_rows == 0) plane_rows = rows;
   const cuuint64_t dims[3] = {inner, rows, planes};
-  const cuuint64_t strides[2] = {inner * elem_bytes, inner * rows * elem_bytes};
+  const cuuint64_t strides[2] = {inner * elem_bytes, inner * plane_rows * elem_bytes};
   const cuuint32_t box[3] = {box_inner, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,

@@ -7,11 +7,13 @@
 
 namespace gb300 {
 
-// 3-D tiled map over a dense [planes, rows, inner] tensor (inner contiguous)
-// with a box of box_inner x box_rows x 1 and 128-byte swizzle; out-of-range
-// elements read as zero.  Returns false if the driver rejects the map.
+// 3-D tiled map over a [planes, rows, inner] tensor (inner contiguous, rows
+// `inner` elements apart, planes `plane_rows` rows apart; 0 = rows) with a
+// box of box_inner x box_rows x 1 and 128-byte swizzle; out-of-range
+// elements (rows >= `rows` included) read as zero.  Returns false if the
+// driver rejects the map.
 bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                      uint64_t inner, uint64_t rows, uint64_t planes, uint32_t elem_bytes,
-                     uint32_t box_inner, uint32_t box_rows);
+                     uint32_t box_inner, uint32_t box_rows, uint64_t plane_rows = 0);
 
 }  // namespace gb300

@@ -37,10 +37,13 @@ def test_library_exports_every_declared_symbol(sdpa_lib):
 
 
 def test_params_struct_layout():
-    assert ctypes.sizeof(B.SdpaParams) == 88
+    assert ctypes.sizeof(B.SdpaParams) == 112
     assert B.SdpaParams.mask.offset == 40
     assert B.SdpaParams.mask_stride.offset == 48
     assert B.SdpaParams.sinks.offset == 80
+    assert B.SdpaParams.kv_capacity.offset == 88
+    assert B.SdpaParams.seq_lens_q.offset == 96
+    assert B.SdpaParams.seq_lens_kv.offset == 104
 
 
 def test_launch_count_is_zero_after_a_rejected_call(sdpa_lib):
@@ -49,7 +52,7 @@ def test_launch_count_is_zero_after_a_rejected_call(sdpa_lib):
 
 
 def test_abi_version_and_status_strings(sdpa_lib):
-    assert S.sdpa_abi_version() == 1
+    assert S.sdpa_abi_version() == 2
     assert S.sdpa_status_string(0) == "ok"
     assert S.sdpa_status_string(2) == "unsupported problem"
     assert S.sdpa_status_string(99) == "unknown status"
@@ -170,3 +173,19 @@ def test_host_entry_pieces_cover_every_head_once(nb, hkv, chunks):
     assert all(0 <= h0 < h1 <= hkv for _, h0, h1 in pieces)
     # every batch in about chunks / nb pieces
     assert len(pieces) == nb * min(hkv, -(-chunks // nb))
+
+
+def test_kv_capacity_and_length_arrays_are_checked(sdpa_lib):
+    # a KV cache must hold at least the keys used
+    p = S.make_params(1, 4, 2, 16, 32, 64, S.SDPA_BF16, 0.125, kv_capacity=31)
+    assert S.sdpa_select_kernel(p) == ("none", 1)
+    assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, None, 0, None) == 1
+    p = S.make_params(1, 4, 2, 16, 32, 64, S.SDPA_BF16, 0.125, kv_capacity=-1)
+    assert S.sdpa_select_kernel(p) == ("none", 1)
+    p = S.make_params(1, 4, 2, 16, 32, 64, S.SDPA_BF16, 0.125, kv_capacity=64)
+    assert S.sdpa_select_kernel(p) == ("prefill_tc", 0)
+    # per-batch length arrays are int32: 4-byte aligned
+    p = S.make_params(1, 4, 2, 16, 32, 64, S.SDPA_BF16, 0.125, seq_lens_q_ptr=258)
+    assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, None, 0, None) == 3
+    p = S.make_params(1, 4, 2, 16, 32, 64, S.SDPA_BF16, 0.125, seq_lens_kv_ptr=258)
+    assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, None, 0, None) == 3

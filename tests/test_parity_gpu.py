@@ -379,3 +379,83 @@ def test_launch_count_reports_kernels_per_call(cuda, monkeypatch):
     assert S.sdpa_last_launch_count() == 1
     S.sdpa_forward(q[:0], q[:0], q[:0])
     assert S.sdpa_last_launch_count() == 0
+
+
+# ------------------------------------------- KV-cache views, per-batch lengths
+def _kv_view_check(B, Hq, Hkv, Lq, Lk, cap, D, dtype, causal, sinks, lens_q, lens_kv,
+                   noalloc=False):
+    """k, v as rows [0, Lk) of a [B, Hkv, cap, D] cache, per-batch lengths.
+    Rows [Lk, cap) hold NaN (never read); rows [len_kv_b, Lk) hold large
+    finite junk (weighted by zero).  Expected: the oracle on the used rows
+    with an explicit -inf mask for padding and the per-batch causal rule."""
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    w = wl(B, Hq, Hkv, Lq, Lk, D, dtype, causal=causal, sinks=sinks)
+    inp = W.make_inputs(w)
+    kc = torch.full((B, Hkv, cap, D), float("nan"), dtype=inp["k"].dtype)
+    vc = kc.clone()
+    kc[:, :, :Lk] = inp["k"]
+    vc[:, :, :Lk] = inp["v"]
+    for b in range(B):
+        kc[b, :, lens_kv[b]:Lk] = 300.0
+        vc[b, :, lens_kv[b]:Lk] = -300.0
+    mask = np.zeros((B, Hq, Lq, Lk))
+    for b in range(B):
+        i = np.arange(Lq)[:, None]
+        j = np.arange(Lk)[None, :]
+        hide = (i >= lens_q[b]) | (j >= lens_kv[b])
+        if causal:
+            hide |= j > i + (lens_kv[b] - lens_q[b])
+        mask[b, :, hide] = -np.inf
+    f = W.as_float64
+    o_ref, l_ref = O.sdpa(f(inp["q"]), f(kc[:, :, :Lk]), f(vc[:, :, :Lk]), w.scale, False, mask,
+                          None if inp["sinks"] is None else f(inp["sinks"]))
+    q = inp["q"].cuda()
+    s = None if inp["sinks"] is None else inp["sinks"].cuda()
+    tq = torch.tensor(lens_q, dtype=torch.int32, device="cuda")
+    tk = torch.tensor(lens_kv, dtype=torch.int32, device="cuda")
+    if noalloc:
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+        p = S.make_params(B, Hq, Hkv, Lq, Lk, D, S.dtype_code(q.dtype), w.scale, causal, None,
+                          (0, 0, 0, 1), None if s is None else s.data_ptr(), kv_capacity=cap,
+                          seq_lens_q_ptr=tq.data_ptr(), seq_lens_kv_ptr=tk.data_ptr())
+        kcd, vcd = kc.cuda(), vc.cuda()
+        st = S._binding.sdpa_forward_decode_noalloc_raw(
+            p, q.data_ptr(), kcd.data_ptr(), vcd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+    else:
+        o, lse = S.sdpa_forward(q, kc.cuda(), vc.cuda(), scale=w.scale, causal=causal, sinks=s,
+                                kv_len=Lk, seq_lens_q=tq, seq_lens_kv=tk)
+    torch.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    compare(w, o.cpu(), lse.cpu(), o_ref, l_ref, None)
+
+
+@pytest.mark.parametrize("dtype,D", [("float16", 64), ("bfloat16", 128), ("float32", 64),
+                                     ("float32", 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_view_prefill(cuda, dtype, D, causal):
+    # batch 1 has more query rows than keys: under the causal rule its first
+    # 50 rows see no key
+    _kv_view_check(3, 4, 2, 260, 300, 384, D, dtype, causal, sinks=True,
+                   lens_q=[260, 150, 0], lens_kv=[300, 100, 50])
+
+
+@pytest.mark.parametrize("dtype,D", [("bfloat16", 512), ("float16", 128), ("float32", 64)])
+def test_kv_view_decode(cuda, dtype, D):
+    _kv_view_check(4, 32, 4, 1, 1024, 1100, D, dtype, False, sinks=True,
+                   lens_q=[1, 1, 1, 0], lens_kv=[1024, 1, 700, 0])
+
+
+def test_kv_view_long_decode_and_few_queries(cuda):
+    _kv_view_check(3, 16, 2, 1, 5000, 6000, 128, "bfloat16", False, sinks=False,
+                   lens_q=[1, 1, 1], lens_kv=[5000, 4097, 1])
+    _kv_view_check(2, 8, 2, 2, 777, 800, 64, "float16", True, sinks=True,
+                   lens_q=[2, 1], lens_kv=[777, 300])
+
+
+def test_kv_view_noalloc(cuda):
+    _kv_view_check(2, 32, 4, 1, 1024, 1100, 512, "bfloat16", False, sinks=True,
+                   lens_q=[1, 1], lens_kv=[1000, 3], noalloc=True)
