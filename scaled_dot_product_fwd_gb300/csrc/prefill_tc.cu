@@ -239,7 +239,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-template <int D, bool BF16, bool X3>
+// LENS: the call passes per-batch length arrays (without them the lengths
+// are the kernel arguments, and the code is that of dense inputs).
+template <int D, bool BF16, bool X3, bool LENS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -280,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = h / a.G;
   // this batch's lengths (padding masks), clamped to the call's maxima; rows
   // at or past Lqb see no key
-  const int Lkb = a.seq_lens_kv ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
-  const int Lqb = a.seq_lens_q ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
+  const int Lkb = (LENS && a.seq_lens_kv) ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
+  const int Lqb = (LENS && a.seq_lens_q) ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
   const int nkv_all = (Lkb + BN - 1) / BN;
   int nkv[NQ];
   int nmax = 0;
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // last key visible to this row (bounds and causal)
     int limit = Lkb - 1;
     if (a.causal) limit = min(limit, qi + (Lkb - Lqb));
-    if (qi >= Lqb) limit = -1;  // a padding row sees no key
+    if (LENS && qi >= Lqb) limit = -1;  // a padding row sees no key
     const T* mrow = nullptr;
     if (a.mask && row_ok)
       mrow = static_cast<const T*>(a.mask) + b * a.ms0 + h * a.ms1 + qi * a.ms2;
@@ -786,7 +788,7 @@ __global__ void __launch_bounds__(256) split_bf16_kernel(const SplitJob job) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // kv_plane_rows: rows per (batch, kv head) in k, v, k2, v2 as passed here
-template <int D, bool BF16, bool X3>
+template <int D, bool BF16, bool X3, bool LENS>
 sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, const void* v,
                           const void* q2, const void* k2, const void* v2, void* o, float* lse,
                           uint64_t kv_plane_rows, const LaunchEnv& env) {
@@ -834,7 +836,7 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   a.wait_ns = env.wait_limit_ns;
   a.seq_lens_q = p.seq_lens_q;
   a.seq_lens_kv = p.seq_lens_kv;
-  auto kern = prefill_tc_kernel<D, BF16, X3>;
+  auto kern = prefill_tc_kernel<D, BF16, X3, LENS>;
   // The setmaxnreg split must fit the registers the kernel is launched with
   // (an increase beyond them would wait forever): check the compiled count
   // once per instantiation.
@@ -861,12 +863,21 @@ sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const voi
                                 const void* v, void* o, float* lse, const LaunchEnv& env) {
   const bool bf16 = p.dtype == SDPA_BF16;
   const uint64_t cap = p.kv_capacity > 0 ? p.kv_capacity : p.seq_len_kv;
-  if (p.head_dim == 64)
-    return bf16 ? launch_impl<64, true, false>(p, q, k, v, q, k, v, o, lse, cap, env)
-                : launch_impl<64, false, false>(p, q, k, v, q, k, v, o, lse, cap, env);
-  if (p.head_dim == 128)
-    return bf16 ? launch_impl<128, true, false>(p, q, k, v, q, k, v, o, lse, cap, env)
-                : launch_impl<128, false, false>(p, q, k, v, q, k, v, o, lse, cap, env);
+  const bool lens = p.seq_lens_q || p.seq_lens_kv;
+  if (p.head_dim == 64) {
+    if (lens)
+      return bf16 ? launch_impl<64, true, false, true>(p, q, k, v, q, k, v, o, lse, cap, env)
+                  : launch_impl<64, false, false, true>(p, q, k, v, q, k, v, o, lse, cap, env);
+    return bf16 ? launch_impl<64, true, false, false>(p, q, k, v, q, k, v, o, lse, cap, env)
+                : launch_impl<64, false, false, false>(p, q, k, v, q, k, v, o, lse, cap, env);
+  }
+  if (p.head_dim == 128) {
+    if (lens)
+      return bf16 ? launch_impl<128, true, false, true>(p, q, k, v, q, k, v, o, lse, cap, env)
+                  : launch_impl<128, false, false, true>(p, q, k, v, q, k, v, o, lse, cap, env);
+    return bf16 ? launch_impl<128, true, false, false>(p, q, k, v, q, k, v, o, lse, cap, env)
+                : launch_impl<128, false, false, false>(p, q, k, v, q, k, v, o, lse, cap, env);
+  }
   return SDPA_ERR_UNSUPPORTED;
 }
 
@@ -912,7 +923,9 @@ sdpa_status_t launch_prefill_x3(const sdpa_params_t& p, const void* q, const voi
   if (nk == 0) job.plane4[1] = job.plane4[2] = 1;  // no keys: nothing to split
   split_bf16_kernel<<<env.num_sms * 8, 256, 0, env.stream>>>(job);
   if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
-  return launch_impl<64, true, true>(p, qh, kh, vh, ql, kl, vl, o, lse, p.seq_len_kv, env);
+  if (p.seq_lens_q || p.seq_lens_kv)
+    return launch_impl<64, true, true, true>(p, qh, kh, vh, ql, kl, vl, o, lse, p.seq_len_kv, env);
+  return launch_impl<64, true, true, false>(p, qh, kh, vh, ql, kl, vl, o, lse, p.seq_len_kv, env);
 }
 
 }  // namespace gb300
