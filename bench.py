@@ -418,13 +418,17 @@ def gb300_arm(args):
         work, unit, scale = w.kv_bytes(), "GB/s", 1e9
         bound, peak, peak_name = "hbm", peaks["hbm_gbs"], " (HBM copy)"
         sustained = peaks["hbm_gbs"]
-        traffic = profile_traffic("decode_split_" + w.name, ["decode.cuh", "decode_combine.cu"])
+        traffic = profile_traffic("decode_split_" + w.name,
+                                  ["decode.cuh", "decode_combine.cu", "ptx.cuh"])
     else:
         work, unit, scale = flops, "TFLOP/s", 1e12
         bound, peak, peak_name = "tensor", peaks["bf16_tflops"], " (bf16 dense, burst)"
         sustained = peaks["bf16_tflops_sustained"]
-        kfile = "prefill_f32.cu" if w.dtype == "float32" else "prefill_tc.cu"
-        traffic = profile_traffic(kfile[:-3] + "_" + w.name, [kfile, "ptx.cuh"])
+        if w.dtype == "float32" and w.D != 64:  # fp32 FMA tiles
+            traffic = profile_traffic("prefill_f32_" + w.name, ["prefill_f32.cu"])
+        else:  # tensor-core kernel (fp32 at D = 64 as bf16 hi/lo parts)
+            tu = "prefill_tc.cu" if w.dtype == "float32" else "prefill_tc_d%d.cu" % w.D
+            traffic = profile_traffic("prefill_tc_" + w.name, ["prefill_tc.cuh", tu, "ptx.cuh"])
     launches = per_call_launches * args.steps
     value = whole_job_rate(work, args.steps, world, secs, scale)
     achieved = work / per_launch / scale

@@ -109,26 +109,6 @@ struct StoreAs<__nv_bfloat16> {
   static __device__ __forceinline__ __nv_bfloat16 c(float x) { return __float2bfloat16_rn(x); }
 };
 
-// Thread-block cluster helpers: barrier over every thread of the cluster
-// (exited threads count as arrived), this CTA's rank, and a 32-bit load from
-// the shared memory of another CTA of the cluster at the address that
-// corresponds to `local` in this one.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
-  uint32_t ra;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
-  return v;
-}
 constexpr int kMaxClusterSplits = 16;
 
 // Pairs of fp32 values in one 64-bit register for the packed f32x2 ops.

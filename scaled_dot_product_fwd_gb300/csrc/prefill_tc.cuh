@@ -1,0 +1,1138 @@
+// prefill_tc.cuh — fused attention forward for fp16/bf16, head_dim 64/128,
+// on the 5th-generation tensor cores of sm_103a: the kernel and its launch.
+// Instantiated per head size in prefill_tc_d64.cu and prefill_tc_d128.cu,
+// and for fp32 inputs (bf16 hi/lo parts, head_dim 64) in prefill_tc.cu.
+//
+// The computation is the tiled online-softmax forward of the rustytorch
+// flash_attention.metal page (forward kernel: per key tile, row max, running
+// max m and sum l, accumulator rescale by exp(m_old - m_new), final O / l
+// and LSE = m + log l), with the options of the MLX pages (causal block
+// skipping, bounds masking of the ragged key tail, additive mask, per-head
+// sinks in the denominator, grouped-query head mapping).
+//
+// GB300 design (not the page's): one CTA owns NQ = 2 query tiles of 128 rows
+// that share every K/V tile.  Warp roles:
+//   warps 0-7  softmax: warpgroup t owns query tile t, one thread per row
+//              (TMEM lane); it also rescales O in TMEM and writes the output;
+//   warp 8     TMA producer: Q tiles once, then K_j, V_j into a ring of
+//              shared-memory buffers (128-byte swizzle);
+//   warp 9     MMA issuer: one elected lane issues tcgen05.mma,
+//              S_t = Q_t K_j^T (A, B from shared memory, fp32 in TMEM) and
+//              O_t += P_t V_j (P from TMEM, written there by the softmax
+//              warps; V from shared memory), while the whole warp runs the
+//              loop in step and meets the other roles only at named
+//              barriers (no shared-memory access between MMAs);
+//   warp 10    stage helper: waits for each K/V stage to land and passes
+//              it to the MMA issuer;
+//   warp 11    idle (completes the control warpgroup).
+// Each ring stage holds K_j and V_j (one full and one empty barrier per
+// step).  TMEM (512 columns): S_0 | S_1 | O_0 | O_1, with P written over
+// the columns of S_t.  The issue order S_0,j+1 right after PV_0,j lets
+// softmax of one tile overlap the MMAs of the other.  The O rescale is
+// lazy: a row's reference max moves only when the new max exceeds it (by
+// more than 8 in log2 units on masked tiles, or so far that a row sum passes
+// 2^15 on interior tiles), so P stays <= 2^15.
+//
+// Scheduling: one CTA per SM, units (query-tile pair, head, batch) in a 1-D
+// grid; causal grids take the heaviest query blocks of every head first.
+// When the unit count leaves a partial last wave, its units go to a second
+// grid (programmatic dependent launch, so it fills SMs as the first drains)
+// that shares each unit's key tiles among the 2 or 4 CTAs of a cluster; the
+// partial results (O, m, l) meet in the finalising CTA's shared memory
+// through bulk copies and merge by the log-sum-exp rule of split-KV decode.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tensor_map.h"
+
+namespace gb300 {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;  // keys per K/V tile
+constexpr int NQ = 2;    // query tiles per CTA
+constexpr int kSoftmaxWarps = 4 * NQ;
+constexpr int kLoadWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+// warps 8-11 form the control warpgroup (producer, MMA issuer, stage
+// helper, one idle warp); it gives registers to the softmax warpgroups with
+// setmaxnreg (launch: 384 x 168 = 256 x 224 + 128 x 56).
+constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
+constexpr uint32_t kSoftmaxRegs = 224;
+constexpr uint32_t kControlRegs = 56;
+// named barriers: kBarP + t (softmax warps of tile t with the MMA warp),
+// kBarK (stage helper with the MMA warp), kBarX + t (below)
+constexpr uint32_t kBarP = 1;
+constexpr uint32_t kBarK = kBarP + NQ;
+constexpr uint32_t kBarX = kBarK + 1;  // + t: the 4 warps of tile t (split units)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units (masked path)
+constexpr float kFusedSumLimit = 32768.0f;  // 2^15: bound on p (fused path)
+constexpr int kMaxSplit = 4;  // CTAs that share the key tiles of one unit
+
+// X3: fp32 inputs given as bf16 hi + lo splits (x = hi + lo + O(2^-16 x));
+// S = Q_hi K_hi^T + Q_hi K_lo^T + Q_lo K_hi^T and O += P_hi V_hi + P_hi V_lo
+// + P_lo V_hi, each product on the bf16 tensor path with fp32 accumulation.
+template <int D, bool X3 = false>
+struct Cfg {
+  static constexpr int CB = D / 64;           // 128-byte column blocks per row
+  static constexpr int TILE = BM * D * 2;     // bytes of one 128-row fp16/bf16 tile
+  static constexpr int QT = X3 ? 2 : 1;       // tiles per query tile (hi, lo)
+  static constexpr int KVT = X3 ? 4 : 2;      // tiles per stage: K (hi, lo), V (hi, lo)
+  static constexpr int NS = X3 ? 2 : ((D == 64) ? 4 : 2);  // ring stages
+  static constexpr int STAGE = KVT * TILE;
+  static constexpr int K_LO = TILE;                  // offsets inside a stage
+  static constexpr int V_OFF = (X3 ? 2 : 1) * TILE;
+  static constexpr int V_LO = 3 * TILE;
+  static constexpr int Q_OFF = 0;
+  static constexpr int RING_OFF = NQ * QT * TILE;
+  static constexpr int BAR_OFF = RING_OFF + NS * STAGE;
+  // q_full, full[NS], empty[NS], s_full[NQ], o_done[NQ], drain, xbar
+  // + xbar: partial results of a split unit received
+  static constexpr int NBARS = 1 + 2 * NS + 2 * NQ + 1 + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t s_col(int t) { return static_cast<uint32_t>(t * BN); }
+  static constexpr uint32_t o_col(int t) { return static_cast<uint32_t>(NQ * BN + t * D); }
+  static_assert(o_col(NQ - 1) + D <= TMEM_COLS, "TMEM budget");
+  // split units: partial results of a tile, fp32 O rows (SLOT_O bytes) in the
+  // ring and m, l (SLOT_ML bytes) over the Q tiles; a CTA holds up to
+  // MAX_SPLIT slots (received ones and the ones it stages to send)
+  static constexpr int SLOT_O = BM * D * 4;
+  static constexpr int SLOT_ML = 2 * BM * 4;
+  static constexpr int MAX_SPLIT = kMaxSplit * SLOT_O <= NS * STAGE ? kMaxSplit : 2;
+  static_assert(MAX_SPLIT * SLOT_O <= NS * STAGE, "partial O slots fit the ring");
+  static_assert(kMaxSplit * SLOT_ML <= NQ * QT * TILE, "partial m, l fit the Q tiles");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct PrefillArgs {
+  int B, Hq, Hkv, G, Lq, Lk;
+  int num_qblocks;
+  // Work units (query block, head, batch) follow the linear block index
+  // from unit0 on; a split grid gives each unit to the ksplit CTAs of a
+  // thread-block cluster, which share its key tiles.
+  int unit0;
+  int ksplit;
+  float sl2;  // scale * log2(e)
+  int causal;
+  const void* mask;
+  long long ms0, ms1, ms2;  // mask element strides (last stride is 1)
+  const float* sinks;
+  void* o;
+  float* lse;
+  int* status;
+  unsigned long long wait_ns;
+  const int* seq_lens_q;   // nullptr or per-batch valid query rows
+  const int* seq_lens_kv;  // nullptr or per-batch valid keys
+};
+
+template <bool BF16>
+struct Elem;
+template <>
+struct Elem<true> {
+  using T = __nv_bfloat16;
+  static __device__ __forceinline__ float to_f(T x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+template <>
+struct Elem<false> {
+  using T = __half;
+  static __device__ __forceinline__ float to_f(T x) { return __half2float(x); }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// ---------------------------------------------------------------- softmax math
+// Pairs of fp32 values in one 64-bit register for the packed f32x2 FMA/add.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x for a pair x in [-125, 128) on the FMA pipe.  x = n + f with n the
+// nearest integer (added to 1.5 * 2^23, whose low mantissa bits then hold n)
+// and f in [-1/2, 1/2]; 2^f from a degree-3 polynomial fitted for this
+// kernel (minimax in relative error on [-1/2, 1/2], max 7.5e-5, below the
+// rounding of the fp16/bf16 P it feeds); 2^n enters as n << 23 added to the
+// exponent field.  The caller clamps x below at -125 so the field stays >= 1.
+__device__ __forceinline__ void exp2_poly_pair(uint64_t X, float& r0, float& r1) {
+  constexpr uint64_t kMagic = 0x4b4000004b400000ull;     // 1.5 * 2^23 (pair)
+  constexpr uint64_t kNegMagic = 0xcb400000cb400000ull;  // -1.5 * 2^23
+  constexpr uint64_t kNeg1 = 0xbf800000bf800000ull;      // -1
+  constexpr uint64_t kC0 = 0x3f7ffb493f7ffb49ull;        // 0.99992806
+  constexpr uint64_t kC1 = 0x3f31798d3f31798dull;        // 0.69326097
+  constexpr uint64_t kC2 = 0x3e786f0d3e786f0dull;        // 0.24261113
+  constexpr uint64_t kC3 = 0x3d61fbb03d61fbb0ull;        // 0.05517167
+  const uint64_t NP = f2_add(X, kMagic);
+  const uint64_t N = f2_add(NP, kNegMagic);
+  const uint64_t F = f2_fma(N, kNeg1, X);
+  uint64_t P = f2_fma(kC3, F, kC2);
+  P = f2_fma(P, F, kC1);
+  P = f2_fma(P, F, kC0);
+  float p0, p1, n0, n1;
+  f2_unpack(P, p0, p1);
+  f2_unpack(NP, n0, n1);
+  r0 = __int_as_float(__float_as_int(p0) + (__float_as_int(n0) << 23));
+  r1 = __int_as_float(__float_as_int(p1) + (__float_as_int(n1) << 23));
+}
+
+// Pairs (bit i of the mask = pair index mod 8) whose exponentials go to the
+// FMA pipe instead of the MUFU unit.
+#ifndef SDPA_POLY_PAIRS_MASK
+#define SDPA_POLY_PAIRS_MASK 0x00
+#endif
+
+// p_i = 2^(s_i * sl2 - m) for one row of raw scores, packed to fp16/bf16
+// pairs; rs receives the fp32 sum of the p_i.
+// With X3, pk2 receives the bf16 residuals p - bf16(p) (P_lo).
+template <bool BF16, int N, bool X3 = false>
+__device__ __forceinline__ void softmax_pairs(const uint32_t (&s)[N], float sl2, float m,
+                                              uint32_t (&pk)[N / 2], float& rs,
+                                              uint32_t* pk2 = nullptr) {
+  const uint64_t SL = f2_pack(sl2, sl2);
+  const uint64_t NM = f2_pack(-m, -m);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const uint64_t X = f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                              SL, NM);
+    float x0, x1, p0, p1;
+    f2_unpack(X, x0, x1);
+    if ((SDPA_POLY_PAIRS_MASK >> (i & 7)) & 1) {
+      exp2_poly_pair(f2_pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f)), p0, p1);
+    } else {
+      p0 = ex2(x0);
+      p1 = ex2(x1);
+    }
+    acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+    pk[i] = Elem<BF16>::pack(p0, p1);
+    if constexpr (X3) {
+      const float h0 = __uint_as_float(pk[i] << 16);
+      const float h1 = __uint_as_float(pk[i] & 0xffff0000u);
+      pk2[i] = Elem<true>::pack(p0 - h0, p1 - h1);
+    }
+  }
+  const uint64_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+  float t0, t1;
+  f2_unpack(t, t0, t1);
+  rs = t0 + t1;
+}
+
+// Max of the raw scores of one row.
+template <int N>
+__device__ __forceinline__ float row_max_raw(const uint32_t (&s)[N]) {
+  float mr[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
+#pragma unroll
+  for (int i = 8; i < N; i += 16)
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
+  return fmaxf(fmax3(mr[0], mr[1], mr[2]), fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7])));
+}
+
+
+// Wait for a phase ignoring the abort flag (used only to drain in-flight
+// asynchronous work before the CTA exits); bounded by limit_ns.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) break;
+  }
+}
+
+// Work unit of a linear block index: (query block, head, batch) and, in a
+// split grid, the CTA's part of the unit's key tiles (= its cluster rank).
+// Causal grids take the heaviest query blocks of every head first.
+struct Unit {
+  int qb, h, b, part;
+};
+template <bool SPLIT>
+__device__ __forceinline__ Unit unit_of(const PrefillArgs& a, uint32_t bx) {
+  Unit w;
+  const int u = a.unit0 + static_cast<int>(SPLIT ? bx / a.ksplit : bx);
+  w.part = SPLIT ? static_cast<int>(bx % a.ksplit) : 0;
+  if (a.causal) {
+    const int hb = a.Hq * a.B;
+    w.qb = a.num_qblocks - 1 - u / hb;
+    w.h = (u % hb) % a.Hq;
+    w.b = (u % hb) / a.Hq;
+  } else {
+    w.qb = u % a.num_qblocks;
+    w.h = (u / a.num_qblocks) % a.Hq;
+    w.b = u / (a.num_qblocks * a.Hq);
+  }
+  return w;
+}
+
+// LENS: the call passes per-batch length arrays (without them the lengths
+// are the kernel arguments, and the code is that of dense inputs).
+// SPLIT: every unit is shared by the CTAs of a cluster (the units of a last,
+// partial wave); its own instantiation, so that whole units run code without
+// the merge.
+template <int D, bool BF16, bool X3, bool LENS, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmQ2,
+                      const __grid_constant__ CUtensorMap tmK2,
+                      const __grid_constant__ CUtensorMap tmV2, const PrefillArgs a) {
+  using C = Cfg<D, X3>;
+  using E = Elem<BF16>;
+  // element type of the output and of the mask: the caller's dtype (fp32 in X3)
+  using T = std::conditional_t<X3, float, typename E::T>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment of the shared-memory window (128-byte swizzle atoms).
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sQ = smem + C::Q_OFF;
+  uint8_t* sRing = smem + C::RING_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* full = bars + 1;
+  uint64_t* empty = full + C::NS;
+  uint64_t* s_full = empty + C::NS;
+  uint64_t* o_done = s_full + NQ;
+  uint64_t* drain = o_done + NQ;
+  uint64_t* xbar = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit (query block, head, batch) and, for a split unit, this
+  // CTA's part of its key tiles
+  const Unit w0 = unit_of<SPLIT>(a, blockIdx.x);
+  const int qb = w0.qb, h = w0.h, b = w0.b, part = w0.part;
+  // a split grid that follows the grid of whole units may start as soon as
+  // every CTA of that grid is running
+  if constexpr (!SPLIT) griddep_launch_dependents();
+  const int m0 = qb * (BM * NQ);
+  const int nt = min(NQ, (a.Lq - m0 + BM - 1) / BM);  // active query tiles (>= 1)
+  const int kvh = h / a.G;
+  // this batch's lengths (padding masks), clamped to the call's maxima; rows
+  // at or past Lqb see no key
+  const int Lkb = (LENS && a.seq_lens_kv) ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
+  const int Lqb = (LENS && a.seq_lens_q) ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
+  const int nkv_all = (Lkb + BN - 1) / BN;
+  // key tiles [jb, je) of this CTA (all of them unless the unit is split;
+  // splits are never causal)
+  const int nparts = SPLIT ? a.ksplit : 1;
+  const int jb = part * nkv_all / nparts;
+  const int je = (part + 1) * nkv_all / nparts;
+  int nkv[NQ];
+  int nmax = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    int n = 0;
+    const int last_row = min(m0 + t * BM + BM - 1, Lqb - 1);  // last row that sees keys
+    if (t < nt && last_row >= m0 + t * BM) {
+      if (a.causal) {
+        const int lim = last_row + (Lkb - Lqb);  // last key visible to the tile
+        n = lim < 0 ? 0 : min(nkv_all, lim / BN + 1);
+      } else {
+        n = je - jb;
+      }
+    }
+    nkv[t] = n;
+    nmax = max(nmax, n);
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int t = 0; t < NQ; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(drain, 1);
+    mbar_init(xbar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{a.wait_ns, abort_flag, a.status};
+  int last_use[C::NS];  // producer: last fill of each ring buffer (-1: none)
+#pragma unroll
+  for (int s = 0; s < C::NS; ++s) last_use[s] = -1;
+
+  // launch: 384 threads x 168 registers; the control warpgroup drops to 56
+  // and the softmax warpgroups rise to 224 (256*224 + 128*56 = 384*168).
+  if (warp >= kSoftmaxWarps) {
+    setmaxnreg_dec<kControlRegs>();
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nt * C::QT * C::TILE));
+      for (int t = 0; t < nt; ++t)
+        for (int cb = 0; cb < C::CB; ++cb) {
+          tma_load_3d(sQ + t * C::QT * C::TILE + cb * BM * 128, &tmQ, q_full, cb * 64,
+                      m0 + t * BM, b * a.Hq + h);
+          if constexpr (X3)
+            tma_load_3d(sQ + (t * C::QT + 1) * C::TILE + cb * BM * 128, &tmQ2, q_full,
+                        cb * 64, m0 + t * BM, b * a.Hq + h);
+        }
+      for (int j = 0; j < nmax; ++j) {
+        const int s = j % C::NS;
+        const int use = j / C::NS;
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, wc)) break;
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        uint8_t* st = sRing + s * C::STAGE;
+        const int kvz = b * a.Hkv + kvh;
+        for (int cb = 0; cb < C::CB; ++cb) {
+          const int key0 = (jb + j) * BN;
+          tma_load_3d(st + cb * BN * 128, &tmK, &full[s], cb * 64, key0, kvz);
+          tma_load_3d(st + C::V_OFF + cb * BN * 128, &tmV, &full[s], cb * 64, key0, kvz);
+          if constexpr (X3) {
+            tma_load_3d(st + C::K_LO + cb * BN * 128, &tmK2, &full[s], cb * 64, key0, kvz);
+            tma_load_3d(st + C::V_LO + cb * BN * 128, &tmV2, &full[s], cb * 64, key0, kvz);
+          }
+        }
+        last_use[s] = use;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    // The whole warp runs the issue loop in step; one lane, picked by
+    // elect.sync inside each instruction, issues, so the warp never branches
+    // around it.  The loop touches no shared memory: the softmax warps of
+    // tile t hand P_t over through named barrier kBarP + t and the stage
+    // helper reports each K/V stage that has landed through kBarK (an
+    // mbarrier poll, a local-memory spill or a warp reconvergence here holds
+    // the issuing thread until the MMAs in flight drain).  Fixed order:
+    // PV_0,j S_0,j+1 PV_1,j S_1,j+1, so each tile's next scores are ready as
+    // early as possible.
+    const uint32_t lead = lane == 0 ? 1u : 0u;
+    constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
+    constexpr uint32_t idO = idesc_f16(BF16, BM, D, false, true);
+    // Descriptors of Q_0 and ring buffer 0.  Other tiles, buffers and K
+    // steps differ only in the start-address field (bits 0-13, 16-byte
+    // units) of the low word, so the loop adds 32-bit offsets to the low
+    // words and pairs them with the fixed high words.
+    const uint64_t q_desc = sdesc(smem_addr(sQ), 16, 1024, kSwizzle128B);
+    const uint64_t k_desc = sdesc(smem_addr(sRing), 16, 1024, kSwizzle128B);
+    const uint64_t v_desc = sdesc(smem_addr(sRing), BN * 128, 1024, kSwizzle128B);
+    const uint32_t qk_hi = static_cast<uint32_t>(q_desc >> 32);
+    const uint32_t v_hi = static_cast<uint32_t>(v_desc >> 32);
+    const uint32_t q_lo = static_cast<uint32_t>(q_desc);
+    const uint32_t k_lo = static_cast<uint32_t>(k_desc);
+    const uint32_t v_lo = static_cast<uint32_t>(v_desc);
+    auto qk = [&](uint32_t lo) { return (static_cast<uint64_t>(qk_hi) << 32) | lo; };
+    auto vv = [&](uint32_t lo) { return (static_cast<uint64_t>(v_hi) << 32) | lo; };
+    auto stage = [](int j) { return j % C::NS; };
+    auto spar = [](int j) { return static_cast<uint32_t>((j / C::NS) & 1); };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, wc));
+    if (nmax > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(&full[stage(0)], spar(0), wc));
+    // after a failed wait the loop still meets every named barrier, without
+    // issuing anything
+    const uint32_t go = ok ? 1u : 0u;
+    // S_t = Q_t K_j^T: both operands K-major, 128-byte swizzle; a K step of
+    // 16 elements is 32 bytes inside a 128-byte row, 4 steps per column block.
+    auto issue_s = [&](int t, int j) {
+      const uint32_t qd = q_lo + static_cast<uint32_t>((t * C::QT * C::TILE) >> 4);
+      const uint32_t kd = k_lo + static_cast<uint32_t>((stage(j) * C::STAGE) >> 4);
+      const uint32_t dS = tmem + C::s_col(t);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+        mma_f16_ss_elect(dS, qk(qd + off), qk(kd + off), idS, kk > 0 ? 1u : 0u, go);
+        if constexpr (X3) {  // Q_hi K_lo^T + Q_lo K_hi^T
+          mma_f16_ss_elect(dS, qk(qd + off), qk(kd + (C::K_LO >> 4) + off), idS, 1u, go);
+          mma_f16_ss_elect(dS, qk(qd + (C::TILE >> 4) + off), qk(kd + off), idS, 1u, go);
+        }
+      }
+    };
+    // O_t += P_t V_j: P (128 x 128, K-major) from TMEM columns of S_t,
+    // 2 elements per column; V MN-major: 64-wide column blocks BN*128 bytes
+    // apart (LBO), 8-key groups 1024 bytes apart (SBO).  In X3, P_hi sits in
+    // the first 64 columns of S_t and P_lo in the next 64.
+    auto issue_pv = [&](int t, int j) {
+      const uint32_t vd = v_lo + static_cast<uint32_t>((stage(j) * C::STAGE + C::V_OFF) >> 4);
+      const uint32_t dO = tmem + C::o_col(t);
+      const uint32_t aP = tmem + C::s_col(t);
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        const uint32_t voff = (kk * 16 * 128) >> 4;
+        mma_f16_ts_elect(dO, aP + kk * 8, vv(vd + voff), idO, (j > 0 || kk > 0) ? 1u : 0u, go);
+        if constexpr (X3) {  // P_hi V_lo + P_lo V_hi
+          mma_f16_ts_elect(dO, aP + kk * 8, vv(vd + ((C::V_LO - C::V_OFF) >> 4) + voff), idO, 1u,
+                           go);
+          mma_f16_ts_elect(dO, aP + BN / 2 + kk * 8, vv(vd + voff), idO, 1u, go);
+        }
+      }
+    };
+    for (int t = 0; t < nt; ++t) {
+      if (nkv[t] == 0) {
+        mma_commit_elect(&o_done[t], go);
+      } else {
+        issue_s(t, 0);
+        mma_commit_elect(&s_full[t], go);
+      }
+    }
+    for (int j = 0; j < nmax; ++j) {
+      bool kwaited = false;
+      // stage j+1 has landed (the helper saw it); once per step
+      auto wait_stage = [&]() {
+        if (!kwaited) {
+          named_bar_sync(kBarK, 64);
+          kwaited = true;
+        }
+      };
+      for (int t = 0; t < nt; ++t) {
+        if (j >= nkv[t]) continue;
+        // P_t,j is in TMEM (4 softmax warps and this one meet)
+        named_bar_sync(kBarP + t, 32 * 5);
+        tc_fence_after();
+        issue_pv(t, j);
+        if (j + 1 < nkv[t]) {
+          wait_stage();
+          issue_s(t, j + 1);
+          mma_commit_elect(&s_full[t], go);
+        } else {
+          mma_commit_elect(&o_done[t], go);
+        }
+      }
+      // stage j (K_j read by S_t,j, V_j by PV_t,j) is free once these land
+      mma_commit_elect(&empty[stage(j)], go);
+    }
+    // every MMA issued by this warp completes before TMEM is freed
+    mma_commit_elect(drain, go);
+    if (go && lead) drain_wait(drain, 0, kDrainNs);
+    __syncwarp();
+  } else if (warp == kMmaWarp + 1) {
+    // -------------------------------------------------------- stage helper
+    // Waits for K/V stage j+1 of every step that reads one and hands it to
+    // the MMA issuer through kBarK (same count of meetings on both sides,
+    // also after a failed wait).
+    bool ok = true;
+    for (int j = 0; j + 1 < nmax; ++j) {
+      const int s = (j + 1) % C::NS;
+      ok = ok && mbar_wait(&full[s], static_cast<uint32_t>(((j + 1) / C::NS) & 1), wc);
+      named_bar_sync(kBarK, 64);
+    }
+  }
+  // a split unit's CTAs meet twice at the end (partial results written, then
+  // read); every thread of the cluster takes part
+  if constexpr (SPLIT) {
+    __syncwarp();
+    cluster_sync_all();
+    cluster_sync_all();
+  }
+  } else {
+    setmaxnreg_inc<kSoftmaxRegs>();
+    // ------------------------------------------------------------- softmax
+    const int t = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;  // row inside the tile = TMEM lane
+    const int qi = m0 + t * BM + r;        // query row
+    const bool row_ok = qi < a.Lq;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::s_col(t);
+    const uint32_t tO = tmem + lane_off + C::o_col(t);
+    // last key visible to this row (bounds and causal)
+    int limit = Lkb - 1;
+    if (a.causal) limit = min(limit, qi + (Lkb - Lqb));
+    if (LENS && qi >= Lqb) limit = -1;  // a padding row sees no key
+    const T* mrow = nullptr;
+    if (a.mask && row_ok)
+      mrow = static_cast<const T*>(a.mask) + b * a.ms0 + h * a.ms1 + qi * a.ms2 + jb * BN;
+    // keys are counted from this CTA's first key tile from here on
+    limit -= jb * BN;
+    float m = -INFINITY;  // reference max (log2 units)
+    float l = 0.f;        // running sum relative to m
+    bool ok = true;
+    // interior tiles take the fused path when the scores need no mask and
+    // the scale is positive (max of raw scores = max of scaled scores)
+    const bool fast_ok = (a.sl2 > 0.f) && (a.mask == nullptr);
+    // Output of the tile (whole units: right after its loop; split units:
+    // after the CTAs of the cluster have exchanged partial results).
+    auto epilogue = [&]() {
+      const int qi = m0 + t * BM + r;
+      const bool row_ok = qi < a.Lq;
+      // A split unit: CTA `part` finalises query tile `part` (part < NQ); each
+      // other CTA sends it its partial result of that tile (O relative to
+      // 2^m, m, l): staged in its own shared memory, then one bulk copy into
+      // a slot of the finaliser's, counted on the finaliser's xbar.  Slot of
+      // CTA q at finaliser t: q - (q > t); the first ksplit - 1 slots receive,
+      // the next ones stage (a CTA that finalises nothing stages in slot t).
+      // The cluster meets once every CTA's MMAs have completed (its buffers
+      // are free) and its expectation is set, and again at the end, so that
+      // no CTA leaves while its copies may still read its shared memory.
+      uint8_t* const slotO = sRing;
+      uint8_t* const slotML = sQ;
+      if constexpr (SPLIT) {
+        for (int t2 = 0; t2 < nt; ++t2)
+          if (ok) ok = mbar_wait(&o_done[t2], 0, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        const int nin = a.ksplit - 1;
+        if (t < nt && t == part && r == 0)
+          mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(nin * (C::SLOT_O + C::SLOT_ML)));
+        const int st = part < NQ ? nin : t;  // staging slot
+        const bool send = t < nt && t != part && ok;
+        if (send) {
+          tc_fence_after();
+          float4* prow = reinterpret_cast<float4*>(slotO + st * C::SLOT_O + r * D * 4);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ob[32];
+            tmem_ld32(tO + c * 32, ob);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (l > 0.f)  // a tile that saw no key holds no O
+                v = make_float4(__uint_as_float(ob[4 * i]), __uint_as_float(ob[4 * i + 1]),
+                                __uint_as_float(ob[4 * i + 2]), __uint_as_float(ob[4 * i + 3]));
+              prow[(c * 8 + i) ^ (r & 7)] = v;
+            }
+          }
+          float* ml = reinterpret_cast<float*>(slotML + st * C::SLOT_ML);
+          ml[r] = m;
+          ml[BM + r] = l;
+          fence_proxy_async_shared();
+        }
+        named_bar_sync(kBarX + t, 128);  // the tile's rows are staged
+        __syncwarp();
+        cluster_sync_all();
+        if (send && r == 0) {
+          const uint32_t dst = static_cast<uint32_t>(t);
+          const int slot = part - (part > t ? 1 : 0);
+          const uint32_t bar = cluster_map(xbar, dst);
+          bulk_copy_to_cluster(cluster_map(slotO + slot * C::SLOT_O, dst),
+                               smem_addr(slotO + st * C::SLOT_O), C::SLOT_O, bar);
+          bulk_copy_to_cluster(cluster_map(slotML + slot * C::SLOT_ML, dst),
+                               smem_addr(slotML + st * C::SLOT_ML), C::SLOT_ML, bar);
+        }
+        // the finaliser waits for its slots whatever happened before: no CTA
+        // may leave while copies into or out of it are in flight
+        if (t < nt && t == part) {
+          const bool got = mbar_wait_cluster(xbar, 0, wc);
+          ok = __all_sync(0xffffffffu, ok && got);
+        }
+      }
+      if (t < nt && ok && (!SPLIT || t == part)) {
+        tc_fence_after();
+        // split unit: merge the other CTAs' partial results of this tile,
+        // M = max of the m's, weights 2^(m - M), l = sum of l * weight
+        float w_own = 1.f;
+        float wq[kMaxSplit - 1];
+        if constexpr (SPLIT) {
+          float M = m;
+          float mq[kMaxSplit - 1], lq[kMaxSplit - 1];
+#pragma unroll
+          for (int q = 0; q < kMaxSplit - 1; ++q) {
+            mq[q] = -INFINITY;
+            lq[q] = 0.f;
+            if (q < a.ksplit - 1) {
+              const float* ml = reinterpret_cast<const float*>(slotML + q * C::SLOT_ML);
+              mq[q] = ml[r];
+              lq[q] = ml[BM + r];
+            }
+            M = fmaxf(M, mq[q]);
+          }
+          w_own = (l > 0.f) ? ex2(m - M) : 0.f;
+          float L = (l > 0.f) ? l * w_own : 0.f;
+#pragma unroll
+          for (int q = 0; q < kMaxSplit - 1; ++q) {
+            wq[q] = (lq[q] > 0.f) ? ex2(mq[q] - M) : 0.f;
+            L += lq[q] * wq[q];
+          }
+          m = M;
+          l = L;
+        }
+        // sink logit joins the denominator only (value row 0)
+        float oscale = 1.f;
+        if (a.sinks) {
+          const float sk = a.sinks[h] * kLog2e;
+          const float mn = fmaxf(m, sk);
+          oscale = ex2(m - mn);
+          l = l * oscale + ex2(sk - mn);
+          m = mn;
+        }
+        const float inv = (l > 0.f) ? oscale / l : 0.f;
+        T* orow = static_cast<T*>(a.o) + ((static_cast<size_t>(b) * a.Hq + h) * a.Lq + qi) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ob[32];
+          tmem_ld32(tO + c * 32, ob);
+          tmem_wait_ld();
+          if constexpr (SPLIT) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              ob[i] = __float_as_uint((w_own > 0.f) ? __uint_as_float(ob[i]) * w_own : 0.f);
+#pragma unroll
+            for (int q = 0; q < kMaxSplit - 1; ++q) {
+              if (q < a.ksplit - 1) {
+                const float4* srow =
+                    reinterpret_cast<const float4*>(slotO + q * C::SLOT_O + r * D * 4);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 v = srow[(c * 8 + i) ^ (r & 7)];
+                  ob[4 * i] = __float_as_uint(fmaf(v.x, wq[q], __uint_as_float(ob[4 * i])));
+                  ob[4 * i + 1] =
+                      __float_as_uint(fmaf(v.y, wq[q], __uint_as_float(ob[4 * i + 1])));
+                  ob[4 * i + 2] =
+                      __float_as_uint(fmaf(v.z, wq[q], __uint_as_float(ob[4 * i + 2])));
+                  ob[4 * i + 3] =
+                      __float_as_uint(fmaf(v.w, wq[q], __uint_as_float(ob[4 * i + 3])));
+                }
+              }
+            }
+          }
+          if constexpr (X3) {  // fp32 output
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              ob[i] = __float_as_uint((inv == 0.f) ? 0.f : __uint_as_float(ob[i]) * inv);
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+            }
+          } else {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float v0 = (inv == 0.f) ? 0.f : __uint_as_float(ob[2 * i]) * inv;
+              const float v1 = (inv == 0.f) ? 0.f : __uint_as_float(ob[2 * i + 1]) * inv;
+              w[i] = E::pack(v0, v1);
+            }
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+          }
+        }
+        if (row_ok && a.lse) {
+          a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.Lq + qi] =
+              (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        }
+      }
+      if constexpr (SPLIT) {  // every copy has landed before any CTA of the cluster leaves
+        __syncwarp();
+        cluster_sync_all();
+      }
+    };
+    if (t < nt) {
+      for (int j = 0; j < nkv[t]; ++j) {
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[t], j & 1, wc));
+        if (ok) {
+          tc_fence_after();
+          uint32_t s[BN];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c)
+            tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+          tmem_wait_ld();
+          const int kv0 = j * BN;
+          float alpha = 1.f;
+          bool resc;
+          float rs;
+          uint32_t pk[BN / 2];
+          uint32_t pk2[X3 ? BN / 2 : 1];  // P_lo (X3)
+          const bool fast = fast_ok && kv0 + BN - 1 <= limit;
+          if constexpr (X3) {
+            // bf16 hi/lo P: computed half a row at a time and stored to TMEM
+            // as soon as each half exists, so that the 128 scores plus one
+            // half of P_hi and P_lo are the most that is live at once.  The
+            // scores are used raw with p = 2^(s * scale*log2e - m) on the
+            // fused path, and as scaled, masked x = s * scale*log2e + bias
+            // (rewritten in place) with p = 2^(x - m) elsewhere.
+            float mul = a.sl2;
+            if (!fast) {
+#pragma unroll
+              for (int i = 0; i < BN; ++i) {
+                float x = __uint_as_float(s[i]) * a.sl2;
+                if (mrow && kv0 + i <= limit) x += to_float(mrow[kv0 + i]) * kLog2e;
+                if (kv0 + i > limit) x = -INFINITY;
+                s[i] = __float_as_uint(x);
+              }
+              mul = 1.f;
+            }
+            // fused rows with a reference max skip the tile max, others take it
+            bool need_max = !fast || !(m > -INFINITY);
+            resc = false;
+            for (int pass = 0; pass < 2; ++pass) {
+              if (need_max) {
+                float mr[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
+#pragma unroll
+                for (int i = 8; i < BN; i += 16)
+#pragma unroll
+                  for (int c = 0; c < 8; ++c)
+                    mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]),
+                                  __uint_as_float(s[i + 2 * c + 1]));
+                const float mx = fmaxf(fmax3(mr[0], mr[1], mr[2]),
+                                       fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7]))) *
+                                 mul;
+                // the fused path always moves to the tile max; the general
+                // path only when it grew by more than the threshold
+                if (fast || mx > m + kRescaleThreshold) {
+                  alpha = ex2(m - mx);  // 0 when m = -inf
+                  m = mx;
+                  resc = true;
+                }
+              }
+              const float mu = (m == -INFINITY) ? 0.f : m;
+              if (pass > 0) tmem_wait_st();  // the first pass's P is overwritten
+              float rs0, rs1;
+              softmax_pairs<BF16, BN / 2, true>(
+                  *reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[0]), mul, mu,
+                  *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[0]), rs0, &pk2[0]);
+              tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+              tmem_st32(tS + BN / 2, *reinterpret_cast<uint32_t(*)[32]>(&pk2[0]));
+              softmax_pairs<BF16, BN / 2, true>(
+                  *reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[BN / 2]), mul, mu,
+                  *reinterpret_cast<uint32_t(*)[BN / 4]>(&pk[BN / 4]), rs1, &pk2[BN / 4]);
+              tmem_st32(tS + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk[BN / 4]));
+              tmem_st32(tS + BN / 2 + BN / 4, *reinterpret_cast<uint32_t(*)[32]>(&pk2[BN / 4]));
+              rs = rs0 + rs1;
+              // a fused row whose sum exceeds 2^15 (its max grew) takes the
+              // tile max and the warp computes the tile again; the second
+              // pass cannot fail (every p <= 1)
+              const bool redo = fast && !need_max && !(rs <= kFusedSumLimit);
+              if (!__any_sync(0xffffffffu, redo)) break;
+              need_max = redo;
+            }
+          } else if (D == 128 ? fast_ok : fast) {
+            // Positive scale, no mask: p = 2^(s * scale*log2e - m) with the
+            // scale folded into one packed FMA per pair, taken against the
+            // current reference max m without looking for the tile max.
+            // Every p is at most the row sum, so a sum <= 2^15 proves all
+            // p <= 2^15 (exact range in fp16 and bf16); only a row whose sum
+            // exceeds it (its max grew) or that has no max yet finds the tile
+            // max of the raw scores and repeats.  At D = 128 the tiles that
+            // cross the row's last visible key (bounds, causal diagonal) take
+            // this path too, with the keys past it scored -inf; at D = 64,
+            // where the softmax warps set the pace, they stay on the general
+            // path below (measured: routing them here slowed the loop).
+            if (!fast) {
+              const int nvis = limit - kv0 + 1;  // visible keys of the row here
+#pragma unroll
+              for (int i = 0; i < BN; ++i)
+                if (i >= nvis) s[i] = 0xff800000u;  // -inf
+            }
+            resc = !(m > -INFINITY);
+            if (!resc) {
+              softmax_pairs<BF16, BN>(s, a.sl2, m, pk, rs);
+              resc = !(rs <= kFusedSumLimit);  // also true for inf or nan
+            }
+            if (resc) {
+              const float mx = row_max_raw(s) * a.sl2;  // -inf: no visible key
+              // (at D = 128 a row may see no key of a masked tile: m stays)
+              if (D == 64 || mx > -INFINITY) {
+                alpha = ex2(m - mx);  // 0 when m = -inf
+                m = mx;
+              }
+              softmax_pairs<BF16, BN>(s, a.sl2, (D == 128 && m == -INFINITY) ? 0.f : m, pk, rs);
+            }
+          } else {
+            float x[BN];
+#pragma unroll
+            for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(s[i]) * a.sl2;
+            if (mrow) {
+#pragma unroll
+              for (int i = 0; i < BN; ++i)
+                if (kv0 + i <= limit) x[i] += to_float(mrow[kv0 + i]) * kLog2e;
+            }
+            if (kv0 + BN - 1 > limit) {
+#pragma unroll
+              for (int i = 0; i < BN; ++i)
+                if (kv0 + i > limit) x[i] = -INFINITY;
+            }
+            float mr[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+            for (int i = 4; i < BN; i += 8)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) mr[c] = fmax3(mr[c], x[i + 2 * c], x[i + 2 * c + 1]);
+            const float mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+            resc = mx > m + kRescaleThreshold;  // true on the first visible tile
+            if (resc) {
+              alpha = ex2(m - mx);  // 0 when m = -inf
+              m = mx;
+            }
+            const float mu = (m == -INFINITY) ? 0.f : m;
+            float rp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < BN / 2; ++i) {
+              const float p0 = ex2(x[2 * i] - mu);
+              const float p1 = ex2(x[2 * i + 1] - mu);
+              rp[i & 3] += p0 + p1;
+              pk[i] = E::pack(p0, p1);
+            }
+            rs = (rp[0] + rp[1]) + (rp[2] + rp[3]);
+          }
+          __syncwarp();
+          l = l * alpha + rs;
+          // O_t holds the sum through PV_{t,j-1} (complete: the commit behind
+          // s_full tracks every earlier MMA); rescale rows whose max moved.
+          if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ob[32];
+              tmem_ld32(tO + c * 32, ob);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ob[i] = __float_as_uint(__uint_as_float(ob[i]) * alpha);
+              tmem_st32(tO + c * 32, ob);
+            }
+          }
+          if constexpr (!X3) {
+            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+          }
+          tmem_wait_st();
+          tc_fence_before();
+        }
+        // hand P_t,j to the MMA warp; met every step, also after a failed wait
+        named_bar_sync(kBarP + t, 32 * 5);
+      }
+      if (ok) ok = mbar_wait(&o_done[t], 0, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if constexpr (!SPLIT) epilogue();
+    }
+    if constexpr (SPLIT) epilogue();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (warp == kLoadWarp && lane == 0 && *abort_flag) {
+    // a role gave up: every copy the producer issued lands before the CTA exits
+    drain_wait(q_full, 0, kDrainNs);
+    for (int s = 0; s < C::NS; ++s)
+      if (last_use[s] >= 0) drain_wait(&full[s], last_use[s] & 1, kDrainNs);
+  }
+  // a split grid ends after the grid of whole units that it overlaps
+  if constexpr (SPLIT) griddep_wait();
+}
+
+// kv_plane_rows: rows per (batch, kv head) in k, v, k2, v2 as passed here
+template <int D, bool BF16, bool X3, bool LENS>
+sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, const void* v,
+                          const void* q2, const void* k2, const void* v2, void* o, float* lse,
+                          uint64_t kv_plane_rows, const LaunchEnv& env, int* grids) {
+  using C = Cfg<D, X3>;
+  const CUtensorMapDataType dt =
+      BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t qz = static_cast<uint64_t>(p.batch) * p.num_q_heads;
+  const uint64_t kz = static_cast<uint64_t>(p.batch) * p.num_kv_heads;
+  // k, v rows per (batch, kv head) may exceed seq_len_kv (a KV cache); the
+  // maps stop at seq_len_kv, so rows past it read as zero and are never loaded
+  const uint64_t cap = kv_plane_rows;
+  CUtensorMap tq, tk, tv, tq2, tk2, tv2;
+  // [B*H, L, D] viewed innermost-first; box 64 x 128 rows, 128-byte swizzle.
+  if (!encode_tiled_3d(&tq, dt, q, D, p.seq_len_q, qz, 2, 64, BM) ||
+      !encode_tiled_3d(&tk, dt, k, D, p.seq_len_kv, kz, 2, 64, BN, cap) ||
+      !encode_tiled_3d(&tv, dt, v, D, p.seq_len_kv, kz, 2, 64, BN, cap))
+    return SDPA_ERR_CUDA;
+  if (X3) {
+    if (!encode_tiled_3d(&tq2, dt, q2, D, p.seq_len_q, qz, 2, 64, BM) ||
+        !encode_tiled_3d(&tk2, dt, k2, D, p.seq_len_kv, kz, 2, 64, BN, cap) ||
+        !encode_tiled_3d(&tv2, dt, v2, D, p.seq_len_kv, kz, 2, 64, BN, cap))
+      return SDPA_ERR_CUDA;
+  } else {
+    tq2 = tq;
+    tk2 = tk;
+    tv2 = tv;
+  }
+  PrefillArgs a;
+  a.B = p.batch;
+  a.Hq = p.num_q_heads;
+  a.Hkv = p.num_kv_heads;
+  a.G = p.num_q_heads / p.num_kv_heads;
+  a.Lq = p.seq_len_q;
+  a.Lk = p.seq_len_kv;
+  a.num_qblocks = (p.seq_len_q + BM * NQ - 1) / (BM * NQ);
+  a.sl2 = p.scale * kLog2e;
+  a.causal = p.causal ? 1 : 0;
+  a.mask = p.mask;
+  a.ms0 = p.mask_stride[0];
+  a.ms1 = p.mask_stride[1];
+  a.ms2 = p.mask_stride[2];
+  a.sinks = p.sinks;
+  a.o = o;
+  a.lse = lse;
+  a.status = env.status;
+  a.wait_ns = env.wait_limit_ns;
+  a.seq_lens_q = p.seq_lens_q;
+  a.seq_lens_kv = p.seq_lens_kv;
+  auto kern = prefill_tc_kernel<D, BF16, X3, LENS, false>;
+  auto kern_split = prefill_tc_kernel<D, BF16, X3, LENS, true>;
+  // The setmaxnreg split must fit the registers the kernel is launched with
+  // (an increase beyond them would wait forever): check the compiled count
+  // once per instantiation.
+  static int regs_ok[2] = {0, 0};  // 0 unknown, 1 fits, -1 does not
+  for (int v2 = 0; v2 < 2; ++v2) {
+    if (regs_ok[v2] == 0) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, v2 ? kern_split : kern) != cudaSuccess) return SDPA_ERR_CUDA;
+      const long alloc = static_cast<long>((fa.numRegs + 7) & ~7) * kThreads;
+      const long need =
+          32L * (kSoftmaxWarps * static_cast<long>(kSoftmaxRegs) + 4L * kControlRegs);
+      regs_ok[v2] = alloc >= need ? 1 : -1;
+    }
+    if (regs_ok[v2] < 0) return SDPA_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(v2 ? kern_split : kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+  }
+  // One CTA per SM: the last wave of units is partial when the unit count is
+  // not a multiple of the SM count.  Those units go to a second grid that
+  // splits each over its key tiles among the CTAs of a cluster (2 or 4,
+  // whichever fits the free SMs), so that the last wave lasts a split, not a
+  // whole unit; it starts while the first grid drains (programmatic
+  // dependent launch).  Causal units differ in length and are ordered
+  // heaviest first instead.
+  const long long units = static_cast<long long>(a.num_qblocks) * p.num_q_heads * p.batch;
+  if (units > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
+  const int U = static_cast<int>(units);
+  const int nkv = (p.seq_len_kv + BN - 1) / BN;
+  int ksplit = 1, tail = 0;
+  const char* force = getenv("GB300_SDPA_PREFILL_SPLIT");  // test override
+  const int forced = force ? atoi(force) : -1;             // 0: never; 2, 4: every unit
+  if (!p.causal && forced != 0) {
+    static int active[2] = {0, 0};  // clusters of 2, 4 that can be resident (-1: none)
+    const int r = U % env.num_sms;
+    // (a split count above C::MAX_SPLIT would overflow the finaliser's slots)
+    const int fk = forced > C::MAX_SPLIT ? C::MAX_SPLIT : forced;
+    for (int k = C::MAX_SPLIT; k >= 2; k /= 2) {
+      const bool want =
+          (fk == k) || (fk < 0 && r > 0 && k * r <= env.num_sms && nkv >= 4 * k);
+      if (!want) continue;
+      int& act = active[k == 2 ? 0 : 1];
+      if (act == 0) {
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = static_cast<unsigned>(k);
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t oc = {};
+        oc.gridDim = dim3(static_cast<unsigned>(k * env.num_sms));
+        oc.blockDim = dim3(kThreads);
+        oc.dynamicSmemBytes = C::SMEM;
+        oc.attrs = at;
+        oc.numAttrs = 1;
+        int n = 0;
+        act = (cudaOccupancyMaxActiveClusters(&n, kern_split, &oc) == cudaSuccess && n > 0) ? n
+                                                                                          : -1;
+        cudaGetLastError();
+      }
+      if (fk == k && act > 0) {
+        ksplit = k;
+        tail = U;
+        break;
+      }
+      if (act >= r) {  // every split unit of the last wave runs at once
+        ksplit = k;
+        tail = r;
+        break;
+      }
+    }
+  }
+  const int n_whole = U - tail;
+  *grids = 0;
+  if (n_whole > 0) {
+    a.unit0 = 0;
+    a.ksplit = 1;
+    kern<<<dim3(static_cast<unsigned>(n_whole)), kThreads, C::SMEM, env.stream>>>(tq, tk, tv, tq2,
+                                                                                  tk2, tv2, a);
+    if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
+    *grids = 1;
+  }
+  if (tail == 0) return SDPA_OK;
+  a.unit0 = n_whole;
+  a.ksplit = ksplit;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(ksplit);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ksplit * tail));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = env.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n_whole > 0 ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, kern_split, tq, tk, tv, tq2, tk2, tv2, a) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  *grids += 1;
+  return SDPA_OK;
+}
+
+}  // namespace
+
+// Head-size entry points (one translation unit each); `grids` receives the
+// number of grids launched (1, or 2 when the last wave is split).
+sdpa_status_t launch_prefill_tc_d64(const sdpa_params_t& p, const void* q, const void* k,
+                                    const void* v, void* o, float* lse, uint64_t kv_plane_rows,
+                                    const LaunchEnv& env, int* grids);
+sdpa_status_t launch_prefill_tc_d128(const sdpa_params_t& p, const void* q, const void* k,
+                                     const void* v, void* o, float* lse, uint64_t kv_plane_rows,
+                                     const LaunchEnv& env, int* grids);
+
+}  // namespace gb300

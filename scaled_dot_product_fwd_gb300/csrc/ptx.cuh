@@ -91,6 +91,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// The same wait with cluster-scope acquire: for a phase completed by copies
+// that other CTAs of the cluster issued.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded by limit_ns only (not by the abort flag): copies in flight into
+// this CTA must land before it leaves.  On timeout it reports the status.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  const WaitCtl& w) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((n & 15u) == 0 && globaltimer_ns() - t0 > w.limit_ns) {
+      *w.abort_flag = 1;
+      atomicExch(w.status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------- TMA
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.
@@ -302,6 +331,58 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // of times: it has no time limit).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Thread-block cluster helpers: barrier over every thread of the cluster
+// (exited threads count as arrived; whole warps), this CTA's rank, the
+// address in another CTA of the cluster that corresponds to `local` in this
+// one, and a 32-bit load from such an address.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_map(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+  return ra;
+}
+__device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_map(local, rank)) : "memory");
+  return v;
+}
+// Bulk copy of `bytes` from this CTA's shared memory (src) to the shared
+// memory of a CTA of the cluster (dst, a cluster address); completion is
+// counted in bytes on the mbarrier at `bar` (a cluster address in the
+// destination CTA).  Both addresses 16-byte aligned; bytes a multiple of 16.
+// The source must not change until the copy has completed.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Orders this thread's generic-proxy writes to shared memory before later
+// reads of it by the async proxy (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Programmatic dependent launch: a grid lets the next grid of its stream
+// (launched with programmatic stream serialization) start before it ends;
+// that grid waits for the earlier one to complete, with its memory visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace gb300

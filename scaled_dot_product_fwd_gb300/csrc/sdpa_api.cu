@@ -202,18 +202,14 @@ sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k,
   env.num_sms = num_sms;
   env.stream = static_cast<cudaStream_t>(stream);
   switch (kern) {
-    case SDPA_KERNEL_PREFILL_TC:
-      st = gb300::launch_prefill_tc(*p, q, k, v, o, lse, env);
-      if (st == SDPA_OK) g_last_launches = 1;
-      return st;
+    case SDPA_KERNEL_PREFILL_TC:  // sets the count itself (1 or 2 grids)
+      return gb300::launch_prefill_tc(*p, q, k, v, o, lse, env);
     case SDPA_KERNEL_PREFILL_F32:
       st = gb300::launch_prefill_f32(*p, q, k, v, o, lse, env);
       if (st == SDPA_OK) g_last_launches = 1;
       return st;
-    case SDPA_KERNEL_PREFILL_TC_F32:  // hi/lo split, then the prefill kernel
-      st = gb300::launch_prefill_x3(*p, q, k, v, o, lse, workspace, env);
-      if (st == SDPA_OK) g_last_launches = 2;
-      return st;
+    case SDPA_KERNEL_PREFILL_TC_F32:  // hi/lo split, then the prefill grids (sets the count)
+      return gb300::launch_prefill_x3(*p, q, k, v, o, lse, workspace, env);
     case SDPA_KERNEL_DECODE_SPLITKV:  // sets the count itself (1 or 2 kernels)
       return gb300::launch_decode(*p, plan, q, k, v, o, lse, workspace, env);
     case SDPA_KERNEL_NO_KEYS:

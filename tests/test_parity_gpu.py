@@ -118,7 +118,10 @@ def test_decode_long_full(cuda):
 
 # ---------------------------------------------------- small shapes, all rows
 PREFILL_SHAPES = [(2, 4, 2, 300, 333), (1, 2, 1, 129, 129), (1, 3, 3, 7, 200), (1, 1, 1, 2, 1),
-                  (1, 2, 2, 256, 256), (2, 8, 1, 97, 1000), (1, 2, 1, 513, 520)]
+                  (1, 2, 2, 256, 256), (2, 8, 1, 97, 1000), (1, 2, 1, 513, 520),
+                  # key tails of exactly one 32-key chunk, of three chunks with a
+                  # short first tile, and of 26 keys under a causal offset
+                  (1, 2, 1, 160, 160), (1, 4, 2, 64, 224), (1, 2, 2, 200, 4250)]
 
 
 @pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
@@ -459,3 +462,44 @@ def test_kv_view_long_decode_and_few_queries(cuda):
 def test_kv_view_noalloc(cuda):
     _kv_view_check(2, 32, 4, 1, 1024, 1100, 512, "bfloat16", False, sinks=True,
                    lens_q=[1, 1], lens_kv=[1000, 3], noalloc=True)
+
+
+# --------------------------------------- prefill units split over a cluster
+SPLIT_CASES = {
+    "f16_d64_gqa": wl(2, 4, 2, 300, 1000, 64, "float16"),
+    "bf16_d128_sinks": wl(1, 3, 1, 260, 333, 128, "bfloat16", sinks=True),
+    # fp32 at D = 64 (bf16 hi/lo products); two key tiles: with four CTAs two
+    # of them have no key tile
+    "f32_d64_two_tiles": wl(1, 2, 2, 129, 200, 64, "float32"),
+    # one key tile: every CTA but one has none; additive mask
+    "f16_d128_mask_one_tile": wl(1, 2, 1, 140, 100, 128, "float16", mask="full"),
+}
+
+
+@pytest.mark.parametrize("ksplit", ["2", "4"])
+@pytest.mark.parametrize("case", sorted(SPLIT_CASES))
+def test_prefill_forced_split(cuda, ksplit, case, monkeypatch):
+    """Every query-block unit split over its key tiles among the 2 or 4 CTAs
+    of a cluster, the partial results merged through distributed shared
+    memory (the form the last partial wave of units takes)."""
+    monkeypatch.setenv("GB300_SDPA_PREFILL_SPLIT", ksplit)
+    check(cuda, SPLIT_CASES[case])
+
+
+@pytest.mark.parametrize("ksplit", ["2", "4"])
+def test_prefill_forced_split_kv_view(cuda, ksplit, monkeypatch):
+    """Split units with per-batch key lengths (some batches shorter than the
+    split count in key tiles, one with no key at all)."""
+    monkeypatch.setenv("GB300_SDPA_PREFILL_SPLIT", ksplit)
+    _kv_view_check(3, 4, 2, 260, 600, 700, 64, "float16", False, sinks=True,
+                   lens_q=[260, 150, 0], lens_kv=[600, 100, 0])
+
+
+def test_prefill_split_off_matches_default(cuda, monkeypatch):
+    """The DiT shape (1292 units: a half-empty last wave on 152 SMs) with and
+    without the split of its last wave: both against the oracle."""
+    w = W.DIT_F16
+    rows = sample_rows(w, n_random=200, tail=40)
+    check(cuda, w, rows)
+    monkeypatch.setenv("GB300_SDPA_PREFILL_SPLIT", "0")
+    check(cuda, w, rows)
