@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define SDPA_ABI_VERSION 2
+#define SDPA_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define SDPA_API __attribute__((visibility("default")))
@@ -123,7 +123,15 @@ typedef enum {
  *      whole key tiles, so v rows [seq_lens_kv[b], seq_len_kv) meet zero
  *      weights there and must hold finite values (rows past seq_len_kv are
  *      never read).
+ *  flags: 0 or SDPA_FLAG_SHARED_GPU (other bits must be 0, else
+ *      SDPA_ERR_INVALID_ARGUMENT).
  */
+/* The call runs beside other work on the GPU (kernels of other streams):
+ * launch shapes are not fitted to an idle GPU.  Without it, a prefill whose
+ * query-tile units leave a partial last wave on the SMs shares the key tiles
+ * of those units among the CTAs of thread-block clusters (a second, shorter
+ * grid); with it, every unit runs whole. */
+#define SDPA_FLAG_SHARED_GPU 0x1u
 typedef struct {
   int32_t batch;
   int32_t num_q_heads;
@@ -139,7 +147,7 @@ typedef struct {
   int64_t mask_stride[4];
   const float* sinks;
   int32_t kv_capacity;          /* ABI 2 */
-  int32_t reserved1;
+  uint32_t flags;               /* ABI 3 (was reserved, 0) */
   const int32_t* seq_lens_q;    /* ABI 2 */
   const int32_t* seq_lens_kv;   /* ABI 2 */
 } sdpa_params_t;

@@ -17,6 +17,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsdpa_gb300.so")
 
 SDPA_F32, SDPA_F16, SDPA_BF16 = 0, 1, 2
+SDPA_FLAG_SHARED_GPU = 0x1
 STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARGUMENT", 2: "SDPA_ERR_UNSUPPORTED",
           3: "SDPA_ERR_MISALIGNED", 4: "SDPA_ERR_WORKSPACE_TOO_SMALL", 5: "SDPA_ERR_CUDA",
           6: "SDPA_ERR_TIMEOUT"}
@@ -38,7 +39,7 @@ class SdpaParams(ctypes.Structure):
                 ("causal", ctypes.c_int32), ("reserved0", ctypes.c_int32),
                 ("mask", ctypes.c_void_p), ("mask_stride", ctypes.c_int64 * 4),
                 ("sinks", ctypes.c_void_p), ("kv_capacity", ctypes.c_int32),
-                ("reserved1", ctypes.c_int32), ("seq_lens_q", ctypes.c_void_p),
+                ("flags", ctypes.c_uint32), ("seq_lens_q", ctypes.c_void_p),
                 ("seq_lens_kv", ctypes.c_void_p)]
 
 
@@ -85,7 +86,7 @@ def load_library(path: str = LIB_PATH):
 
 def make_params(B, Hq, Hkv, Lq, Lk, D, dtype, scale, causal=False, mask_ptr=None,
                 mask_stride=(0, 0, 0, 1), sinks_ptr=None, kv_capacity=0, seq_lens_q_ptr=None,
-                seq_lens_kv_ptr=None) -> SdpaParams:
+                seq_lens_kv_ptr=None, flags=0) -> SdpaParams:
     p = SdpaParams()
     p.batch, p.num_q_heads, p.num_kv_heads = int(B), int(Hq), int(Hkv)
     p.seq_len_q, p.seq_len_kv, p.head_dim = int(Lq), int(Lk), int(D)
@@ -98,7 +99,7 @@ def make_params(B, Hq, Hkv, Lq, Lk, D, dtype, scale, causal=False, mask_ptr=None
         p.mask_stride[i] = int(mask_stride[i])
     p.sinks = sinks_ptr
     p.kv_capacity = int(kv_capacity)
-    p.reserved1 = 0
+    p.flags = int(flags)
     p.seq_lens_q = seq_lens_q_ptr
     p.seq_lens_kv = seq_lens_kv_ptr
     return p
@@ -179,7 +180,7 @@ def _workspace(nbytes: int, device):
 
 def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=None,
                  lse=None, return_lse=True, workspace=None, stream=None, kv_len=None,
-                 seq_lens_q=None, seq_lens_kv=None):
+                 seq_lens_q=None, seq_lens_kv=None, shared_gpu=False):
     """O (and LSE) of softmax(scale * q k^T + mask [+ sinks]) v on the GPU.
 
     q [B, Hq, Lq, D], k/v [B, Hkv, C, D]: contiguous CUDA tensors of one
@@ -189,7 +190,9 @@ def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=N
     [B, Hq, Lq, Lk] (additive).  sinks: None or float32 [Hq].  seq_lens_q,
     seq_lens_kv: None or int32 CUDA tensors [B] of per-batch lengths (padding
     masks; rows past a batch's query length see no key).  scale defaults to
-    1/sqrt(D).  Returns (o, lse) or o.
+    1/sqrt(D).  shared_gpu: the call runs beside other kernels (sets
+    SDPA_FLAG_SHARED_GPU: launch shapes not fitted to an idle GPU).  Returns
+    (o, lse) or o.
     """
     torch = _torch()
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -237,7 +240,7 @@ def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=N
         sinks_ptr = sinks.data_ptr()
     params = make_params(B, Hq, Hkv, Lq, Lk, D, dt, scale, causal, mask_ptr, mstride, sinks_ptr,
                          kv_capacity=cap if cap != Lk else 0, seq_lens_q_ptr=lens[0],
-                         seq_lens_kv_ptr=lens[1])
+                         seq_lens_kv_ptr=lens[1], flags=SDPA_FLAG_SHARED_GPU if shared_gpu else 0)
     if out is None:
         out = torch.empty((B, Hq, Lq, D), dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
@@ -392,7 +395,7 @@ def _host_pipeline(torch, c, q, k, v, scale, causal, mask, sinks, out, lse, chun
                          mask=None if mexp is None else mexp[b:b + 1, g0:g1],
                          sinks=None if sinks is None else sinks[g0:g1],
                          out=c["o"][b:b + 1, g0:g1], lse=c["l"][b:b + 1, g0:g1],
-                         workspace=ws[i % 2])
+                         workspace=ws[i % 2], shared_gpu=True)
             e_c = torch.cuda.Event()
             e_c.record(s_c)
         s_out.wait_event(e_c)

@@ -1052,7 +1052,8 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   int ksplit = 1, tail = 0;
   const char* force = getenv("GB300_SDPA_PREFILL_SPLIT");  // test override
   const int forced = force ? atoi(force) : -1;             // 0: never; 2, 4: every unit
-  if (!p.causal && forced != 0) {
+  // (not for a call that shares the GPU: its last wave is not idle SMs)
+  if (!p.causal && forced != 0 && (forced > 0 || !(p.flags & SDPA_FLAG_SHARED_GPU))) {
     static int active[2] = {0, 0};  // clusters of 2, 4 that can be resident (-1: none)
     const int r = U % env.num_sms;
     // (a split count above C::MAX_SPLIT would overflow the finaliser's slots)

@@ -54,6 +54,7 @@ sdpa_status_t validate_problem(const sdpa_params_t* p) {
       if (p->mask_stride[i] < 0) return SDPA_ERR_INVALID_ARGUMENT;
     if (p->mask_stride[3] != 1) return SDPA_ERR_INVALID_ARGUMENT;
   }
+  if ((p->flags & ~SDPA_FLAG_SHARED_GPU) != 0) return SDPA_ERR_INVALID_ARGUMENT;
   if (p->kv_capacity < 0 || (p->kv_capacity > 0 && p->kv_capacity < p->seq_len_kv))
     return SDPA_ERR_INVALID_ARGUMENT;
   if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 512) return SDPA_ERR_UNSUPPORTED;

@@ -52,7 +52,7 @@ def test_launch_count_is_zero_after_a_rejected_call(sdpa_lib):
 
 
 def test_abi_version_and_status_strings(sdpa_lib):
-    assert S.sdpa_abi_version() == 2
+    assert S.sdpa_abi_version() == 3
     assert S.sdpa_status_string(0) == "ok"
     assert S.sdpa_status_string(2) == "unsupported problem"
     assert S.sdpa_status_string(99) == "unknown status"
@@ -173,6 +173,15 @@ def test_host_entry_pieces_cover_every_head_once(nb, hkv, chunks):
     assert all(0 <= h0 < h1 <= hkv for _, h0, h1 in pieces)
     # every batch in about chunks / nb pieces
     assert len(pieces) == nb * min(hkv, -(-chunks // nb))
+
+
+def test_flags_are_checked(sdpa_lib):
+    p = S.make_params(1, 4, 2, 300, 300, 64, S.SDPA_F16, 0.125, flags=S.SDPA_FLAG_SHARED_GPU)
+    assert S.sdpa_select_kernel(p) == ("prefill_tc", 0)
+    for bad in (2, 0x80000000):
+        p = S.make_params(1, 4, 2, 300, 300, 64, S.SDPA_F16, 0.125, flags=bad)
+        assert S.sdpa_select_kernel(p) == ("none", 1)
+        assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, None, 0, None) == 1
 
 
 def test_kv_capacity_and_length_arrays_are_checked(sdpa_lib):

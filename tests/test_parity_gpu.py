@@ -495,11 +495,24 @@ def test_prefill_forced_split_kv_view(cuda, ksplit, monkeypatch):
                    lens_q=[260, 150, 0], lens_kv=[600, 100, 0])
 
 
-def test_prefill_split_off_matches_default(cuda, monkeypatch):
-    """The DiT shape (1292 units: a half-empty last wave on 152 SMs) with and
-    without the split of its last wave: both against the oracle."""
+def test_prefill_tail_split_and_shared_gpu(cuda):
+    """The DiT shape (1292 units: a half-empty last wave on 152 SMs): by
+    default its last wave goes to a second, split grid; with shared_gpu
+    (SDPA_FLAG_SHARED_GPU) every unit runs whole in one grid.  Both against
+    the oracle."""
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
     w = W.DIT_F16
     rows = sample_rows(w, n_random=200, tail=40)
-    check(cuda, w, rows)
-    monkeypatch.setenv("GB300_SDPA_PREFILL_SPLIT", "0")
-    check(cuda, w, rows)
+    inp = W.make_inputs(w)
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    o_ref, lse_ref = oracle_rows(w, inp, rows)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    units = w.B * w.Hq * (-(-w.Lq // 256))
+    r = units % nsm
+    for shared in (False, True):
+        o, lse = S.sdpa_forward(q, k, v, scale=w.scale, shared_gpu=shared)
+        torch.cuda.synchronize()
+        grids = S.sdpa_last_launch_count()
+        assert grids == (1 if shared or r == 0 or 2 * r > nsm else 2)
+        compare(w, o.cpu(), lse.cpu(), o_ref, lse_ref, rows)
