@@ -21,8 +21,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Layout: q is [B, Hq, Lq, D], k and v are [B, Hkv, Lk, D], o is
- *    [B, Hq, Lq, D], all dense row-major ("contiguous"), element type
- *    params->dtype.  lse is [B, Hq, Lq] float32, dense.  The query head h
+ *    [B, Hq, Lq, D], element type params->dtype, dense row-major
+ *    ("contiguous") unless SDPA_FLAG_STRIDES gives their strides (the D
+ *    dimension stays contiguous).  lse is [B, Hq, Lq] float32, dense.  The query head h
  *    reads key/value head floor(h / (Hq / Hkv)) (contiguous head groups).
  *  - Pointers q, k, v, o, lse, mask, sinks and workspace are DEVICE pointers
  *    owned by the caller; the library never allocates, frees or retains them.
@@ -47,7 +48,7 @@
 extern "C" {
 #endif
 
-#define SDPA_ABI_VERSION 3
+#define SDPA_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define SDPA_API __attribute__((visibility("default")))
@@ -103,8 +104,11 @@ typedef enum {
  *  mask: NULL or an additive bias added to the scaled scores, element type
  *      dtype, addressed as mask[b*s0 + h*s1 + i*s2 + j*s3] with
  *      mask_stride = {s0, s1, s2, s3} in ELEMENTS; a stride of 0 broadcasts
- *      that dimension; s3 must be 1.  -inf entries remove a key.  When both
- *      mask and causal are given, both apply.
+ *      that dimension; s3 must be 1.  -inf entries remove a key.  With
+ *      SDPA_FLAG_BOOL_MASK it is a boolean mask instead: one byte per
+ *      element (same addressing, strides in bytes), nonzero = the key is
+ *      visible to the query, zero = removed.  When both mask and causal are
+ *      given, both apply.
  *  sinks: NULL or float32 [Hq]: one extra logit per query head that enters
  *      the softmax denominator only (a key with a zero value row).  It is
  *      not multiplied by scale and not masked.
@@ -123,8 +127,15 @@ typedef enum {
  *      whole key tiles, so v rows [seq_lens_kv[b], seq_len_kv) meet zero
  *      weights there and must hold finite values (rows past seq_len_kv are
  *      never read).
- *  flags: 0 or SDPA_FLAG_SHARED_GPU (other bits must be 0, else
+ *  flags: an OR of the SDPA_FLAG_* bits below (other bits must be 0, else
  *      SDPA_ERR_INVALID_ARGUMENT).
+ *  q_stride, k_stride, v_stride, o_stride (ABI 4): read only with
+ *      SDPA_FLAG_STRIDES (a caller built against ABI 3 leaves the flag clear
+ *      and need not provide them).  Element strides of dimensions B, H and L
+ *      of each tensor (D is contiguous), each >= 0 and, times the element
+ *      size, a multiple of 16 bytes; o must not overlap q, k or v.  They
+ *      replace the dense layout and kv_capacity (which must then be 0).
+ *      Example: [B, L, H, D] tensors ("BSHD") have strides {L*H*D, D, H*D}.
  */
 /* The call runs beside other work on the GPU (kernels of other streams):
  * launch shapes are not fitted to an idle GPU.  Without it, a prefill whose
@@ -132,6 +143,10 @@ typedef enum {
  * of those units among the CTAs of thread-block clusters (a second, shorter
  * grid); with it, every unit runs whole. */
 #define SDPA_FLAG_SHARED_GPU 0x1u
+/* mask is boolean (bytes, nonzero = visible) instead of an additive bias. */
+#define SDPA_FLAG_BOOL_MASK 0x2u
+/* q_stride, k_stride, v_stride and o_stride give the tensors' layouts. */
+#define SDPA_FLAG_STRIDES 0x4u
 typedef struct {
   int32_t batch;
   int32_t num_q_heads;
@@ -150,6 +165,10 @@ typedef struct {
   uint32_t flags;               /* ABI 3 (was reserved, 0) */
   const int32_t* seq_lens_q;    /* ABI 2 */
   const int32_t* seq_lens_kv;   /* ABI 2 */
+  int64_t q_stride[3];          /* ABI 4, with SDPA_FLAG_STRIDES */
+  int64_t k_stride[3];
+  int64_t v_stride[3];
+  int64_t o_stride[3];
 } sdpa_params_t;
 
 /*

@@ -97,6 +97,13 @@ def _prepare(q, k, v, mask, sinks, rows):
         raise ValueError("shape mismatch")
     mstride = None
     if mask is not None:
+        mask = np.asarray(mask)
+        if mask.dtype == np.bool_:
+            # A boolean mask keeps the keys it marks True and removes the
+            # others (mlx 0.30.7 scaled_dot_product_attention.cpp: the CUDA
+            # backend declares no boolean-mask support, so a boolean mask
+            # reaches it as the additive mask 0 / -inf).
+            mask = np.where(mask, 0.0, -np.inf)
         mask = np.ascontiguousarray(mask, dtype=np.float64)
         view = np.broadcast_to(mask, (B, Hq, Lq, Lk))
         mstride = np.array([s // 8 for s in view.strides], dtype=np.int64)

@@ -8,7 +8,7 @@ The work runs in the CUDA kernels of ``libsdpa_gb300.so`` (C ABI in
 ``include/sdpa.h``); this package only marshals arguments.
 """
 from ._binding import (EXPORTS, KERNELS, LIB_PATH, SDPA_BF16, SDPA_F16, SDPA_F32,
-                       SDPA_FLAG_SHARED_GPU, STATUS,
+                       SDPA_FLAG_BOOL_MASK, SDPA_FLAG_SHARED_GPU, SDPA_FLAG_STRIDES, STATUS,
                        SdpaError, SdpaParams, dtype_code, load_library, make_params,
                        sdpa_abi_version, sdpa_debug_set_wait_limit_ns, sdpa_device_status,
                        sdpa_last_launch_count,
@@ -21,5 +21,5 @@ __all__ = ["sdpa_forward", "sdpa_forward_host", "sdpa_forward_raw", "sdpa_worksp
            "sdpa_abi_version", "sdpa_last_launch_count", "make_params", "SdpaParams", "SdpaError",
            "load_library",
            "EXPORTS", "KERNELS", "STATUS", "LIB_PATH", "SDPA_F32", "SDPA_F16", "SDPA_BF16",
-           "SDPA_FLAG_SHARED_GPU",
+           "SDPA_FLAG_SHARED_GPU", "SDPA_FLAG_BOOL_MASK", "SDPA_FLAG_STRIDES",
            "dtype_code"]

@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(PKG, "libsdpa_gb300.so")
 
 SDPA_F32, SDPA_F16, SDPA_BF16 = 0, 1, 2
 SDPA_FLAG_SHARED_GPU = 0x1
+SDPA_FLAG_BOOL_MASK = 0x2
+SDPA_FLAG_STRIDES = 0x4
 STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARGUMENT", 2: "SDPA_ERR_UNSUPPORTED",
           3: "SDPA_ERR_MISALIGNED", 4: "SDPA_ERR_WORKSPACE_TOO_SMALL", 5: "SDPA_ERR_CUDA",
           6: "SDPA_ERR_TIMEOUT"}
@@ -40,7 +42,9 @@ class SdpaParams(ctypes.Structure):
                 ("mask", ctypes.c_void_p), ("mask_stride", ctypes.c_int64 * 4),
                 ("sinks", ctypes.c_void_p), ("kv_capacity", ctypes.c_int32),
                 ("flags", ctypes.c_uint32), ("seq_lens_q", ctypes.c_void_p),
-                ("seq_lens_kv", ctypes.c_void_p)]
+                ("seq_lens_kv", ctypes.c_void_p), ("q_stride", ctypes.c_int64 * 3),
+                ("k_stride", ctypes.c_int64 * 3), ("v_stride", ctypes.c_int64 * 3),
+                ("o_stride", ctypes.c_int64 * 3)]
 
 
 class SdpaError(RuntimeError):
@@ -86,7 +90,9 @@ def load_library(path: str = LIB_PATH):
 
 def make_params(B, Hq, Hkv, Lq, Lk, D, dtype, scale, causal=False, mask_ptr=None,
                 mask_stride=(0, 0, 0, 1), sinks_ptr=None, kv_capacity=0, seq_lens_q_ptr=None,
-                seq_lens_kv_ptr=None, flags=0) -> SdpaParams:
+                seq_lens_kv_ptr=None, flags=0, strides=None) -> SdpaParams:
+    """strides: None, or element strides (batch, head, row) of q, k, v and o
+    as four 3-tuples; sets SDPA_FLAG_STRIDES."""
     p = SdpaParams()
     p.batch, p.num_q_heads, p.num_kv_heads = int(B), int(Hq), int(Hkv)
     p.seq_len_q, p.seq_len_kv, p.head_dim = int(Lq), int(Lk), int(D)
@@ -100,6 +106,12 @@ def make_params(B, Hq, Hkv, Lq, Lk, D, dtype, scale, causal=False, mask_ptr=None
     p.sinks = sinks_ptr
     p.kv_capacity = int(kv_capacity)
     p.flags = int(flags)
+    if strides is not None:
+        p.flags |= SDPA_FLAG_STRIDES
+        for field, st in zip(("q_stride", "k_stride", "v_stride", "o_stride"), strides):
+            arr = getattr(p, field)
+            for i in range(3):
+                arr[i] = int(st[i])
     p.seq_lens_q = seq_lens_q_ptr
     p.seq_lens_kv = seq_lens_kv_ptr
     return p
@@ -183,11 +195,14 @@ def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=N
                  seq_lens_q=None, seq_lens_kv=None, shared_gpu=False):
     """O (and LSE) of softmax(scale * q k^T + mask [+ sinks]) v on the GPU.
 
-    q [B, Hq, Lq, D], k/v [B, Hkv, C, D]: contiguous CUDA tensors of one
-    dtype (float32, float16 or bfloat16).  The keys are rows [0, Lk) of k and
-    v, Lk = kv_len (default C: with kv_len < C, k and v are a fixed-capacity
-    KV cache).  mask: None or a tensor of q's dtype broadcastable to
-    [B, Hq, Lq, Lk] (additive).  sinks: None or float32 [Hq].  seq_lens_q,
+    q [B, Hq, Lq, D], k/v [B, Hkv, C, D]: CUDA tensors of one dtype (float32,
+    float16 or bfloat16) whose last dimension is contiguous; any strides of
+    the other dimensions (multiples of 16 bytes), e.g. a [B, L, H, D] tensor
+    seen through .transpose(1, 2).  The keys are rows [0, Lk) of k and v, Lk
+    = kv_len (default C: with kv_len < C, k and v are a fixed-capacity KV
+    cache).  out defaults to q's layout.  mask: None, a tensor of q's dtype
+    broadcastable to [B, Hq, Lq, Lk] (additive), or a bool tensor of that
+    shape (True = the key is visible).  sinks: None or float32 [Hq].  seq_lens_q,
     seq_lens_kv: None or int32 CUDA tensors [B] of per-batch lengths (padding
     masks; rows past a batch's query length see no key).  scale defaults to
     1/sqrt(D).  shared_gpu: the call runs beside other kernels (sets
@@ -200,8 +215,8 @@ def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=N
     for t in (q, k, v):
         if not t.is_cuda:
             raise ValueError("q, k, v must be CUDA tensors")
-        if not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous")
+        if t.stride(-1) != 1:
+            raise ValueError("the last dimension of q, k, v must be contiguous")
     if q.dtype != k.dtype or q.dtype != v.dtype:
         raise TypeError("q, k, v must share a dtype")
     B, Hq, Lq, D = q.shape
@@ -224,9 +239,12 @@ def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=N
         scale = 1.0 / math.sqrt(D)
     dt = dtype_code(q.dtype)
     mask_ptr, mstride = None, (0, 0, 0, 1)
+    flags = SDPA_FLAG_SHARED_GPU if shared_gpu else 0
     if mask is not None:
-        if mask.dtype != q.dtype or mask.device != q.device:
-            raise TypeError("mask must have q's dtype and device")
+        if (mask.dtype != q.dtype and mask.dtype != torch.bool) or mask.device != q.device:
+            raise TypeError("mask must have q's dtype (or bool) and q's device")
+        if mask.dtype == torch.bool:
+            flags |= SDPA_FLAG_BOOL_MASK
         mexp = mask.expand(B, Hq, Lq, Lk)
         mstride = tuple(int(s) for s in mexp.stride())
         if Lk == 1:
@@ -238,11 +256,17 @@ def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=N
             raise TypeError("sinks must be a float32 CUDA tensor with Hq elements")
         sinks = sinks.contiguous()
         sinks_ptr = sinks.data_ptr()
-    params = make_params(B, Hq, Hkv, Lq, Lk, D, dt, scale, causal, mask_ptr, mstride, sinks_ptr,
-                         kv_capacity=cap if cap != Lk else 0, seq_lens_q_ptr=lens[0],
-                         seq_lens_kv_ptr=lens[1], flags=SDPA_FLAG_SHARED_GPU if shared_gpu else 0)
     if out is None:
-        out = torch.empty((B, Hq, Lq, D), dtype=q.dtype, device=q.device)
+        out = torch.empty_like(q)  # q's layout (a dense permutation stays one)
+    elif (tuple(out.shape) != (B, Hq, Lq, D) or out.dtype != q.dtype or not out.is_cuda
+          or out.stride(-1) != 1):
+        raise ValueError("out must be a CUDA tensor like q with a contiguous last dimension")
+    dense = all(t.is_contiguous() for t in (q, k, v, out))
+    strides = None if dense else tuple(tuple(int(s) for s in t.stride()[:3])
+                                       for t in (q, k, v, out))
+    params = make_params(B, Hq, Hkv, Lq, Lk, D, dt, scale, causal, mask_ptr, mstride, sinks_ptr,
+                         kv_capacity=cap if (dense and cap != Lk) else 0, seq_lens_q_ptr=lens[0],
+                         seq_lens_kv_ptr=lens[1], flags=flags, strides=strides)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
     nbytes = sdpa_workspace_size(params)

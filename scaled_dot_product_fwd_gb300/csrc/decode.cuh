@@ -53,7 +53,9 @@ struct SplitArgs {
   int Hq, Hkv, G, Lk;
   int Lq;           // query rows per head (1 for decode, up to 8 for multi-query)
   int causal;       // bottom-right: key j visible to row i iff j <= i + Lk - Lq
-  int kv_cap;       // rows per (batch, kv head) in k and v (>= Lk)
+  // element strides (batch, head, row) of q, k, v and o; D is contiguous
+  long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2, os0, os1, os2;
+  int mask_bool;    // mask holds bytes, nonzero = visible
   const int* seq_lens_q;   // nullptr or per-batch valid query rows
   const int* seq_lens_kv;  // nullptr or per-batch valid keys
   int num_groups;   // groups of HG query rows per kv head (rows: G heads x Lq)
@@ -274,15 +276,14 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   __syncthreads();
   const WaitCtl wc{a.wait_ns, abort_flag, a.status};
 
-  const size_t kv_row0 = (static_cast<size_t>(b) * a.Hkv + kvh) * a.kv_cap;
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     int last_use[8];  // last fill of each stage (-1: none)
 #pragma unroll
     for (int s = 0; s < 8; ++s) last_use[s] = -1;
     if (lane == 0) {
-      const T* kg = static_cast<const T*>(a.k) + (kv_row0 + key_begin) * D;
-      const T* vg = static_cast<const T*>(a.v) + (kv_row0 + key_begin) * D;
+      const T* kg = static_cast<const T*>(a.k) + b * a.ks0 + kvh * a.ks1 + key_begin * a.ks2;
+      const T* vg = static_cast<const T*>(a.v) + b * a.vs0 + kvh * a.vs1 + key_begin * a.vs2;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % NS;
         const int use = t / NS;
@@ -292,8 +293,21 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
         const uint32_t bytes = static_cast<uint32_t>(rows * D * sizeof(T));
         mbar_arrive_expect_tx(&full[s], 2 * bytes);
         uint8_t* st = ring + static_cast<size_t>(s) * C::STAGE_BYTES;
-        bulk_load(st, kg + static_cast<size_t>(t) * C::TK * D, bytes, &full[s]);
-        bulk_load(st + C::TILE_BYTES, vg + static_cast<size_t>(t) * C::TK * D, bytes, &full[s]);
+        // a tile's rows are one copy when they are contiguous, else one per row
+        const long long r0 = static_cast<long long>(t) * C::TK;
+        if (a.ks2 == D) {
+          bulk_load(st, kg + r0 * D, bytes, &full[s]);
+        } else {
+          for (int r = 0; r < rows; ++r)
+            bulk_load(st + r * D * sizeof(T), kg + (r0 + r) * a.ks2, D * sizeof(T), &full[s]);
+        }
+        if (a.vs2 == D) {
+          bulk_load(st + C::TILE_BYTES, vg + r0 * D, bytes, &full[s]);
+        } else {
+          for (int r = 0; r < rows; ++r)
+            bulk_load(st + C::TILE_BYTES + r * D * sizeof(T), vg + (r0 + r) * a.vs2,
+                      D * sizeof(T), &full[s]);
+        }
         last_use[s] = use;
       }
     }
@@ -320,15 +334,18 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   // The group's HG rows are (query head, query row) pairs of this kv head:
   // row rr of the kv head is head kvh * G + rr / Lq, query row rr % Lq.
   const int R = a.G * a.Lq;  // rows per kv head
-  auto row_index = [&](int rr) {  // global query row [b, hq, qi]
+  auto row_index = [&](int rr) {  // global query row [b, hq, qi] (lse, workspace)
     const int hq = kvh * a.G + rr / a.Lq;
     return (static_cast<size_t>(b) * a.Hq + hq) * a.Lq + rr % a.Lq;
+  };
+  auto q_off = [&](int rr) {  // element offset of a query row in q
+    return b * a.qs0 + (kvh * a.G + rr / a.Lq) * a.qs1 + (rr % a.Lq) * a.qs2;
   };
   uint64_t q2[HG][C::NP2];
 #pragma unroll
   for (int hh = 0; hh < HG; ++hh) {
     const int rr = grp * HG + hh;
-    const T* qrow = static_cast<const T*>(a.q) + row_index(rr < R ? rr : 0) * D;
+    const T* qrow = static_cast<const T*>(a.q) + q_off(rr < R ? rr : 0);
 #pragma unroll
     for (int pi = 0; pi < C::NPIECE; ++pi) {
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -344,9 +361,16 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   int my_limit = Lkb - 1;
   if (a.causal) my_limit = min(my_limit, my_qi + (Lkb - Lqb));
   if (my_qi >= Lqb) my_limit = -1;  // a padding row sees no key
+  // additive mask row (mrow) or boolean mask row (mrowb)
   const T* mrow = nullptr;
-  if (a.mask && my_head_ok)
-    mrow = static_cast<const T*>(a.mask) + b * a.ms0 + my_hq * a.ms1 + my_qi * a.ms2;
+  const uint8_t* mrowb = nullptr;
+  if (a.mask && my_head_ok) {
+    const long long moff = b * a.ms0 + my_hq * a.ms1 + my_qi * a.ms2;
+    if (a.mask_bool)
+      mrowb = static_cast<const uint8_t*>(a.mask) + moff;
+    else
+      mrow = static_cast<const T*>(a.mask) + moff;
+  }
 
   uint64_t acc2[HG][C::NP2];
   float lsum[HG];
@@ -401,6 +425,8 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
       x = -INFINITY;
     } else if (mrow) {
       x += Ld<T>::f(mrow[key]) * kLog2e;
+    } else if (mrowb && !mrowb[key]) {
+      x = -INFINITY;
     }
     // tile max of head hl: lanes differing below HBIT or in the row bits
     float tmax = x;
@@ -590,7 +616,8 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
 #pragma unroll
     for (int q = 0; q < kMaxClusterSplits; ++q)
       if (q < S) acc = fmaf(wts[hh * kMaxClusterSplits + q], pv[q], acc);
-    static_cast<T*>(a.o)[row_index(rr) * D + d] = StoreAs<T>::c(acc * hinv[hh]);
+    static_cast<T*>(a.o)[b * a.os0 + (kvh * a.G + rr / a.Lq) * a.os1 + (rr % a.Lq) * a.os2 + d] =
+        StoreAs<T>::c(acc * hinv[hh]);
   }
   cluster_sync_all();
 }

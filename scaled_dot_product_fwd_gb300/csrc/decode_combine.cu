@@ -30,6 +30,7 @@ struct CombineArgs {
   const float* sinks;
   int Hq, num_splits, D;
   int rows_per_head;  // query rows per (batch, head): 1 for decode
+  long long os0, os1, os2;  // element strides of o (batch, head, row)
 };
 
 constexpr int kMaxSplits = 1024;  // upper bound of the split plan
@@ -78,7 +79,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
   L = block_reduce(L, false, red);  // its barriers also publish w[]
   if (a.sinks && M != -INFINITY) L += ex2(sk - M);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  T* orow = static_cast<T*>(a.o) + row * a.D;
+  const size_t bh = row / a.rows_per_head;
+  T* orow = static_cast<T*>(a.o) + static_cast<long long>(bh / a.Hq) * a.os0 +
+            static_cast<long long>(hq) * a.os1 +
+            static_cast<long long>(row - bh * a.rows_per_head) * a.os2;
   const float4* wo = reinterpret_cast<const float4*>(a.ws_o + row * S * a.D);
   const int D4 = a.D / 4;
   for (int c = threadIdx.x; c < D4; c += kCombineThreads) {
@@ -207,7 +211,19 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   a.G = p.num_q_heads / p.num_kv_heads;
   a.Lk = p.seq_len_kv;
   a.Lq = p.seq_len_q;
-  a.kv_cap = p.kv_capacity > 0 ? p.kv_capacity : p.seq_len_kv;
+  a.qs0 = p.q_stride[0];
+  a.qs1 = p.q_stride[1];
+  a.qs2 = p.q_stride[2];
+  a.ks0 = p.k_stride[0];
+  a.ks1 = p.k_stride[1];
+  a.ks2 = p.k_stride[2];
+  a.vs0 = p.v_stride[0];
+  a.vs1 = p.v_stride[1];
+  a.vs2 = p.v_stride[2];
+  a.os0 = p.o_stride[0];
+  a.os1 = p.o_stride[1];
+  a.os2 = p.o_stride[2];
+  a.mask_bool = (p.flags & SDPA_FLAG_BOOL_MASK) ? 1 : 0;
   a.seq_lens_q = p.seq_lens_q;
   a.seq_lens_kv = p.seq_lens_kv;
   a.causal = p.causal ? 1 : 0;
@@ -256,6 +272,9 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   c.num_splits = plan.num_splits;
   c.D = p.head_dim;
   c.rows_per_head = p.seq_len_q;
+  c.os0 = p.o_stride[0];
+  c.os1 = p.o_stride[1];
+  c.os2 = p.o_stride[2];
   st = launch_combine(p.dtype, c, static_cast<unsigned>(p.batch) * p.num_q_heads * p.seq_len_q,
                       env.stream);
   if (st == SDPA_OK) set_last_launches(2);
@@ -273,6 +292,9 @@ sdpa_status_t launch_no_keys(const sdpa_params_t& p, void* o, float* lse, const 
   c.num_splits = 0;
   c.D = p.head_dim;
   c.rows_per_head = p.seq_len_q;
+  c.os0 = p.o_stride[0];
+  c.os1 = p.o_stride[1];
+  c.os2 = p.o_stride[2];
   const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q;
   if (rows > 0x7fffffffu) return SDPA_ERR_UNSUPPORTED;
   return launch_combine(p.dtype, c, static_cast<unsigned>(rows), env.stream);

@@ -99,5 +99,5 @@ extern "C" sdpa_status_t sdpa_forward_decode_noalloc(const sdpa_params_t* p, con
   env.wait_limit_ns = gb300::current_wait_limit_ns();
   env.num_sms = num_sms;
   env.stream = static_cast<cudaStream_t>(stream);
-  return gb300::launch_decode(*p, plan, q, k, v, o, lse, scratch, env);
+  return gb300::launch_decode(gb300::normalized_params(*p), plan, q, k, v, o, lse, scratch, env);
 }

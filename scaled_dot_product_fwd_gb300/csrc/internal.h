@@ -40,6 +40,10 @@ int* status_word_current_device();
 uint64_t current_wait_limit_ns();
 // Kernels enqueued by the calling thread's last call (sdpa_last_launch_count).
 void set_last_launches(int n);
+// The problem with SDPA_FLAG_STRIDES set and every tensor's strides filled
+// in (the dense layout and kv_capacity written out when the caller gave no
+// strides).  Launchers take parameters in this form.
+sdpa_params_t normalized_params(const sdpa_params_t& p);
 
 sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const void* k,
                                 const void* v, void* o, float* lse, const LaunchEnv& env);

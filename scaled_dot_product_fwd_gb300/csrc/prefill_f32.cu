@@ -38,7 +38,9 @@ struct F32Args {
   const float* mask;
   long long ms0, ms1, ms2;
   const float* sinks;
-  int kv_cap;              // rows per (batch, kv head) in k and v (>= Lk)
+  int mask_bool;           // mask holds bytes, nonzero = visible
+  // element strides (batch, head, row) of q, k, v and o; D is contiguous
+  long long qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2, os0, os1, os2;
   const int* seq_lens_q;   // nullptr or per-batch valid query rows
   const int* seq_lens_kv;  // nullptr or per-batch valid keys
 };
@@ -70,9 +72,9 @@ __global__ void __launch_bounds__(kF32Threads) prefill_f32_kernel(const F32Args 
   const int h = blockIdx.y, b = blockIdx.z;
   const int kvh = h / a.G;
   const int q0 = qb * FBM;
-  const float* qbase = a.q + ((static_cast<size_t>(b) * a.Hq + h) * a.Lq) * D;
-  const float* kbase = a.k + ((static_cast<size_t>(b) * a.Hkv + kvh) * a.kv_cap) * D;
-  const float* vbase = a.v + ((static_cast<size_t>(b) * a.Hkv + kvh) * a.kv_cap) * D;
+  const float* qbase = a.q + b * a.qs0 + h * a.qs1;
+  const float* kbase = a.k + b * a.ks0 + kvh * a.ks1;
+  const float* vbase = a.v + b * a.vs0 + kvh * a.vs1;
   // this batch's lengths (padding masks), clamped to the call's maxima
   const int Lkb = a.seq_lens_kv ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
   const int Lqb = a.seq_lens_q ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
@@ -81,20 +83,24 @@ __global__ void __launch_bounds__(kF32Threads) prefill_f32_kernel(const F32Args 
   for (int e = tid; e < FBM * D / 4; e += kF32Threads) {
     const int r = e / (D / 4), c4 = e % (D / 4);
     float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (q0 + r < a.Lq) val = reinterpret_cast<const float4*>(qbase + static_cast<size_t>(q0 + r) * D)[c4];
+    if (q0 + r < a.Lq) val = reinterpret_cast<const float4*>(qbase + (q0 + r) * a.qs2)[c4];
     reinterpret_cast<float4*>(sQ + r * D)[c4] = val;
   }
 
   int qrow[4], limit[4];
-  const float* mrow[4];
+  const float* mrow[4];     // additive mask rows
+  const uint8_t* mrowb[4];  // boolean mask rows
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     qrow[i] = q0 + ty * 4 + i;
     limit[i] = Lkb - 1;
     if (a.causal) limit[i] = min(limit[i], qrow[i] + (Lkb - Lqb));
     if (qrow[i] >= Lqb) limit[i] = -1;  // a padding row sees no key
-    mrow[i] = (a.mask && qrow[i] < a.Lq) ? a.mask + b * a.ms0 + h * a.ms1 + qrow[i] * a.ms2
-                                          : nullptr;
+    const long long moff = b * a.ms0 + h * a.ms1 + qrow[i] * a.ms2;
+    const bool has = a.mask && qrow[i] < a.Lq;
+    mrow[i] = (has && !a.mask_bool) ? a.mask + moff : nullptr;
+    mrowb[i] =
+        (has && a.mask_bool) ? reinterpret_cast<const uint8_t*>(a.mask) + moff : nullptr;
   }
   // keys needed by the block: up to the last visible key of its last row
   int kend = q0 < Lqb ? Lkb : 0;
@@ -123,8 +129,8 @@ __global__ void __launch_bounds__(kF32Threads) prefill_f32_kernel(const F32Args 
       const int r = e / (D / 4), c4 = e % (D / 4);
       float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
       if (k0 + r < Lkb) {  // keys past the batch's length are never read
-        kv = reinterpret_cast<const float4*>(kbase + static_cast<size_t>(k0 + r) * D)[c4];
-        vv = reinterpret_cast<const float4*>(vbase + static_cast<size_t>(k0 + r) * D)[c4];
+        kv = reinterpret_cast<const float4*>(kbase + (k0 + r) * a.ks2)[c4];
+        vv = reinterpret_cast<const float4*>(vbase + (k0 + r) * a.vs2)[c4];
       }
       reinterpret_cast<float4*>(sK + r * C::KP)[c4] = kv;
       reinterpret_cast<float4*>(sV + r * D)[c4] = vv;
@@ -165,7 +171,8 @@ __global__ void __launch_bounds__(kF32Threads) prefill_f32_kernel(const F32Args 
       for (int c = 0; c < 4; ++c) {
         const int kj = k0 + tx + 16 * c;
         float xv = s[i][c] * a.sl2;
-        if (mrow[i] && kj < a.Lk) xv += mrow[i][kj] * kLog2e;
+        if (mrow[i] && kj <= limit[i]) xv += mrow[i][kj] * kLog2e;
+        if (mrowb[i] && kj <= limit[i] && !mrowb[i][kj]) xv = -INFINITY;
         if (kj > limit[i]) xv = -INFINITY;
         x[c] = xv;
         mx = fmaxf(mx, xv);
@@ -229,7 +236,7 @@ __global__ void __launch_bounds__(kF32Threads) prefill_f32_kernel(const F32Args 
     }
     const float inv = (li > 0.f) ? oscale / li : 0.f;
     if (qi < a.Lq) {
-      float* orow = a.o + ((static_cast<size_t>(b) * a.Hq + h) * a.Lq + qi) * D;
+      float* orow = a.o + b * a.os0 + h * a.os1 + qi * a.os2;
 #pragma unroll
       for (int c = 0; c < OC; ++c) {
         float4 w;
@@ -268,7 +275,19 @@ sdpa_status_t launch_f32_impl(const sdpa_params_t& p, const void* q, const void*
   a.ms1 = p.mask_stride[1];
   a.ms2 = p.mask_stride[2];
   a.sinks = p.sinks;
-  a.kv_cap = p.kv_capacity > 0 ? p.kv_capacity : p.seq_len_kv;
+  a.mask_bool = (p.flags & SDPA_FLAG_BOOL_MASK) ? 1 : 0;
+  a.qs0 = p.q_stride[0];
+  a.qs1 = p.q_stride[1];
+  a.qs2 = p.q_stride[2];
+  a.ks0 = p.k_stride[0];
+  a.ks1 = p.k_stride[1];
+  a.ks2 = p.k_stride[2];
+  a.vs0 = p.v_stride[0];
+  a.vs1 = p.v_stride[1];
+  a.vs2 = p.v_stride[2];
+  a.os0 = p.o_stride[0];
+  a.os1 = p.o_stride[1];
+  a.os2 = p.o_stride[2];
   a.seq_lens_q = p.seq_lens_q;
   a.seq_lens_kv = p.seq_lens_kv;
   auto kern = prefill_f32_kernel<D>;

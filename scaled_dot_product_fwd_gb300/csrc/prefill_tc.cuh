@@ -136,6 +136,8 @@ struct PrefillArgs {
   unsigned long long wait_ns;
   const int* seq_lens_q;   // nullptr or per-batch valid query rows
   const int* seq_lens_kv;  // nullptr or per-batch valid keys
+  int mask_bool;           // mask holds bytes, nonzero = visible (EXT only)
+  long long os0, os1, os2; // element strides of o (batch, head, row; EXT only)
 };
 
 template <bool BF16>
@@ -306,12 +308,13 @@ __device__ __forceinline__ Unit unit_of(const PrefillArgs& a, uint32_t bx) {
   return w;
 }
 
-// LENS: the call passes per-batch length arrays (without them the lengths
-// are the kernel arguments, and the code is that of dense inputs).
+// EXT: extended inputs (per-batch length arrays, a boolean mask, or an
+// output that is not dense [B, Hq, Lq, D]); without them the lengths are the
+// kernel arguments and the code is that of dense inputs.
 // SPLIT: every unit is shared by the CTAs of a cluster (the units of a last,
 // partial wave); its own instantiation, so that whole units run code without
 // the merge.
-template <int D, bool BF16, bool X3, bool LENS, bool SPLIT>
+template <int D, bool BF16, bool X3, bool EXT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -355,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kvh = h / a.G;
   // this batch's lengths (padding masks), clamped to the call's maxima; rows
   // at or past Lqb see no key
-  const int Lkb = (LENS && a.seq_lens_kv) ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
-  const int Lqb = (LENS && a.seq_lens_q) ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
+  const int Lkb = (EXT && a.seq_lens_kv) ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
+  const int Lqb = (EXT && a.seq_lens_q) ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
   const int nkv_all = (Lkb + BN - 1) / BN;
   // key tiles [jb, je) of this CTA (all of them unless the unit is split;
   // splits are never causal)
@@ -422,11 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nt * C::QT * C::TILE));
       for (int t = 0; t < nt; ++t)
         for (int cb = 0; cb < C::CB; ++cb) {
-          tma_load_3d(sQ + t * C::QT * C::TILE + cb * BM * 128, &tmQ, q_full, cb * 64,
-                      m0 + t * BM, b * a.Hq + h);
+          tma_load_4d(sQ + t * C::QT * C::TILE + cb * BM * 128, &tmQ, q_full, cb * 64,
+                      m0 + t * BM, h, b);
           if constexpr (X3)
-            tma_load_3d(sQ + (t * C::QT + 1) * C::TILE + cb * BM * 128, &tmQ2, q_full,
-                        cb * 64, m0 + t * BM, b * a.Hq + h);
+            tma_load_4d(sQ + (t * C::QT + 1) * C::TILE + cb * BM * 128, &tmQ2, q_full,
+                        cb * 64, m0 + t * BM, h, b);
         }
       for (int j = 0; j < nmax; ++j) {
         const int s = j % C::NS;
@@ -434,14 +437,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, wc)) break;
         mbar_arrive_expect_tx(&full[s], C::STAGE);
         uint8_t* st = sRing + s * C::STAGE;
-        const int kvz = b * a.Hkv + kvh;
         for (int cb = 0; cb < C::CB; ++cb) {
           const int key0 = (jb + j) * BN;
-          tma_load_3d(st + cb * BN * 128, &tmK, &full[s], cb * 64, key0, kvz);
-          tma_load_3d(st + C::V_OFF + cb * BN * 128, &tmV, &full[s], cb * 64, key0, kvz);
+          tma_load_4d(st + cb * BN * 128, &tmK, &full[s], cb * 64, key0, kvh, b);
+          tma_load_4d(st + C::V_OFF + cb * BN * 128, &tmV, &full[s], cb * 64, key0, kvh, b);
           if constexpr (X3) {
-            tma_load_3d(st + C::K_LO + cb * BN * 128, &tmK2, &full[s], cb * 64, key0, kvz);
-            tma_load_3d(st + C::V_LO + cb * BN * 128, &tmV2, &full[s], cb * 64, key0, kvz);
+            tma_load_4d(st + C::K_LO + cb * BN * 128, &tmK2, &full[s], cb * 64, key0, kvh, b);
+            tma_load_4d(st + C::V_LO + cb * BN * 128, &tmV2, &full[s], cb * 64, key0, kvh, b);
           }
         }
         last_use[s] = use;
@@ -587,10 +589,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // last key visible to this row (bounds and causal)
     int limit = Lkb - 1;
     if (a.causal) limit = min(limit, qi + (Lkb - Lqb));
-    if (LENS && qi >= Lqb) limit = -1;  // a padding row sees no key
+    if (EXT && qi >= Lqb) limit = -1;  // a padding row sees no key
+    // additive mask row (mrow) or, with EXT, boolean mask row (mrowb)
     const T* mrow = nullptr;
-    if (a.mask && row_ok)
-      mrow = static_cast<const T*>(a.mask) + b * a.ms0 + h * a.ms1 + qi * a.ms2 + jb * BN;
+    const uint8_t* mrowb = nullptr;
+    if (a.mask && row_ok) {
+      const long long moff = b * a.ms0 + h * a.ms1 + qi * a.ms2 + jb * BN;
+      if (EXT && a.mask_bool)
+        mrowb = static_cast<const uint8_t*>(a.mask) + moff;
+      else
+        mrow = static_cast<const T*>(a.mask) + moff;
+    }
     // keys are counted from this CTA's first key tile from here on
     limit -= jb * BN;
     float m = -INFINITY;  // reference max (log2 units)
@@ -705,7 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mn;
         }
         const float inv = (l > 0.f) ? oscale / l : 0.f;
-        T* orow = static_cast<T*>(a.o) + ((static_cast<size_t>(b) * a.Hq + h) * a.Lq + qi) * D;
+        T* orow = EXT ? static_cast<T*>(a.o) + (b * a.os0 + h * a.os1 + qi * a.os2)
+                      : static_cast<T*>(a.o) + ((static_cast<size_t>(b) * a.Hq + h) * a.Lq + qi) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ob[32];
@@ -800,6 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < BN; ++i) {
                 float x = __uint_as_float(s[i]) * a.sl2;
                 if (mrow && kv0 + i <= limit) x += to_float(mrow[kv0 + i]) * kLog2e;
+                if (EXT && mrowb && kv0 + i <= limit && !mrowb[kv0 + i]) x = -INFINITY;
                 if (kv0 + i > limit) x = -INFINITY;
                 s[i] = __float_as_uint(x);
               }
@@ -892,6 +903,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < BN; ++i)
                 if (kv0 + i <= limit) x[i] += to_float(mrow[kv0 + i]) * kLog2e;
             }
+            if constexpr (EXT) {
+              if (mrowb) {
+#pragma unroll
+                for (int i = 0; i < BN; ++i)
+                  if (kv0 + i <= limit && !mrowb[kv0 + i]) x[i] = -INFINITY;
+              }
+            }
             if (kv0 + BN - 1 > limit) {
 #pragma unroll
               for (int i = 0; i < BN; ++i)
@@ -968,29 +986,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (SPLIT) griddep_wait();
 }
 
-// kv_plane_rows: rows per (batch, kv head) in k, v, k2, v2 as passed here
-template <int D, bool BF16, bool X3, bool LENS>
+// Element strides (batch, head, row) of q, k and v as passed to launch_impl
+// (in X3, of the hi/lo copies; q2, k2, v2 share them).
+struct QkvStrides {
+  int64_t q[3], k[3], v[3];
+};
+
+template <int D, bool BF16, bool X3, bool EXT>
 sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, const void* v,
                           const void* q2, const void* k2, const void* v2, void* o, float* lse,
-                          uint64_t kv_plane_rows, const LaunchEnv& env, int* grids) {
+                          const QkvStrides& st, const LaunchEnv& env, int* grids) {
   using C = Cfg<D, X3>;
   const CUtensorMapDataType dt =
       BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const uint64_t qz = static_cast<uint64_t>(p.batch) * p.num_q_heads;
-  const uint64_t kz = static_cast<uint64_t>(p.batch) * p.num_kv_heads;
-  // k, v rows per (batch, kv head) may exceed seq_len_kv (a KV cache); the
-  // maps stop at seq_len_kv, so rows past it read as zero and are never loaded
-  const uint64_t cap = kv_plane_rows;
+  const uint64_t B = p.batch, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+  const uint64_t Lq = p.seq_len_q, Lk = p.seq_len_kv;
+  // [B, H, L, D] with the given strides, viewed innermost-first; box 64 x 128
+  // rows, 128-byte swizzle.  The maps stop at Lq and Lk: rows past them (a KV
+  // cache keeps more) read as zero and are never loaded.
   CUtensorMap tq, tk, tv, tq2, tk2, tv2;
-  // [B*H, L, D] viewed innermost-first; box 64 x 128 rows, 128-byte swizzle.
-  if (!encode_tiled_3d(&tq, dt, q, D, p.seq_len_q, qz, 2, 64, BM) ||
-      !encode_tiled_3d(&tk, dt, k, D, p.seq_len_kv, kz, 2, 64, BN, cap) ||
-      !encode_tiled_3d(&tv, dt, v, D, p.seq_len_kv, kz, 2, 64, BN, cap))
+  auto enc = [&](CUtensorMap* m, const void* base, uint64_t L, uint64_t H, uint32_t box_rows,
+                 const int64_t (&sd)[3]) {
+    return encode_tiled_4d(m, dt, base, D, L, H, B, 2, 64, box_rows, sd[2], sd[1], sd[0]);
+  };
+  if (!enc(&tq, q, Lq, Hq, BM, st.q) || !enc(&tk, k, Lk, Hkv, BN, st.k) ||
+      !enc(&tv, v, Lk, Hkv, BN, st.v))
     return SDPA_ERR_CUDA;
   if (X3) {
-    if (!encode_tiled_3d(&tq2, dt, q2, D, p.seq_len_q, qz, 2, 64, BM) ||
-        !encode_tiled_3d(&tk2, dt, k2, D, p.seq_len_kv, kz, 2, 64, BN, cap) ||
-        !encode_tiled_3d(&tv2, dt, v2, D, p.seq_len_kv, kz, 2, 64, BN, cap))
+    if (!enc(&tq2, q2, Lq, Hq, BM, st.q) || !enc(&tk2, k2, Lk, Hkv, BN, st.k) ||
+        !enc(&tv2, v2, Lk, Hkv, BN, st.v))
       return SDPA_ERR_CUDA;
   } else {
     tq2 = tq;
@@ -1018,8 +1042,12 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   a.wait_ns = env.wait_limit_ns;
   a.seq_lens_q = p.seq_lens_q;
   a.seq_lens_kv = p.seq_lens_kv;
-  auto kern = prefill_tc_kernel<D, BF16, X3, LENS, false>;
-  auto kern_split = prefill_tc_kernel<D, BF16, X3, LENS, true>;
+  a.mask_bool = (p.flags & SDPA_FLAG_BOOL_MASK) ? 1 : 0;
+  a.os0 = p.o_stride[0];
+  a.os1 = p.o_stride[1];
+  a.os2 = p.o_stride[2];
+  auto kern = prefill_tc_kernel<D, BF16, X3, EXT, false>;
+  auto kern_split = prefill_tc_kernel<D, BF16, X3, EXT, true>;
   // The setmaxnreg split must fit the registers the kernel is launched with
   // (an increase beyond them would wait forever): check the compiled count
   // once per instantiation.
@@ -1127,13 +1155,24 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
 
 }  // namespace
 
-// Head-size entry points (one translation unit each); `grids` receives the
-// number of grids launched (1, or 2 when the last wave is split).
+// Whether a call needs the EXT instantiation: per-batch lengths, a boolean
+// mask, or an output that is not dense [B, Hq, Lq, D] (p normalised: strides
+// filled in).
+inline bool prefill_needs_ext(const sdpa_params_t& p) {
+  const int64_t D = p.head_dim;
+  const bool dense_o = p.o_stride[2] == D && p.o_stride[1] == p.seq_len_q * D &&
+                       p.o_stride[0] == static_cast<int64_t>(p.num_q_heads) * p.seq_len_q * D;
+  return p.seq_lens_q || p.seq_lens_kv || (p.mask && (p.flags & SDPA_FLAG_BOOL_MASK)) || !dense_o;
+}
+
+// Head-size entry points (one translation unit each), p normalised;
+// `grids` receives the number of grids launched (1, or 2 when the last
+// wave is split).
 sdpa_status_t launch_prefill_tc_d64(const sdpa_params_t& p, const void* q, const void* k,
-                                    const void* v, void* o, float* lse, uint64_t kv_plane_rows,
-                                    const LaunchEnv& env, int* grids);
+                                    const void* v, void* o, float* lse, const LaunchEnv& env,
+                                    int* grids);
 sdpa_status_t launch_prefill_tc_d128(const sdpa_params_t& p, const void* q, const void* k,
-                                     const void* v, void* o, float* lse, uint64_t kv_plane_rows,
-                                     const LaunchEnv& env, int* grids);
+                                     const void* v, void* o, float* lse, const LaunchEnv& env,
+                                     int* grids);
 
 }  // namespace gb300

@@ -14,7 +14,9 @@
 // raises instead of falling back).
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <atomic>
 #include <mutex>
@@ -54,9 +56,21 @@ sdpa_status_t validate_problem(const sdpa_params_t* p) {
       if (p->mask_stride[i] < 0) return SDPA_ERR_INVALID_ARGUMENT;
     if (p->mask_stride[3] != 1) return SDPA_ERR_INVALID_ARGUMENT;
   }
-  if ((p->flags & ~SDPA_FLAG_SHARED_GPU) != 0) return SDPA_ERR_INVALID_ARGUMENT;
+  if ((p->flags & ~(SDPA_FLAG_SHARED_GPU | SDPA_FLAG_BOOL_MASK | SDPA_FLAG_STRIDES)) != 0)
+    return SDPA_ERR_INVALID_ARGUMENT;
   if (p->kv_capacity < 0 || (p->kv_capacity > 0 && p->kv_capacity < p->seq_len_kv))
     return SDPA_ERR_INVALID_ARGUMENT;
+  if (p->flags & SDPA_FLAG_STRIDES) {
+    // explicit layouts replace kv_capacity; rows of every tensor 16-byte aligned
+    if (p->kv_capacity != 0) return SDPA_ERR_INVALID_ARGUMENT;
+    const int64_t es = p->dtype == SDPA_F32 ? 4 : 2;
+    const int64_t* st[4] = {p->q_stride, p->k_stride, p->v_stride, p->o_stride};
+    for (const int64_t* s : st)
+      for (int i = 0; i < 3; ++i) {
+        if (s[i] < 0) return SDPA_ERR_INVALID_ARGUMENT;
+        if ((s[i] * es) % 16 != 0) return SDPA_ERR_MISALIGNED;
+      }
+  }
   if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 512) return SDPA_ERR_UNSUPPORTED;
   // cuDNN's bottom-right causal mask is undefined for Tq > Tkv (mlx 0.30.7
   // supports_sdpa_cudnn); the same rule holds here.
@@ -64,6 +78,29 @@ sdpa_status_t validate_problem(const sdpa_params_t* p) {
   // head_dim 512 is served by the vector path only (up to 8 query rows).
   if (p->head_dim == 512 && p->seq_len_q > kMaxDecodeRows) return SDPA_ERR_UNSUPPORTED;
   return SDPA_OK;
+}
+
+// The dense layout (and kv_capacity) written out as strides, so that every
+// launcher reads the layout from the stride fields.  Reads the caller's
+// stride fields only when it set SDPA_FLAG_STRIDES (a caller built against
+// an earlier ABI has no such fields).
+sdpa_params_t normalized(const sdpa_params_t* p) {
+  sdpa_params_t n;
+  if (p->flags & SDPA_FLAG_STRIDES) return *p;
+  memset(&n, 0, sizeof(n));
+  memcpy(&n, p, offsetof(sdpa_params_t, q_stride));
+  const int64_t D = p->head_dim;
+  const int64_t cap = p->kv_capacity > 0 ? p->kv_capacity : p->seq_len_kv;
+  const int64_t qs[3] = {static_cast<int64_t>(p->num_q_heads) * p->seq_len_q * D,
+                         static_cast<int64_t>(p->seq_len_q) * D, D};
+  const int64_t ks[3] = {static_cast<int64_t>(p->num_kv_heads) * cap * D, cap * D, D};
+  for (int i = 0; i < 3; ++i) {
+    n.q_stride[i] = n.o_stride[i] = qs[i];
+    n.k_stride[i] = n.v_stride[i] = ks[i];
+  }
+  n.kv_capacity = 0;
+  n.flags |= SDPA_FLAG_STRIDES;
+  return n;
 }
 
 bool nothing_to_do(const sdpa_params_t* p) {
@@ -121,6 +158,8 @@ int* status_word_current_device() {
 uint64_t current_wait_limit_ns() { return g_wait_ns.load(); }
 
 void set_last_launches(int n) { g_last_launches = n; }
+
+sdpa_params_t normalized_params(const sdpa_params_t& p) { return normalized(&p); }
 
 }  // namespace gb300
 
@@ -202,19 +241,21 @@ sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k,
   env.wait_limit_ns = g_wait_ns.load();
   env.num_sms = num_sms;
   env.stream = static_cast<cudaStream_t>(stream);
+  // every launcher reads the layout from the stride fields
+  const sdpa_params_t n = normalized(p);
   switch (kern) {
     case SDPA_KERNEL_PREFILL_TC:  // sets the count itself (1 or 2 grids)
-      return gb300::launch_prefill_tc(*p, q, k, v, o, lse, env);
+      return gb300::launch_prefill_tc(n, q, k, v, o, lse, env);
     case SDPA_KERNEL_PREFILL_F32:
-      st = gb300::launch_prefill_f32(*p, q, k, v, o, lse, env);
+      st = gb300::launch_prefill_f32(n, q, k, v, o, lse, env);
       if (st == SDPA_OK) g_last_launches = 1;
       return st;
     case SDPA_KERNEL_PREFILL_TC_F32:  // hi/lo split, then the prefill grids (sets the count)
-      return gb300::launch_prefill_x3(*p, q, k, v, o, lse, workspace, env);
+      return gb300::launch_prefill_x3(n, q, k, v, o, lse, workspace, env);
     case SDPA_KERNEL_DECODE_SPLITKV:  // sets the count itself (1 or 2 kernels)
-      return gb300::launch_decode(*p, plan, q, k, v, o, lse, workspace, env);
+      return gb300::launch_decode(n, plan, q, k, v, o, lse, workspace, env);
     case SDPA_KERNEL_NO_KEYS:
-      st = gb300::launch_no_keys(*p, o, lse, env);
+      st = gb300::launch_no_keys(n, o, lse, env);
       if (st == SDPA_OK) g_last_launches = 1;
       return st;
     default:

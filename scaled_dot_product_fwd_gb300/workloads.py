@@ -33,7 +33,9 @@ class Workload:
     causal: bool = False
     sinks: bool = False
     sink_scale: float = 1.0
-    mask: str | None = None  # None | "full" | "row" (broadcast over heads/batch) | "key"
+    # None | "full" | "row" (broadcast over heads/batch) | "key": additive;
+    # "bool_full" | "bool_key": boolean (True = visible)
+    mask: str | None = None
     seed: int = 0
 
     @property
@@ -100,7 +102,13 @@ def make_inputs(w: Workload):
         sinks = torch.from_numpy(
             (rng.standard_normal(size=(w.Hq,), dtype=np.float32) * np.float32(w.sink_scale)))
     mask = None
-    if w.mask is not None:
+    if w.mask in ("bool_full", "bool_key"):
+        shape = (w.B, w.Hq, w.Lq, w.Lk) if w.mask == "bool_full" else (w.B, 1, 1, w.Lk)
+        keep = rng.random(size=shape) >= 0.3  # about 30% of the keys removed
+        if w.mask == "bool_full":
+            keep[0, 0, 0, :] = False  # one row sees no key
+        mask = torch.from_numpy(keep)
+    elif w.mask is not None:
         shape = {"full": (w.B, w.Hq, w.Lq, w.Lk), "row": (1, 1, w.Lq, w.Lk),
                  "key": (w.B, 1, 1, w.Lk)}[w.mask]
         m = rng.standard_normal(size=shape, dtype=np.float32)

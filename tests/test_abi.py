@@ -37,13 +37,17 @@ def test_library_exports_every_declared_symbol(sdpa_lib):
 
 
 def test_params_struct_layout():
-    assert ctypes.sizeof(B.SdpaParams) == 112
+    assert ctypes.sizeof(B.SdpaParams) == 208
     assert B.SdpaParams.mask.offset == 40
     assert B.SdpaParams.mask_stride.offset == 48
     assert B.SdpaParams.sinks.offset == 80
     assert B.SdpaParams.kv_capacity.offset == 88
     assert B.SdpaParams.seq_lens_q.offset == 96
     assert B.SdpaParams.seq_lens_kv.offset == 104
+    assert B.SdpaParams.q_stride.offset == 112
+    assert B.SdpaParams.k_stride.offset == 136
+    assert B.SdpaParams.v_stride.offset == 160
+    assert B.SdpaParams.o_stride.offset == 184
 
 
 def test_launch_count_is_zero_after_a_rejected_call(sdpa_lib):
@@ -52,7 +56,7 @@ def test_launch_count_is_zero_after_a_rejected_call(sdpa_lib):
 
 
 def test_abi_version_and_status_strings(sdpa_lib):
-    assert S.sdpa_abi_version() == 3
+    assert S.sdpa_abi_version() == 4
     assert S.sdpa_status_string(0) == "ok"
     assert S.sdpa_status_string(2) == "unsupported problem"
     assert S.sdpa_status_string(99) == "unknown status"
@@ -178,10 +182,34 @@ def test_host_entry_pieces_cover_every_head_once(nb, hkv, chunks):
 def test_flags_are_checked(sdpa_lib):
     p = S.make_params(1, 4, 2, 300, 300, 64, S.SDPA_F16, 0.125, flags=S.SDPA_FLAG_SHARED_GPU)
     assert S.sdpa_select_kernel(p) == ("prefill_tc", 0)
-    for bad in (2, 0x80000000):
+    for ok in (S.SDPA_FLAG_BOOL_MASK, S.SDPA_FLAG_SHARED_GPU | S.SDPA_FLAG_BOOL_MASK):
+        p = S.make_params(1, 4, 2, 300, 300, 64, S.SDPA_F16, 0.125, flags=ok)
+        assert S.sdpa_select_kernel(p) == ("prefill_tc", 0)
+    for bad in (8, 0x80000000):
         p = S.make_params(1, 4, 2, 300, 300, 64, S.SDPA_F16, 0.125, flags=bad)
         assert S.sdpa_select_kernel(p) == ("none", 1)
         assert S.sdpa_forward_raw(p, 256, 256, 256, 256, None, None, 0, None) == 1
+
+
+def test_strides_are_checked(sdpa_lib):
+    B, H, L, D = 1, 4, 300, 64
+    dense = (H * L * D, L * D, D)
+    bshd = (L * H * D, D, H * D)  # [B, L, H, D] seen as [B, H, L, D]
+    p = S.make_params(B, H, H, L, L, D, S.SDPA_F16, 0.125, strides=(bshd, bshd, bshd, dense))
+    assert p.flags & S.SDPA_FLAG_STRIDES
+    assert S.sdpa_select_kernel(p) == ("prefill_tc", 0)
+    # a negative stride is invalid; a row stride of 3 fp16 elements (6 bytes)
+    # breaks the 16-byte rule; strides replace kv_capacity
+    p = S.make_params(B, H, H, L, L, D, S.SDPA_F16, 0.125, strides=(dense, (-1, L * D, D), dense, dense))
+    assert S.sdpa_select_kernel(p) == ("none", 1)
+    p = S.make_params(B, H, H, L, L, D, S.SDPA_F16, 0.125, strides=(dense, dense, (H * L * D, L * D, 3), dense))
+    assert S.sdpa_select_kernel(p) == ("none", 3)
+    p = S.make_params(B, H, H, L, L, D, S.SDPA_F16, 0.125, kv_capacity=400,
+                      strides=(dense, dense, dense, dense))
+    assert S.sdpa_select_kernel(p) == ("none", 1)
+    # fp32 rows: 4 elements are 16 bytes
+    p = S.make_params(B, H, H, L, L, D, S.SDPA_F32, 0.125, strides=(dense, dense, (H * L * D, L * D, 68), dense))
+    assert S.sdpa_select_kernel(p) == ("prefill_tc_f32", 0)
 
 
 def test_kv_capacity_and_length_arrays_are_checked(sdpa_lib):

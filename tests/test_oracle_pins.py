@@ -245,9 +245,45 @@ def pin_online_bruteforce(orc):
     return bool(ok)
 
 
+def pin_bool_mask_selects_keys(orc):
+    """A boolean mask keeps exactly the keys it marks True: each row equals
+    plain attention over the selected keys alone (K and V rows dropped, no
+    -inf arithmetic), with sinks and the causal rule; a row with no key
+    selected gives O = 0 and LSE = -inf (the sink with sinks)."""
+    ok = True
+    for causal in (False, True):
+        for with_sinks in (False, True):
+            B, Hq, Hkv, Lq, Lk, D = 2, 4, 2, 5, 7, 3
+            q, k, v = rand(B, Hq, Lq, D), rand(B, Hkv, Lk, D), rand(B, Hkv, Lk, D)
+            sel = RNG.random((B, Hq, Lq, Lk)) < 0.6
+            sel[0, 1, 2, :] = False  # one row keeps nothing
+            sinks = rand(Hq) if with_sinks else None
+            o, lse = orc.sdpa(q, k, v, 0.7, causal, sel, sinks)
+            for b in range(B):
+                for h in range(Hq):
+                    g = h // (Hq // Hkv)
+                    for i in range(Lq):
+                        keep = [j for j in range(Lk) if sel[b, h, i, j]
+                                and (not causal or j <= i + Lk - Lq)]
+                        logits = [0.7 * float(q[b, h, i] @ k[b, g, j]) for j in keep]
+                        if with_sinks:
+                            logits.append(float(sinks[h]))
+                        if not logits:
+                            ok &= np.all(o[b, h, i] == 0) and np.isneginf(lse[b, h, i])
+                            continue
+                        mx = max(logits)
+                        w = [math.exp(x - mx) for x in logits]
+                        den = sum(w)
+                        ref = sum(w[n] * v[b, g, j] for n, j in enumerate(keep)) / den \
+                            if keep else np.zeros(D)
+                        ok &= close(o[b, h, i], ref) and close(lse[b, h, i], mx + math.log(den))
+    return bool(ok)
+
+
 PINS = [pin_textbook, pin_probs_sum_to_one, pin_constant_v, pin_single_key, pin_causal_row0,
         pin_uniform, pin_sinks_shrink, pin_mask_shift, pin_mask_orientation, pin_permutation,
-        pin_gqa, pin_split_combine, pin_two_keys, pin_fully_masked, pin_online_bruteforce]
+        pin_gqa, pin_split_combine, pin_two_keys, pin_fully_masked, pin_online_bruteforce,
+        pin_bool_mask_selects_keys]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

@@ -39,7 +39,9 @@ def run_gpu(torch, w, inp):
 
 def oracle_rows(w, inp, rows):
     f = W.as_float64
-    mask = None if inp["mask"] is None else f(inp["mask"])
+    mask = inp["mask"]
+    if mask is not None:  # boolean masks go to the oracle as booleans
+        mask = mask.numpy() if mask.dtype == __import__("torch").bool else f(mask)
     sinks = None if inp["sinks"] is None else f(inp["sinks"])
     return O.sdpa(f(inp["q"]), f(inp["k"]), f(inp["v"]), w.scale, w.causal, mask, sinks,
                   rows=rows)
@@ -516,3 +518,104 @@ def test_prefill_tail_split_and_shared_gpu(cuda):
         grids = S.sdpa_last_launch_count()
         assert grids == (1 if shared or r == 0 or 2 * r > nsm else 2)
         compare(w, o.cpu(), lse.cpu(), o_ref, lse_ref, rows)
+
+
+# ------------------------------------------- boolean masks (True = visible)
+BOOL_CASES = {
+    "prefill_f16_d64": wl(2, 4, 2, 300, 333, 64, "float16", mask="bool_full"),
+    "prefill_bf16_d128_causal_sinks": wl(1, 4, 1, 260, 300, 128, "bfloat16", causal=True,
+                                         sinks=True, mask="bool_key"),
+    "prefill_f32_d64_hilo": wl(1, 2, 2, 129, 200, 64, "float32", mask="bool_full"),
+    "prefill_f32_d128_fma": wl(1, 2, 1, 100, 150, 128, "float32", mask="bool_full", sinks=True),
+    "decode_bf16_d128_sinks": wl(2, 8, 2, 1, 1000, 128, "bfloat16", mask="bool_full",
+                                 sinks=True),
+    "decode_f16_d512": wl(1, 32, 4, 1, 1024, 512, "float16", mask="bool_key"),
+    "few_queries_f16_causal": wl(1, 8, 2, 2, 777, 64, "float16", causal=True, mask="bool_full"),
+}
+
+
+@pytest.mark.parametrize("case", sorted(BOOL_CASES))
+def test_bool_mask(cuda, case):
+    check(cuda, BOOL_CASES[case])
+
+
+# ------------------------------------ non-contiguous q, k, v, o (D contiguous)
+def _bshd(t):
+    """[B, H, L, D] values stored as a dense [B, L, H, D] tensor, seen as
+    [B, H, L, D] (strides L*H*D, D, H*D)."""
+    return t.transpose(1, 2).contiguous().transpose(1, 2)
+
+
+def _strided_check(w, layout, monkeypatch=None, split=None):
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    if split is not None:
+        monkeypatch.setenv("GB300_SDPA_PREFILL_SPLIT", split)
+    inp = W.make_inputs(w)
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    mask = None if inp["mask"] is None else inp["mask"].cuda()
+    sinks = None if inp["sinks"] is None else inp["sinks"].cuda()
+    out, kv_len = None, None
+    if layout == "bshd":  # inputs [B, L, H, D]; out takes q's layout
+        q, k, v = _bshd(q), _bshd(k), _bshd(v)
+    elif layout == "kv_cache_bshd":  # k, v: rows [0, Lk) of a [B, C, Hkv, D] cache
+        C = w.Lk + 37
+        kc = torch.full((w.B, C, w.Hkv, w.D), float("nan"), dtype=k.dtype, device="cuda")
+        vc = kc.clone()
+        kc[:, :w.Lk] = k.transpose(1, 2)
+        vc[:, :w.Lk] = v.transpose(1, 2)
+        k, v, kv_len = kc.transpose(1, 2), vc.transpose(1, 2), w.Lk
+        out = _bshd(torch.empty_like(q))
+    elif layout == "padded_rows":  # rows of q, k, v and o padded to 2 D elements
+        def pad(t):
+            big = torch.zeros(t.shape[:3] + (2 * w.D,), dtype=t.dtype, device="cuda")
+            big[..., :w.D] = t
+            return big[..., :w.D]
+        q, k, v = pad(q), pad(k), pad(v)
+        out = pad(torch.zeros_like(q))
+    # (with one kv head the cache view is contiguous: the kv_capacity form)
+    o, lse = S.sdpa_forward(q, k, v, scale=w.scale, causal=w.causal, mask=mask, sinks=sinks,
+                            out=out, kv_len=kv_len)
+    torch.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    if layout == "bshd":
+        assert o.stride() == q.stride()  # the output keeps q's layout
+    o_ref, lse_ref = oracle_rows(w, inp, None)
+    compare(w, o.contiguous().cpu(), lse.cpu(), o_ref, lse_ref, None)
+
+
+STRIDE_CASES = {
+    "prefill_f16_d64": wl(2, 4, 2, 300, 333, 64, "float16", sinks=True),
+    "prefill_bf16_d128_causal": wl(1, 4, 1, 260, 300, 128, "bfloat16", causal=True,
+                                   mask="bool_key"),
+    "prefill_f32_d64_hilo": wl(1, 2, 2, 129, 200, 64, "float32", mask="full"),
+    "prefill_f32_d128_fma": wl(1, 2, 1, 100, 150, 128, "float32"),
+    "decode_bf16_d128": wl(2, 8, 2, 1, 1000, 128, "bfloat16", sinks=True),
+    "decode_f32_d512": wl(1, 32, 4, 1, 1024, 512, "float32"),
+    "few_queries_f16_d64": wl(1, 8, 2, 2, 777, 64, "float16", causal=True),
+}
+
+
+@pytest.mark.parametrize("layout", ["bshd", "kv_cache_bshd", "padded_rows"])
+@pytest.mark.parametrize("case", sorted(STRIDE_CASES))
+def test_strided_layouts(cuda, case, layout):
+    _strided_check(STRIDE_CASES[case], layout)
+
+
+@pytest.mark.parametrize("split", ["2", "4"])
+def test_strided_output_split_units(cuda, split, monkeypatch):
+    """Split units (partial results merged in the cluster) writing a strided
+    output."""
+    _strided_check(wl(1, 4, 2, 300, 1000, 64, "float16"), "kv_cache_bshd", monkeypatch, split)
+
+
+def test_strided_no_keys(cuda):
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    q = _bshd(torch.randn(2, 4, 5, 64, device="cuda", dtype=torch.float16))
+    kk = torch.zeros(2, 4, 0, 64, device="cuda", dtype=torch.float16)
+    out = _bshd(torch.full_like(q, 7.0))
+    o, lse = S.sdpa_forward(q, kk, kk, out=out)
+    torch.cuda.synchronize()
+    assert o.data_ptr() == out.data_ptr()
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
