@@ -326,7 +326,82 @@ def secondary(torch, S, device, stream, peaks):
                        "input_copies": copies, "timing": "CUDA graph of 20 calls, replayed"}
     out["decode_kvcache_b8_cap32768_d128_bf16_ragged"] = run_kvcache_decode(torch, S, device,
                                                                              peaks)
+    out.update(run_layout_variants(torch, S, device, peaks))
     return out
+
+
+def run_layout_variants(torch, S, device, peaks):
+    """The DiT prefill and the long decode on other input forms: [B, L, H, D]
+    tensors seen through a transpose (strided q, k, v, o) and a boolean key
+    mask.  Synthetic N(0, 1) data drawn on the device; prefill inputs rotate
+    over 3 copies (> 2 x L2), the decode K/V (1 GiB) exceeds L2."""
+    from scaled_dot_product_fwd_gb300 import workloads as W
+    g = torch.Generator(device=device).manual_seed(0)
+    res = {}
+
+    def bshd(B, H, L, D, dt):
+        return torch.randn(B, L, H, D, device=device, dtype=dt, generator=g).transpose(1, 2)
+
+    def time_calls(calls, steps):
+        for i in range(3):
+            calls[i % len(calls)]()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            calls[i % len(calls)]()
+        e1.record()
+        torch.cuda.synchronize()
+        if S.sdpa_device_status() != 0:
+            raise RuntimeError("device status set during a layout variant")
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+    w = W.DIT_F16
+    dt = torch.float16
+    sets = [tuple(bshd(w.B, h, w.Lq, w.D, dt) for h in (w.Hq, w.Hkv, w.Hkv)) for _ in range(3)]
+    outs = [torch.empty_like(st[0]) for st in sets]
+    calls = [lambda st=st, o=o: S.sdpa_forward(*st, scale=w.scale, out=o, return_lse=False)
+             for st, o in zip(sets, outs)]
+    sec = time_calls(calls, 20)
+    t = w.flops() / sec / 1e12
+    res[w.name + "_bshd"] = {"value": round(t, 1), "unit": "TFLOP/s",
+                             "ms_per_call": round(sec * 1e3, 4),
+                             "frac_of_bf16_peak": round(t / peaks["bf16_tflops"], 4),
+                             "layout": "q, k, v, o stored [B, L, H, D] (SDPA_FLAG_STRIDES)"}
+    keep = torch.rand(w.B, 1, 1, w.Lk, device=device, generator=g) >= 0.1
+    calls = [lambda st=st, o=o: S.sdpa_forward(*st, scale=w.scale, mask=keep, out=o,
+                                               return_lse=False)
+             for st, o in zip(sets, outs)]
+    sec = time_calls(calls, 20)
+    vis = int(keep.sum().item()) * w.Hq * w.Lq  # visible (query, key) pairs
+    tv = 4 * w.D * vis / sec / 1e12
+    res[w.name + "_bool_key_mask_bshd"] = {
+        "value": round(tv, 1), "unit": "TFLOP/s", "ms_per_call": round(sec * 1e3, 4),
+        "frac_of_bf16_peak": round(tv / peaks["bf16_tflops"], 4),
+        "flops": "4 D per visible (query, key) pair (about 90 % of the keys kept)"}
+    del sets, outs, calls
+    wd = W.DECODE_LONG
+    q = torch.randn(wd.B, wd.Hq, 1, wd.D, device=device, dtype=torch.bfloat16, generator=g)
+    k = bshd(wd.B, wd.Hkv, wd.Lk, wd.D, torch.bfloat16)
+    v = bshd(wd.B, wd.Hkv, wd.Lk, wd.D, torch.bfloat16)
+    o = torch.empty_like(q)
+    gr = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device)
+    S.sdpa_forward(q, k, v, scale=wd.scale, out=o, return_lse=False)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(gr, stream=side):
+            for _ in range(20):
+                S.sdpa_forward(q, k, v, scale=wd.scale, out=o, return_lse=False)
+    torch.cuda.synchronize()
+    sec = time_calls([gr.replay], 10) / 20
+    gb = wd.kv_bytes() / sec / 1e9
+    res[wd.name + "_kv_bshd"] = {
+        "value": round(gb, 1), "unit": "GB/s", "us_per_call": round(sec * 1e6, 2),
+        "frac_of_hbm": round(gb / peaks["hbm_gbs"], 4),
+        "layout": "k, v stored [B, L, Hkv, D]: one bulk copy per key row",
+        "timing": "CUDA graph of 20 calls, replayed"}
+    return res
 
 
 def run_kvcache_decode(torch, S, device, peaks):

@@ -137,7 +137,7 @@ struct PrefillArgs {
   const int* seq_lens_q;   // nullptr or per-batch valid query rows
   const int* seq_lens_kv;  // nullptr or per-batch valid keys
   int mask_bool;           // mask holds bytes, nonzero = visible (EXT only)
-  long long os0, os1, os2; // element strides of o (batch, head, row; EXT only)
+  long long os0, os1, os2; // element strides of o (batch, head, row)
 };
 
 template <bool BF16>
@@ -308,9 +308,9 @@ __device__ __forceinline__ Unit unit_of(const PrefillArgs& a, uint32_t bx) {
   return w;
 }
 
-// EXT: extended inputs (per-batch length arrays, a boolean mask, or an
-// output that is not dense [B, Hq, Lq, D]); without them the lengths are the
-// kernel arguments and the code is that of dense inputs.
+// EXT: extended inputs (per-batch length arrays or a boolean mask); without
+// them the lengths are the kernel arguments and the code is that of plain
+// inputs (any strides of q, k, v and o).
 // SPLIT: every unit is shared by the CTAs of a cluster (the units of a last,
 // partial wave); its own instantiation, so that whole units run code without
 // the merge.
@@ -714,8 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mn;
         }
         const float inv = (l > 0.f) ? oscale / l : 0.f;
-        T* orow = EXT ? static_cast<T*>(a.o) + (b * a.os0 + h * a.os1 + qi * a.os2)
-                      : static_cast<T*>(a.o) + ((static_cast<size_t>(b) * a.Hq + h) * a.Lq + qi) * D;
+        T* orow = static_cast<T*>(a.o) + (b * a.os0 + h * a.os1 + qi * a.os2);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ob[32];
@@ -1155,14 +1154,10 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
 
 }  // namespace
 
-// Whether a call needs the EXT instantiation: per-batch lengths, a boolean
-// mask, or an output that is not dense [B, Hq, Lq, D] (p normalised: strides
-// filled in).
+// Whether a call needs the EXT instantiation: per-batch lengths or a boolean
+// mask.
 inline bool prefill_needs_ext(const sdpa_params_t& p) {
-  const int64_t D = p.head_dim;
-  const bool dense_o = p.o_stride[2] == D && p.o_stride[1] == p.seq_len_q * D &&
-                       p.o_stride[0] == static_cast<int64_t>(p.num_q_heads) * p.seq_len_q * D;
-  return p.seq_lens_q || p.seq_lens_kv || (p.mask && (p.flags & SDPA_FLAG_BOOL_MASK)) || !dense_o;
+  return p.seq_lens_q || p.seq_lens_kv || (p.mask && (p.flags & SDPA_FLAG_BOOL_MASK));
 }
 
 // Head-size entry points (one translation unit each), p normalised;
