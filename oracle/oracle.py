@@ -185,3 +185,53 @@ def sdpa(*args, **kw):
 def sdpa_online(*args, **kw):
     """Tiled online-softmax recurrence; see OracleLib.sdpa_online."""
     return default().sdpa_online(*args, **kw)
+
+
+def sdpa_backward(q, k, v, d_o, scale, causal=False, mask=None, sinks=None):
+    """Gradients dQ, dK, dV of the attention forward, written out from the
+    plain definition in float64 (the backward kernels of the rustytorch
+    flash_attention.metal page: P recomputed as exp(S - LSE), D_i = dO_i . O_i,
+    dS = P * (dO V^T - D), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO;
+    the options are those of the mlx 0.30.7 cuDNN backward graph: attention
+    scale, bottom-right causal mask, additive bias, sink token).
+
+    q [B, Hq, Lq, D], k, v [B, Hkv, Lk, D], d_o [B, Hq, Lq, D]; mask as for
+    sdpa (additive, broadcastable, or boolean); sinks [Hq] or None.  The sink
+    is a logit with a zero value row: it enters the denominator, so P and the
+    gradients of q, k, v account for it; no gradient is returned for it, nor
+    for the mask.  Query heads h read kv head h // (Hq / Hkv); dK and dV sum
+    over the heads of a group.  Rows that see no key (and no sink) have
+    P = 0.  Returns (dq, dk, dv) as float64 arrays.
+    """
+    q, k, v, mask, _, sinks, _, (B, Hq, Hkv, Lq, Lk, D) = _prepare(q, k, v, mask, sinks, None)
+    d_o = np.ascontiguousarray(d_o, dtype=np.float64)
+    G = Hq // Hkv
+    kk = np.repeat(k, G, axis=1)  # [B, Hq, Lk, D]: the kv head of every query head
+    vv = np.repeat(v, G, axis=1)
+    s = scale * np.matmul(q, np.swapaxes(kk, -1, -2))  # [B, Hq, Lq, Lk]
+    if mask is not None:
+        s = s + np.broadcast_to(mask, s.shape)
+    if causal:
+        vis = np.tril(np.ones((Lq, Lk), bool), k=Lk - Lq)  # key j visible iff j <= i + Lk - Lq
+        s = np.where(vis, s, -np.inf)
+    # log-sum-exp over the keys and the sink logit
+    parts = [s]
+    if sinks is not None:
+        parts.append(np.broadcast_to(sinks.reshape(1, Hq, 1, 1), (B, Hq, Lq, 1)))
+    full = np.concatenate(parts, axis=-1)
+    mx = np.max(full, axis=-1, keepdims=True)
+    seen = np.isfinite(mx)
+    mx_safe = np.where(seen, mx, 0.0)
+    with np.errstate(divide="ignore"):  # rows that see nothing: log 0, unused below
+        lse = mx_safe + np.log(np.sum(np.exp(full - mx_safe), axis=-1, keepdims=True))
+    p = np.where(seen, np.exp(s - np.where(seen, lse, 0.0)), 0.0)  # [B, Hq, Lq, Lk]
+    o = np.matmul(p, vv)
+    dv_h = np.matmul(np.swapaxes(p, -1, -2), d_o)  # per query head
+    dp = np.matmul(d_o, np.swapaxes(vv, -1, -2))
+    dvec = np.sum(d_o * o, axis=-1, keepdims=True)
+    ds = p * (dp - dvec)
+    dq = scale * np.matmul(ds, kk)
+    dk_h = scale * np.matmul(np.swapaxes(ds, -1, -2), q)
+    dk = dk_h.reshape(B, Hkv, G, Lk, D).sum(axis=2)
+    dv = dv_h.reshape(B, Hkv, G, Lk, D).sum(axis=2)
+    return dq, dk, dv

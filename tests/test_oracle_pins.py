@@ -329,3 +329,68 @@ def test_planted_mistakes_are_caught(name, tmp_path):
     mutant = O.compile_variant(text.replace(old, new, 1), str(tmp_path / ("m_%s.so" % name)))
     failed = [p.__name__ for p in PINS if not p(mutant)]
     assert failed, "planted mistake %s passed every pin" % name
+
+
+# ------------------------------------------------------------ backward oracle
+def _fd_grads(q, k, v, d_o, scale, causal, mask, sinks, h=1e-6):
+    """Central differences of L = sum(O * dO) through the forward oracle."""
+    def loss(q_, k_, v_):
+        o, _ = O.sdpa(q_, k_, v_, scale, causal, mask, sinks)
+        return float(np.sum(o * d_o))
+    out = []
+    for which in range(3):
+        base = [q.copy(), k.copy(), v.copy()]
+        g = np.zeros_like(base[which])
+        it = np.nditer(g, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus = [a.copy() for a in base]
+            minus = [a.copy() for a in base]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            g[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
+        out.append(g)
+    return out
+
+
+@pytest.mark.parametrize("variant", ["plain", "causal", "mask", "bool_mask", "sinks_gqa",
+                                     "causal_mask_sinks"])
+def test_backward_oracle_matches_finite_differences(variant):
+    """dQ, dK, dV of the backward oracle equal the central differences of the
+    pinned forward oracle (loss = sum O * dO) on small problems."""
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, Lq, Lk, D = 1, 2, 2, 3, 4, 3
+    if variant in ("sinks_gqa", "causal_mask_sinks"):
+        Hq, Hkv = 4, 2
+    q, k, v = (rng.standard_normal(s) for s in ((B, Hq, Lq, D), (B, Hkv, Lk, D), (B, Hkv, Lk, D)))
+    d_o = rng.standard_normal((B, Hq, Lq, D))
+    causal = variant in ("causal", "causal_mask_sinks")
+    mask = sinks = None
+    if variant in ("mask", "causal_mask_sinks"):
+        mask = rng.standard_normal((B, Hq, Lq, Lk))
+        mask[0, 0, 1, 2] = -np.inf
+    if variant == "bool_mask":
+        mask = rng.random((B, Hq, Lq, Lk)) < 0.7
+        mask[0, 1, 0, :] = False  # a row that sees nothing: zero gradients
+    if variant in ("sinks_gqa", "causal_mask_sinks"):
+        sinks = rng.standard_normal(Hq)
+    got = O.sdpa_backward(q, k, v, d_o, 0.8, causal, mask, sinks)
+    want = _fd_grads(q, k, v, d_o, 0.8, causal, mask, sinks)
+    for g, w in zip(got, want):
+        assert np.max(np.abs(g - w)) < 1e-6 * max(1.0, np.max(np.abs(w)))
+
+
+def test_backward_oracle_closed_forms():
+    """q = 0 gives uniform attention: dV_j = (1/Lk) sum_i dO_i over the group's
+    heads and dK = 0 (no score depends on k).  Without sinks the scores of a
+    row are invariant to adding one vector to every key, so sum_j dK_j = 0."""
+    rng = np.random.default_rng(8)
+    B, Hq, Hkv, Lq, Lk, D = 2, 4, 2, 5, 6, 3
+    k, v = rng.standard_normal((B, Hkv, Lk, D)), rng.standard_normal((B, Hkv, Lk, D))
+    d_o = rng.standard_normal((B, Hq, Lq, D))
+    dq, dk, dv = O.sdpa_backward(np.zeros((B, Hq, Lq, D)), k, v, d_o, 0.7)
+    want = d_o.reshape(B, Hkv, 2, Lq, D).sum(axis=(2, 3))[:, :, None, :] / Lk
+    assert close(dv, np.broadcast_to(want, dv.shape)) and close(dk, np.zeros_like(dk))
+    q = rng.standard_normal((B, Hq, Lq, D))
+    dq, dk, dv = O.sdpa_backward(q, k, v, d_o, 0.7, causal=True)
+    assert close(dk.sum(axis=2), np.zeros((B, Hkv, D)))
