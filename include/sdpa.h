@@ -206,6 +206,36 @@ SDPA_API sdpa_status_t sdpa_forward(const sdpa_params_t* params,
                            void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/*
+ * sdpa_backward_workspace_size — bytes of device workspace that sdpa_backward
+ * needs (an fp32 dQ accumulator [B, Hq, Lq, D] and two fp32 [B, Hq, Lq]
+ * arrays); 0 for an invalid or unsupported problem.  Pure host function.
+ */
+SDPA_API size_t sdpa_backward_workspace_size(const sdpa_params_t* params);
+
+/*
+ * sdpa_backward — gradients of the forward pass (the backward kernels of the
+ * rustytorch flash_attention.metal page: P = exp(S - LSE), D_i = dO_i . O_i,
+ * dS = P (dO V^T - D), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO; with
+ * the options of the mlx cuDNN backward graph: scale, bottom-right causal
+ * mask, additive or boolean mask, sink token).  The problem description is
+ * the forward's (same params); supported: dtype fp16 or bf16, head_dim 64 or
+ * 128, no per-batch length arrays (else SDPA_ERR_UNSUPPORTED).
+ *  q, k, v, o, lse: the forward's inputs, output and log-sum-exp (lse is
+ *      required: the forward must have been asked for it).
+ *  d_o: gradient of the loss with respect to o, in o's layout.
+ *  dq, dk, dv: outputs in the layouts of q, k and v (their dtype).  With
+ *      grouped-query heads dk and dv sum over the query heads of each group.
+ *      The sink and the mask receive no gradient.
+ *  workspace / workspace_bytes: at least sdpa_backward_workspace_size(params)
+ *      bytes, 256-byte aligned; contents need no initialisation.
+ * Asynchronous on `stream`; errors as for sdpa_forward.
+ */
+SDPA_API sdpa_status_t sdpa_backward(const sdpa_params_t* params, const void* q, const void* k,
+                                     const void* v, const void* o, const void* d_o,
+                                     const float* lse, void* dq, void* dk, void* dv,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* sdpa_status_string — static, NUL-terminated text for a status code. */
 SDPA_API const char* sdpa_status_string(sdpa_status_t status);
 

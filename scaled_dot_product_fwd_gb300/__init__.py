@@ -11,14 +11,15 @@ from ._binding import (EXPORTS, KERNELS, LIB_PATH, SDPA_BF16, SDPA_F16, SDPA_F32
                        SDPA_FLAG_BOOL_MASK, SDPA_FLAG_SHARED_GPU, SDPA_FLAG_STRIDES, STATUS,
                        SdpaError, SdpaParams, dtype_code, load_library, make_params,
                        sdpa_abi_version, sdpa_debug_set_wait_limit_ns, sdpa_device_status,
-                       sdpa_last_launch_count,
+                       sdpa_last_launch_count, sdpa_backward, sdpa_backward_workspace_size,
                        sdpa_forward, sdpa_forward_host, sdpa_forward_raw, sdpa_select_kernel,
                        sdpa_status_string,
                        sdpa_workspace_size)
 
 __all__ = ["sdpa_forward", "sdpa_forward_host", "sdpa_forward_raw", "sdpa_workspace_size", "sdpa_select_kernel",
            "sdpa_status_string", "sdpa_device_status", "sdpa_debug_set_wait_limit_ns",
-           "sdpa_abi_version", "sdpa_last_launch_count", "make_params", "SdpaParams", "SdpaError",
+           "sdpa_abi_version", "sdpa_last_launch_count", "sdpa_backward",
+           "sdpa_backward_workspace_size", "make_params", "SdpaParams", "SdpaError",
            "load_library",
            "EXPORTS", "KERNELS", "STATUS", "LIB_PATH", "SDPA_F32", "SDPA_F16", "SDPA_BF16",
            "SDPA_FLAG_SHARED_GPU", "SDPA_FLAG_BOOL_MASK", "SDPA_FLAG_STRIDES",

@@ -29,7 +29,8 @@ KERNELS = {0: "none", 1: "prefill_tc", 2: "prefill_f32", 3: "decode_splitkv", 4:
 # Every symbol include/sdpa.h declares.
 EXPORTS = ("sdpa_workspace_size", "sdpa_select_kernel", "sdpa_forward", "sdpa_status_string",
            "sdpa_device_status", "sdpa_debug_set_wait_limit_ns", "sdpa_abi_version",
-           "sdpa_forward_decode_noalloc", "sdpa_last_launch_count")
+           "sdpa_forward_decode_noalloc", "sdpa_last_launch_count",
+           "sdpa_backward_workspace_size", "sdpa_backward")
 
 
 class SdpaParams(ctypes.Structure):
@@ -84,6 +85,11 @@ def load_library(path: str = LIB_PATH):
             lib.sdpa_last_launch_count.restype = ctypes.c_int
             lib.sdpa_forward_decode_noalloc.argtypes = [P] + [ctypes.c_void_p] * 6
             lib.sdpa_forward_decode_noalloc.restype = ctypes.c_int
+            lib.sdpa_backward_workspace_size.argtypes = [P]
+            lib.sdpa_backward_workspace_size.restype = ctypes.c_size_t
+            lib.sdpa_backward.argtypes = [P] + [ctypes.c_void_p] * 10 + [ctypes.c_size_t,
+                                                                         ctypes.c_void_p]
+            lib.sdpa_backward.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -144,6 +150,88 @@ def sdpa_forward_decode_noalloc_raw(params: SdpaParams, q, k, v, o, lse, stream)
     addresses; partial results in the library's static device scratch)."""
     pp = ctypes.byref(params) if params is not None else None
     return int(load_library().sdpa_forward_decode_noalloc(pp, q, k, v, o, lse, stream))
+
+
+def sdpa_backward_raw(params: SdpaParams, q, k, v, o, d_o, lse, dq, dk, dv, workspace,
+                      workspace_bytes, stream) -> int:
+    """Direct call of the backward entry point with integer device addresses."""
+    pp = ctypes.byref(params) if params is not None else None
+    return int(load_library().sdpa_backward(pp, q, k, v, o, d_o, lse, dq, dk, dv, workspace,
+                                            int(workspace_bytes), stream))
+
+
+def sdpa_backward_workspace_size(params: SdpaParams) -> int:
+    return int(load_library().sdpa_backward_workspace_size(ctypes.byref(params)))
+
+
+def sdpa_backward(q, k, v, o, lse, d_o, scale=None, causal=False, mask=None, sinks=None,
+                  dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of sdpa_forward on the GPU (fp16/bf16, head_dim 64 or 128).
+
+    q, k, v, mask, sinks, scale and causal as given to sdpa_forward; o and
+    lse its outputs; d_o the gradient of the loss with respect to o (o's
+    shape and dtype).  Tensors need a contiguous last dimension; dq, dk, dv
+    default to the layouts of q, k, v.  dk and dv sum over the query heads of
+    each kv head.  Returns (dq, dk, dv).
+    """
+    torch = _torch()
+    for t in (q, k, v, o, d_o):
+        if t.dim() != 4 or not t.is_cuda or t.stride(-1) != 1:
+            raise ValueError("q, k, v, o, d_o must be 4-D CUDA tensors with a contiguous last "
+                             "dimension")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == d_o.dtype):
+        raise TypeError("q, k, v, o, d_o must share a dtype")
+    B, Hq, Lq, D = q.shape
+    _, Hkv, Lk, _ = k.shape
+    if v.shape != k.shape or o.shape != q.shape or d_o.shape != q.shape:
+        raise ValueError("shape mismatch")
+    if lse is None or lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Lq) \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be the forward's contiguous float32 [B, Hq, Lq] output")
+    if d_o.stride() != o.stride():
+        raise ValueError("d_o must have o's layout (strides)")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    flags = 0
+    mask_ptr, mstride = None, (0, 0, 0, 1)
+    if mask is not None:
+        if (mask.dtype != q.dtype and mask.dtype != torch.bool) or mask.device != q.device:
+            raise TypeError("mask must have q's dtype (or bool) and q's device")
+        if mask.dtype == torch.bool:
+            flags |= SDPA_FLAG_BOOL_MASK
+        mexp = mask.expand(B, Hq, Lq, Lk)
+        mstride = tuple(int(s) for s in mexp.stride())
+        if Lk == 1:
+            mstride = mstride[:3] + (1,)
+        mask_ptr = mexp.data_ptr()
+    sinks_ptr = None
+    if sinks is not None:
+        if sinks.dtype != torch.float32 or not sinks.is_cuda or sinks.numel() != Hq:
+            raise TypeError("sinks must be a float32 CUDA tensor with Hq elements")
+        sinks = sinks.contiguous()
+        sinks_ptr = sinks.data_ptr()
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for g, t in ((dq, q), (dk, k), (dv, v)):
+        if g.shape != t.shape or g.dtype != t.dtype or g.stride() != t.stride():
+            raise ValueError("dq, dk, dv must have the shapes, dtype and layouts of q, k, v")
+    strides = tuple(tuple(int(s) for s in t.stride()[:3]) for t in (q, k, v, o))
+    params = make_params(B, Hq, Hkv, Lq, Lk, D, dtype_code(q.dtype), scale, causal, mask_ptr,
+                         mstride, sinks_ptr, flags=flags, strides=strides)
+    nbytes = sdpa_backward_workspace_size(params)
+    if workspace is None and nbytes > 0:
+        workspace = _workspace(nbytes, q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    st = sdpa_backward_raw(params, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           d_o.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                           dv.data_ptr(), ws_ptr, ws_bytes, stream)
+    if st != 0:
+        raise SdpaError(st, sdpa_status_string(st))
+    return dq, dk, dv
 
 
 def sdpa_device_status(stream=None) -> int:

@@ -1,0 +1,638 @@
+// backward.cu — gradients dQ, dK, dV of the attention forward (fp16/bf16,
+// head_dim 64/128) on the 5th-generation tensor cores of sm_103a.
+//
+// The computation is the backward pass of the rustytorch flash_attention.metal
+// page (backward kernels for dQ and for dK, dV): P recomputed from the
+// forward's log-sum-exp, P = exp(S - LSE); D_i = dO_i . O_i; dS = P (dP - D)
+// with dP = dO V^T; dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO; with the
+// options of the mlx cuDNN backward graph (attention scale, bottom-right
+// causal mask, additive bias, sink token: the sink enters through LSE).
+//
+// GB300 design (not the page's): one CTA per (key tile of 128 keys, kv head,
+// batch) owns dK and dV of its keys in TMEM for the whole pass (no atomics)
+// and walks the query tiles of every query head of the group.  Per query
+// tile the MMA warp computes S^T = K Q^T and dP^T = V dO^T with the keys as
+// TMEM lanes, so the compute warps (one thread per key) turn a row of S^T
+// into P^T and dS^T and write them back to TMEM as the A operands of
+// dV += P^T dO and dK += dS^T Q; dS^T also goes to shared memory (128-byte
+// swizzled rows of keys), the MN-major A operand of dQ = dS K, whose tile the
+// compute warps then add into an fp32 workspace with vector reductions.
+// Before the pass a small kernel computes D_i and LSE in log2 units per query
+// row and clears the dQ workspace; after it, another scales dQ and stores it
+// in the input dtype.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tensor_map.h"
+
+namespace gb300 {
+namespace {
+
+constexpr int kBT = 128;            // keys per CTA tile = query rows per step
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kBwdThreads = 32 * 6;
+constexpr float kLog2eB = 1.4426950408889634f;
+constexpr uint32_t kBarLse = 1;     // named barrier: the compute warps
+
+template <int D>
+struct BwdCfg {
+  static constexpr int CB = D / 64;             // 128-byte column blocks per row
+  static constexpr int TILE = kBT * D * 2;      // one 128-row fp16/bf16 tile
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + TILE;
+  static constexpr int Q_OFF = V_OFF + TILE;
+  static constexpr int DO_OFF = Q_OFF + TILE;
+  static constexpr int DS_OFF = DO_OFF + TILE;  // dS^T: 128 keys x 128 query rows
+  static constexpr int DS_BYTES = kBT * kBT * 2;
+  static constexpr int LSE_OFF = DS_OFF + DS_BYTES;  // 128 floats
+  static constexpr int DV_OFF = LSE_OFF + kBT * 4;   // 128 floats
+  static constexpr int BAR_OFF = DV_OFF + kBT * 4;
+  // kv_full, q_full, s_full, p_ready, mma_done, dq_read, drain
+  static constexpr int NBARS = 7;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+  // + alignment slack; at least 116 KB so that one CTA holds an SM (each
+  // allocates all 512 TMEM columns)
+  static constexpr int SMEM = (MISC_OFF + 16 + 1024) > 116 * 1024 ? (MISC_OFF + 16 + 1024)
+                                                                   : 116 * 1024;
+  // TMEM: S^T (P^T packed over its first 64 columns) | dP^T (dS^T packed) |
+  // dV | dK | dQ (D = 64; at D = 128 dQ reuses the S^T columns once the dV
+  // MMA, issued before it, has read P^T)
+  static constexpr uint32_t COL_S = 0;
+  static constexpr uint32_t COL_DP = 128;
+  static constexpr uint32_t COL_DV = 256;
+  static constexpr uint32_t COL_DK = 256 + D;
+  static constexpr uint32_t COL_DQ = D == 64 ? 384 : 0;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct BwdArgs {
+  int B, Hq, Hkv, G, Lq, Lk;
+  float sl2;    // scale * log2(e)
+  float scale;
+  int causal;
+  const void* mask;
+  long long ms0, ms1, ms2;
+  int mask_bool;
+  const float* lse2;  // [B, Hq, Lq]: LSE in log2 units (+inf: the row sees nothing)
+  const float* dvec;  // [B, Hq, Lq]: D_i = dO_i . O_i
+  float* dq_acc;      // [B, Hq, Lq, D] fp32, cleared before the pass
+  void* dk;
+  void* dv;
+  long long dks0, dks1, dks2, dvs0, dvs1, dvs2;  // element strides of dk, dv
+  int* status;
+  unsigned long long wait_ns;
+};
+
+template <bool BF16>
+struct BwdElem;
+template <>
+struct BwdElem<true> {
+  using T = __nv_bfloat16;
+  static __device__ __forceinline__ float to_f(T x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ T from_f(float x) { return __float2bfloat16_rn(x); }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+template <>
+struct BwdElem<false> {
+  using T = __half;
+  static __device__ __forceinline__ float to_f(T x) { return __half2float(x); }
+  static __device__ __forceinline__ T from_f(float x) { return __float2half_rn(x); }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
+
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- pre / post
+// Per query row (b, h, i): D_i = dO_i . O_i, LSE in log2 units (+inf for a
+// row that saw nothing, so that every P of it is 0), and a cleared dQ row.
+// One warp per row.
+struct PreArgs {
+  const void* o;
+  const void* d_o;
+  const float* lse;
+  float* lse2;
+  float* dvec;
+  float* dq_acc;
+  int Hq, Lq, D;
+  long long os0, os1, os2;  // strides of o and dO (dO has o's layout)
+  long long rows;
+};
+
+template <typename T>
+__device__ __forceinline__ float ld_f(const T* p);
+template <>
+__device__ __forceinline__ float ld_f(const __half* p) { return __half2float(*p); }
+template <>
+__device__ __forceinline__ float ld_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= a.rows) return;
+  const long long i = row % a.Lq;
+  const long long bh = row / a.Lq;
+  const long long h = bh % a.Hq, b = bh / a.Hq;
+  const long long off = b * a.os0 + h * a.os1 + i * a.os2;
+  const T* o = static_cast<const T*>(a.o) + off;
+  const T* g = static_cast<const T*>(a.d_o) + off;
+  float s = 0.f;
+  for (int d = lane; d < a.D; d += 32) s = fmaf(ld_f(o + d), ld_f(g + d), s);
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+  float* dq = a.dq_acc + row * a.D;
+  for (int d = lane; d < a.D; d += 32) dq[d] = 0.f;
+  if (lane == 0) {
+    a.dvec[row] = s;
+    const float l = a.lse[row];
+    a.lse2[row] = (l == -INFINITY) ? INFINITY : l * kLog2eB;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ T cvt(float x);
+template <>
+__device__ __forceinline__ __half cvt<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 cvt<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// dQ = scale * dq_acc in the input dtype, q's layout.  One warp per row.
+struct PostArgs {
+  const float* dq_acc;
+  void* dq;
+  int Hq, Lq, D;
+  float scale;
+  long long qs0, qs1, qs2;
+  long long rows;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_post_kernel(const PostArgs a) {
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= a.rows) return;
+  const long long i = row % a.Lq;
+  const long long bh = row / a.Lq;
+  const long long h = bh % a.Hq, b = bh / a.Hq;
+  T* dq = static_cast<T*>(a.dq) + b * a.qs0 + h * a.qs1 + i * a.qs2;
+  const float* src = a.dq_acc + row * a.D;
+  for (int d = lane; d < a.D; d += 32) dq[d] = cvt<T>(src[d] * a.scale);
+}
+
+// Wait for a phase ignoring the abort flag (drains in-flight asynchronous
+// work before the CTA exits); bounded by limit_ns.
+__device__ __forceinline__ void bwd_drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) break;
+  }
+}
+
+// ---------------------------------------------------------------- main pass
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+               const BwdArgs a) {
+  using C = BwdCfg<D>;
+  using E = BwdElem<BF16>;
+  using T = typename E::T;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sK = smem + C::K_OFF;
+  uint8_t* sV = smem + C::V_OFF;
+  uint8_t* sQ = smem + C::Q_OFF;
+  uint8_t* sDO = smem + C::DO_OFF;
+  uint8_t* sDS = smem + C::DS_OFF;
+  float* sLse = reinterpret_cast<float*>(smem + C::LSE_OFF);
+  float* sDv = reinterpret_cast<float*>(smem + C::DV_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* s_full = bars + 2;
+  uint64_t* p_ready = bars + 3;
+  uint64_t* mma_done = bars + 4;
+  uint64_t* dq_read = bars + 5;
+  uint64_t* drain = bars + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int j0 = blockIdx.x * kBT;  // first key of the tile
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int off = a.Lk - a.Lq;      // bottom-right causal: key j visible to row i iff j <= i + off
+  // query tiles of each head that hold a row seeing a key of this tile
+  const int nqt = (a.Lq + kBT - 1) / kBT;
+  int qt0 = 0;
+  if (a.causal && j0 - off > 0) qt0 = (j0 - off) / kBT;
+  const int per_head = nqt > qt0 ? nqt - qt0 : 0;
+  const int nsteps = a.G * per_head;  // (query head of the group, query tile) pairs
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(q_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, kBT);
+    mbar_init(mma_done, 1);
+    mbar_init(dq_read, kBT);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{a.wait_ns, abort_flag, a.status};
+  int q_issued = -1;  // producer: last step whose Q, dO copies were issued
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
+      for (int cb = 0; cb < C::CB; ++cb) {
+        tma_load_4d(sK + cb * kBT * 128, &tmK, kv_full, cb * 64, j0, kvh, b);
+        tma_load_4d(sV + cb * kBT * 128, &tmV, kv_full, cb * 64, j0, kvh, b);
+      }
+      for (int s = 0; s < nsteps; ++s) {
+        // the previous step's MMAs have read Q and dO
+        if (s > 0 && !mbar_wait(mma_done, (s - 1) & 1, wc)) break;
+        const int hq = kvh * a.G + s / per_head;
+        const int q0 = (qt0 + s % per_head) * kBT;
+        mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+        for (int cb = 0; cb < C::CB; ++cb) {
+          tma_load_4d(sQ + cb * kBT * 128, &tmQ, q_full, cb * 64, q0, hq, b);
+          tma_load_4d(sDO + cb * kBT * 128, &tmDO, q_full, cb * 64, q0, hq, b);
+        }
+        q_issued = s;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      // K-major operands (S^T = K Q^T, dP^T = V dO^T): a K step of 16
+      // elements is 32 bytes inside a 128-byte row, 4 steps per column block
+      auto kmaj = [&](const uint8_t* base, int kk) {
+        return sdesc(smem_addr(base) + (kk >> 2) * (kBT * 128) + (kk & 3) * 32, 16, 1024,
+                     kSwizzle128B);
+      };
+      // MN-major operands (rows along K, 64-wide column blocks kBT*128 bytes
+      // apart, 8-row groups 1024 bytes apart); a K step is 16 rows
+      auto mnmaj = [&](const uint8_t* base, int kk) {
+        return sdesc(smem_addr(base) + kk * 16 * 128, kBT * 128, 1024, kSwizzle128B);
+      };
+      constexpr uint32_t idS = idesc_f16(BF16, kBT, kBT, false, false);
+      constexpr uint32_t idKV = idesc_f16(BF16, kBT, D, false, true);
+      constexpr uint32_t idQ = idesc_f16(BF16, kBT, D, true, true);
+      bool ok = mbar_wait(kv_full, 0, wc);
+      for (int s = 0; s < nsteps && ok; ++s) {
+        ok = mbar_wait(q_full, s & 1, wc);
+        // the compute warps have read the previous dQ tile (its columns and,
+        // at D = 128, the S^T columns are written again below)
+        if (ok && s > 0) ok = mbar_wait(dq_read, (s - 1) & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          mma_f16_ss(tmem + C::COL_S, kmaj(sK, kk), kmaj(sQ, kk), idS, kk > 0 ? 1u : 0u);
+          mma_f16_ss(tmem + C::COL_DP, kmaj(sV, kk), kmaj(sDO, kk), idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        if (!mbar_wait(p_ready, s & 1, wc)) break;
+        tc_fence_after();
+        // dV += P^T dO and dK += dS^T Q (A from TMEM: 128 query rows, two
+        // elements per column); dQ = dS K (A: dS^T rows in shared memory)
+#pragma unroll
+        for (int kk = 0; kk < kBT / 16; ++kk) {
+          const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+          mma_f16_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8, mnmaj(sDO, kk), idKV, acc);
+          mma_f16_ts(tmem + C::COL_DK, tmem + C::COL_DP + kk * 8, mnmaj(sQ, kk), idKV, acc);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kBT / 16; ++kk)
+          mma_f16_ss(tmem + C::COL_DQ, mnmaj(sDS, kk), mnmaj(sK, kk), idQ, kk > 0 ? 1u : 0u);
+        mma_commit(mma_done);
+      }
+      // every MMA issued here completes before TMEM is freed
+      mma_commit(drain);
+      bwd_drain_wait(drain, 0, kDrainNs);
+    }
+  } else {
+    // ------------------------------------------------------- compute warps
+    // Thread r owns key j0 + r for P^T and dS^T (TMEM lane r) and query row
+    // q0 + r of the dQ tile.  Every step meets the same barriers, also after
+    // a failed wait (no path can hang).
+    const int r = threadIdx.x;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int jr = j0 + r;
+    bool ok = true;
+    for (int s = 0; s < nsteps; ++s) {
+      const int hq = kvh * a.G + s / per_head;
+      const int q0 = (qt0 + s % per_head) * kBT;
+      const size_t rowbase = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq;
+      {  // LSE (log2 units) and D of the step's 128 query rows
+        const int i = q0 + r;
+        sLse[r] = i < a.Lq ? a.lse2[rowbase + i] : INFINITY;  // +inf: P = 0
+        sDv[r] = i < a.Lq ? a.dvec[rowbase + i] : 0.f;
+      }
+      named_bar_sync(kBarLse, kBT);
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(s_full, s & 1, wc));
+      if (ok) {
+        tc_fence_after();
+        // mask entries of this key for the tile's rows (ms2 apart): additive
+        // (mrow) or boolean (mrowb)
+        const T* mrow = nullptr;
+        const uint8_t* mrowb = nullptr;
+        if (a.mask && jr < a.Lk) {
+          const long long moff = b * a.ms0 + hq * a.ms1 + q0 * a.ms2 + jr;
+          if (a.mask_bool)
+            mrowb = static_cast<const uint8_t*>(a.mask) + moff;
+          else
+            mrow = static_cast<const T*>(a.mask) + moff;
+        }
+        // two halves of 64 query rows: P^T packed over S^T columns [32h, 32h+32)
+        // (already read), dS^T over dP^T's, and dS^T into shared memory
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t sv[64], dp[64];
+          tmem_ld32(tmem + lane_off + C::COL_S + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+          tmem_ld32(tmem + lane_off + C::COL_S + hf * 64 + 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+          tmem_ld32(tmem + lane_off + C::COL_DP + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+          tmem_ld32(tmem + lane_off + C::COL_DP + hf * 64 + 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+          tmem_wait_ld();
+          uint32_t pk[32], dk[32];
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2) {
+            float pv[2], dv2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = hf * 64 + 2 * c2 + e;  // query row within the tile
+              const int i = q0 + c;
+              bool vis = jr < a.Lk && i < a.Lq && (!a.causal || jr <= i + off);
+              float x = __uint_as_float(sv[2 * c2 + e]) * a.sl2;
+              if (vis && mrowb) vis = mrowb[static_cast<long long>(c) * a.ms2] != 0;
+              if (vis && mrow) x += E::to_f(mrow[static_cast<long long>(c) * a.ms2]) * kLog2eB;
+              const float p = vis ? ex2(x - sLse[c]) : 0.f;
+              pv[e] = p;
+              dv2[e] = p * (__uint_as_float(dp[2 * c2 + e]) - sDv[c]);
+            }
+            pk[c2] = E::pack(pv[0], pv[1]);
+            dk[c2] = E::pack(dv2[0], dv2[1]);
+          }
+          tmem_st32(tmem + lane_off + C::COL_S + hf * 32, pk);
+          tmem_st32(tmem + lane_off + C::COL_DP + hf * 32, dk);
+          // dS^T row r, query rows 64h..64h+63: column block h, 16-byte chunks
+          // swizzled by the row (128-byte swizzle)
+          uint8_t* drow = sDS + hf * (kBT * 128) + r * 128;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(drow + ((ch ^ (r & 7)) << 4)) =
+                make_uint4(dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+        }
+        tmem_wait_st();
+        fence_proxy_async_shared();  // dS^T is read by the dQ MMA
+        tc_fence_before();
+      }
+      mbar_arrive(p_ready);
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(mma_done, s & 1, wc));
+      if (ok) {
+        tc_fence_after();
+        const int i = q0 + r;  // TMEM lane r is query row q0 + r of the dQ tile
+        float* dst = a.dq_acc + (rowbase + i) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + C::COL_DQ + c * 32, v);
+          tmem_wait_ld();
+          if (i < a.Lq) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]),
+                         __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
+                         __uint_as_float(v[4 * e + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_read);
+    }
+    // dK (scaled) and dV of key jr: complete after the last step's MMAs.
+    // The TMEM loads are warp-collective: every lane takes them (ok is
+    // warp-uniform) and only keys inside Lk are stored.
+    if (ok) {
+      tc_fence_after();
+      const bool key_ok = jr < a.Lk;
+      T* dkrow = static_cast<T*>(a.dk) + b * a.dks0 + kvh * a.dks1 + jr * a.dks2;
+      T* dvrow = static_cast<T*>(a.dv) + b * a.dvs0 + kvh * a.dvs1 + jr * a.dvs2;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t kv[32], vv[32];
+        if (nsteps > 0) {
+          tmem_ld32(tmem + lane_off + C::COL_DK + c * 32, kv);
+          tmem_ld32(tmem + lane_off + C::COL_DV + c * 32, vv);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) kv[e] = vv[e] = 0u;
+        }
+        uint32_t wk[16], wv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          wk[e] = E::pack(__uint_as_float(kv[2 * e]) * a.scale, __uint_as_float(kv[2 * e + 1]) * a.scale);
+          wv[e] = E::pack(__uint_as_float(vv[2 * e]), __uint_as_float(vv[2 * e + 1]));
+        }
+        if (key_ok) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            reinterpret_cast<uint4*>(dkrow + c * 32)[e] =
+                make_uint4(wk[4 * e], wk[4 * e + 1], wk[4 * e + 2], wk[4 * e + 3]);
+            reinterpret_cast<uint4*>(dvrow + c * 32)[e] =
+                make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (warp == kProducerWarp && lane == 0 && *abort_flag) {
+    // a role gave up: every copy the producer issued lands before the CTA exits
+    bwd_drain_wait(kv_full, 0, kDrainNs);
+    if (q_issued >= 0) bwd_drain_wait(q_full, q_issued & 1, kDrainNs);
+  }
+}
+
+size_t align256b(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+size_t backward_workspace(const sdpa_params_t& p) {
+  const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q;
+  return align256b(rows * p.head_dim * 4) + 2 * align256b(rows * 4);
+}
+
+namespace {
+
+template <int D, bool BF16>
+sdpa_status_t launch_bwd_impl(const sdpa_params_t& p, const void* q, const void* k,
+                              const void* v, const void* o, const void* d_o, const float* lse,
+                              void* dq, void* dk, void* dv, void* workspace,
+                              const LaunchEnv& env) {
+  using C = BwdCfg<D>;
+  using T = typename BwdElem<BF16>::T;
+  const long long rows = static_cast<long long>(p.batch) * p.num_q_heads * p.seq_len_q;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(w);
+  float* lse2 = reinterpret_cast<float*>(w + align256b(rows * D * 4));
+  float* dvec = reinterpret_cast<float*>(w + align256b(rows * D * 4) + align256b(rows * 4));
+  // D_i, LSE in log2 units, cleared dQ accumulator
+  PreArgs pa;
+  pa.o = o;
+  pa.d_o = d_o;
+  pa.lse = lse;
+  pa.lse2 = lse2;
+  pa.dvec = dvec;
+  pa.dq_acc = dq_acc;
+  pa.Hq = p.num_q_heads;
+  pa.Lq = p.seq_len_q;
+  pa.D = D;
+  pa.os0 = p.o_stride[0];
+  pa.os1 = p.o_stride[1];
+  pa.os2 = p.o_stride[2];
+  pa.rows = rows;
+  const unsigned row_blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+  int launched = 0;
+  if (rows > 0) {
+    bwd_pre_kernel<T><<<row_blocks, 256, 0, env.stream>>>(pa);
+    if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
+    ++launched;
+  }
+  if (p.seq_len_kv > 0) {
+    const CUtensorMapDataType dt =
+        BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t B = p.batch, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+    const uint64_t Lq = p.seq_len_q, Lk = p.seq_len_kv;
+    CUtensorMap tq, tk, tv, tdo;
+    auto enc = [&](CUtensorMap* m, const void* base, uint64_t L, uint64_t H,
+                   const int64_t (&sd)[3]) {
+      return encode_tiled_4d(m, dt, base, D, L, H, B, 2, 64, kBT, sd[2], sd[1], sd[0]);
+    };
+    // dO has o's layout; with no query row the Q and dO maps are never
+    // read (they describe k's first row so that the driver accepts them)
+    const bool noq = Lq == 0 || Hq == 0;
+    if (!enc(&tq, noq ? k : q, noq ? 1 : Lq, noq ? 1 : Hq, noq ? p.k_stride : p.q_stride) ||
+        !enc(&tk, k, Lk, Hkv, p.k_stride) || !enc(&tv, v, Lk, Hkv, p.v_stride) ||
+        !enc(&tdo, noq ? k : d_o, noq ? 1 : Lq, noq ? 1 : Hq, noq ? p.k_stride : p.o_stride))
+      return SDPA_ERR_CUDA;
+    BwdArgs a;
+    a.B = p.batch;
+    a.Hq = p.num_q_heads;
+    a.Hkv = p.num_kv_heads;
+    a.G = p.num_q_heads / p.num_kv_heads;
+    a.Lq = p.seq_len_q;
+    a.Lk = p.seq_len_kv;
+    a.sl2 = p.scale * kLog2eB;
+    a.scale = p.scale;
+    a.causal = p.causal ? 1 : 0;
+    a.mask = p.mask;
+    a.ms0 = p.mask_stride[0];
+    a.ms1 = p.mask_stride[1];
+    a.ms2 = p.mask_stride[2];
+    a.mask_bool = (p.flags & SDPA_FLAG_BOOL_MASK) ? 1 : 0;
+    a.lse2 = lse2;
+    a.dvec = dvec;
+    a.dq_acc = dq_acc;
+    a.dk = dk;
+    a.dv = dv;
+    a.dks0 = p.k_stride[0];  // dK has k's layout, dV v's
+    a.dks1 = p.k_stride[1];
+    a.dks2 = p.k_stride[2];
+    a.dvs0 = p.v_stride[0];
+    a.dvs1 = p.v_stride[1];
+    a.dvs2 = p.v_stride[2];
+    a.status = env.status;
+    a.wait_ns = env.wait_limit_ns;
+    auto kern = bwd_kernel<D, BF16>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+        cudaSuccess)
+      return SDPA_ERR_CUDA;
+    const dim3 grid((p.seq_len_kv + kBT - 1) / kBT, p.num_kv_heads, p.batch);
+    kern<<<grid, kBwdThreads, C::SMEM, env.stream>>>(tq, tk, tv, tdo, a);
+    if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
+    ++launched;
+  }
+  PostArgs qa;
+  qa.dq_acc = dq_acc;
+  qa.dq = dq;
+  qa.Hq = p.num_q_heads;
+  qa.Lq = p.seq_len_q;
+  qa.D = D;
+  qa.scale = p.scale;
+  qa.qs0 = p.q_stride[0];  // dQ has q's layout
+  qa.qs1 = p.q_stride[1];
+  qa.qs2 = p.q_stride[2];
+  qa.rows = rows;
+  if (rows > 0) {
+    bwd_post_kernel<T><<<row_blocks, 256, 0, env.stream>>>(qa);
+    if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
+    ++launched;
+  }
+  set_last_launches(launched);
+  return SDPA_OK;
+}
+
+}  // namespace
+
+sdpa_status_t launch_backward(const sdpa_params_t& p, const void* q, const void* k,
+                              const void* v, const void* o, const void* d_o, const float* lse,
+                              void* dq, void* dk, void* dv, void* workspace,
+                              const LaunchEnv& env) {
+  const bool bf16 = p.dtype == SDPA_BF16;
+  if (p.head_dim == 64)
+    return bf16 ? launch_bwd_impl<64, true>(p, q, k, v, o, d_o, lse, dq, dk, dv, workspace, env)
+                : launch_bwd_impl<64, false>(p, q, k, v, o, d_o, lse, dq, dk, dv, workspace, env);
+  if (p.head_dim == 128)
+    return bf16 ? launch_bwd_impl<128, true>(p, q, k, v, o, d_o, lse, dq, dk, dv, workspace, env)
+                : launch_bwd_impl<128, false>(p, q, k, v, o, d_o, lse, dq, dk, dv, workspace, env);
+  return SDPA_ERR_UNSUPPORTED;
+}
+
+}  // namespace gb300

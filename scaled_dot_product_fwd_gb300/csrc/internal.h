@@ -61,4 +61,13 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
                             const void* k, const void* v, void* o, float* lse, void* workspace,
                             const LaunchEnv& env);
 
+// Backward pass (fp16/bf16, D = 64 or 128; p normalised): dQ, dK, dV in the
+// layouts of q, k, v; dO in o's layout; lse the forward's.  Workspace:
+// backward_workspace(p) bytes (fp32 dQ accumulator, LSE in log2 units, D).
+size_t backward_workspace(const sdpa_params_t& p);
+sdpa_status_t launch_backward(const sdpa_params_t& p, const void* q, const void* k,
+                              const void* v, const void* o, const void* d_o, const float* lse,
+                              void* dq, void* dk, void* dv, void* workspace,
+                              const LaunchEnv& env);
+
 }  // namespace gb300

@@ -263,6 +263,56 @@ sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k,
   }
 }
 
+// ------------------------------------------------------------------ backward
+namespace {
+sdpa_status_t validate_backward(const sdpa_params_t* p) {
+  const sdpa_status_t st = validate_problem(p);
+  if (st != SDPA_OK) return st;
+  if (p->dtype != SDPA_F16 && p->dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128) return SDPA_ERR_UNSUPPORTED;
+  if (p->seq_lens_q || p->seq_lens_kv) return SDPA_ERR_UNSUPPORTED;
+  return SDPA_OK;
+}
+}  // namespace
+
+size_t sdpa_backward_workspace_size(const sdpa_params_t* params) {
+  if (validate_backward(params) != SDPA_OK) return 0;
+  return gb300::backward_workspace(*params);
+}
+
+sdpa_status_t sdpa_backward(const sdpa_params_t* p, const void* q, const void* k,
+                            const void* v, const void* o, const void* d_o, const float* lse,
+                            void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  sdpa_status_t st = validate_backward(p);
+  if (st != SDPA_OK) return st;
+  const bool has_q = static_cast<int64_t>(p->batch) * p->num_q_heads * p->seq_len_q > 0;
+  const bool has_k = static_cast<int64_t>(p->batch) * p->num_kv_heads * p->seq_len_kv > 0;
+  if (!has_q && !has_k) return SDPA_OK;
+  if (has_q && (!q || !o || !d_o || !lse || !dq)) return SDPA_ERR_INVALID_ARGUMENT;
+  if (has_k && (!k || !v || !dk || !dv)) return SDPA_ERR_INVALID_ARGUMENT;
+  const void* p16[] = {q, k, v, o, d_o, dq, dk, dv, p->mask};
+  for (const void* ptr : p16)
+    if (ptr && !aligned(ptr, 16)) return SDPA_ERR_MISALIGNED;
+  if (lse && !aligned(lse, 4)) return SDPA_ERR_MISALIGNED;
+  const size_t need = gb300::backward_workspace(*p);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return SDPA_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 256)) return SDPA_ERR_MISALIGNED;
+  }
+  int* status = nullptr;
+  int num_sms = 0;
+  if (!device_state(nullptr, &status, &num_sms)) return SDPA_ERR_CUDA;
+  gb300::LaunchEnv env;
+  env.status = status;
+  env.wait_limit_ns = g_wait_ns.load();
+  env.num_sms = num_sms;
+  env.stream = static_cast<cudaStream_t>(stream);
+  // (no key: dQ = 0 from the cleared accumulator; no query: dK = dV = 0)
+  return gb300::launch_backward(normalized(p), q, k, v, o, d_o, lse, dq, dk, dv, workspace, env);
+}
+
 sdpa_status_t sdpa_device_status(void* stream) {
   int* status = nullptr;
   if (!device_state(nullptr, &status, nullptr)) return SDPA_ERR_CUDA;
