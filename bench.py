@@ -327,7 +327,51 @@ def secondary(torch, S, device, stream, peaks):
     out["decode_kvcache_b8_cap32768_d128_bf16_ragged"] = run_kvcache_decode(torch, S, device,
                                                                              peaks)
     out.update(run_layout_variants(torch, S, device, peaks))
+    out.update(run_backward(torch, S, device, peaks))
     return out
+
+
+def run_backward(torch, S, device, peaks):
+    """Backward pass (sdpa_backward: pre, main and post kernels) on the DiT
+    fp16 and causal GQA bf16 shapes; TFLOP/s counts 2.5 x the forward's
+    algorithmic FLOPs (S recomputed, dP, dV, dK, dQ: five products of the
+    forward's two).  Synthetic N(0, 1) q, k, v, dO drawn on the device; o and
+    lse from the forward."""
+    from scaled_dot_product_fwd_gb300 import workloads as W
+    g = torch.Generator(device=device).manual_seed(1)
+    res = {}
+    for w in (W.DIT_F16, W.CAUSAL_GQA):
+        dt = torch.float16 if w.dtype == "float16" else torch.bfloat16
+        q = torch.randn(w.B, w.Hq, w.Lq, w.D, device=device, dtype=dt, generator=g)
+        k = torch.randn(w.B, w.Hkv, w.Lk, w.D, device=device, dtype=dt, generator=g)
+        v = torch.randn(w.B, w.Hkv, w.Lk, w.D, device=device, dtype=dt, generator=g)
+        o, lse = S.sdpa_forward(q, k, v, scale=w.scale, causal=w.causal)
+        d_o = torch.randn(o.shape, device=device, dtype=dt, generator=g)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def call():
+            S.sdpa_backward(q, k, v, o, lse, d_o, scale=w.scale, causal=w.causal, dq=dq, dk=dk,
+                            dv=dv)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 10
+        e0.record()
+        for _ in range(n):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        if S.sdpa_device_status() != 0:
+            raise RuntimeError("device status set during the backward")
+        sec = e0.elapsed_time(e1) / 1e3 / n
+        t = 2.5 * w.flops() / sec / 1e12
+        res[w.name + "_backward"] = {
+            "value": round(t, 1), "unit": "TFLOP/s", "ms_per_call": round(sec * 1e3, 4),
+            "frac_of_bf16_peak": round(t / peaks["bf16_tflops"], 4),
+            "kernels_per_call": S.sdpa_last_launch_count()}
+    return res
 
 
 def run_layout_variants(torch, S, device, peaks):
