@@ -33,11 +33,22 @@ namespace gb300 {
 namespace {
 
 constexpr int kBT = 128;            // keys per CTA tile = query rows per step
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kBwdThreads = 32 * 6;
+// 8 compute warps: warp w reads TMEM lanes 32 (w % 4) .. +31 (keys; query rows
+// for dQ) and takes half w / 4 of the columns.  Warps 8-11 form the control
+// warpgroup (producer, MMA issuer, two idle warps) and give registers to the
+// compute warpgroups with setmaxnreg (launch: 384 x 168 = 256 x 224 + 128 x 56).
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = 32 * kComputeWarps;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kBwdThreads = 32 * 12;
+constexpr uint32_t kComputeRegs = 224;
+constexpr uint32_t kControlRegs = 56;
 constexpr float kLog2eB = 1.4426950408889634f;
-constexpr uint32_t kBarLse = 1;     // named barrier: the compute warps
+// named barriers: kBarLse (the compute warps), kBarPair + q (the two warps
+// that share TMEM lane quarter q)
+constexpr uint32_t kBarLse = 1;
+constexpr uint32_t kBarPair = 2;
 
 template <int D>
 struct BwdCfg {
@@ -254,9 +265,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(kv_full, 1);
     mbar_init(q_full, 1);
     mbar_init(s_full, 1);
-    mbar_init(p_ready, kBT);
+    mbar_init(p_ready, kComputeThreads);
     mbar_init(mma_done, 1);
-    mbar_init(dq_read, kBT);
+    mbar_init(dq_read, kComputeThreads);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -272,6 +283,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const WaitCtl wc{a.wait_ns, abort_flag, a.status};
   int q_issued = -1;  // producer: last step whose Q, dO copies were issued
 
+  if (warp >= kComputeWarps) {
+    setmaxnreg_dec<kControlRegs>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -347,13 +360,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(drain);
       bwd_drain_wait(drain, 0, kDrainNs);
     }
+  }
+  // warps 10 and 11: idle
   } else {
+    setmaxnreg_inc<kComputeRegs>();
     // ------------------------------------------------------- compute warps
-    // Thread r owns key j0 + r for P^T and dS^T (TMEM lane r) and query row
-    // q0 + r of the dQ tile.  Every step meets the same barriers, also after
-    // a failed wait (no path can hang).
-    const int r = threadIdx.x;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // Thread (warp w, lane) owns key j0 + 32 (w % 4) + lane (TMEM lane) for
+    // P^T and dS^T on query columns [64 h, 64 h + 64) with h = w / 4, and
+    // query row q0 + 32 (w % 4) + lane of the dQ tile on D/2 of its columns.
+    // Every step meets the same barriers, also after a failed wait (no path
+    // can hang).
+    const int quarter = warp & 3;
+    const int hf = warp >> 2;
+    const int r = quarter * 32 + lane;  // TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int jr = j0 + r;
     bool ok = true;
     for (int s = 0; s < nsteps; ++s) {
@@ -361,14 +381,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int q0 = (qt0 + s % per_head) * kBT;
       const size_t rowbase = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq;
       {  // LSE (log2 units) and D of the step's 128 query rows
-        const int i = q0 + r;
-        sLse[r] = i < a.Lq ? a.lse2[rowbase + i] : INFINITY;  // +inf: P = 0
-        sDv[r] = i < a.Lq ? a.dvec[rowbase + i] : 0.f;
+        const int t = threadIdx.x & (kBT - 1);
+        const int i = q0 + t;
+        if (threadIdx.x < kBT)
+          sLse[t] = i < a.Lq ? a.lse2[rowbase + i] : INFINITY;  // +inf: P = 0
+        else
+          sDv[t] = i < a.Lq ? a.dvec[rowbase + i] : 0.f;
       }
-      named_bar_sync(kBarLse, kBT);
+      named_bar_sync(kBarLse, kComputeThreads);
       ok = __all_sync(0xffffffffu, ok && mbar_wait(s_full, s & 1, wc));
+      uint32_t sv[64], dp[64];
       if (ok) {
         tc_fence_after();
+        tmem_ld32(tmem + lane_off + C::COL_S + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(tmem + lane_off + C::COL_S + hf * 64 + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld32(tmem + lane_off + C::COL_DP + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+        tmem_ld32(tmem + lane_off + C::COL_DP + hf * 64 + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+        tmem_wait_ld();
+      }
+      // P^T and dS^T are written packed over the first 64 columns of S^T and
+      // dP^T, which the other warp of this quarter reads: both have read first
+      named_bar_sync(kBarPair + quarter, 64);
+      if (ok) {
+        // visible query columns of this key: [clo, chi) of the tile
+        int clo = 0, chi = min(kBT, a.Lq - q0);
+        if (jr >= a.Lk) chi = 0;
+        if (a.causal) clo = min(max(jr - off - q0, 0), kBT);
         // mask entries of this key for the tile's rows (ms2 apart): additive
         // (mrow) or boolean (mrowb)
         const T* mrow = nullptr;
@@ -380,47 +420,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           else
             mrow = static_cast<const T*>(a.mask) + moff;
         }
-        // two halves of 64 query rows: P^T packed over S^T columns [32h, 32h+32)
-        // (already read), dS^T over dP^T's, and dS^T into shared memory
+        uint32_t pk[32], dk[32];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t sv[64], dp[64];
-          tmem_ld32(tmem + lane_off + C::COL_S + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-          tmem_ld32(tmem + lane_off + C::COL_S + hf * 64 + 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-          tmem_ld32(tmem + lane_off + C::COL_DP + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-          tmem_ld32(tmem + lane_off + C::COL_DP + hf * 64 + 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
-          tmem_wait_ld();
-          uint32_t pk[32], dk[32];
+        for (int c2 = 0; c2 < 32; ++c2) {
+          float pv[2], dv2[2];
 #pragma unroll
-          for (int c2 = 0; c2 < 32; ++c2) {
-            float pv[2], dv2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int c = hf * 64 + 2 * c2 + e;  // query row within the tile
-              const int i = q0 + c;
-              bool vis = jr < a.Lk && i < a.Lq && (!a.causal || jr <= i + off);
-              float x = __uint_as_float(sv[2 * c2 + e]) * a.sl2;
+          for (int e = 0; e < 2; ++e) {
+            const int c = hf * 64 + 2 * c2 + e;  // query row within the tile
+            bool vis = c >= clo && c < chi;
+            float x = __uint_as_float(sv[2 * c2 + e]) * a.sl2;
+            if (mrow || mrowb) {
               if (vis && mrowb) vis = mrowb[static_cast<long long>(c) * a.ms2] != 0;
               if (vis && mrow) x += E::to_f(mrow[static_cast<long long>(c) * a.ms2]) * kLog2eB;
-              const float p = vis ? ex2(x - sLse[c]) : 0.f;
-              pv[e] = p;
-              dv2[e] = p * (__uint_as_float(dp[2 * c2 + e]) - sDv[c]);
             }
-            pk[c2] = E::pack(pv[0], pv[1]);
-            dk[c2] = E::pack(dv2[0], dv2[1]);
+            const float p = vis ? ex2(x - sLse[c]) : 0.f;
+            pv[e] = p;
+            dv2[e] = p * (__uint_as_float(dp[2 * c2 + e]) - sDv[c]);
           }
-          tmem_st32(tmem + lane_off + C::COL_S + hf * 32, pk);
-          tmem_st32(tmem + lane_off + C::COL_DP + hf * 32, dk);
-          // dS^T row r, query rows 64h..64h+63: column block h, 16-byte chunks
-          // swizzled by the row (128-byte swizzle)
-          uint8_t* drow = sDS + hf * (kBT * 128) + r * 128;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(drow + ((ch ^ (r & 7)) << 4)) =
-                make_uint4(dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+          pk[c2] = E::pack(pv[0], pv[1]);
+          dk[c2] = E::pack(dv2[0], dv2[1]);
         }
+        tmem_st32(tmem + lane_off + C::COL_S + hf * 32, pk);
+        tmem_st32(tmem + lane_off + C::COL_DP + hf * 32, dk);
+        // dS^T row r, query rows 64h..64h+63: column block h, 16-byte chunks
+        // swizzled by the row (128-byte swizzle)
+        uint8_t* drow = sDS + hf * (kBT * 128) + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(drow + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
         tmem_wait_st();
         fence_proxy_async_shared();  // dS^T is read by the dQ MMA
         tc_fence_before();
@@ -430,11 +458,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) {
         tc_fence_after();
         const int i = q0 + r;  // TMEM lane r is query row q0 + r of the dQ tile
-        float* dst = a.dq_acc + (rowbase + i) * D;
+        float* dst = a.dq_acc + (rowbase + i) * D + hf * (D / 2);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::COL_DQ + c * 32, v);
+          tmem_ld32(tmem + lane_off + C::COL_DQ + hf * (D / 2) + c * 32, v);
           tmem_wait_ld();
           if (i < a.Lq) {
 #pragma unroll
@@ -448,20 +476,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(dq_read);
     }
-    // dK (scaled) and dV of key jr: complete after the last step's MMAs.
-    // The TMEM loads are warp-collective: every lane takes them (ok is
-    // warp-uniform) and only keys inside Lk are stored.
+    // dK (scaled) and dV of key jr, D/2 columns per warp: complete after the
+    // last step's MMAs.  The TMEM loads are warp-collective: every lane takes
+    // them (ok is warp-uniform) and only keys inside Lk are stored.
     if (ok) {
       tc_fence_after();
       const bool key_ok = jr < a.Lk;
-      T* dkrow = static_cast<T*>(a.dk) + b * a.dks0 + kvh * a.dks1 + jr * a.dks2;
-      T* dvrow = static_cast<T*>(a.dv) + b * a.dvs0 + kvh * a.dvs1 + jr * a.dvs2;
+      T* dkrow = static_cast<T*>(a.dk) + b * a.dks0 + kvh * a.dks1 + jr * a.dks2 + hf * (D / 2);
+      T* dvrow = static_cast<T*>(a.dv) + b * a.dvs0 + kvh * a.dvs1 + jr * a.dvs2 + hf * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t kv[32], vv[32];
         if (nsteps > 0) {
-          tmem_ld32(tmem + lane_off + C::COL_DK + c * 32, kv);
-          tmem_ld32(tmem + lane_off + C::COL_DV + c * 32, vv);
+          tmem_ld32(tmem + lane_off + C::COL_DK + hf * (D / 2) + c * 32, kv);
+          tmem_ld32(tmem + lane_off + C::COL_DV + hf * (D / 2) + c * 32, vv);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -470,7 +498,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t wk[16], wv[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          wk[e] = E::pack(__uint_as_float(kv[2 * e]) * a.scale, __uint_as_float(kv[2 * e + 1]) * a.scale);
+          wk[e] = E::pack(__uint_as_float(kv[2 * e]) * a.scale,
+                          __uint_as_float(kv[2 * e + 1]) * a.scale);
           wv[e] = E::pack(__uint_as_float(vv[2 * e]), __uint_as_float(vv[2 * e + 1]));
         }
         if (key_ok) {
@@ -591,6 +620,18 @@ sdpa_status_t launch_bwd_impl(const sdpa_params_t& p, const void* q, const void*
     a.status = env.status;
     a.wait_ns = env.wait_limit_ns;
     auto kern = bwd_kernel<D, BF16>;
+    // The setmaxnreg split must fit the registers the kernel is launched with
+    // (an increase beyond them would wait forever): check once.
+    static int regs_ok = 0;  // 0 unknown, 1 fits, -1 does not
+    if (regs_ok == 0) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SDPA_ERR_CUDA;
+      const long alloc = static_cast<long>((fa.numRegs + 7) & ~7) * kBwdThreads;
+      const long need = static_cast<long>(kComputeThreads) * kComputeRegs +
+                        static_cast<long>(kBwdThreads - kComputeThreads) * kControlRegs;
+      regs_ok = alloc >= need ? 1 : -1;
+    }
+    if (regs_ok < 0) return SDPA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
         cudaSuccess)
       return SDPA_ERR_CUDA;
