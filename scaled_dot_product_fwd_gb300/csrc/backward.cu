@@ -54,17 +54,20 @@ template <int D>
 struct BwdCfg {
   static constexpr int CB = D / 64;             // 128-byte column blocks per row
   static constexpr int TILE = kBT * D * 2;      // one 128-row fp16/bf16 tile
+  // stages of the Q, dO ring (the next step's tiles load during this one;
+  // one stage at D = 128, where shared memory holds no second)
+  static constexpr int NST = D == 64 ? 2 : 1;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE;
-  static constexpr int Q_OFF = V_OFF + TILE;
-  static constexpr int DO_OFF = Q_OFF + TILE;
-  static constexpr int DS_OFF = DO_OFF + TILE;  // dS^T: 128 keys x 128 query rows
+  static constexpr int Q_OFF = V_OFF + TILE;          // NST tiles
+  static constexpr int DO_OFF = Q_OFF + NST * TILE;   // NST tiles
+  static constexpr int DS_OFF = DO_OFF + NST * TILE;  // dS^T: 128 keys x 128 query rows
   static constexpr int DS_BYTES = kBT * kBT * 2;
   static constexpr int LSE_OFF = DS_OFF + DS_BYTES;  // 128 floats
   static constexpr int DV_OFF = LSE_OFF + kBT * 4;   // 128 floats
   static constexpr int BAR_OFF = DV_OFF + kBT * 4;
-  // kv_full, q_full, s_full, p_ready, mma_done, dq_read, drain
-  static constexpr int NBARS = 7;
+  // kv_full, q_full[2], q_empty[2], s_full, p_ready, mma_done, dq_read, drain
+  static constexpr int NBARS = 10;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
   // + alignment slack; at least 116 KB so that one CTA holds an SM (each
   // allocates all 512 TMEM columns)
@@ -239,12 +242,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* sDv = reinterpret_cast<float*>(smem + C::DV_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;
-  uint64_t* s_full = bars + 2;
-  uint64_t* p_ready = bars + 3;
-  uint64_t* mma_done = bars + 4;
-  uint64_t* dq_read = bars + 5;
-  uint64_t* drain = bars + 6;
+  uint64_t* q_full = bars + 1;   // [2]: stage filled
+  uint64_t* q_empty = bars + 3;  // [2]: stage read by its step's MMAs
+  uint64_t* s_full = bars + 5;
+  uint64_t* p_ready = bars + 6;
+  uint64_t* mma_done = bars + 7;
+  uint64_t* dq_read = bars + 8;
+  uint64_t* drain = bars + 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -263,7 +267,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(q_full, 1);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(&q_full[st], 1);
+      mbar_init(&q_empty[st], 1);
+    }
     mbar_init(s_full, 1);
     mbar_init(p_ready, kComputeThreads);
     mbar_init(mma_done, 1);
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{a.wait_ns, abort_flag, a.status};
-  int q_issued = -1;  // producer: last step whose Q, dO copies were issued
+  int q_last[2] = {-1, -1};  // producer: last use of each Q, dO stage (-1: none)
 
   if (warp >= kComputeWarps) {
     setmaxnreg_dec<kControlRegs>();
@@ -298,16 +305,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_4d(sV + cb * kBT * 128, &tmV, kv_full, cb * 64, j0, kvh, b);
       }
       for (int s = 0; s < nsteps; ++s) {
-        // the previous step's MMAs have read Q and dO
-        if (s > 0 && !mbar_wait(mma_done, (s - 1) & 1, wc)) break;
+        const int st = s % C::NST;
+        const int use = s / C::NST;
+        // the stage's previous step's MMAs have read its Q and dO
+        if (use > 0 && !mbar_wait(&q_empty[st], (use - 1) & 1, wc)) break;
         const int hq = kvh * a.G + s / per_head;
         const int q0 = (qt0 + s % per_head) * kBT;
-        mbar_arrive_expect_tx(q_full, 2 * C::TILE);
+        mbar_arrive_expect_tx(&q_full[st], 2 * C::TILE);
         for (int cb = 0; cb < C::CB; ++cb) {
-          tma_load_4d(sQ + cb * kBT * 128, &tmQ, q_full, cb * 64, q0, hq, b);
-          tma_load_4d(sDO + cb * kBT * 128, &tmDO, q_full, cb * 64, q0, hq, b);
+          tma_load_4d(sQ + st * C::TILE + cb * kBT * 128, &tmQ, &q_full[st], cb * 64, q0, hq, b);
+          tma_load_4d(sDO + st * C::TILE + cb * kBT * 128, &tmDO, &q_full[st], cb * 64, q0, hq,
+                      b);
         }
-        q_issued = s;
+        q_last[st] = use;
       }
     }
   } else if (warp == kMmaWarp) {
@@ -329,16 +339,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idQ = idesc_f16(BF16, kBT, D, true, true);
       bool ok = mbar_wait(kv_full, 0, wc);
       for (int s = 0; s < nsteps && ok; ++s) {
-        ok = mbar_wait(q_full, s & 1, wc);
-        // the compute warps have read the previous dQ tile (its columns and,
-        // at D = 128, the S^T columns are written again below)
-        if (ok && s > 0) ok = mbar_wait(dq_read, (s - 1) & 1, wc);
+        const int st = s % C::NST;
+        const uint8_t* q_st = sQ + st * C::TILE;
+        const uint8_t* do_st = sDO + st * C::TILE;
+        ok = mbar_wait(&q_full[st], (s / C::NST) & 1, wc);
+        // At D = 128 the dQ tile shares the S^T columns: the compute warps
+        // have read the previous one.  (At D = 64 its own columns are written
+        // only after p_ready, which the compute warps give after reading it.)
+        if (ok && D == 128 && s > 0) ok = mbar_wait(dq_read, (s - 1) & 1, wc);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          mma_f16_ss(tmem + C::COL_S, kmaj(sK, kk), kmaj(sQ, kk), idS, kk > 0 ? 1u : 0u);
-          mma_f16_ss(tmem + C::COL_DP, kmaj(sV, kk), kmaj(sDO, kk), idS, kk > 0 ? 1u : 0u);
+          mma_f16_ss(tmem + C::COL_S, kmaj(sK, kk), kmaj(q_st, kk), idS, kk > 0 ? 1u : 0u);
+          mma_f16_ss(tmem + C::COL_DP, kmaj(sV, kk), kmaj(do_st, kk), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(s_full);
         if (!mbar_wait(p_ready, s & 1, wc)) break;
@@ -348,12 +362,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBT / 16; ++kk) {
           const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-          mma_f16_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8, mnmaj(sDO, kk), idKV, acc);
-          mma_f16_ts(tmem + C::COL_DK, tmem + C::COL_DP + kk * 8, mnmaj(sQ, kk), idKV, acc);
+          mma_f16_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8, mnmaj(do_st, kk), idKV, acc);
+          mma_f16_ts(tmem + C::COL_DK, tmem + C::COL_DP + kk * 8, mnmaj(q_st, kk), idKV, acc);
         }
 #pragma unroll
         for (int kk = 0; kk < kBT / 16; ++kk)
           mma_f16_ss(tmem + C::COL_DQ, mnmaj(sDS, kk), mnmaj(sK, kk), idQ, kk > 0 ? 1u : 0u);
+        mma_commit(&q_empty[st]);
         mma_commit(mma_done);
       }
       // every MMA issued here completes before TMEM is freed
@@ -376,19 +391,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int jr = j0 + r;
     bool ok = true;
+    // LSE (log2 units; threads 0-127) or D (threads 128-255) of one query row
+    // of a step, loaded a step ahead (+inf LSE: P = 0)
+    auto row_stat = [&](int s) {
+      const int hq = kvh * a.G + s / per_head;
+      const int i = (qt0 + s % per_head) * kBT + (threadIdx.x & (kBT - 1));
+      const size_t row = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq + i;
+      if (threadIdx.x < kBT) return i < a.Lq ? a.lse2[row] : INFINITY;
+      return i < a.Lq ? a.dvec[row] : 0.f;
+    };
+    float stat = nsteps > 0 ? row_stat(0) : 0.f;
     for (int s = 0; s < nsteps; ++s) {
       const int hq = kvh * a.G + s / per_head;
       const int q0 = (qt0 + s % per_head) * kBT;
       const size_t rowbase = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq;
-      {  // LSE (log2 units) and D of the step's 128 query rows
-        const int t = threadIdx.x & (kBT - 1);
-        const int i = q0 + t;
-        if (threadIdx.x < kBT)
-          sLse[t] = i < a.Lq ? a.lse2[rowbase + i] : INFINITY;  // +inf: P = 0
-        else
-          sDv[t] = i < a.Lq ? a.dvec[rowbase + i] : 0.f;
-      }
+      // every thread has finished the previous step's P (it passed that
+      // step's mma_done): the values may be replaced
+      if (threadIdx.x < kBT)
+        sLse[threadIdx.x] = stat;
+      else
+        sDv[threadIdx.x - kBT] = stat;
       named_bar_sync(kBarLse, kComputeThreads);
+      if (s + 1 < nsteps) stat = row_stat(s + 1);
       ok = __all_sync(0xffffffffu, ok && mbar_wait(s_full, s & 1, wc));
       uint32_t sv[64], dp[64];
       if (ok) {
@@ -525,7 +549,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kProducerWarp && lane == 0 && *abort_flag) {
     // a role gave up: every copy the producer issued lands before the CTA exits
     bwd_drain_wait(kv_full, 0, kDrainNs);
-    if (q_issued >= 0) bwd_drain_wait(q_full, q_issued & 1, kDrainNs);
+    for (int st = 0; st < 2; ++st)
+      if (q_last[st] >= 0) bwd_drain_wait(&q_full[st], q_last[st] & 1, kDrainNs);
   }
 }
 
