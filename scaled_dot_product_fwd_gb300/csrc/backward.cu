@@ -127,6 +127,39 @@ struct BwdElem<false> {
   }
 };
 
+// Pairs of fp32 values in one 64-bit register for the packed f32x2 ops.
+__device__ __forceinline__ uint64_t bf2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void bf2_unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t bf2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t bf2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t bf2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// 16-byte shared-memory load (32-bit shared address)
+__device__ __forceinline__ float4 bld4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
                "f"(d)
@@ -238,6 +271,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sQ = smem + C::Q_OFF;
   uint8_t* sDO = smem + C::DO_OFF;
   uint8_t* sDS = smem + C::DS_OFF;
+  // per step: -LSE (log2 units) and -D of the 128 query rows
   float* sLse = reinterpret_cast<float*>(smem + C::LSE_OFF);
   float* sDv = reinterpret_cast<float*>(smem + C::DV_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -391,14 +425,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int jr = j0 + r;
     bool ok = true;
-    // LSE (log2 units; threads 0-127) or D (threads 128-255) of one query row
-    // of a step, loaded a step ahead (+inf LSE: P = 0)
+    // -LSE (log2 units; threads 0-127) or -D (threads 128-255) of one query
+    // row of a step, loaded a step ahead (-inf: P = 0)
     auto row_stat = [&](int s) {
       const int hq = kvh * a.G + s / per_head;
       const int i = (qt0 + s % per_head) * kBT + (threadIdx.x & (kBT - 1));
       const size_t row = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq + i;
-      if (threadIdx.x < kBT) return i < a.Lq ? a.lse2[row] : INFINITY;
-      return i < a.Lq ? a.dvec[row] : 0.f;
+      if (threadIdx.x < kBT) return i < a.Lq ? -a.lse2[row] : -INFINITY;
+      return i < a.Lq ? -a.dvec[row] : 0.f;
     };
     float stat = nsteps > 0 ? row_stat(0) : 0.f;
     for (int s = 0; s < nsteps; ++s) {
@@ -445,6 +479,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mrow = static_cast<const T*>(a.mask) + moff;
         }
         uint32_t pk[32], dk[32];
+        const bool plain = clo <= hf * 64 && chi >= hf * 64 + 64 && !mrow && !mrowb;
+        if (__all_sync(0xffffffffu, plain)) {
+          // every column of this half visible, no mask: p = 2^(s sl2 - LSE),
+          // dS = p (dP - D) in packed pairs, -LSE and -D read 8 columns at a time
+          const uint64_t SL = bf2_pack(a.sl2, a.sl2);
+          const uint32_t la = smem_addr(sLse + hf * 64), da = smem_addr(sDv + hf * 64);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const float4 l0 = bld4(la + c8 * 32), l1 = bld4(la + c8 * 32 + 16);
+            const float4 d0 = bld4(da + c8 * 32), d1 = bld4(da + c8 * 32 + 16);
+            const float nl[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+            const float nd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+              const int c2 = c8 * 4 + pp;
+              const uint64_t X = bf2_fma(bf2_pack(__uint_as_float(sv[2 * c2]),
+                                                  __uint_as_float(sv[2 * c2 + 1])),
+                                         SL, bf2_pack(nl[2 * pp], nl[2 * pp + 1]));
+              float x0, x1;
+              bf2_unpack(X, x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              const uint64_t DS = bf2_mul(
+                  bf2_pack(p0, p1),
+                  bf2_add(bf2_pack(__uint_as_float(dp[2 * c2]), __uint_as_float(dp[2 * c2 + 1])),
+                          bf2_pack(nd[2 * pp], nd[2 * pp + 1])));
+              float s0, s1;
+              bf2_unpack(DS, s0, s1);
+              pk[c2] = E::pack(p0, p1);
+              dk[c2] = E::pack(s0, s1);
+            }
+          }
+        } else {
 #pragma unroll
         for (int c2 = 0; c2 < 32; ++c2) {
           float pv[2], dv2[2];
@@ -457,12 +523,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               if (vis && mrowb) vis = mrowb[static_cast<long long>(c) * a.ms2] != 0;
               if (vis && mrow) x += E::to_f(mrow[static_cast<long long>(c) * a.ms2]) * kLog2eB;
             }
-            const float p = vis ? ex2(x - sLse[c]) : 0.f;
+            const float p = vis ? ex2(x + sLse[c]) : 0.f;
             pv[e] = p;
-            dv2[e] = p * (__uint_as_float(dp[2 * c2 + e]) - sDv[c]);
+            dv2[e] = p * (__uint_as_float(dp[2 * c2 + e]) + sDv[c]);
           }
           pk[c2] = E::pack(pv[0], pv[1]);
           dk[c2] = E::pack(dv2[0], dv2[1]);
+        }
         }
         tmem_st32(tmem + lane_off + C::COL_S + hf * 32, pk);
         tmem_st32(tmem + lane_off + C::COL_DP + hf * 32, dk);
