@@ -63,9 +63,10 @@ struct BwdCfg {
   static constexpr int DO_OFF = Q_OFF + NST * TILE;   // NST tiles
   static constexpr int DS_OFF = DO_OFF + NST * TILE;  // dS^T: 128 keys x 128 query rows
   static constexpr int DS_BYTES = kBT * kBT * 2;
-  static constexpr int LSE_OFF = DS_OFF + DS_BYTES;  // 128 floats
-  static constexpr int DV_OFF = LSE_OFF + kBT * 4;   // 128 floats
-  static constexpr int BAR_OFF = DV_OFF + kBT * 4;
+  // -LSE and -D of a step's 128 query rows, two buffers each (step parity)
+  static constexpr int LSE_OFF = DS_OFF + DS_BYTES;  // 2 x 128 floats
+  static constexpr int DV_OFF = LSE_OFF + 2 * kBT * 4;
+  static constexpr int BAR_OFF = DV_OFF + 2 * kBT * 4;
   // kv_full, q_full[2], q_empty[2], s_full, p_ready, mma_done, dq_read, drain
   static constexpr int NBARS = 10;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
@@ -74,13 +75,17 @@ struct BwdCfg {
   static constexpr int SMEM = (MISC_OFF + 16 + 1024) > 116 * 1024 ? (MISC_OFF + 16 + 1024)
                                                                    : 116 * 1024;
   // TMEM: S^T (P^T packed over its first 64 columns) | dP^T (dS^T packed) |
-  // dV | dK | dQ (D = 64; at D = 128 dQ reuses the S^T columns once the dV
-  // MMA, issued before it, has read P^T)
+  // dV | dK | dQ x 2 (D = 64; at D = 128 dQ reuses the S^T columns once the
+  // dV MMA, issued before it, has read P^T)
   static constexpr uint32_t COL_S = 0;
   static constexpr uint32_t COL_DP = 128;
   static constexpr uint32_t COL_DV = 256;
   static constexpr uint32_t COL_DK = 256 + D;
+  // dQ: at D = 64 two buffers (step s in buffer s % 2, read while the next
+  // step's MMAs run); at D = 128 one, over the S^T columns
+  static constexpr bool PIPE_DQ = D == 64;
   static constexpr uint32_t COL_DQ = D == 64 ? 384 : 0;
+  static constexpr uint32_t dq_col(int s) { return PIPE_DQ ? COL_DQ + (s & 1) * 64 : COL_DQ; }
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
 #pragma unroll
         for (int kk = 0; kk < kBT / 16; ++kk)
-          mma_f16_ss(tmem + C::COL_DQ, mnmaj(sDS, kk), mnmaj(sK, kk), idQ, kk > 0 ? 1u : 0u);
+          mma_f16_ss(tmem + C::dq_col(s), mnmaj(sDS, kk), mnmaj(sK, kk), idQ, kk > 0 ? 1u : 0u);
         mma_commit(&q_empty[st]);
         mma_commit(mma_done);
       }
@@ -435,16 +440,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       return i < a.Lq ? -a.dvec[row] : 0.f;
     };
     float stat = nsteps > 0 ? row_stat(0) : 0.f;
+    // dQ tile of step s (TMEM lane r = query row q0 + r) added into the fp32
+    // accumulator, D/2 columns per warp
+    auto read_dq = [&](int s) {
+      if (!ok) return;
+      tc_fence_after();
+      const int hq = kvh * a.G + s / per_head;
+      const int i = (qt0 + s % per_head) * kBT + r;
+      float* dst = a.dq_acc + ((static_cast<size_t>(b) * a.Hq + hq) * a.Lq + i) * D + hf * (D / 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + C::dq_col(s) + hf * (D / 2) + c * 32, v);
+        tmem_wait_ld();
+        if (i < a.Lq) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                       __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+        }
+      }
+    };
     for (int s = 0; s < nsteps; ++s) {
       const int hq = kvh * a.G + s / per_head;
       const int q0 = (qt0 + s % per_head) * kBT;
       const size_t rowbase = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq;
-      // every thread has finished the previous step's P (it passed that
-      // step's mma_done): the values may be replaced
+      // buffer s % 2: a thread reaches this step's barrier only after every
+      // thread has passed the previous one, so the buffer of step s - 2 is free
+      float* const sl = sLse + (s & 1) * kBT;
+      float* const sd = sDv + (s & 1) * kBT;
       if (threadIdx.x < kBT)
-        sLse[threadIdx.x] = stat;
+        sl[threadIdx.x] = stat;
       else
-        sDv[threadIdx.x - kBT] = stat;
+        sd[threadIdx.x - kBT] = stat;
       named_bar_sync(kBarLse, kComputeThreads);
       if (s + 1 < nsteps) stat = row_stat(s + 1);
       ok = __all_sync(0xffffffffu, ok && mbar_wait(s_full, s & 1, wc));
@@ -484,7 +512,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // every column of this half visible, no mask: p = 2^(s sl2 - LSE),
           // dS = p (dP - D) in packed pairs, -LSE and -D read 8 columns at a time
           const uint64_t SL = bf2_pack(a.sl2, a.sl2);
-          const uint32_t la = smem_addr(sLse + hf * 64), da = smem_addr(sDv + hf * 64);
+          const uint32_t la = smem_addr(sl + hf * 64), da = smem_addr(sd + hf * 64);
 #pragma unroll
           for (int c8 = 0; c8 < 8; ++c8) {
             const float4 l0 = bld4(la + c8 * 32), l1 = bld4(la + c8 * 32 + 16);
@@ -523,9 +551,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               if (vis && mrowb) vis = mrowb[static_cast<long long>(c) * a.ms2] != 0;
               if (vis && mrow) x += E::to_f(mrow[static_cast<long long>(c) * a.ms2]) * kLog2eB;
             }
-            const float p = vis ? ex2(x + sLse[c]) : 0.f;
+            const float p = vis ? ex2(x + sl[c]) : 0.f;
             pv[e] = p;
-            dv2[e] = p * (__uint_as_float(dp[2 * c2 + e]) + sDv[c]);
+            dv2[e] = p * (__uint_as_float(dp[2 * c2 + e]) + sd[c]);
           }
           pk[c2] = E::pack(pv[0], pv[1]);
           dk[c2] = E::pack(dv2[0], dv2[1]);
@@ -544,28 +572,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_proxy_async_shared();  // dS^T is read by the dQ MMA
         tc_fence_before();
       }
-      mbar_arrive(p_ready);
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(mma_done, s & 1, wc));
-      if (ok) {
-        tc_fence_after();
-        const int i = q0 + r;  // TMEM lane r is query row q0 + r of the dQ tile
-        float* dst = a.dq_acc + (rowbase + i) * D + hf * (D / 2);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::COL_DQ + hf * (D / 2) + c * 32, v);
-          tmem_wait_ld();
-          if (i < a.Lq) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]),
-                         __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
-                         __uint_as_float(v[4 * e + 3]));
-          }
-        }
+      if constexpr (C::PIPE_DQ) {
+        // Step s-1's MMAs are complete (waited before this thread's p_ready
+        // arrival, so the phase cannot be confused with step s's); its dQ tile
+        // is read while step s's MMAs write the other buffer.
+        if (s > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(mma_done, (s - 1) & 1, wc));
+        mbar_arrive(p_ready);
+        if (s > 0) read_dq(s - 1);
+      } else {
+        mbar_arrive(p_ready);
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(mma_done, s & 1, wc));
+        read_dq(s);
+        tc_fence_before();
+        mbar_arrive(dq_read);
       }
-      tc_fence_before();
-      mbar_arrive(dq_read);
+    }
+    if constexpr (C::PIPE_DQ) {  // the last step's dQ tile
+      if (nsteps > 0) {
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(mma_done, (nsteps - 1) & 1, wc));
+        read_dq(nsteps - 1);
+      }
     }
     // dK (scaled) and dV of key jr, D/2 columns per warp: complete after the
     // last step's MMAs.  The TMEM loads are warp-collective: every lane takes
