@@ -451,8 +451,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + C::dq_col(s) + hf * (D / 2) + c * 32, v);
-        tmem_wait_ld();
+        __syncwarp();  // .aligned TMEM access after per-lane stores
+        tmem_ld32_sync(tmem + lane_off + C::dq_col(s) + hf * (D / 2) + c * 32, v);
         if (i < a.Lq) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -479,13 +479,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t sv[64], dp[64];
       if (ok) {
         tc_fence_after();
-        tmem_ld32(tmem + lane_off + C::COL_S + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(tmem + lane_off + C::COL_S + hf * 64 + 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld32(tmem + lane_off + C::COL_DP + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-        tmem_ld32(tmem + lane_off + C::COL_DP + hf * 64 + 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
-        tmem_wait_ld();
+        const uint32_t ts = tmem + lane_off + C::COL_S + hf * 64;
+        const uint32_t td = tmem + lane_off + C::COL_DP + hf * 64;
+        // tcgen05.ld/st are .aligned: the warp reconverges before each one
+        // (the code around them branches per lane)
+        __syncwarp();
+        tmem_ld4x32_sync(ts, ts + 32, td, td + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]),
+                         *reinterpret_cast<uint32_t(*)[32]>(&sv[32]),
+                         *reinterpret_cast<uint32_t(*)[32]>(&dp[0]),
+                         *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
       }
       // P^T and dS^T are written packed over the first 64 columns of S^T and
       // dP^T, which the other warp of this quarter reads: both have read first
@@ -559,6 +561,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dk[c2] = E::pack(dv2[0], dv2[1]);
         }
         }
+        __syncwarp();
         tmem_st32(tmem + lane_off + C::COL_S + hf * 32, pk);
         tmem_st32(tmem + lane_off + C::COL_DP + hf * 32, dk);
         // dS^T row r, query rows 64h..64h+63: column block h, 16-byte chunks
@@ -605,9 +608,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int c = 0; c < D / 64; ++c) {
         uint32_t kv[32], vv[32];
         if (nsteps > 0) {
-          tmem_ld32(tmem + lane_off + C::COL_DK + hf * (D / 2) + c * 32, kv);
-          tmem_ld32(tmem + lane_off + C::COL_DV + hf * (D / 2) + c * 32, vv);
-          tmem_wait_ld();
+          __syncwarp();
+          tmem_ld2x32_sync(tmem + lane_off + C::COL_DK + hf * (D / 2) + c * 32,
+                           tmem + lane_off + C::COL_DV + hf * (D / 2) + c * 32, kv, vv);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) kv[e] = vv[e] = 0u;

@@ -275,6 +275,12 @@ __device__ __forceinline__ float row_max_raw(const uint32_t (&s)[N]) {
 }
 
 
+// Bring the cache line holding global address p into L1 (a hint; p must
+// point into a live allocation).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // Wait for a phase ignoring the abort flag (used only to drain in-flight
 // asynchronous work before the CTA exits); bounded by limit_ns.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -600,6 +606,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         mrow = static_cast<const T*>(a.mask) + moff;
     }
+    // A boolean mask row that every query row shares (row stride 0, e.g. a
+    // key padding mask) is read by the warp together, one byte per lane and
+    // key, and spread to the lanes as bits by ballots; a mask with a row per
+    // query takes 16-byte loads where the row is 16-byte aligned.
+    const bool mshared = EXT && a.mask && a.mask_bool && a.ms2 == 0;
+    const uint8_t* mkey = nullptr;
+    if (mshared)
+      mkey = static_cast<const uint8_t*>(a.mask) + b * a.ms0 + h * a.ms1 + jb * BN;
+    const int mkeys = Lkb - jb * BN;  // keys of this batch from the first tile on
+    const bool mrow16 = EXT && mrowb && !mshared &&
+                        (reinterpret_cast<uintptr_t>(mrowb) & 15u) == 0;
     // keys are counted from this CTA's first key tile from here on
     limit -= jb * BN;
     float m = -INFINITY;  // reference max (log2 units)
@@ -608,6 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // interior tiles take the fused path when the scores need no mask and
     // the scale is positive (max of raw scores = max of scaled scores)
     const bool fast_ok = (a.sl2 > 0.f) && (a.mask == nullptr);
+    // tiles that may hold invisible keys take the fused path too at D = 128,
+    // and with extended inputs (a boolean mask, per-batch lengths) at any D
+    constexpr bool kFusedPartial = (D == 128) || EXT;
+    const bool fused_ok = (a.sl2 > 0.f) && (a.mask == nullptr || (EXT && a.mask_bool));
     // Output of the tile (whole units: right after its loop; split units:
     // after the CTAs of the cluster have exchanged partial results).
     auto epilogue = [&]() {
@@ -635,12 +656,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool send = t < nt && t != part && ok;
         if (send) {
           tc_fence_after();
+          __syncwarp();
           float4* prow = reinterpret_cast<float4*>(slotO + st * C::SLOT_O + r * D * 4);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t ob[32];
-            tmem_ld32(tO + c * 32, ob);
-            tmem_wait_ld();
+            tmem_ld32_sync(tO + c * 32, ob);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -715,11 +736,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float inv = (l > 0.f) ? oscale / l : 0.f;
         T* orow = static_cast<T*>(a.o) + (b * a.os0 + h * a.os1 + qi * a.os2);
+        __syncwarp();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ob[32];
-          tmem_ld32(tO + c * 32, ob);
-          tmem_wait_ld();
+          tmem_ld32_sync(tO + c * 32, ob);
           if constexpr (SPLIT) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -781,14 +802,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (t < nt) {
       for (int j = 0; j < nkv[t]; ++j) {
+        // the tile's boolean mask, fetched before its scores are waited for:
+        // vb[c] bit l = key 32c + l (shared row); a per-query row that is
+        // 16-byte aligned is brought into L1 here and loaded after the wait
+        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
+        if constexpr (EXT) {
+          const int kv0 = j * BN;
+          if (mshared) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int i = kv0 + 32 * c + lane;
+              vb[c] = __ballot_sync(0xffffffffu, i < mkeys && mkey[i] != 0);
+            }
+          } else if (mrow16 && kv0 + BN - 1 <= limit) {
+            prefetch_l1(mrowb + kv0);
+            prefetch_l1(mrowb + kv0 + BN - 16);
+          }
+        }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[t], j & 1, wc));
         if (ok) {
           tc_fence_after();
           uint32_t s[BN];
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c)
-            tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-          tmem_wait_ld();
+          static_assert(BN == 128, "score tile of 4 x 32 TMEM columns");
+          // tcgen05.ld/st are .aligned: the whole warp executes each one
+          // together.  Code before them may branch per lane (mask and bounds
+          // tests, spin waits); without an explicit reconvergence point the
+          // compiler may leave the warp split here (measured: a build did, and
+          // the loaded scores were wrong).
+          __syncwarp();
+          tmem_ld4x32_sync(tS, tS + 32, tS + 64, tS + 96,
+                           *reinterpret_cast<uint32_t(*)[32]>(&s[0]),
+                           *reinterpret_cast<uint32_t(*)[32]>(&s[32]),
+                           *reinterpret_cast<uint32_t(*)[32]>(&s[64]),
+                           *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
           const int kv0 = j * BN;
           float alpha = 1.f;
           bool resc;
@@ -842,6 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               const float mu = (m == -INFINITY) ? 0.f : m;
               if (pass > 0) tmem_wait_st();  // the first pass's P is overwritten
+              __syncwarp();
               float rs0, rs1;
               softmax_pairs<BF16, BN / 2, true>(
                   *reinterpret_cast<const uint32_t(*)[BN / 2]>(&s[0]), mul, mu,
@@ -861,23 +908,47 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!__any_sync(0xffffffffu, redo)) break;
               need_max = redo;
             }
-          } else if (D == 128 ? fast_ok : fast) {
-            // Positive scale, no mask: p = 2^(s * scale*log2e - m) with the
-            // scale folded into one packed FMA per pair, taken against the
-            // current reference max m without looking for the tile max.
-            // Every p is at most the row sum, so a sum <= 2^15 proves all
-            // p <= 2^15 (exact range in fp16 and bf16); only a row whose sum
-            // exceeds it (its max grew) or that has no max yet finds the tile
-            // max of the raw scores and repeats.  At D = 128 the tiles that
-            // cross the row's last visible key (bounds, causal diagonal) take
-            // this path too, with the keys past it scored -inf; at D = 64,
-            // where the softmax warps set the pace, they stay on the general
-            // path below (measured: routing them here slowed the loop).
+          } else if (kFusedPartial ? fused_ok : fast) {
+            // Positive scale, no additive mask: p = 2^(s * scale*log2e - m)
+            // with the scale folded into one packed FMA per pair, taken
+            // against the current reference max m without looking for the
+            // tile max.  Every p is at most the row sum, so a sum <= 2^15
+            // proves all p <= 2^15 (exact range in fp16 and bf16); only a row
+            // whose sum exceeds it (its max grew) or that has no max yet finds
+            // the tile max of the raw scores and repeats.  At D = 128, and
+            // with extended inputs at any D, the tiles that cross the row's
+            // last visible key (bounds, causal diagonal) or carry a boolean
+            // mask take this path too, with their invisible keys scored -inf;
+            // at D = 64 on plain inputs, where the softmax warps set the pace,
+            // the few boundary tiles stay on the general path below
+            // (measured: routing them here slowed the loop).
             if (!fast) {
               const int nvis = limit - kv0 + 1;  // visible keys of the row here
 #pragma unroll
               for (int i = 0; i < BN; ++i)
                 if (i >= nvis) s[i] = 0xff800000u;  // -inf
+              if constexpr (EXT) {
+                if (mshared) {
+#pragma unroll
+                  for (int i = 0; i < BN; ++i)
+                    if (!((vb[i >> 5] >> (i & 31)) & 1u)) s[i] = 0xff800000u;
+                } else if (mrow16 && kv0 + BN - 1 <= limit) {
+                  const uint4* src = reinterpret_cast<const uint4*>(mrowb + kv0);
+#pragma unroll
+                  for (int c = 0; c < BN / 16; ++c) {
+                    const uint4 q4 = src[c];
+                    const uint32_t wd[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                      if (((wd[e >> 2] >> (8 * (e & 3))) & 0xffu) == 0u)
+                        s[16 * c + e] = 0xff800000u;
+                  }
+                } else if (mrowb) {
+#pragma unroll
+                  for (int i = 0; i < BN; ++i)
+                    if (kv0 + i <= limit && !mrowb[kv0 + i]) s[i] = 0xff800000u;
+                }
+              }
             }
             resc = !(m > -INFINITY);
             if (!resc) {
@@ -886,12 +957,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (resc) {
               const float mx = row_max_raw(s) * a.sl2;  // -inf: no visible key
-              // (at D = 128 a row may see no key of a masked tile: m stays)
-              if (D == 64 || mx > -INFINITY) {
+              // (a row may see no key of a partial tile: m stays)
+              if (!kFusedPartial || mx > -INFINITY) {
                 alpha = ex2(m - mx);  // 0 when m = -inf
                 m = mx;
               }
-              softmax_pairs<BF16, BN>(s, a.sl2, (D == 128 && m == -INFINITY) ? 0.f : m, pk, rs);
+              softmax_pairs<BF16, BN>(s, a.sl2, (kFusedPartial && m == -INFINITY) ? 0.f : m,
+                                      pk, rs);
             }
           } else {
             float x[BN];
@@ -941,11 +1013,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O_t holds the sum through PV_{t,j-1} (complete: the commit behind
           // s_full tracks every earlier MMA); rescale rows whose max moved.
           if (j > 0 && __any_sync(0xffffffffu, resc)) {
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t ob[32];
-              tmem_ld32(tO + c * 32, ob);
-              tmem_wait_ld();
+              tmem_ld32_sync(tO + c * 32, ob);
 #pragma unroll
               for (int i = 0; i < 32; ++i) ob[i] = __float_as_uint(__uint_as_float(ob[i]) * alpha);
               tmem_st32(tO + c * 32, ob);

@@ -531,12 +531,71 @@ BOOL_CASES = {
                                  sinks=True),
     "decode_f16_d512": wl(1, 32, 4, 1, 1024, 512, "float16", mask="bool_key"),
     "few_queries_f16_causal": wl(1, 8, 2, 2, 777, 64, "float16", causal=True, mask="bool_full"),
+    # rows of 512 and 384 keys: every mask row 16-byte aligned (vector loads)
+    "prefill_f16_d64_rows16": wl(2, 4, 2, 300, 512, 64, "float16", mask="bool_full"),
+    "prefill_bf16_d128_rows16_sinks": wl(1, 4, 2, 200, 384, 128, "bfloat16", mask="bool_full",
+                                         sinks=True),
+    # a key mask shared by the query rows under the causal rule, ragged tail
+    "prefill_bf16_d64_key_causal": wl(2, 4, 2, 300, 333, 64, "bfloat16", causal=True,
+                                      mask="bool_key"),
+    "prefill_f16_d64_key_gqa": wl(1, 8, 1, 257, 1000, 64, "float16", mask="bool_key"),
 }
 
 
 @pytest.mark.parametrize("case", sorted(BOOL_CASES))
 def test_bool_mask(cuda, case):
     check(cuda, BOOL_CASES[case])
+
+
+@pytest.mark.parametrize("D,dtype,kind", [(64, "float16", "bool_key"),
+                                          (64, "bfloat16", "bool_full"),
+                                          (128, "float16", "bool_key")])
+def test_bool_mask_negative_scale(cuda, D, dtype, kind):
+    # a negative scale turns the row max of the raw scores into the row min:
+    # the kernels take their general (unfused) softmax
+    import scaled_dot_product_fwd_gb300 as S
+    w = wl(2, 4, 2, 200, 333, D, dtype, mask=kind)
+    inp = W.make_inputs(w)
+    q, k, v = (to_dev(inp[x], cuda) for x in ("q", "k", "v"))
+    o, lse = S.sdpa_forward(q, k, v, scale=-w.scale, mask=inp["mask"].cuda())
+    cuda.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    f = W.as_float64
+    o_ref, lse_ref = O.sdpa(f(inp["q"]), f(inp["k"]), f(inp["v"]), -w.scale, False,
+                            inp["mask"].numpy())
+    compare(w, o.cpu(), lse.cpu(), o_ref, lse_ref, None)
+
+
+@pytest.mark.parametrize("D,dtype,kind,causal", [(64, "float16", "bool_key", False),
+                                                 (64, "bfloat16", "bool_full", True),
+                                                 (128, "bfloat16", "bool_key", True)])
+def test_bool_mask_with_lengths(cuda, D, dtype, kind, causal):
+    # per-batch query and key lengths together with a boolean mask; the
+    # expected values take both as one additive 0 / -inf mask
+    import scaled_dot_product_fwd_gb300 as S
+    B, Hq, Hkv, Lq, Lk = 3, 4, 2, 300, 400
+    lens_q, lens_kv = [300, 129, 0], [400, 250, 77]
+    w = wl(B, Hq, Hkv, Lq, Lk, D, dtype, causal=False, mask=kind)
+    inp = W.make_inputs(w)
+    keep = np.broadcast_to(inp["mask"].numpy(), (B, Hq, Lq, Lk))
+    add = np.where(keep, 0.0, -np.inf)
+    for b in range(B):
+        i = np.arange(Lq)[:, None]
+        j = np.arange(Lk)[None, :]
+        hide = (i >= lens_q[b]) | (j >= lens_kv[b])
+        if causal:
+            hide |= j > i + (lens_kv[b] - lens_q[b])
+        add[b, :, hide] = -np.inf
+    f = W.as_float64
+    o_ref, lse_ref = O.sdpa(f(inp["q"]), f(inp["k"]), f(inp["v"]), w.scale, False, add)
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    tq = cuda.tensor(lens_q, dtype=cuda.int32, device="cuda")
+    tk = cuda.tensor(lens_kv, dtype=cuda.int32, device="cuda")
+    o, lse = S.sdpa_forward(q, k, v, scale=w.scale, causal=causal, mask=inp["mask"].cuda(),
+                            seq_lens_q=tq, seq_lens_kv=tk)
+    cuda.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    compare(w, o.cpu(), lse.cpu(), o_ref, lse_ref, None)
 
 
 # ------------------------------------ non-contiguous q, k, v, o (D contiguous)
