@@ -115,6 +115,25 @@ struct Cfg {
   static_assert(MAX_SPLIT * SLOT_O <= NS * STAGE, "partial O slots fit the ring");
   static_assert(kMaxSplit * SLOT_ML <= NQ * QT * TILE, "partial m, l fit the Q tiles");
   static_assert(SMEM <= 232448, "shared memory budget");
+  // Boolean key-mask bias (extended inputs, fp16/bf16): per ring stage a
+  // chunk of BN keys x 16 columns whose column 0 holds 0 (visible) or -inf
+  // per key, and per query tile a chunk of BM rows whose column 0 holds 1;
+  // one more K step of S = Q K^T then adds the bias.  No-swizzle K-major
+  // layout: core matrices of 8 rows x 16 bytes, the two of a row group
+  // (columns 0-7, 8-15) 128 bytes apart (LBO), row groups 256 bytes apart
+  // (SBO).
+  static constexpr int BIAS_CHUNK = BN * 32;
+  static constexpr int BIAS_LBO = 128;
+  static constexpr int BIAS_SBO = 256;
+  static constexpr int KB_OFF = (MISC_OFF + 16 + 127) / 128 * 128;
+  static constexpr int QB_OFF = KB_OFF + NS * BIAS_CHUNK;
+  static constexpr int SMEM_EXT = X3 ? SMEM : QB_OFF + NQ * BIAS_CHUNK + 1024;
+  static_assert(BM == BN, "one bias chunk shape for keys and query rows");
+  static_assert(SMEM_EXT <= 232448, "shared memory budget (extended inputs)");
+  // byte offset of (row, column 0) inside a bias chunk
+  static constexpr uint32_t bias_at(int r) {
+    return static_cast<uint32_t>((r >> 3) * BIAS_SBO + (r & 7) * 16);
+  }
 };
 
 struct PrefillArgs {
@@ -346,6 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_done = s_full + NQ;
   uint64_t* drain = o_done + NQ;
   uint64_t* xbar = drain + 1;
+  uint8_t* sKB = smem + C::KB_OFF;  // key-mask bias chunks (extended inputs)
+  uint8_t* sQB = smem + C::QB_OFF;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -409,6 +430,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
+  // A boolean mask row that every query row shares (row stride 0, e.g. a key
+  // padding mask) enters S through the tensor cores on the fused path: the
+  // producer writes each stage's key bias (0 / -inf), the query chunks hold
+  // 1 in column 0, and the MMA warp adds one K step.  Written here through
+  // the generic proxy, read by the tensor cores: zero the key chunks, write
+  // the query chunks, then a proxy fence before the CTA barrier.
+  const bool kbias = EXT && !X3 && a.mask && a.mask_bool && a.ms2 == 0 && a.sl2 > 0.f;
+  if (kbias) {
+    const uint32_t one = BF16 ? 0x3f80u : 0x3c00u;
+    uint4* z = reinterpret_cast<uint4*>(sKB);
+    constexpr int n16 = (C::NS + NQ) * C::BIAS_CHUNK / 16;
+    constexpr int q16 = C::NS * C::BIAS_CHUNK / 16;  // first word of the query chunks
+    for (int i = threadIdx.x; i < n16; i += kThreads) {
+      // a query-chunk word of columns 0-7 starts a 256-byte row group's first half
+      const bool col0 = i >= q16 && ((i * 16) % C::BIAS_SBO) < C::BIAS_LBO;
+      z[i] = make_uint4(col0 ? one : 0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_shared();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -437,6 +477,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(sQ + (t * C::QT + 1) * C::TILE + cb * BM * 128, &tmQ2, q_full,
                         cb * 64, m0 + t * BM, h, b);
         }
+    }
+    if (kbias) {
+      // the whole warp fills the stages: each lane writes the bias of keys
+      // 32c + lane of the tile before lane 0 arms the stage's barrier
+      const uint8_t* mk = static_cast<const uint8_t*>(a.mask) + b * a.ms0 + h * a.ms1;
+      const uint16_t ninf = BF16 ? 0xff80u : 0xfc00u;
+      for (int j = 0; j < nmax; ++j) {
+        const int s = j % C::NS;
+        const int use = j / C::NS;
+        const bool w = use == 0 || mbar_wait(&empty[s], (use - 1) & 1, wc);
+        if (!__all_sync(0xffffffffu, w)) break;
+        const int key0 = (jb + j) * BN;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          const int r = 32 * c + lane;
+          const bool vis = key0 + r < Lkb && mk[key0 + r] != 0;
+          *reinterpret_cast<uint16_t*>(sKB + s * C::BIAS_CHUNK + C::bias_at(r)) =
+              vis ? static_cast<uint16_t>(0) : ninf;
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          uint8_t* st = sRing + s * C::STAGE;
+          for (int cb = 0; cb < C::CB; ++cb) {
+            tma_load_4d(st + cb * BN * 128, &tmK, &full[s], cb * 64, key0, kvh, b);
+            tma_load_4d(st + C::V_OFF + cb * BN * 128, &tmV, &full[s], cb * 64, key0, kvh, b);
+          }
+        }
+        last_use[s] = use;
+      }
+    } else if (lane == 0) {
       for (int j = 0; j < nmax; ++j) {
         const int s = j % C::NS;
         const int use = j / C::NS;
@@ -482,6 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t k_lo = static_cast<uint32_t>(k_desc);
     const uint32_t v_lo = static_cast<uint32_t>(v_desc);
     auto qk = [&](uint32_t lo) { return (static_cast<uint64_t>(qk_hi) << 32) | lo; };
+    // key-mask bias chunks (no swizzle): query chunk t, key chunk of a stage
+    const uint64_t qb_desc = sdesc(smem_addr(sQB), C::BIAS_LBO, C::BIAS_SBO, 0);
+    const uint64_t kb_desc = sdesc(smem_addr(sKB), C::BIAS_LBO, C::BIAS_SBO, 0);
     auto vv = [&](uint32_t lo) { return (static_cast<uint64_t>(v_hi) << 32) | lo; };
     auto stage = [](int j) { return j % C::NS; };
     auto spar = [](int j) { return static_cast<uint32_t>((j / C::NS) & 1); };
@@ -504,6 +579,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16_ss_elect(dS, qk(qd + off), qk(kd + (C::K_LO >> 4) + off), idS, 1u, go);
           mma_f16_ss_elect(dS, qk(qd + (C::TILE >> 4) + off), qk(kd + off), idS, 1u, go);
         }
+      }
+      if constexpr (EXT && !X3) {  // + 1 * bias_j: the key mask
+        if (kbias)
+          mma_f16_ss_elect(dS, qb_desc + static_cast<uint32_t>((t * C::BIAS_CHUNK) >> 4),
+                           kb_desc + static_cast<uint32_t>((stage(j) * C::BIAS_CHUNK) >> 4),
+                           idS, 1u, go);
       }
     };
     // O_t += P_t V_j: P (128 x 128, K-major) from TMEM columns of S_t,
@@ -606,17 +687,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         mrow = static_cast<const T*>(a.mask) + moff;
     }
-    // A boolean mask row that every query row shares (row stride 0, e.g. a
-    // key padding mask) is read by the warp together, one byte per lane and
-    // key, and spread to the lanes as bits by ballots; a mask with a row per
-    // query takes 16-byte loads where the row is 16-byte aligned.
-    const bool mshared = EXT && a.mask && a.mask_bool && a.ms2 == 0;
-    const uint8_t* mkey = nullptr;
-    if (mshared)
-      mkey = static_cast<const uint8_t*>(a.mask) + b * a.ms0 + h * a.ms1 + jb * BN;
-    const int mkeys = Lkb - jb * BN;  // keys of this batch from the first tile on
-    const bool mrow16 = EXT && mrowb && !mshared &&
-                        (reinterpret_cast<uintptr_t>(mrowb) & 15u) == 0;
+    // A boolean mask row shared by every query row reaches the fused path
+    // through S itself (kbias); a mask with a row per query takes 16-byte
+    // loads where the row is 16-byte aligned.
+    const bool mrow16 = EXT && mrowb && !kbias && (reinterpret_cast<uintptr_t>(mrowb) & 15u) == 0;
     // keys are counted from this CTA's first key tile from here on
     limit -= jb * BN;
     float m = -INFINITY;  // reference max (log2 units)
@@ -802,19 +876,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (t < nt) {
       for (int j = 0; j < nkv[t]; ++j) {
-        // the tile's boolean mask, fetched before its scores are waited for:
-        // vb[c] bit l = key 32c + l (shared row); a per-query row that is
-        // 16-byte aligned is brought into L1 here and loaded after the wait
-        uint32_t vb[4] = {~0u, ~0u, ~0u, ~0u};
+        // a per-query mask row that is 16-byte aligned is brought into L1
+        // before the scores are waited for, and loaded after
         if constexpr (EXT) {
           const int kv0 = j * BN;
-          if (mshared) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int i = kv0 + 32 * c + lane;
-              vb[c] = __ballot_sync(0xffffffffu, i < mkeys && mkey[i] != 0);
-            }
-          } else if (mrow16 && kv0 + BN - 1 <= limit) {
+          if (mrow16 && kv0 + BN - 1 <= limit) {
             prefetch_l1(mrowb + kv0);
             prefetch_l1(mrowb + kv0 + BN - 16);
           }
@@ -923,15 +989,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the few boundary tiles stay on the general path below
             // (measured: routing them here slowed the loop).
             if (!fast) {
-              const int nvis = limit - kv0 + 1;  // visible keys of the row here
+              if (kv0 + BN - 1 > limit) {
+                const int nvis = limit - kv0 + 1;  // visible keys of the row here
 #pragma unroll
-              for (int i = 0; i < BN; ++i)
-                if (i >= nvis) s[i] = 0xff800000u;  // -inf
+                for (int i = 0; i < BN; ++i)
+                  if (i >= nvis) s[i] = 0xff800000u;  // -inf
+              }
+              // a boolean mask row of this query row (a shared one is already
+              // in S: kbias)
               if constexpr (EXT) {
-                if (mshared) {
-#pragma unroll
-                  for (int i = 0; i < BN; ++i)
-                    if (!((vb[i >> 5] >> (i & 31)) & 1u)) s[i] = 0xff800000u;
+                if (kbias) {
+                  // nothing to apply
                 } else if (mrow16 && kv0 + BN - 1 <= limit) {
                   const uint4* src = reinterpret_cast<const uint4*>(mrowb + kv0);
 #pragma unroll
@@ -1068,6 +1136,8 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
                           const void* q2, const void* k2, const void* v2, void* o, float* lse,
                           const QkvStrides& st, const LaunchEnv& env, int* grids) {
   using C = Cfg<D, X3>;
+  // extended inputs carry the key-mask bias chunks
+  constexpr int kSmem = EXT ? C::SMEM_EXT : C::SMEM;
   const CUtensorMapDataType dt =
       BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const uint64_t B = p.batch, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
@@ -1134,7 +1204,7 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
     }
     if (regs_ok[v2] < 0) return SDPA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(v2 ? kern_split : kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
+                             kSmem) != cudaSuccess)
       return SDPA_ERR_CUDA;
   }
   // One CTA per SM: the last wave of units is partial when the unit count is
@@ -1171,7 +1241,7 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
         cudaLaunchConfig_t oc = {};
         oc.gridDim = dim3(static_cast<unsigned>(k * env.num_sms));
         oc.blockDim = dim3(kThreads);
-        oc.dynamicSmemBytes = C::SMEM;
+        oc.dynamicSmemBytes = kSmem;
         oc.attrs = at;
         oc.numAttrs = 1;
         int n = 0;
@@ -1196,7 +1266,7 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   if (n_whole > 0) {
     a.unit0 = 0;
     a.ksplit = 1;
-    kern<<<dim3(static_cast<unsigned>(n_whole)), kThreads, C::SMEM, env.stream>>>(tq, tk, tv, tq2,
+    kern<<<dim3(static_cast<unsigned>(n_whole)), kThreads, kSmem, env.stream>>>(tq, tk, tv, tq2,
                                                                                   tk2, tv2, a);
     if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
     *grids = 1;
@@ -1214,7 +1284,7 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ksplit * tail));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = env.stream;
   cfg.attrs = attr;
   cfg.numAttrs = n_whole > 0 ? 2 : 1;
