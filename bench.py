@@ -376,8 +376,8 @@ def run_backward(torch, S, device, peaks):
 
 def run_layout_variants(torch, S, device, peaks):
     """The DiT prefill and the long decode on other input forms: [B, L, H, D]
-    tensors seen through a transpose (strided q, k, v, o) and a boolean key
-    mask.  Synthetic N(0, 1) data drawn on the device; prefill inputs rotate
+    tensors seen through a transpose (strided q, k, v, o), a boolean key mask
+    and an additive key mask.  Synthetic N(0, 1) data drawn on the device; prefill inputs rotate
     over 3 copies (> 2 x L2), the decode K/V (1 GiB) exceeds L2."""
     from scaled_dot_product_fwd_gb300 import workloads as W
     g = torch.Generator(device=device).manual_seed(0)
@@ -423,6 +423,19 @@ def run_layout_variants(torch, S, device, peaks):
         "value": round(tv, 1), "unit": "TFLOP/s", "ms_per_call": round(sec * 1e3, 4),
         "frac_of_bf16_peak": round(tv / peaks["bf16_tflops"], 4),
         "flops": "4 D per visible (query, key) pair (about 90 % of the keys kept)"}
+    bias = torch.randn(w.B, 1, 1, w.Lk, device=device, generator=g).to(dt)
+    hide = torch.rand(w.B, 1, 1, w.Lk, device=device, generator=g) < 0.1
+    bias[hide] = float("-inf")
+    calls = [lambda st=st, o=o: S.sdpa_forward(*st, scale=w.scale, mask=bias, out=o,
+                                               return_lse=False)
+             for st, o in zip(sets, outs)]
+    sec = time_calls(calls, 20)
+    vis = int((~hide).sum().item()) * w.Hq * w.Lq
+    tv = 4 * w.D * vis / sec / 1e12
+    res[w.name + "_additive_key_mask_bshd"] = {
+        "value": round(tv, 1), "unit": "TFLOP/s", "ms_per_call": round(sec * 1e3, 4),
+        "frac_of_bf16_peak": round(tv / peaks["bf16_tflops"], 4),
+        "flops": "4 D per visible (query, key) pair (N(0, 1) bias, about 10 % -inf)"}
     del sets, outs, calls
     wd = W.DECODE_LONG
     q = torch.randn(wd.B, wd.Hq, 1, wd.D, device=device, dtype=torch.bfloat16, generator=g)

@@ -157,6 +157,12 @@ struct PrefillArgs {
   const int* seq_lens_kv;  // nullptr or per-batch valid keys
   int mask_bool;           // mask holds bytes, nonzero = visible (EXT only)
   long long os0, os1, os2; // element strides of o (batch, head, row)
+  // key-mask bias step (EXT, fp16/bf16): the mask row is shared by every
+  // query row (row stride 0) and the scale is positive.  qbias holds the
+  // query chunk's columns 0 and 1 (two fp16/bf16 values): 1 and 0 for a
+  // boolean mask, 1/scale as hi + lo for an additive one.
+  int kbias;
+  uint32_t qbias;
 };
 
 template <bool BF16>
@@ -430,22 +436,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
-  // A boolean mask row that every query row shares (row stride 0, e.g. a key
-  // padding mask) enters S through the tensor cores on the fused path: the
-  // producer writes each stage's key bias (0 / -inf), the query chunks hold
-  // 1 in column 0, and the MMA warp adds one K step.  Written here through
+  // A mask row that every query row shares (row stride 0, e.g. a key padding
+  // mask) enters S through the tensor cores on the fused path: the producer
+  // writes each stage's key bias (boolean: 0 / -inf in column 0; additive:
+  // the mask value in columns 0 and 1), the query chunks hold qbias, and the
+  // MMA warp adds one K step: S + bias / scale, so x = S * scale*log2e gains
+  // mask * log2e.  Written here through
   // the generic proxy, read by the tensor cores: zero the key chunks, write
   // the query chunks, then a proxy fence before the CTA barrier.
-  const bool kbias = EXT && !X3 && a.mask && a.mask_bool && a.ms2 == 0 && a.sl2 > 0.f;
+  const bool kbias = EXT && !X3 && a.kbias;
   if (kbias) {
-    const uint32_t one = BF16 ? 0x3f80u : 0x3c00u;
     uint4* z = reinterpret_cast<uint4*>(sKB);
     constexpr int n16 = (C::NS + NQ) * C::BIAS_CHUNK / 16;
     constexpr int q16 = C::NS * C::BIAS_CHUNK / 16;  // first word of the query chunks
     for (int i = threadIdx.x; i < n16; i += kThreads) {
       // a query-chunk word of columns 0-7 starts a 256-byte row group's first half
       const bool col0 = i >= q16 && ((i * 16) % C::BIAS_SBO) < C::BIAS_LBO;
-      z[i] = make_uint4(col0 ? one : 0u, 0u, 0u, 0u);
+      z[i] = make_uint4(col0 ? a.qbias : 0u, 0u, 0u, 0u);
     }
     fence_proxy_async_shared();
   }
@@ -481,8 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kbias) {
       // the whole warp fills the stages: each lane writes the bias of keys
       // 32c + lane of the tile before lane 0 arms the stage's barrier
-      const uint8_t* mk = static_cast<const uint8_t*>(a.mask) + b * a.ms0 + h * a.ms1;
-      const uint16_t ninf = BF16 ? 0xff80u : 0xfc00u;
+      const long long moff = b * a.ms0 + h * a.ms1;
+      const uint8_t* mk = static_cast<const uint8_t*>(a.mask) + moff;                 // boolean
+      const uint16_t* mv = static_cast<const uint16_t*>(a.mask) + moff;               // additive
+      const uint32_t ninf = BF16 ? 0xff80u : 0xfc00u;
       for (int j = 0; j < nmax; ++j) {
         const int s = j % C::NS;
         const int use = j / C::NS;
@@ -492,9 +501,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
           const int r = 32 * c + lane;
-          const bool vis = key0 + r < Lkb && mk[key0 + r] != 0;
-          *reinterpret_cast<uint16_t*>(sKB + s * C::BIAS_CHUNK + C::bias_at(r)) =
-              vis ? static_cast<uint16_t>(0) : ninf;
+          const int key = key0 + r;
+          uint32_t v = ninf;  // keys past this batch's length: -inf
+          if (key < Lkb) {
+            if (a.mask_bool) {
+              v = mk[key] != 0 ? 0u : ninf;
+            } else {
+              // columns 0 and 1 (1/scale = hi + lo); with lo = 0 column 1
+              // stays 0, so that a -inf mask value never meets a zero
+              const uint32_t m16 = mv[key];
+              v = m16 | ((a.qbias >> 16) != 0u ? (m16 << 16) : 0u);
+            }
+          }
+          *reinterpret_cast<uint32_t*>(sKB + s * C::BIAS_CHUNK + C::bias_at(r)) = v;
         }
         fence_proxy_async_shared();
         __syncwarp();
@@ -702,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tiles that may hold invisible keys take the fused path too at D = 128,
     // and with extended inputs (a boolean mask, per-batch lengths) at any D
     constexpr bool kFusedPartial = (D == 128) || EXT;
-    const bool fused_ok = (a.sl2 > 0.f) && (a.mask == nullptr || (EXT && a.mask_bool));
+    const bool fused_ok = (a.sl2 > 0.f) && (a.mask == nullptr || (EXT && (a.mask_bool || kbias)));
     // Output of the tile (whole units: right after its loop; split units:
     // after the CTAs of the cluster have exchanged partial results).
     auto epilogue = [&]() {
@@ -1187,6 +1206,36 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   a.os0 = p.o_stride[0];
   a.os1 = p.o_stride[1];
   a.os2 = p.o_stride[2];
+  a.kbias = 0;
+  a.qbias = 0;
+  if (EXT && !X3 && p.mask && p.mask_stride[2] == 0 && p.scale > 0.f) {
+    if (p.flags & SDPA_FLAG_BOOL_MASK) {
+      a.kbias = 1;
+      a.qbias = BF16 ? 0x3f80u : 0x3c00u;  // 1, 0
+    } else {
+      // 1/scale = hi + lo: hi rounded toward zero so that lo >= 0 (a -inf
+      // mask value then gives -inf in both products)
+      const float inv = 1.f / p.scale;
+      uint32_t hi, lo;
+      bool fits = true;
+      if (BF16) {
+        const __nv_bfloat16_raw h = __float2bfloat16_rz(inv);
+        const __nv_bfloat16_raw l = __float2bfloat16_rn(inv - __bfloat162float(h));
+        hi = h.x;
+        lo = l.x;
+      } else {
+        fits = inv <= 65504.f;
+        const __half_raw h = __float2half_rz(inv);
+        const __half_raw l = __float2half_rn(inv - __half2float(h));
+        hi = h.x;
+        lo = l.x;
+      }
+      if (fits) {
+        a.kbias = 1;
+        a.qbias = hi | (lo << 16);
+      }
+    }
+  }
   auto kern = prefill_tc_kernel<D, BF16, X3, EXT, false>;
   auto kern_split = prefill_tc_kernel<D, BF16, X3, EXT, true>;
   // The setmaxnreg split must fit the registers the kernel is launched with
@@ -1296,10 +1345,11 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
 
 }  // namespace
 
-// Whether a call needs the EXT instantiation: per-batch lengths or a boolean
-// mask.
+// Whether a call needs the EXT instantiation: per-batch lengths, a boolean
+// mask, or a mask row shared by every query row (the key-mask bias step).
 inline bool prefill_needs_ext(const sdpa_params_t& p) {
-  return p.seq_lens_q || p.seq_lens_kv || (p.mask && (p.flags & SDPA_FLAG_BOOL_MASK));
+  return p.seq_lens_q || p.seq_lens_kv ||
+         (p.mask && ((p.flags & SDPA_FLAG_BOOL_MASK) || p.mask_stride[2] == 0));
 }
 
 // Head-size entry points (one translation unit each), p normalised;

@@ -141,9 +141,29 @@ def test_prefill_small(cuda, dtype, D, causal, shape):
 @pytest.mark.parametrize("mask", ["full", "row", "key"])
 @pytest.mark.parametrize("sinks", [False, True])
 @pytest.mark.parametrize("Lq", [1, 150])
-def test_mask_and_sinks(cuda, dtype, mask, sinks, Lq):
-    D = 128
+@pytest.mark.parametrize("D", [64, 128])
+def test_mask_and_sinks(cuda, dtype, mask, sinks, Lq, D):
     check(cuda, wl(2, 4, 2, Lq, 300, D, dtype, mask=mask, sinks=sinks, causal=(Lq > 1)))
+
+
+@pytest.mark.parametrize("dtype,D", [("float16", 64), ("bfloat16", 64), ("float16", 128),
+                                     ("bfloat16", 128)])
+@pytest.mark.parametrize("scale_mul", [1.0, 0.37, 3.0])
+def test_additive_key_mask_scales(cuda, dtype, D, scale_mul):
+    # an additive mask row shared by the query rows enters S as one more
+    # tensor-core step with 1/scale split into two 16-bit values; scales
+    # whose inverse is exact (lo = 0) and inexact, several tiles, GQA
+    import scaled_dot_product_fwd_gb300 as S
+    w = wl(2, 8, 2, 300, 700, D, dtype, mask="key")
+    inp = W.make_inputs(w)
+    scale = w.scale * scale_mul
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    o, lse = S.sdpa_forward(q, k, v, scale=scale, mask=inp["mask"].cuda())
+    cuda.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    f = W.as_float64
+    o_ref, lse_ref = O.sdpa(f(inp["q"]), f(inp["k"]), f(inp["v"]), scale, False, f(inp["mask"]))
+    compare(w, o.cpu(), lse.cpu(), o_ref, lse_ref, None)
 
 
 @pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
