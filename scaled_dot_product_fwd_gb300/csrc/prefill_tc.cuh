@@ -171,6 +171,7 @@ template <>
 struct Elem<true> {
   using T = __nv_bfloat16;
   static __device__ __forceinline__ float to_f(T x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ float bits_to_f(uint32_t h) { return __uint_as_float(h << 16); }
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -180,6 +181,9 @@ template <>
 struct Elem<false> {
   using T = __half;
   static __device__ __forceinline__ float to_f(T x) { return __half2float(x); }
+  static __device__ __forceinline__ float bits_to_f(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+  }
   static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -710,6 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // through S itself (kbias); a mask with a row per query takes 16-byte
     // loads where the row is 16-byte aligned.
     const bool mrow16 = EXT && mrowb && !kbias && (reinterpret_cast<uintptr_t>(mrowb) & 15u) == 0;
+    const bool mrowa16 = EXT && mrow && !kbias && (reinterpret_cast<uintptr_t>(mrow) & 15u) == 0;
     // keys are counted from this CTA's first key tile from here on
     limit -= jb * BN;
     float m = -INFINITY;  // reference max (log2 units)
@@ -721,7 +726,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tiles that may hold invisible keys take the fused path too at D = 128,
     // and with extended inputs (a boolean mask, per-batch lengths) at any D
     constexpr bool kFusedPartial = (D == 128) || EXT;
-    const bool fused_ok = (a.sl2 > 0.f) && (a.mask == nullptr || (EXT && (a.mask_bool || kbias)));
+    // With extended inputs a mask takes the fused path too: a shared row is
+    // in S already (kbias); a boolean row sets -inf (16-byte loads where
+    // aligned, else byte loads); an additive row adds mask / scale to the
+    // raw scores (x = S * scale*log2e then gains mask * log2e) when every
+    // lane's row is 16-byte aligned (a warp-wide choice: the host routes
+    // calls whose additive rows are not all aligned to the plain
+    // instantiation, and a warp never runs both paths).  Other warps take
+    // the general path.
+    const bool mvec = __all_sync(0xffffffffu, mrowb ? mrow16 : (mrow ? mrowa16 : true));
+    const bool fused_ok =
+        (a.sl2 > 0.f) && (a.mask == nullptr || (EXT && (kbias || a.mask_bool || mvec)));
+    const float rscale = kLog2e / a.sl2;  // 1 / scale
     // Output of the tile (whole units: right after its loop; split units:
     // after the CTAs of the cluster have exchanged partial results).
     auto epilogue = [&]() {
@@ -895,13 +911,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (t < nt) {
       for (int j = 0; j < nkv[t]; ++j) {
-        // a per-query mask row that is 16-byte aligned is brought into L1
-        // before the scores are waited for, and loaded after
+        // a 16-byte aligned per-query mask row is brought into L1 before the
+        // scores are waited for, and loaded after with 16-byte loads
+        // (measured: prefetching unaligned rows, read byte by byte, slowed
+        // the loop)
         if constexpr (EXT) {
           const int kv0 = j * BN;
-          if (mrow16 && kv0 + BN - 1 <= limit) {
-            prefetch_l1(mrowb + kv0);
-            prefetch_l1(mrowb + kv0 + BN - 16);
+          if (kv0 + BN - 1 <= limit) {
+            if (mrow16) {
+              prefetch_l1(mrowb + kv0);
+              prefetch_l1(mrowb + kv0 + BN - 1);
+            } else if (mrowa16) {
+              prefetch_l1(mrow + kv0);
+              prefetch_l1(mrow + kv0 + BN - 1);
+            }
           }
         }
         ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[t], j & 1, wc));
@@ -1034,6 +1057,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                   for (int i = 0; i < BN; ++i)
                     if (kv0 + i <= limit && !mrowb[kv0 + i]) s[i] = 0xff800000u;
+                } else if (mrow && mrowa16 && kv0 + BN - 1 <= limit) {
+                  // additive row, 16-byte aligned: 8 values per load
+                  const uint4* src = reinterpret_cast<const uint4*>(mrow + kv0);
+#pragma unroll
+                  for (int c = 0; c < BN / 8; ++c) {
+                    const uint4 q4 = src[c];
+                    const uint32_t wd[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                      const float mv = E::bits_to_f((wd[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+                      s[8 * c + e] =
+                          __float_as_uint(fmaf(mv, rscale, __uint_as_float(s[8 * c + e])));
+                    }
+                  }
+                } else if (mrow) {
+#pragma unroll
+                  for (int i = 0; i < BN; ++i)
+                    if (kv0 + i <= limit)
+                      s[i] = __float_as_uint(
+                          fmaf(to_float(mrow[kv0 + i]), rscale, __uint_as_float(s[i])));
                 }
               }
             }
@@ -1345,11 +1388,22 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
 
 }  // namespace
 
-// Whether a call needs the EXT instantiation: per-batch lengths, a boolean
-// mask, or a mask row shared by every query row (the key-mask bias step).
+// Whether a call takes the EXT instantiation: per-batch lengths, a boolean
+// mask, a mask row shared by every query row (the key-mask bias step), or an
+// additive mask whose rows are all 16-byte aligned.  Other additive masks
+// stay on the plain instantiation's general path (measured faster there for
+// unaligned rows than any EXT path).
 inline bool prefill_needs_ext(const sdpa_params_t& p) {
-  return p.seq_lens_q || p.seq_lens_kv ||
-         (p.mask && ((p.flags & SDPA_FLAG_BOOL_MASK) || p.mask_stride[2] == 0));
+  if (p.seq_lens_q || p.seq_lens_kv) return true;
+  if (!p.mask) return false;
+  if ((p.flags & SDPA_FLAG_BOOL_MASK) || p.mask_stride[2] == 0) return true;
+  // an additive mask with a row per query: the fused path with 16-byte
+  // loads when every row is 16-byte aligned (fp16/bf16)
+  if (p.dtype == SDPA_F32) return false;
+  const int64_t es = 2;
+  bool aligned = (reinterpret_cast<uintptr_t>(p.mask) & 15u) == 0;
+  for (int d = 0; d < 3; ++d) aligned = aligned && (p.mask_stride[d] * es) % 16 == 0;
+  return aligned;
 }
 
 // Head-size entry points (one translation unit each), p normalised;

@@ -569,8 +569,10 @@ def test_bool_mask(cuda, case):
 
 @pytest.mark.parametrize("D,dtype,kind", [(64, "float16", "bool_key"),
                                           (64, "bfloat16", "bool_full"),
-                                          (128, "float16", "bool_key")])
-def test_bool_mask_negative_scale(cuda, D, dtype, kind):
+                                          (128, "float16", "bool_key"),
+                                          (64, "float16", "full"),
+                                          (128, "bfloat16", "key")])
+def test_mask_negative_scale(cuda, D, dtype, kind):
     # a negative scale turns the row max of the raw scores into the row min:
     # the kernels take their general (unfused) softmax
     import scaled_dot_product_fwd_gb300 as S
@@ -581,9 +583,20 @@ def test_bool_mask_negative_scale(cuda, D, dtype, kind):
     cuda.cuda.synchronize()
     assert S.sdpa_device_status() == 0
     f = W.as_float64
-    o_ref, lse_ref = O.sdpa(f(inp["q"]), f(inp["k"]), f(inp["v"]), -w.scale, False,
-                            inp["mask"].numpy())
+    m = inp["mask"]
+    m = m.numpy() if m.dtype == cuda.bool else f(m)
+    o_ref, lse_ref = O.sdpa(f(inp["q"]), f(inp["k"]), f(inp["v"]), -w.scale, False, m)
     compare(w, o.cpu(), lse.cpu(), o_ref, lse_ref, None)
+
+
+# additive masks with a row per query: rows of 512 keys are 16-byte aligned
+# (vector loads), rows of 333 keys mostly not; GQA, causal, several tiles
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Lk", [512, 333])
+@pytest.mark.parametrize("causal", [False, True])
+def test_additive_row_mask(cuda, dtype, D, Lk, causal):
+    check(cuda, wl(2, 8, 2, 300, Lk, D, dtype, mask="full", causal=causal, sinks=causal))
 
 
 @pytest.mark.parametrize("D,dtype,kind,causal", [(64, "float16", "bool_key", False),
