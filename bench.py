@@ -652,9 +652,19 @@ def main():
     ap.add_argument("--workload", default="dit_b2_h38_l4250_d64_f16")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the backward pass workloads and print them (a profiling "
+                         "target; not the benchmark line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.backward_only:
+        import torch
+        import scaled_dot_product_fwd_gb300 as S
+        torch.cuda.set_device(0)
+        peaks, _ = load_peaks()
+        print(json.dumps(run_backward(torch, S, "cuda", peaks)), flush=True)
+        return
     if args.impl == "reference":
         reference_arm(args)
     else:
