@@ -63,8 +63,12 @@ struct BwdCfg {
   static constexpr int DO_OFF = Q_OFF + NST * TILE;   // NST tiles
   static constexpr int DS_OFF = DO_OFF + NST * TILE;  // dS^T: 128 keys x 128 query rows
   static constexpr int DS_BYTES = kBT * kBT * 2;
+  // D = 64: the MMAs of step s+1's S^T and dP^T are issued before step s's
+  // dQ MMA, which then runs while the compute warps work on step s+1: dS^T
+  // has two buffers (step parity)
+  static constexpr int NDS = D == 64 ? 2 : 1;
   // -LSE and -D of a step's 128 query rows, two buffers each (step parity)
-  static constexpr int LSE_OFF = DS_OFF + DS_BYTES;  // 2 x 128 floats
+  static constexpr int LSE_OFF = DS_OFF + NDS * DS_BYTES;  // 2 x 128 floats
   static constexpr int DV_OFF = LSE_OFF + 2 * kBT * 4;
   static constexpr int BAR_OFF = DV_OFF + 2 * kBT * 4;
   // kv_full, q_full[2], q_empty[2], s_full, p_ready, mma_done, dq_read, drain
@@ -84,6 +88,8 @@ struct BwdCfg {
   // dQ: at D = 64 two buffers (step s in buffer s % 2, read while the next
   // step's MMAs run); at D = 128 one, over the S^T columns
   static constexpr bool PIPE_DQ = D == 64;
+  static_assert(!PIPE_DQ || NDS == 2, "the pipelined dQ reads one dS^T buffer while the next is written");
+  static constexpr int ds_off(int s) { return DS_OFF + (NDS == 2 ? (s & 1) * DS_BYTES : 0); }
   static constexpr uint32_t COL_DQ = D == 64 ? 384 : 0;
   static constexpr uint32_t dq_col(int s) { return PIPE_DQ ? COL_DQ + (s & 1) * 64 : COL_DQ; }
   static constexpr uint32_t TMEM_COLS = 512;
@@ -275,7 +281,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sV = smem + C::V_OFF;
   uint8_t* sQ = smem + C::Q_OFF;
   uint8_t* sDO = smem + C::DO_OFF;
-  uint8_t* sDS = smem + C::DS_OFF;
   // per step: -LSE (log2 units) and -D of the 128 query rows
   float* sLse = reinterpret_cast<float*>(smem + C::LSE_OFF);
   float* sDv = reinterpret_cast<float*>(smem + C::DV_OFF);
@@ -377,38 +382,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idKV = idesc_f16(BF16, kBT, D, false, true);
       constexpr uint32_t idQ = idesc_f16(BF16, kBT, D, true, true);
       bool ok = mbar_wait(kv_full, 0, wc);
-      for (int s = 0; s < nsteps && ok; ++s) {
+      // S^T = K Q^T and dP^T = V dO^T of step s (Q, dO stage s % NST)
+      auto issue_sdp = [&](int s) {
         const int st = s % C::NST;
         const uint8_t* q_st = sQ + st * C::TILE;
         const uint8_t* do_st = sDO + st * C::TILE;
-        ok = mbar_wait(&q_full[st], (s / C::NST) & 1, wc);
-        // At D = 128 the dQ tile shares the S^T columns: the compute warps
-        // have read the previous one.  (At D = 64 its own columns are written
-        // only after p_ready, which the compute warps give after reading it.)
-        if (ok && D == 128 && s > 0) ok = mbar_wait(dq_read, (s - 1) & 1, wc);
-        if (!ok) break;
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           mma_f16_ss(tmem + C::COL_S, kmaj(sK, kk), kmaj(q_st, kk), idS, kk > 0 ? 1u : 0u);
           mma_f16_ss(tmem + C::COL_DP, kmaj(sV, kk), kmaj(do_st, kk), idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
-        if (!mbar_wait(p_ready, s & 1, wc)) break;
-        tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q (A from TMEM: 128 query rows, two
-        // elements per column); dQ = dS K (A: dS^T rows in shared memory)
+      };
+      // dV += P^T dO and dK += dS^T Q (A from TMEM: 128 query rows, two
+      // elements per column)
+      auto issue_dkv = [&](int s) {
+        const int st = s % C::NST;
+        const uint8_t* q_st = sQ + st * C::TILE;
+        const uint8_t* do_st = sDO + st * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < kBT / 16; ++kk) {
           const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
           mma_f16_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8, mnmaj(do_st, kk), idKV, acc);
           mma_f16_ts(tmem + C::COL_DK, tmem + C::COL_DP + kk * 8, mnmaj(q_st, kk), idKV, acc);
         }
+      };
+      // dQ = dS K (A: dS^T rows in shared memory)
+      auto issue_dq = [&](int s) {
+        const uint8_t* ds = smem + C::ds_off(s);
 #pragma unroll
         for (int kk = 0; kk < kBT / 16; ++kk)
-          mma_f16_ss(tmem + C::dq_col(s), mnmaj(sDS, kk), mnmaj(sK, kk), idQ, kk > 0 ? 1u : 0u);
-        mma_commit(&q_empty[st]);
-        mma_commit(mma_done);
+          mma_f16_ss(tmem + C::dq_col(s), mnmaj(ds, kk), mnmaj(sK, kk), idQ, kk > 0 ? 1u : 0u);
+      };
+      if constexpr (C::PIPE_DQ) {
+        // Order per step: dV_s, dK_s, then S^T and dP^T of step s+1 (they
+        // overwrite the columns dV_s and dK_s read: the MMAs run in issue
+        // order), then dQ_s, which runs while the compute warps start on
+        // step s+1 (dS^T and dQ have two buffers each).
+        if (ok && nsteps > 0) {
+          ok = mbar_wait(&q_full[0], 0, wc);
+          if (ok) {
+            tc_fence_after();
+            issue_sdp(0);
+            mma_commit(s_full);
+          }
+        }
+        for (int s = 0; s < nsteps && ok; ++s) {
+          if (!mbar_wait(p_ready, s & 1, wc)) break;
+          tc_fence_after();
+          issue_dkv(s);
+          mma_commit(&q_empty[s % C::NST]);
+          if (s + 1 < nsteps) {
+            const int st1 = (s + 1) % C::NST;
+            if (!mbar_wait(&q_full[st1], ((s + 1) / C::NST) & 1, wc)) break;
+            tc_fence_after();
+            issue_sdp(s + 1);
+            mma_commit(s_full);
+          }
+          issue_dq(s);
+          mma_commit(mma_done);
+        }
+      } else {
+        for (int s = 0; s < nsteps && ok; ++s) {
+          const int st = s % C::NST;
+          ok = mbar_wait(&q_full[st], (s / C::NST) & 1, wc);
+          // At D = 128 the dQ tile shares the S^T columns: the compute warps
+          // have read the previous one.
+          if (ok && s > 0) ok = mbar_wait(dq_read, (s - 1) & 1, wc);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sdp(s);
+          mma_commit(s_full);
+          if (!mbar_wait(p_ready, s & 1, wc)) break;
+          tc_fence_after();
+          issue_dkv(s);
+          issue_dq(s);
+          mma_commit(&q_empty[st]);
+          mma_commit(mma_done);
+        }
       }
       // every MMA issued here completes before TMEM is freed
       mma_commit(drain);
@@ -566,7 +616,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_st32(tmem + lane_off + C::COL_DP + hf * 32, dk);
         // dS^T row r, query rows 64h..64h+63: column block h, 16-byte chunks
         // swizzled by the row (128-byte swizzle)
-        uint8_t* drow = sDS + hf * (kBT * 128) + r * 128;
+        uint8_t* drow = smem + C::ds_off(s) + hf * (kBT * 128) + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
           *reinterpret_cast<uint4*>(drow + ((ch ^ (r & 7)) << 4)) =
