@@ -589,6 +589,41 @@ def test_mask_negative_scale(cuda, D, dtype, kind):
     compare(w, o.cpu(), lse.cpu(), o_ref, lse_ref, None)
 
 
+@pytest.mark.parametrize("D,dtype", [(64, "float16"), (128, "bfloat16")])
+@pytest.mark.parametrize("boolean", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_mask_edges(cuda, D, dtype, boolean, causal):
+    # key masks on the tensor-core bias step: one row per (batch, head)
+    # ([B, Hq, 1, Lk], head offsets in the mask), batch 1 hides every key
+    # (its rows see nothing: O = 0, LSE = -inf), large finite biases
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    B, Hq, Hkv, Lq, Lk = 2, 4, 2, 260, 333
+    w = wl(B, Hq, Hkv, Lq, Lk, D, dtype, causal=causal)
+    inp = W.make_inputs(w)
+    rng = np.random.default_rng(11)
+    if boolean:
+        keep = rng.random((B, Hq, 1, Lk)) >= 0.3
+        keep[1] = False
+        m_host = torch.from_numpy(keep)
+        m_ref = keep
+    else:
+        vals = rng.standard_normal((B, Hq, 1, Lk)) * 4.0
+        vals[rng.random((B, Hq, 1, Lk)) < 0.2] = -np.inf
+        vals[0, 0, 0, :5] = -60000.0  # large finite
+        vals[1] = -np.inf
+        m_host = torch.from_numpy(vals.astype(np.float32)).to(inp["q"].dtype)
+        m_ref = W.as_float64(m_host)
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    o, lse = S.sdpa_forward(q, k, v, scale=w.scale, causal=causal, mask=m_host.cuda())
+    cuda.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    f = W.as_float64
+    o_ref, lse_ref = O.sdpa(f(inp["q"]), f(inp["k"]), f(inp["v"]), w.scale, causal, m_ref)
+    assert np.all(np.isneginf(lse_ref[1]))
+    compare(w, o.cpu(), lse.cpu(), o_ref, lse_ref, None)
+
+
 # additive masks with a row per query: rows of 512 keys are 16-byte aligned
 # (vector loads), rows of 333 keys mostly not; GQA, causal, several tiles
 @pytest.mark.parametrize("dtype", ["float16", "bfloat16"])
