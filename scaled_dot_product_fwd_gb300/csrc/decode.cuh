@@ -35,9 +35,11 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tensor_map.h"
 
 namespace gb300 {
 namespace dec {
@@ -78,6 +80,12 @@ struct SplitArgs {
   // Failure-detection test hook: when set, the producer does not issue the
   // copies of the last tile, so the consumers' bounded wait on it expires.
   int debug_drop_last;
+  // K and V rows that are not contiguous (e.g. [B, L, Hkv, D] storage): one
+  // tiled tensor copy per tile (box D x TK rows, no swizzle, rows past Lk
+  // read as zero) instead of one bulk copy per row; set by the launcher when
+  // the driver accepts both maps.
+  int use_tma;
+  CUtensorMap tmK, tmV;
 };
 
 template <typename T>
@@ -236,7 +244,7 @@ struct SplitCfg {
 
 template <typename T, int D, int HG, int KB>
 __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
-    decode_split_kernel(const SplitArgs a) {
+    decode_split_kernel(const __grid_constant__ SplitArgs a) {
   using C = SplitCfg<T, D, HG, KB>;
   using Wd = Widen<T>;
   extern __shared__ uint8_t smem_raw[];
@@ -291,10 +299,20 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
         if (a.debug_drop_last && t == ntiles - 1) break;
         const int rows = min(C::TK, nkeys - t * C::TK);
         const uint32_t bytes = static_cast<uint32_t>(rows * D * sizeof(T));
-        mbar_arrive_expect_tx(&full[s], 2 * bytes);
         uint8_t* st = ring + static_cast<size_t>(s) * C::STAGE_BYTES;
-        // a tile's rows are one copy when they are contiguous, else one per row
         const long long r0 = static_cast<long long>(t) * C::TK;
+        if (a.use_tma) {
+          // whole TK-row boxes: rows past the split hold keys the consumers
+          // skip, rows past Lk read as zero
+          const int key = key_begin + static_cast<int>(r0);
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::TILE_BYTES));
+          tma_load_4d(st, &a.tmK, &full[s], 0, key, kvh, b);
+          tma_load_4d(st + C::TILE_BYTES, &a.tmV, &full[s], 0, key, kvh, b);
+          last_use[s] = use;
+          continue;
+        }
+        mbar_arrive_expect_tx(&full[s], 2 * bytes);
+        // a tile's rows are one copy when they are contiguous, else one per row
         if (a.ks2 == D) {
           bulk_load(st, kg + r0 * D, bytes, &full[s]);
         } else {
@@ -629,6 +647,22 @@ sdpa_status_t launch_split(SplitArgs a, int batch, cudaStream_t stream, bool* me
   using C = SplitCfg<T, D, HG, KB>;
   auto kern = decode_split_kernel<T, D, HG, KB>;
   const size_t smem = C::smem_bytes(a.stages);
+  // rows that are not contiguous: tiled tensor copies when the driver takes
+  // the maps (box D x TK, at most 256 elements per side)
+  a.use_tma = 0;
+  if ((a.ks2 != D || a.vs2 != D) && D <= 256 && C::TK <= 256) {
+    const CUtensorMapDataType dt = sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : std::is_same<T, __half>::value
+                                       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t es = static_cast<uint32_t>(sizeof(T));
+    const bool okk = encode_tiled_4d(&a.tmK, dt, a.k, D, a.Lk, a.Hkv, batch, es, D, C::TK,
+                                     a.ks2, a.ks1, a.ks0, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const bool okv = okk && encode_tiled_4d(&a.tmV, dt, a.v, D, a.Lk, a.Hkv, batch, es, D,
+                                            C::TK, a.vs2, a.vs1, a.vs0,
+                                            CU_TENSOR_MAP_SWIZZLE_NONE);
+    a.use_tma = okv ? 1 : 0;
+  }
   cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)

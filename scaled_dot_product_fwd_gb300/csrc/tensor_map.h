@@ -19,11 +19,12 @@ bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ba
 // 4-D tiled map over a [batches, heads, rows, inner] tensor with element
 // strides row_stride, head_stride, batch_stride (inner contiguous; each
 // stride times elem_bytes a multiple of 16), box box_inner x box_rows x 1 x 1,
-// 128-byte swizzle; out-of-range elements read as zero.  Returns false if the
-// driver rejects the map.
+// 128-byte swizzle unless given; out-of-range elements read as zero.  Returns
+// false if the driver rejects the map.
 bool encode_tiled_4d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                      uint64_t inner, uint64_t rows, uint64_t heads, uint64_t batches,
                      uint32_t elem_bytes, uint32_t box_inner, uint32_t box_rows,
-                     uint64_t row_stride, uint64_t head_stride, uint64_t batch_stride);
+                     uint64_t row_stride, uint64_t head_stride, uint64_t batch_stride,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 }  // namespace gb300
