@@ -15,7 +15,8 @@
 //   warps 0-7  softmax: warpgroup t owns query tile t, one thread per row
 //              (TMEM lane); it also rescales O in TMEM and writes the output;
 //   warp 8     TMA producer: Q tiles once, then K_j, V_j into a ring of
-//              shared-memory buffers (128-byte swizzle);
+//              shared-memory buffers (128-byte swizzle), and with a shared
+//              key-mask row each stage's key bias column (kbias);
 //   warp 9     MMA issuer: one elected lane issues tcgen05.mma,
 //              S_t = Q_t K_j^T (A, B from shared memory, fp32 in TMEM) and
 //              O_t += P_t V_j (P from TMEM, written there by the softmax
@@ -343,9 +344,11 @@ __device__ __forceinline__ Unit unit_of(const PrefillArgs& a, uint32_t bx) {
   return w;
 }
 
-// EXT: extended inputs (per-batch length arrays or a boolean mask); without
-// them the lengths are the kernel arguments and the code is that of plain
-// inputs (any strides of q, k, v and o).
+// EXT: extended inputs (per-batch length arrays, a boolean mask, a mask row
+// shared by every query row, or additive rows that are all 16-byte aligned);
+// without them the lengths are the kernel arguments and the code is that of
+// plain inputs (any strides of q, k, v and o; other additive masks on the
+// general softmax path).
 // SPLIT: every unit is shared by the CTAs of a cluster (the units of a last,
 // partial wave); its own instantiation, so that whole units run code without
 // the merge.
@@ -710,9 +713,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         mrow = static_cast<const T*>(a.mask) + moff;
     }
-    // A boolean mask row shared by every query row reaches the fused path
-    // through S itself (kbias); a mask with a row per query takes 16-byte
-    // loads where the row is 16-byte aligned.
+    // A mask row shared by every query row (boolean or additive) reaches the
+    // fused path through S itself (kbias); a mask with a row per query takes
+    // 16-byte loads where the row is 16-byte aligned.
     const bool mrow16 = EXT && mrowb && !kbias && (reinterpret_cast<uintptr_t>(mrowb) & 15u) == 0;
     const bool mrowa16 = EXT && mrow && !kbias && (reinterpret_cast<uintptr_t>(mrow) & 15u) == 0;
     // keys are counted from this CTA's first key tile from here on
@@ -724,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the scale is positive (max of raw scores = max of scaled scores)
     const bool fast_ok = (a.sl2 > 0.f) && (a.mask == nullptr);
     // tiles that may hold invisible keys take the fused path too at D = 128,
-    // and with extended inputs (a boolean mask, per-batch lengths) at any D
+    // and with extended inputs (masks, per-batch lengths) at any D
     constexpr bool kFusedPartial = (D == 128) || EXT;
     // With extended inputs a mask takes the fused path too: a shared row is
     // in S already (kbias); a boolean row sets -inf (16-byte loads where
@@ -1037,8 +1040,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < BN; ++i)
                   if (i >= nvis) s[i] = 0xff800000u;  // -inf
               }
-              // a boolean mask row of this query row (a shared one is already
-              // in S: kbias)
+              // the mask row of this query row (a shared one is already in S:
+              // kbias)
               if constexpr (EXT) {
                 if (kbias) {
                   // nothing to apply
