@@ -514,7 +514,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int s = 0; s < nsteps; ++s) {
       const int hq = kvh * a.G + s / per_head;
       const int q0 = (qt0 + s % per_head) * kBT;
-      const size_t rowbase = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq;
       // buffer s % 2: a thread reaches this step's barrier only after every
       // thread has passed the previous one, so the buffer of step s - 2 is free
       float* const sl = sLse + (s & 1) * kBT;
