@@ -735,8 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // raw scores (x = S * scale*log2e then gains mask * log2e) when every
     // lane's row is 16-byte aligned (a warp-wide choice: the host routes
     // calls whose additive rows are not all aligned to the plain
-    // instantiation, and a warp never runs both paths).  Other warps take
-    // the general path.
+    // instantiation, and a warp never runs both paths), on tiles inside the
+    // row's visible keys.  Other warps and tiles take the general path.
     const bool mvec = __all_sync(0xffffffffu, mrowb ? mrow16 : (mrow ? mrowa16 : true));
     const bool fused_ok =
         (a.sl2 > 0.f) && (a.mask == nullptr || (EXT && (kbias || a.mask_bool || mvec)));
@@ -1019,7 +1019,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!__any_sync(0xffffffffu, redo)) break;
               need_max = redo;
             }
-          } else if (kFusedPartial ? fused_ok : fast) {
+          } else if (kFusedPartial ? fused_ok && !(mrow && !kbias && kv0 + BN - 1 > limit)
+                                   : fast) {
             // Positive scale, no additive mask: p = 2^(s * scale*log2e - m)
             // with the scale folded into one packed FMA per pair, taken
             // against the current reference max m without looking for the
@@ -1074,12 +1075,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                           __float_as_uint(fmaf(mv, rscale, __uint_as_float(s[8 * c + e])));
                     }
                   }
-                } else if (mrow) {
-#pragma unroll
-                  for (int i = 0; i < BN; ++i)
-                    if (kv0 + i <= limit)
-                      s[i] = __float_as_uint(
-                          fmaf(to_float(mrow[kv0 + i]), rscale, __uint_as_float(s[i])));
                 }
               }
             }
