@@ -48,6 +48,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <type_traits>
 
@@ -98,9 +99,10 @@ struct Cfg {
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = NQ * QT * TILE;
   static constexpr int BAR_OFF = RING_OFF + NS * STAGE;
-  // q_full, full[NS], empty[NS], s_full[NQ], o_done[NQ], drain, xbar
-  // + xbar: partial results of a split unit received
-  static constexpr int NBARS = 1 + 2 * NS + 2 * NQ + 1 + 1;
+  // q_full, full[NS], empty[NS], s_full[NQ], o_done[NQ], drain, xbar,
+  // q_empty; xbar: partial results of a split unit received; q_empty: the
+  // unit's last S products have read the Q tiles
+  static constexpr int NBARS = 1 + 2 * NS + 2 * NQ + 1 + 1 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -145,6 +147,9 @@ struct PrefillArgs {
   // thread-block cluster, which share its key tiles.
   int unit0;
   int ksplit;
+  // units of the grid (whole units: CTA x takes unit0 + x, unit0 + x +
+  // gridDim.x, ... below unit0 + nunits)
+  int nunits;
   float sl2;  // scale * log2(e)
   int causal;
   const void* mask;
@@ -344,6 +349,52 @@ __device__ __forceinline__ Unit unit_of(const PrefillArgs& a, uint32_t bx) {
   return w;
 }
 
+// Geometry of one work unit for one CTA: query block, head, batch, the
+// CTA's part of a split unit, first query row, active query tiles, kv head,
+// the batch's lengths (padding masks, clamped to the call's maxima: rows at
+// or past Lqb see no key), the CTA's first key tile and the key tiles of each
+// query tile (all of the CTA's part; causal: up to the tile's last visible
+// key; splits are never causal).
+struct Geo {
+  int qb, h, b, part, m0, nt, kvh, Lkb, Lqb, jb, nmax;
+  int nkv[NQ];
+};
+template <bool EXT, bool SPLIT>
+__device__ __forceinline__ Geo unit_geo(const PrefillArgs& a, uint32_t bx) {
+  Geo g;
+  const Unit w = unit_of<SPLIT>(a, bx);
+  g.qb = w.qb;
+  g.h = w.h;
+  g.b = w.b;
+  g.part = w.part;
+  g.m0 = w.qb * (BM * NQ);
+  g.nt = min(NQ, (a.Lq - g.m0 + BM - 1) / BM);  // >= 1
+  g.kvh = w.h / a.G;
+  g.Lkb = (EXT && a.seq_lens_kv) ? min(max(a.seq_lens_kv[w.b], 0), a.Lk) : a.Lk;
+  g.Lqb = (EXT && a.seq_lens_q) ? min(max(a.seq_lens_q[w.b], 0), a.Lq) : a.Lq;
+  const int nkv_all = (g.Lkb + BN - 1) / BN;
+  const int nparts = SPLIT ? a.ksplit : 1;
+  g.jb = w.part * nkv_all / nparts;
+  const int je = (w.part + 1) * nkv_all / nparts;
+  g.nmax = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    int n = 0;
+    const int last_row = min(g.m0 + t * BM + BM - 1, g.Lqb - 1);  // last row that sees keys
+    if (t < g.nt && last_row >= g.m0 + t * BM) {
+      if (a.causal) {
+        const int lim = last_row + (g.Lkb - g.Lqb);  // last key visible to the tile
+        n = lim < 0 ? 0 : min(nkv_all, lim / BN + 1);
+      } else {
+        n = je - g.jb;
+      }
+    }
+    g.nkv[t] = n;
+    g.nmax = max(g.nmax, n);
+  }
+  return g;
+}
+
 // EXT: extended inputs (per-batch length arrays, a boolean mask, a mask row
 // shared by every query row, or additive rows that are all 16-byte aligned);
 // without them the lengths are the kernel arguments and the code is that of
@@ -378,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_done = s_full + NQ;
   uint64_t* drain = o_done + NQ;
   uint64_t* xbar = drain + 1;
+  uint64_t* q_empty = xbar + 1;
   uint8_t* sKB = smem + C::KB_OFF;  // key-mask bias chunks (extended inputs)
   uint8_t* sQB = smem + C::QB_OFF;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
@@ -386,43 +438,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit (query block, head, batch) and, for a split unit, this
-  // CTA's part of its key tiles
-  const Unit w0 = unit_of<SPLIT>(a, blockIdx.x);
-  const int qb = w0.qb, h = w0.h, b = w0.b, part = w0.part;
   // a split grid that follows the grid of whole units may start as soon as
   // every CTA of that grid is running
   if constexpr (!SPLIT) griddep_launch_dependents();
-  const int m0 = qb * (BM * NQ);
-  const int nt = min(NQ, (a.Lq - m0 + BM - 1) / BM);  // active query tiles (>= 1)
-  const int kvh = h / a.G;
-  // this batch's lengths (padding masks), clamped to the call's maxima; rows
-  // at or past Lqb see no key
-  const int Lkb = (EXT && a.seq_lens_kv) ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
-  const int Lqb = (EXT && a.seq_lens_q) ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
-  const int nkv_all = (Lkb + BN - 1) / BN;
-  // key tiles [jb, je) of this CTA (all of them unless the unit is split;
-  // splits are never causal)
-  const int nparts = SPLIT ? a.ksplit : 1;
-  const int jb = part * nkv_all / nparts;
-  const int je = (part + 1) * nkv_all / nparts;
-  int nkv[NQ];
-  int nmax = 0;
-#pragma unroll
-  for (int t = 0; t < NQ; ++t) {
-    int n = 0;
-    const int last_row = min(m0 + t * BM + BM - 1, Lqb - 1);  // last row that sees keys
-    if (t < nt && last_row >= m0 + t * BM) {
-      if (a.causal) {
-        const int lim = last_row + (Lkb - Lqb);  // last key visible to the tile
-        n = lim < 0 ? 0 : min(nkv_all, lim / BN + 1);
-      } else {
-        n = je - jb;
-      }
-    }
-    nkv[t] = n;
-    nmax = max(nmax, n);
-  }
+  // Units of this CTA.  A split grid gives one unit to the ksplit CTAs of a
+  // cluster.  The grid of whole units may be persistent: CTA x takes units
+  // x, x + gridDim.x, ... below nunits, and every role runs on from one unit
+  // into the next (the producer loads the next unit's Q once the last S
+  // products of the current one have read the Q tiles, and its K/V through
+  // the same ring; the MMA warp issues its first S products right behind the
+  // current unit's last P V), so that the start of a unit overlaps the end
+  // of the previous one.
+  const int bxi = static_cast<int>(blockIdx.x);
+  const int gdx = static_cast<int>(gridDim.x);
+  const int n_my = SPLIT ? 1 : (bxi < a.nunits ? (a.nunits - 1 - bxi) / gdx + 1 : 0);
+  auto geo = [&](int it) {
+    return unit_geo<EXT, SPLIT>(a, static_cast<uint32_t>(SPLIT ? bxi : bxi + it * gdx));
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -436,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     mbar_init(xbar, 1);
+    mbar_init(q_empty, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -469,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{a.wait_ns, abort_flag, a.status};
   int last_use[C::NS];  // producer: last fill of each ring buffer (-1: none)
+  int last_q = -1;      // producer: last unit whose Q tiles it loaded
 #pragma unroll
   for (int s = 0; s < C::NS; ++s) last_use[s] = -1;
 
@@ -478,79 +512,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     setmaxnreg_dec<kControlRegs>();
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
+    // Per unit: its Q tiles (after the previous unit's last S products have
+    // read them), then K_j, V_j into the ring, which runs on across units.
+    // With the key-mask bias step the whole warp fills each stage's bias
+    // chunk before lane 0 arms the stage; otherwise lane 0 alone works.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(nt * C::QT * C::TILE));
-      for (int t = 0; t < nt; ++t)
-        for (int cb = 0; cb < C::CB; ++cb) {
-          tma_load_4d(sQ + t * C::QT * C::TILE + cb * BM * 128, &tmQ, q_full, cb * 64,
-                      m0 + t * BM, h, b);
-          if constexpr (X3)
-            tma_load_4d(sQ + (t * C::QT + 1) * C::TILE + cb * BM * 128, &tmQ2, q_full,
-                        cb * 64, m0 + t * BM, h, b);
-        }
     }
-    if (kbias) {
-      // the whole warp fills the stages: each lane writes the bias of keys
-      // 32c + lane of the tile before lane 0 arms the stage's barrier
-      const long long moff = b * a.ms0 + h * a.ms1;
-      const uint8_t* mk = static_cast<const uint8_t*>(a.mask) + moff;                 // boolean
-      const uint16_t* mv = static_cast<const uint16_t*>(a.mask) + moff;               // additive
+    if (kbias || lane == 0) {
       const uint32_t ninf = BF16 ? 0xff80u : 0xfc00u;
-      for (int j = 0; j < nmax; ++j) {
-        const int s = j % C::NS;
-        const int use = j / C::NS;
-        const bool w = use == 0 || mbar_wait(&empty[s], (use - 1) & 1, wc);
-        if (!__all_sync(0xffffffffu, w)) break;
-        const int key0 = (jb + j) * BN;
+      int g = 0;  // ring stages filled so far
+      bool pok = true;
+      for (int it = 0; it < n_my && pok; ++it) {
+        const Geo u = geo(it);
+        if (lane == 0) {
+          if (it > 0) pok = mbar_wait(q_empty, (it - 1) & 1, wc);
+          if (pok) {
+            last_q = it;
+            mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(u.nt * C::QT * C::TILE));
+            for (int t = 0; t < u.nt; ++t)
+              for (int cb = 0; cb < C::CB; ++cb) {
+                tma_load_4d(sQ + t * C::QT * C::TILE + cb * BM * 128, &tmQ, q_full, cb * 64,
+                            u.m0 + t * BM, u.h, u.b);
+                if constexpr (X3)
+                  tma_load_4d(sQ + (t * C::QT + 1) * C::TILE + cb * BM * 128, &tmQ2, q_full,
+                              cb * 64, u.m0 + t * BM, u.h, u.b);
+              }
+          }
+        }
+        if (kbias) pok = __shfl_sync(0xffffffffu, pok ? 1 : 0, 0) != 0;
+        if (!pok) break;
+        const long long moff = kbias ? u.b * a.ms0 + u.h * a.ms1 : 0;
+        const uint8_t* mk = static_cast<const uint8_t*>(a.mask) + moff;    // boolean
+        const uint16_t* mv = static_cast<const uint16_t*>(a.mask) + moff;  // additive
+        for (int j = 0; j < u.nmax; ++j, ++g) {
+          const int s = g % C::NS;
+          const int use = g / C::NS;
+          const int key0 = (u.jb + j) * BN;
+          if (kbias) {
+            // each lane writes the bias of keys 32c + lane of the tile
+            const bool w = use == 0 || mbar_wait(&empty[s], (use - 1) & 1, wc);
+            if (!__all_sync(0xffffffffu, w)) {
+              pok = false;
+              break;
+            }
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          const int r = 32 * c + lane;
-          const int key = key0 + r;
-          uint32_t v = ninf;  // keys past this batch's length: -inf
-          if (key < Lkb) {
-            if (a.mask_bool) {
-              v = mk[key] != 0 ? 0u : ninf;
-            } else {
-              // columns 0 and 1 (1/scale = hi + lo); with lo = 0 column 1
-              // stays 0, so that a -inf mask value never meets a zero
-              const uint32_t m16 = mv[key];
-              v = m16 | ((a.qbias >> 16) != 0u ? (m16 << 16) : 0u);
+            for (int c = 0; c < BN / 32; ++c) {
+              const int r = 32 * c + lane;
+              const int key = key0 + r;
+              uint32_t v = ninf;  // keys past this batch's length: -inf
+              if (key < u.Lkb) {
+                if (a.mask_bool) {
+                  v = mk[key] != 0 ? 0u : ninf;
+                } else {
+                  // columns 0 and 1 (1/scale = hi + lo); with lo = 0 column 1
+                  // stays 0, so that a -inf mask value never meets a zero
+                  const uint32_t m16 = mv[key];
+                  v = m16 | ((a.qbias >> 16) != 0u ? (m16 << 16) : 0u);
+                }
+              }
+              *reinterpret_cast<uint32_t*>(sKB + s * C::BIAS_CHUNK + C::bias_at(r)) = v;
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+          } else if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, wc)) {
+            pok = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], C::STAGE);
+            uint8_t* st = sRing + s * C::STAGE;
+            for (int cb = 0; cb < C::CB; ++cb) {
+              tma_load_4d(st + cb * BN * 128, &tmK, &full[s], cb * 64, key0, u.kvh, u.b);
+              tma_load_4d(st + C::V_OFF + cb * BN * 128, &tmV, &full[s], cb * 64, key0, u.kvh,
+                          u.b);
+              if constexpr (X3) {
+                tma_load_4d(st + C::K_LO + cb * BN * 128, &tmK2, &full[s], cb * 64, key0, u.kvh,
+                            u.b);
+                tma_load_4d(st + C::V_LO + cb * BN * 128, &tmV2, &full[s], cb * 64, key0, u.kvh,
+                            u.b);
+              }
             }
           }
-          *reinterpret_cast<uint32_t*>(sKB + s * C::BIAS_CHUNK + C::bias_at(r)) = v;
+          last_use[s] = use;
         }
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], C::STAGE);
-          uint8_t* st = sRing + s * C::STAGE;
-          for (int cb = 0; cb < C::CB; ++cb) {
-            tma_load_4d(st + cb * BN * 128, &tmK, &full[s], cb * 64, key0, kvh, b);
-            tma_load_4d(st + C::V_OFF + cb * BN * 128, &tmV, &full[s], cb * 64, key0, kvh, b);
-          }
-        }
-        last_use[s] = use;
-      }
-    } else if (lane == 0) {
-      for (int j = 0; j < nmax; ++j) {
-        const int s = j % C::NS;
-        const int use = j / C::NS;
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, wc)) break;
-        mbar_arrive_expect_tx(&full[s], C::STAGE);
-        uint8_t* st = sRing + s * C::STAGE;
-        for (int cb = 0; cb < C::CB; ++cb) {
-          const int key0 = (jb + j) * BN;
-          tma_load_4d(st + cb * BN * 128, &tmK, &full[s], cb * 64, key0, kvh, b);
-          tma_load_4d(st + C::V_OFF + cb * BN * 128, &tmV, &full[s], cb * 64, key0, kvh, b);
-          if constexpr (X3) {
-            tma_load_4d(st + C::K_LO + cb * BN * 128, &tmK2, &full[s], cb * 64, key0, kvh, b);
-            tma_load_4d(st + C::V_LO + cb * BN * 128, &tmV2, &full[s], cb * 64, key0, kvh, b);
-          }
-        }
-        last_use[s] = use;
       }
     }
   } else if (warp == kMmaWarp) {
@@ -561,9 +608,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile t hand P_t over through named barrier kBarP + t and the stage
     // helper reports each K/V stage that has landed through kBarK (an
     // mbarrier poll, a local-memory spill or a warp reconvergence here holds
-    // the issuing thread until the MMAs in flight drain).  Fixed order:
+    // the issuing thread until the MMAs in flight drain), also at the start
+    // of each unit (Q and the first K/V stage landed).  Fixed order:
     // PV_0,j S_0,j+1 PV_1,j S_1,j+1, so each tile's next scores are ready as
-    // early as possible.
+    // early as possible; the next unit's S_t,0 follow its last P V products.
     const uint32_t lead = lane == 0 ? 1u : 0u;
     constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
     constexpr uint32_t idO = idesc_f16(BF16, BM, D, false, true);
@@ -584,18 +632,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t qb_desc = sdesc(smem_addr(sQB), C::BIAS_LBO, C::BIAS_SBO, 0);
     const uint64_t kb_desc = sdesc(smem_addr(sKB), C::BIAS_LBO, C::BIAS_SBO, 0);
     auto vv = [&](uint32_t lo) { return (static_cast<uint64_t>(v_hi) << 32) | lo; };
-    auto stage = [](int j) { return j % C::NS; };
-    auto spar = [](int j) { return static_cast<uint32_t>((j / C::NS) & 1); };
-    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0, wc));
-    if (nmax > 0) ok = __all_sync(0xffffffffu, ok && mbar_wait(&full[stage(0)], spar(0), wc));
-    // after a failed wait the loop still meets every named barrier, without
-    // issuing anything
-    const uint32_t go = ok ? 1u : 0u;
+    // ring stage of the g-th K/V tile loaded by this CTA
+    auto stage = [](int g) { return g % C::NS; };
+    // The issuer never waits on an mbarrier itself, so it does not learn of
+    // a wait that gave up elsewhere; it keeps issuing (the products may then
+    // read stale tiles: the call reports the timeout and its results are
+    // not used) and meets every named barrier, so that no role can hang.
+    const uint32_t go = 1u;
     // S_t = Q_t K_j^T: both operands K-major, 128-byte swizzle; a K step of
     // 16 elements is 32 bytes inside a 128-byte row, 4 steps per column block.
-    auto issue_s = [&](int t, int j) {
+    auto issue_s = [&](int t, int g) {
       const uint32_t qd = q_lo + static_cast<uint32_t>((t * C::QT * C::TILE) >> 4);
-      const uint32_t kd = k_lo + static_cast<uint32_t>((stage(j) * C::STAGE) >> 4);
+      const uint32_t kd = k_lo + static_cast<uint32_t>((stage(g) * C::STAGE) >> 4);
       const uint32_t dS = tmem + C::s_col(t);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -609,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (EXT && !X3) {  // + 1 * bias_j: the key mask
         if (kbias)
           mma_f16_ss_elect(dS, qb_desc + static_cast<uint32_t>((t * C::BIAS_CHUNK) >> 4),
-                           kb_desc + static_cast<uint32_t>((stage(j) * C::BIAS_CHUNK) >> 4),
+                           kb_desc + static_cast<uint32_t>((stage(g) * C::BIAS_CHUNK) >> 4),
                            idS, 1u, go);
       }
     };
@@ -617,14 +665,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 2 elements per column; V MN-major: 64-wide column blocks BN*128 bytes
     // apart (LBO), 8-key groups 1024 bytes apart (SBO).  In X3, P_hi sits in
     // the first 64 columns of S_t and P_lo in the next 64.
-    auto issue_pv = [&](int t, int j) {
-      const uint32_t vd = v_lo + static_cast<uint32_t>((stage(j) * C::STAGE + C::V_OFF) >> 4);
+    auto issue_pv = [&](int t, int g, bool first) {
+      const uint32_t vd = v_lo + static_cast<uint32_t>((stage(g) * C::STAGE + C::V_OFF) >> 4);
       const uint32_t dO = tmem + C::o_col(t);
       const uint32_t aP = tmem + C::s_col(t);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {
         const uint32_t voff = (kk * 16 * 128) >> 4;
-        mma_f16_ts_elect(dO, aP + kk * 8, vv(vd + voff), idO, (j > 0 || kk > 0) ? 1u : 0u, go);
+        mma_f16_ts_elect(dO, aP + kk * 8, vv(vd + voff), idO, (!first || kk > 0) ? 1u : 0u, go);
         if constexpr (X3) {  // P_hi V_lo + P_lo V_hi
           mma_f16_ts_elect(dO, aP + kk * 8, vv(vd + ((C::V_LO - C::V_OFF) >> 4) + voff), idO, 1u,
                            go);
@@ -632,54 +680,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    for (int t = 0; t < nt; ++t) {
-      if (nkv[t] == 0) {
-        mma_commit_elect(&o_done[t], go);
-      } else {
-        issue_s(t, 0);
-        mma_commit_elect(&s_full[t], go);
-      }
-    }
-    for (int j = 0; j < nmax; ++j) {
-      bool kwaited = false;
-      // stage j+1 has landed (the helper saw it); once per step
-      auto wait_stage = [&]() {
-        if (!kwaited) {
-          named_bar_sync(kBarK, 64);
-          kwaited = true;
-        }
-      };
-      for (int t = 0; t < nt; ++t) {
-        if (j >= nkv[t]) continue;
-        // P_t,j is in TMEM (4 softmax warps and this one meet)
-        named_bar_sync(kBarP + t, 32 * 5);
-        tc_fence_after();
-        issue_pv(t, j);
-        if (j + 1 < nkv[t]) {
-          wait_stage();
-          issue_s(t, j + 1);
-          mma_commit_elect(&s_full[t], go);
-        } else {
+    int g0 = 0;  // K/V tiles of earlier units (ring position of this unit's first)
+    for (int it = 0; it < n_my; ++it) {
+      const Geo u = geo(it);
+      // this unit's Q tiles and first K/V stage have landed (stage helper)
+      named_bar_sync(kBarK, 64);
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < NQ; ++t) {
+        if (t >= u.nt) continue;
+        if (u.nkv[t] == 0) {
           mma_commit_elect(&o_done[t], go);
+        } else {
+          issue_s(t, g0);
+          mma_commit_elect(&s_full[t], go);
         }
       }
-      // stage j (K_j read by S_t,j, V_j by PV_t,j) is free once these land
-      mma_commit_elect(&empty[stage(j)], go);
+      // the Q tiles are free for the next unit once the last S products of
+      // this one have completed
+      if (u.nmax <= 1) mma_commit_elect(q_empty, go);
+      for (int j = 0; j < u.nmax; ++j) {
+        bool kwaited = false;
+        // stage j+1 has landed (the helper saw it); once per step
+        auto wait_stage = [&]() {
+          if (!kwaited) {
+            named_bar_sync(kBarK, 64);
+            kwaited = true;
+          }
+        };
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) {
+          if (t >= u.nt || j >= u.nkv[t]) continue;
+          // P_t,j is in TMEM (4 softmax warps and this one meet)
+          named_bar_sync(kBarP + t, 32 * 5);
+          tc_fence_after();
+          issue_pv(t, g0 + j, j == 0);
+          if (j + 1 < u.nkv[t]) {
+            wait_stage();
+            issue_s(t, g0 + j + 1);
+            mma_commit_elect(&s_full[t], go);
+          } else {
+            mma_commit_elect(&o_done[t], go);
+          }
+        }
+        if (j == u.nmax - 2) mma_commit_elect(q_empty, go);
+        // stage j (K_j read by S_t,j, V_j by PV_t,j) is free once these land
+        mma_commit_elect(&empty[stage(g0 + j)], go);
+      }
+      g0 += u.nmax;
     }
     // every MMA issued by this warp completes before TMEM is freed
     mma_commit_elect(drain, go);
-    if (go && lead) drain_wait(drain, 0, kDrainNs);
+    if (lead) drain_wait(drain, 0, kDrainNs);
     __syncwarp();
   } else if (warp == kMmaWarp + 1) {
     // -------------------------------------------------------- stage helper
-    // Waits for K/V stage j+1 of every step that reads one and hands it to
-    // the MMA issuer through kBarK (same count of meetings on both sides,
-    // also after a failed wait).
+    // Per unit: waits for its Q tiles and first K/V stage, then for stage
+    // j+1 of every step that reads one, and hands each to the MMA issuer
+    // through kBarK (same count of meetings on both sides, also after a
+    // failed wait).
     bool ok = true;
-    for (int j = 0; j + 1 < nmax; ++j) {
-      const int s = (j + 1) % C::NS;
-      ok = ok && mbar_wait(&full[s], static_cast<uint32_t>(((j + 1) / C::NS) & 1), wc);
+    int g0 = 0;
+    for (int it = 0; it < n_my; ++it) {
+      const Geo u = geo(it);
+      ok = ok && mbar_wait(q_full, static_cast<uint32_t>(it & 1), wc);
+      if (u.nmax > 0)
+        ok = ok && mbar_wait(&full[g0 % C::NS], static_cast<uint32_t>((g0 / C::NS) & 1), wc);
       named_bar_sync(kBarK, 64);
+      for (int j = 0; j + 1 < u.nmax; ++j) {
+        const int g = g0 + j + 1;
+        ok = ok && mbar_wait(&full[g % C::NS], static_cast<uint32_t>((g / C::NS) & 1), wc);
+        named_bar_sync(kBarK, 64);
+      }
+      g0 += u.nmax;
     }
   }
   // a split unit's CTAs meet twice at the end (partial results written, then
@@ -694,11 +767,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- softmax
     const int t = warp >> 2;
     const int r = (warp & 3) * 32 + lane;  // row inside the tile = TMEM lane
-    const int qi = m0 + t * BM + r;        // query row
-    const bool row_ok = qi < a.Lq;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::s_col(t);
     const uint32_t tO = tmem + lane_off + C::o_col(t);
+    bool ok = true;
+    int sph = 0;  // phases of s_full[t] consumed (earlier units)
+    int oph = 0;  // phases of o_done[t] consumed (earlier units)
+    for (int it = 0; it < n_my; ++it) {
+    const Geo u = geo(it);
+    const int qb = u.qb, h = u.h, b = u.b, part = u.part, m0 = u.m0, nt = u.nt;
+    const int Lkb = u.Lkb, Lqb = u.Lqb, jb = u.jb;
+    const int nkv_t = t == 0 ? u.nkv[0] : u.nkv[1];
+    (void)qb;
+    const int qi = m0 + t * BM + r;        // query row
+    const bool row_ok = qi < a.Lq;
     // last key visible to this row (bounds and causal)
     int limit = Lkb - 1;
     if (a.causal) limit = min(limit, qi + (Lkb - Lqb));
@@ -722,7 +804,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     limit -= jb * BN;
     float m = -INFINITY;  // reference max (log2 units)
     float l = 0.f;        // running sum relative to m
-    bool ok = true;
     // interior tiles take the fused path when the scores need no mask and
     // the scale is positive (max of raw scores = max of scaled scores)
     const bool fast_ok = (a.sl2 > 0.f) && (a.mask == nullptr);
@@ -913,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     if (t < nt) {
-      for (int j = 0; j < nkv[t]; ++j) {
+      for (int j = 0; j < nkv_t; ++j) {
         // a 16-byte aligned per-query mask row is brought into L1 before the
         // scores are waited for, and loaded after with 16-byte loads
         // (measured: prefetching unaligned rows, read byte by byte, slowed
@@ -930,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[t], j & 1, wc));
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(&s_full[t], (sph + j) & 1, wc));
         if (ok) {
           tc_fence_after();
           uint32_t s[BN];
@@ -1161,11 +1242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // hand P_t,j to the MMA warp; met every step, also after a failed wait
         named_bar_sync(kBarP + t, 32 * 5);
       }
-      if (ok) ok = mbar_wait(&o_done[t], 0, wc);
+      if (ok) ok = mbar_wait(&o_done[t], static_cast<uint32_t>(oph & 1), wc);
       ok = __all_sync(0xffffffffu, ok);
       if constexpr (!SPLIT) epilogue();
+      sph += nkv_t;
+      ++oph;
     }
     if constexpr (SPLIT) epilogue();
+    }  // units
   }
 
   __syncwarp();
@@ -1177,7 +1261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kLoadWarp && lane == 0 && *abort_flag) {
     // a role gave up: every copy the producer issued lands before the CTA exits
-    drain_wait(q_full, 0, kDrainNs);
+    if (last_q >= 0) drain_wait(q_full, static_cast<uint32_t>(last_q & 1), kDrainNs);
     for (int s = 0; s < C::NS; ++s)
       if (last_use[s] >= 0) drain_wait(&full[s], last_use[s] & 1, kDrainNs);
   }
@@ -1356,14 +1440,22 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   if (n_whole > 0) {
     a.unit0 = 0;
     a.ksplit = 1;
-    kern<<<dim3(static_cast<unsigned>(n_whole)), kThreads, kSmem, env.stream>>>(tq, tk, tv, tq2,
-                                                                                  tk2, tv2, a);
+    a.nunits = n_whole;
+    // Persistent grid (one CTA per SM looping over units) for units of equal
+    // length; causal units differ in length and keep one CTA per unit, so
+    // that the hardware hands each SM its next unit as it frees up; a call
+    // that shares the GPU keeps one CTA per unit as well.
+    const bool persist = !p.causal && !(p.flags & SDPA_FLAG_SHARED_GPU);
+    const int grid = persist ? std::min(n_whole, env.num_sms) : n_whole;
+    kern<<<dim3(static_cast<unsigned>(grid)), kThreads, kSmem, env.stream>>>(tq, tk, tv, tq2, tk2,
+                                                                             tv2, a);
     if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
     *grids = 1;
   }
   if (tail == 0) return SDPA_OK;
   a.unit0 = n_whole;
   a.ksplit = ksplit;
+  a.nunits = tail;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(ksplit);

@@ -404,6 +404,12 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrive at a named barrier without waiting (the waiting side uses
+// named_bar_sync with the same thread count).  A caller must not arrive
+// again before the barrier's phase has completed.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 // Thread-block cluster helpers: barrier over every thread of the cluster
 // (exited threads count as arrived; whole warps), this CTA's rank, the
