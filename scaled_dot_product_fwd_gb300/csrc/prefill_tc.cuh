@@ -395,6 +395,21 @@ __device__ __forceinline__ Geo unit_geo(const PrefillArgs& a, uint32_t bx) {
   return g;
 }
 
+// Key columns whose exponentials are computed for key tile j of a unit
+// (counted from the CTA's first): BN, except that on the last, ragged tile
+// of a plain call at head_dim 64 without causal masking only its keys,
+// rounded up to 32, are (the columns past them are masked: P = 0 there).
+template <int D, bool X3, bool EXT>
+__device__ __forceinline__ int tile_cols(const PrefillArgs& a, const Geo& u, int j) {
+  if constexpr (D != 64 || X3 || EXT) {
+    return BN;
+  } else {
+    if (a.causal) return BN;
+    const int keys = u.Lkb - (u.jb + j) * BN;
+    return keys >= BN ? BN : ((keys + 31) >> 5) << 5;
+  }
+}
+
 // EXT: extended inputs (per-batch length arrays, a boolean mask, a mask row
 // shared by every query row, or additive rows that are all 16-byte aligned);
 // without them the lengths are the kernel arguments and the code is that of
@@ -442,18 +457,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every CTA of that grid is running
   if constexpr (!SPLIT) griddep_launch_dependents();
   // Units of this CTA.  A split grid gives one unit to the ksplit CTAs of a
-  // cluster.  The grid of whole units may be persistent: CTA x takes units
-  // x, x + gridDim.x, ... below nunits, and every role runs on from one unit
-  // into the next (the producer loads the next unit's Q once the last S
+  // cluster.  The grid of whole units may be persistent: in round k CTA x
+  // takes unit k G + x (k even) or k G + G - 1 - x (k odd), G = gridDim.x,
+  // below nunits (the snake order evens out causal units, which come
+  // heaviest first), and every role runs on from one unit into the next (the producer loads the next unit's Q once the last S
   // products of the current one have read the Q tiles, and its K/V through
   // the same ring; the MMA warp issues its first S products right behind the
   // current unit's last P V), so that the start of a unit overlaps the end
   // of the previous one.
   const int bxi = static_cast<int>(blockIdx.x);
   const int gdx = static_cast<int>(gridDim.x);
-  const int n_my = SPLIT ? 1 : (bxi < a.nunits ? (a.nunits - 1 - bxi) / gdx + 1 : 0);
+  const int rounds = a.nunits / gdx;
+  const int rem = a.nunits - rounds * gdx;
+  const int n_my =
+      SPLIT ? 1 : rounds + ((rem > 0 && ((rounds & 1) ? bxi >= gdx - rem : bxi < rem)) ? 1 : 0);
   auto geo = [&](int it) {
-    return unit_geo<EXT, SPLIT>(a, static_cast<uint32_t>(SPLIT ? bxi : bxi + it * gdx));
+    const int x = (it & 1) ? gdx - 1 - bxi : bxi;
+    return unit_geo<EXT, SPLIT>(a, static_cast<uint32_t>(SPLIT ? bxi : it * gdx + x));
   };
 
   if (threadIdx.x == 0) {
@@ -1208,12 +1228,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mu = (m == -INFINITY) ? 0.f : m;
             float rp[4] = {0.f, 0.f, 0.f, 0.f};
+            // columns past a narrowed tile's nw are not computed (P = 0)
+            const int nw = tile_cols<D, X3, EXT>(a, u, j);
 #pragma unroll
-            for (int i = 0; i < BN / 2; ++i) {
-              const float p0 = ex2(x[2 * i] - mu);
-              const float p1 = ex2(x[2 * i + 1] - mu);
-              rp[i & 3] += p0 + p1;
-              pk[i] = E::pack(p0, p1);
+            for (int c = 0; c < BN / 32; ++c) {
+              if (c * 32 < nw) {
+#pragma unroll
+                for (int i = 16 * c; i < 16 * c + 16; ++i) {
+                  const float p0 = ex2(x[2 * i] - mu);
+                  const float p1 = ex2(x[2 * i + 1] - mu);
+                  rp[i & 3] += p0 + p1;
+                  pk[i] = E::pack(p0, p1);
+                }
+              } else {
+#pragma unroll
+                for (int i = 16 * c; i < 16 * c + 16; ++i) pk[i] = 0u;
+              }
             }
             rs = (rp[0] + rp[1]) + (rp[2] + rp[3]);
           }
@@ -1441,11 +1471,9 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
     a.unit0 = 0;
     a.ksplit = 1;
     a.nunits = n_whole;
-    // Persistent grid (one CTA per SM looping over units) for units of equal
-    // length; causal units differ in length and keep one CTA per unit, so
-    // that the hardware hands each SM its next unit as it frees up; a call
-    // that shares the GPU keeps one CTA per unit as well.
-    const bool persist = !p.causal && !(p.flags & SDPA_FLAG_SHARED_GPU);
+    // Persistent grid (one CTA per SM looping over units); a call that
+    // shares the GPU keeps one CTA per unit.
+    const bool persist = !(p.flags & SDPA_FLAG_SHARED_GPU);
     const int grid = persist ? std::min(n_whole, env.num_sms) : n_whole;
     kern<<<dim3(static_cast<unsigned>(grid)), kThreads, kSmem, env.stream>>>(tq, tk, tv, tq2, tk2,
                                                                              tv2, a);

@@ -123,7 +123,9 @@ PREFILL_SHAPES = [(2, 4, 2, 300, 333), (1, 2, 1, 129, 129), (1, 3, 3, 7, 200), (
                   (1, 2, 2, 256, 256), (2, 8, 1, 97, 1000), (1, 2, 1, 513, 520),
                   # key tails of exactly one 32-key chunk, of three chunks with a
                   # short first tile, and of 26 keys under a causal offset
-                  (1, 2, 1, 160, 160), (1, 4, 2, 64, 224), (1, 2, 2, 200, 4250)]
+                  (1, 2, 1, 160, 160), (1, 4, 2, 64, 224), (1, 2, 2, 200, 4250),
+                  # a last key tile of exactly 64 keys
+                  (1, 2, 2, 130, 192)]
 
 
 @pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
