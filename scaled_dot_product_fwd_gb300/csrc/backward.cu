@@ -220,7 +220,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
   if (lane == 0) {
     a.dvec[row] = s;
     const float l = a.lse[row];
-    a.lse2[row] = (l == -INFINITY) ? INFINITY : l * kLog2eB;
+    // A row that saw no key, or only keys whose mask values were huge (LSE
+    // -2^100 * scale, beside which its scores vanish), takes no part: P = 0
+    // there.  For the latter that is exact for dQ and dK (the scores do not
+    // reach the output) and leaves out its share dO / n of those keys' dV.
+    a.lse2[row] = (l == -INFINITY || l <= -kMaskBig) ? INFINITY : l * kLog2eB;
   }
 }
 
@@ -600,7 +604,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             float x = __uint_as_float(sv[2 * c2 + e]) * a.sl2;
             if (mrow || mrowb) {
               if (vis && mrowb) vis = mrowb[static_cast<long long>(c) * a.ms2] != 0;
-              if (vis && mrow) x += E::to_f(mrow[static_cast<long long>(c) * a.ms2]) * kLog2eB;
+              if (vis && mrow)
+                x += mask_log2(E::to_f(mrow[static_cast<long long>(c) * a.ms2]), mask_huge_log2(a.sl2));
             }
             const float p = vis ? ex2(x + sl[c]) : 0.f;
             pv[e] = p;

@@ -68,7 +68,11 @@ struct SplitArgs {
   const void* mask;
   long long ms0, ms1, ms2;  // batch, head and row strides of the mask (key stride 1)
   float* ws_o;    // [B, Hq, num_splits, D], normalised partial outputs
-  float* ws_lse;  // [B, Hq, num_splits], log2-domain log-sum-exp
+  // [B, Hq, num_splits][2]: each split's running max m (log2 units) and sum
+  // l relative to it.  Carried apart rather than as m + log2 l: a row whose
+  // keys all carry a huge mask value has m at the huge-mask value, beside
+  // which log2 l vanishes in fp32, yet l still weighs the split.
+  float* ws_ml;
   // in-cluster merge (set by the launcher): output, LSE and sinks
   void* o;
   float* lse;
@@ -228,10 +232,10 @@ struct SplitCfg {
   // per-warp broadcast buffer: (p, p) pairs per (head, key), then HG factors
   static constexpr int PB_WORDS = 2 * HG * KB + ((HG + 1) & ~1);
   static constexpr int COMBINE_BYTES = kConsumerWarps * HG * (D + 2) * 4;
-  // in-cluster merge, after the warps' states: partial O [HG][D], lse [HG],
-  // split weights [HG][16], 1/L [HG]
+  // in-cluster merge, after the warps' states: partial O [HG][D], m and l
+  // [HG][2], split weights [HG][16], 1/L [HG]
   static constexpr int MERGE_BYTES =
-      COMBINE_BYTES + (HG * D + HG + HG * kMaxClusterSplits + HG) * 4;
+      COMBINE_BYTES + (HG * D + 2 * HG + HG * kMaxClusterSplits + HG) * 4;
   static_assert(LR * EPL == D && RPW * LR == 32, "lane layout");
   static_assert(KB % RPW == 0 && NVL <= LR, "batch layout");
   static_assert((TILE_BYTES % 16) == 0, "bulk copy granularity");
@@ -442,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
     if (key >= key_end || key > my_limit) {
       x = -INFINITY;
     } else if (mrow) {
-      x += Ld<T>::f(mrow[key]) * kLog2e;
+      x += mask_log2(Ld<T>::f(mrow[key]), mask_huge_log2(a.sl2));
     } else if (mrowb && !mrowb[key]) {
       x = -INFINITY;
     }
@@ -534,9 +538,9 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   }
   named_bar_sync(2, kConsumerWarps * 32);
   const bool aborted = *abort_flag != 0;
-  // this split's state of head hh: normalised partial output at column d
-  // and the log2-domain log-sum-exp
-  auto split_state = [&](int hh, int d, float& o_out, float& lse_out) {
+  // this split's state of head hh: normalised partial output at column d,
+  // running max m (log2 units) and the sum l relative to it
+  auto split_state = [&](int hh, int d, float& o_out, float& m_out, float& l_out) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wm[w * HG + hh]);
@@ -550,18 +554,22 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
       }
     }
     o_out = (L > 0.f) ? O / L : 0.f;
-    lse_out = (L > 0.f) ? M + __log2f(L) : -INFINITY;
+    m_out = (L > 0.f) ? M : -INFINITY;
+    l_out = L;
   };
   if (!a.cluster) {
     if (aborted) return;
     for (int e = threadIdx.x; e < HG * D; e += kConsumerWarps * 32) {
       const int hh = e / D, d = e % D;
       if (grp * HG + hh >= R) continue;
-      float ov, lv;
-      split_state(hh, d, ov, lv);
+      float ov, mv, lv;
+      split_state(hh, d, ov, mv, lv);
       const size_t row = row_index(grp * HG + hh) * a.num_splits + split;
       a.ws_o[row * D + d] = ov;
-      if (d == 0) a.ws_lse[row] = lv;
+      if (d == 0) {
+        a.ws_ml[2 * row] = mv;
+        a.ws_ml[2 * row + 1] = lv;
+      }
     }
     return;
   }
@@ -571,48 +579,53 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
   // used: the status word reports the timeout), so that no CTA leaves while
   // another still reads its shared memory.
   float* cpo = wacc + kConsumerWarps * HG * D;  // [HG][D] partial output
-  float* cpl = cpo + HG * D;                    // [HG] lse (log2)
-  float* wts = cpl + HG;                        // [HG][kMaxClusterSplits]
+  float* cpl = cpo + HG * D;                    // [HG][2] m (log2), l
+  float* wts = cpl + 2 * HG;                    // [HG][kMaxClusterSplits]
   float* hinv = wts + HG * kMaxClusterSplits;   // [HG] 1 / L
   for (int e = threadIdx.x; e < HG * D; e += kConsumerWarps * 32) {
     const int hh = e / D, d = e % D;
-    float ov = 0.f, lv = -INFINITY;
-    if (!aborted && grp * HG + hh < R) split_state(hh, d, ov, lv);
+    float ov = 0.f, mv = -INFINITY, lv = 0.f;
+    if (!aborted && grp * HG + hh < R) split_state(hh, d, ov, mv, lv);
     cpo[e] = ov;
-    if (d == 0) cpl[hh] = lv;
+    if (d == 0) {
+      cpl[2 * hh] = mv;
+      cpl[2 * hh + 1] = lv;
+    }
   }
   cluster_sync_all();
   const int S = a.num_splits;
   const uint32_t rank = cluster_rank();
   if (threadIdx.x < HG) {
-    // weights 2^(lse_s - M) of the splits, and the sink in the denominator
+    // weights l_s 2^(m_s - M) of the splits, and the sink in the denominator
     const int hh = threadIdx.x;
     const int rr = grp * HG + hh;
     const bool valid = rr < R;
     const int hq = kvh * a.G + (valid ? rr / a.Lq : 0);
     // all remote loads in flight before any is used
-    float lq[kMaxClusterSplits];
-#pragma unroll
-    for (int q = 0; q < kMaxClusterSplits; ++q)
-      if (q < S) lq[q] = ld_cluster(cpl + hh, static_cast<uint32_t>(q));
-    float M = -INFINITY;
+    float mq[kMaxClusterSplits], lq[kMaxClusterSplits];
 #pragma unroll
     for (int q = 0; q < kMaxClusterSplits; ++q)
       if (q < S) {
-        wts[hh * kMaxClusterSplits + q] = lq[q];
-        M = fmaxf(M, lq[q]);
+        mq[q] = ld_cluster(cpl + 2 * hh, static_cast<uint32_t>(q));
+        lq[q] = ld_cluster(cpl + 2 * hh + 1, static_cast<uint32_t>(q));
       }
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kMaxClusterSplits; ++q)
+      if (q < S) M = fmaxf(M, mq[q]);
     float sk = -INFINITY;
     if (a.sinks && valid) {
       sk = a.sinks[hq] * kLog2e;
       M = fmaxf(M, sk);
     }
     float L = 0.f;
-    for (int q = 0; q < S; ++q) {
-      const float w = (M == -INFINITY) ? 0.f : ex2(wts[hh * kMaxClusterSplits + q] - M);
-      wts[hh * kMaxClusterSplits + q] = w;
-      L += w;
-    }
+#pragma unroll
+    for (int q = 0; q < kMaxClusterSplits; ++q)
+      if (q < S) {
+        const float w = (lq[q] > 0.f) ? lq[q] * ex2(mq[q] - M) : 0.f;
+        wts[hh * kMaxClusterSplits + q] = w;
+        L += w;
+      }
     if (a.sinks && M != -INFINITY) L += ex2(sk - M);
     hinv[hh] = (L > 0.f) ? 1.f / L : 0.f;
     if (rank == 0 && a.lse && valid && !aborted)

@@ -24,7 +24,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 struct CombineArgs {
   const float* ws_o;
-  const float* ws_lse;
+  const float* ws_ml;  // [rows][splits][2]: m (log2 units), l
   void* o;
   float* lse;
   const float* sinks;
@@ -61,9 +61,9 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
   const size_t row = blockIdx.x;  // (b * Hq + hq) * rows_per_head + i
   const int hq = static_cast<int>((row / a.rows_per_head) % a.Hq);
   const int S = a.num_splits;
-  const float* ls = a.ws_lse + row * S;
+  const float* ml = a.ws_ml + row * S * 2;
   float M = -INFINITY;
-  for (int s = threadIdx.x; s < S; s += kCombineThreads) M = fmaxf(M, ls[s]);
+  for (int s = threadIdx.x; s < S; s += kCombineThreads) M = fmaxf(M, ml[2 * s]);
   M = block_reduce(M, true, red);
   float sk = -INFINITY;
   if (a.sinks) {
@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
   }
   float L = 0.f;
   for (int s = threadIdx.x; s < S; s += kCombineThreads) {
-    const float e = (M == -INFINITY) ? 0.f : ex2(ls[s] - M);
+    const float l = ml[2 * s + 1];
+    const float e = (l > 0.f) ? l * ex2(ml[2 * s] - M) : 0.f;
     w[s] = e;
     L += e;
   }
@@ -190,7 +191,7 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   out->stages = stages;
   out->cluster = cluster;  // the launcher checks the final split count
   const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * splits;
-  out->workspace = align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
+  out->workspace = align256(rows * D * sizeof(float)) + align256(rows * 2 * sizeof(float));
   return true;
 }
 
@@ -200,8 +201,8 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   const size_t rows =
       static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * plan.num_splits;
   float* ws_o = static_cast<float*>(workspace);
-  float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                           align256(rows * p.head_dim * sizeof(float)));
+  float* ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                          align256(rows * p.head_dim * sizeof(float)));
   dec::SplitArgs a;
   a.q = q;
   a.k = k;
@@ -237,7 +238,7 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   a.ms1 = p.mask_stride[1];
   a.ms2 = p.mask_stride[2];
   a.ws_o = ws_o;
-  a.ws_lse = ws_lse;
+  a.ws_ml = ws_ml;
   a.o = o;
   a.lse = lse;
   a.sinks = p.sinks;
@@ -264,7 +265,7 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   }
   dec::CombineArgs c;
   c.ws_o = ws_o;
-  c.ws_lse = ws_lse;
+  c.ws_ml = ws_ml;
   c.o = o;
   c.lse = lse;
   c.sinks = p.sinks;
@@ -284,7 +285,7 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
 sdpa_status_t launch_no_keys(const sdpa_params_t& p, void* o, float* lse, const LaunchEnv& env) {
   dec::CombineArgs c;
   c.ws_o = nullptr;
-  c.ws_lse = nullptr;
+  c.ws_ml = nullptr;
   c.o = o;
   c.lse = lse;
   c.sinks = p.sinks;

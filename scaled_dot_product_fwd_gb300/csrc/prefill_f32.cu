@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kF32Threads) prefill_f32_kernel(const F32Args 
       for (int c = 0; c < 4; ++c) {
         const int kj = k0 + tx + 16 * c;
         float xv = s[i][c] * a.sl2;
-        if (mrow[i] && kj <= limit[i]) xv += mrow[i][kj] * kLog2e;
+        if (mrow[i] && kj <= limit[i]) xv += mask_log2(mrow[i][kj], mask_huge_log2(a.sl2));
         if (mrowb[i] && kj <= limit[i] && !mrowb[i][kj]) xv = -INFINITY;
         if (kj > limit[i]) xv = -INFINITY;
         x[c] = xv;

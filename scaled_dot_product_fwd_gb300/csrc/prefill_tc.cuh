@@ -169,6 +169,7 @@ struct PrefillArgs {
   // boolean mask, 1/scale as hi + lo for an additive one.
   int kbias;
   uint32_t qbias;
+
 };
 
 template <bool BF16>
@@ -295,18 +296,27 @@ __device__ __forceinline__ void softmax_pairs(const uint32_t (&s)[N], float sl2,
   rs = t0 + t1;
 }
 
-// Max of the raw scores of one row.
+// Max of the N values of one row (N a multiple of 16): eight running maxima
+// (every column read exactly once), then combined.
 template <int N>
-__device__ __forceinline__ float row_max_raw(const uint32_t (&s)[N]) {
+__device__ __forceinline__ float row_max16(const float (&x)[N]) {
+  static_assert(N % 16 == 0, "row length");
   float mr[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
+  for (int c = 0; c < 8; ++c) mr[c] = x[c];
+  // columns 8 .. N - 9 in pairs, then the last 8 singly
 #pragma unroll
-  for (int i = 8; i < N; i += 16)
+  for (int i = 8; i + 16 <= N - 8; i += 16)
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]), __uint_as_float(s[i + 2 * c + 1]));
+    for (int c = 0; c < 8; ++c) mr[c] = fmax3(mr[c], x[i + 2 * c], x[i + 2 * c + 1]);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) mr[c] = fmaxf(mr[c], x[N - 8 + c]);
   return fmaxf(fmax3(mr[0], mr[1], mr[2]), fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7])));
+}
+// Max of the raw scores (fp32 bit patterns) of one row.
+template <int N>
+__device__ __forceinline__ float row_max_raw(const uint32_t (&s)[N]) {
+  return row_max16(*reinterpret_cast<const float(*)[N]>(&s[0]));
 }
 
 
@@ -512,7 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < n16; i += kThreads) {
       // a query-chunk word of columns 0-7 starts a 256-byte row group's first half
       const bool col0 = i >= q16 && ((i * 16) % C::BIAS_SBO) < C::BIAS_LBO;
-      z[i] = make_uint4(col0 ? a.qbias : 0u, 0u, 0u, 0u);
+      // column 2 of the query chunks holds 1 (huge key-mask values)
+      z[i] = make_uint4(col0 ? a.qbias : 0u, col0 ? (BF16 ? 0x3f80u : 0x3c00u) : 0u, 0u, 0u);
     }
     fence_proxy_async_shared();
   }
@@ -583,17 +594,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int r = 32 * c + lane;
               const int key = key0 + r;
               uint32_t v = ninf;  // keys past this batch's length: -inf
+              uint32_t v2 = 0u;   // columns 2, 3
               if (key < u.Lkb) {
                 if (a.mask_bool) {
                   v = mk[key] != 0 ? 0u : ninf;
                 } else {
                   // columns 0 and 1 (1/scale = hi + lo); with lo = 0 column 1
-                  // stays 0, so that a -inf mask value never meets a zero
+                  // stays 0, so that a -inf mask value never meets a zero.  A
+                  // finite value of magnitude 2^64 or more goes to column 2
+                  // (query side 1) as -+2^100, so that S is exactly that.
                   const uint32_t m16 = mv[key];
-                  v = m16 | ((a.qbias >> 16) != 0u ? (m16 << 16) : 0u);
+                  const uint32_t mag = m16 & 0x7fffu;
+                  if (BF16 && mag >= 0x5f80u && mag < 0x7f80u) {
+                    v = 0u;
+                    v2 = (m16 & 0x8000u) | 0x7180u;  // 2^100
+                  } else {
+                    v = m16 | ((a.qbias >> 16) != 0u ? (m16 << 16) : 0u);
+                  }
                 }
               }
-              *reinterpret_cast<uint32_t*>(sKB + s * C::BIAS_CHUNK + C::bias_at(r)) = v;
+              if constexpr (BF16) {  // columns 0-3 (fp16 holds no huge value: column 2 stays 0)
+                *reinterpret_cast<uint2*>(sKB + s * C::BIAS_CHUNK + C::bias_at(r)) = make_uint2(v, v2);
+              } else {
+                *reinterpret_cast<uint32_t*>(sKB + s * C::BIAS_CHUNK + C::bias_at(r)) = v;
+              }
             }
             fence_proxy_async_shared();
             __syncwarp();
@@ -842,6 +866,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool fused_ok =
         (a.sl2 > 0.f) && (a.mask == nullptr || (EXT && (kbias || a.mask_bool || mvec)));
     const float rscale = kLog2e / a.sl2;  // 1 / scale
+    // Huge mask values (magnitude 2^64 or more) exist only in bfloat16 and
+    // float masks.  Key masks (one row shared by the query rows) give them
+    // their exact form: on the key-mask MMA step (bfloat16) and, in the fp32
+    // hi/lo kernel, on the extended instantiation's general path.  Masks with
+    // a row per query keep the plain product, whose unrolled code is a third
+    // of the size (carried by the boundary tiles' general path, its size
+    // alone measured 3.5 % of the unmasked DiT loop): there a finite value
+    // whose scaled product overflows fp32 acts as -inf.
+    constexpr bool kHugeMask = EXT && X3;
+    const float mhuge = mask_huge_log2(a.sl2);  // a huge mask value in log2 units
+    auto mlog2 = [&](float mv) { return kHugeMask ? mask_log2(mv, mhuge) : mv * kLog2e; };
     // Output of the tile (whole units: right after its loop; split units:
     // after the CTAs of the cluster have exchanged partial results).
     auto epilogue = [&]() {
@@ -1066,7 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int i = 0; i < BN; ++i) {
                 float x = __uint_as_float(s[i]) * a.sl2;
-                if (mrow && kv0 + i <= limit) x += to_float(mrow[kv0 + i]) * kLog2e;
+                if (mrow && kv0 + i <= limit) x += mlog2(to_float(mrow[kv0 + i]));
                 if (EXT && mrowb && kv0 + i <= limit && !mrowb[kv0 + i]) x = -INFINITY;
                 if (kv0 + i > limit) x = -INFINITY;
                 s[i] = __float_as_uint(x);
@@ -1078,18 +1113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             resc = false;
             for (int pass = 0; pass < 2; ++pass) {
               if (need_max) {
-                float mr[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) mr[c] = __uint_as_float(s[c]);
-#pragma unroll
-                for (int i = 8; i < BN; i += 16)
-#pragma unroll
-                  for (int c = 0; c < 8; ++c)
-                    mr[c] = fmax3(mr[c], __uint_as_float(s[i + 2 * c]),
-                                  __uint_as_float(s[i + 2 * c + 1]));
-                const float mx = fmaxf(fmax3(mr[0], mr[1], mr[2]),
-                                       fmaxf(fmax3(mr[3], mr[4], mr[5]), fmaxf(mr[6], mr[7]))) *
-                                 mul;
+                const float mx = row_max_raw(s) * mul;
                 // the fused path always moves to the tile max; the general
                 // path only when it grew by more than the threshold
                 if (fast || mx > m + kRescaleThreshold) {
@@ -1201,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mrow) {
 #pragma unroll
               for (int i = 0; i < BN; ++i)
-                if (kv0 + i <= limit) x[i] += to_float(mrow[kv0 + i]) * kLog2e;
+                if (kv0 + i <= limit) x[i] += mlog2(to_float(mrow[kv0 + i]));
             }
             if constexpr (EXT) {
               if (mrowb) {
@@ -1215,12 +1239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < BN; ++i)
                 if (kv0 + i > limit) x[i] = -INFINITY;
             }
-            float mr[4] = {x[0], x[1], x[2], x[3]};
-#pragma unroll
-            for (int i = 4; i < BN; i += 8)
-#pragma unroll
-              for (int c = 0; c < 4; ++c) mr[c] = fmax3(mr[c], x[i + 2 * c], x[i + 2 * c + 1]);
-            const float mx = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+            const float mx = row_max16(x);
             resc = mx > m + kRescaleThreshold;  // true on the first visible tile
             if (resc) {
               alpha = ex2(m - mx);  // 0 when m = -inf
@@ -1363,6 +1382,7 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   a.os2 = p.o_stride[2];
   a.kbias = 0;
   a.qbias = 0;
+
   if (EXT && !X3 && p.mask && p.mask_stride[2] == 0 && p.scale > 0.f) {
     if (p.flags & SDPA_FLAG_BOOL_MASK) {
       a.kbias = 1;
@@ -1388,6 +1408,7 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
       if (fits) {
         a.kbias = 1;
         a.qbias = hi | (lo << 16);
+
       }
     }
   }

@@ -389,6 +389,31 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Additive mask values.  A finite mask value of magnitude 2^64 or more (the
+// most negative bfloat16 or float, a common padding value, is one) is one
+// beside which the float64 definition loses every score: s + mask is mask
+// itself.  Such a value enters as -+2^100 in raw-score units, i.e. as the
+// exact product -+2^100 * scale*log2(e) in log2 units: scores vanish beside
+// it in fp32 too and its products with the scale stay exact, so a key so
+// masked weighs nothing beside any key that is not, and a row masked that
+// way throughout attends to its keys uniformly, as the definition does
+// (its LSE is then -2^100 * scale).  -inf stays -inf (the key is removed);
+// smaller values enter as they are.
+constexpr float kMaskBig = 0x1p64f;       // magnitude from which a value is huge
+constexpr float kMaskHugeRaw = 0x1p100f;  // its value in raw-score units
+// its value in log2 units for a call whose scale * log2(e) is sl2 (taken as
+// at least 2^-20 in magnitude)
+__host__ __device__ __forceinline__ float mask_huge_log2(float sl2) {
+  const float m = sl2 < 0.f ? -sl2 : sl2;
+  return kMaskHugeRaw * (m > 0x1p-20f ? m : 0x1p-20f);
+}
+// mask * log2(e); huge is mask_huge_log2(sl2)
+__device__ __forceinline__ float mask_log2(float mv, float huge) {
+  return (mv == -INFINITY) ? mv
+                           : (fabsf(mv) >= kMaskBig ? copysignf(huge, mv)
+                                                    : mv * 1.4426950408889634f);
+}
+
 // Warpgroup-wide register budget change (all warps of the warpgroup).
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {
@@ -403,12 +428,6 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // of times: it has no time limit).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-// Arrive at a named barrier without waiting (the waiting side uses
-// named_bar_sync with the same thread count).  A caller must not arrive
-// again before the barrier's phase has completed.
-__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Thread-block cluster helpers: barrier over every thread of the cluster

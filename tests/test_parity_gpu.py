@@ -748,3 +748,64 @@ def test_strided_no_keys(cuda):
     torch.cuda.synchronize()
     assert o.data_ptr() == out.data_ptr()
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+# ------------------------------------- masks holding the dtype's lowest finite value
+LOWEST_CASES = [("key", 150, 300), ("row", 150, 304), ("row", 150, 300), ("full", 150, 300),
+                ("key", 1, 300), ("full", 4, 1000)]
+
+
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("kind,Lq,Lk", LOWEST_CASES, ids=lambda c: str(c))
+def test_lowest_finite_mask(cuda, dtype, D, kind, Lq, Lk):
+    """Additive masks that use the dtype's most negative finite value as padding.
+
+    The float64 definition gives softmax(s + low) on a row masked by it
+    throughout, which for bfloat16/float32's lowest value (about -3.4e38) is
+    the uniform average of V: the scores vanish beside the mask.  Keys masked
+    by it in other rows weigh nothing.  Key masks (one row shared by the
+    query rows), the single-query path and the fp32 head-dim-128 kernel give
+    such rows that result, with LSE -2^100 * scale (a mask value of magnitude
+    2^64 or more enters as 2^100 in raw-score units); fp16's lowest value
+    (-65504) is an ordinary value everywhere (LSE within 1e-6 relative).  On
+    the tensor-core paths for masks with a row per query, a bfloat16/float
+    value whose scaled product overflows fp32 acts as -inf: a row masked by
+    it throughout sees no key (O = 0, LSE = -inf).  Every other row matches
+    the oracle at the usual bars.
+    """
+    torch = cuda
+    w = wl(2, 4, 2, Lq, Lk, D, dtype, mask=kind, causal=False)
+    inp = W.make_inputs(w)
+    m = inp["mask"].clone()
+    low = torch.finfo(m.dtype).min
+    if kind == "row":       # [1, 1, Lq, Lk]: the first rows entirely, every third key of the rest
+        m[:, :, : min(Lq, 10), :] = low
+        m[:, :, 10:, ::3] = low
+    else:                   # batch 0 entirely, every third key of batch 1
+        m[0] = low
+        m[1, ..., ::3] = low
+    inp["mask"] = m
+    o_gpu, lse_gpu = run_gpu(torch, w, inp)
+    o_ref, lse_ref = oracle_rows(w, inp, None)
+    og = W.as_float64(o_gpu).reshape(-1, D)
+    lg = lse_gpu.double().numpy().reshape(-1)
+    o_ref, lse_ref = o_ref.reshape(-1, D), lse_ref.reshape(-1)
+    assert np.all(np.isfinite(og))
+    per_query_tc = kind != "key" and Lq > 2 and (dtype == "bfloat16" or (dtype == "float32" and D == 64))
+    gone = (lse_ref < -1e30) if per_query_tc else np.zeros_like(lse_ref, dtype=bool)
+    if gone.any():          # rows that see no key on the per-query tensor-core paths
+        assert np.all(np.isneginf(lg[gone])) and np.all(og[gone] == 0)
+    keep = ~gone
+    err = np.abs(og[keep] - o_ref[keep])
+    assert err.max() <= TOL[dtype], "max |dO| %.3g" % err.max()
+    assert err.mean() <= MEAN_TOL
+    big = (lse_ref < -1e4) & keep
+    norm = keep & ~big
+    assert np.all(np.isfinite(lg[keep]))
+    lerr = np.abs(lg[norm] - lse_ref[norm]).max()
+    assert lerr <= LSE_TOL, "max |dLSE| %.3g" % lerr
+    mid = big & (lse_ref > -1e30)
+    assert np.all(np.abs(lg[mid] - lse_ref[mid]) <= 1e-6 * np.abs(lse_ref[mid]))
+    hug = big & ~mid
+    assert np.allclose(lg[hug], -(2.0 ** 100) * w.scale, rtol=1e-5, atol=0)
