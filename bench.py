@@ -587,8 +587,10 @@ def gb300_arm(args):
         "clocks": clk.summary(),
         "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "method": "sdpa_forward_host: pinned host q, k, v in, o, lse out, copies "
-                          "overlapped with the kernels piece by piece, replayed as one CUDA graph"},
+                "method": "C call sdpa_forward_host (include/sdpa.h) through ctypes: pinned "
+                          "host q, k, v in, o, lse out; one cudaMemcpyAsync per piece and "
+                          "tensor on the library's copy streams, overlapped with the other "
+                          "pieces' kernels"},
     }
     if rank == 0 and not args.no_secondary:
         result["secondary"] = secondary(torch, S, device, stream, peaks)

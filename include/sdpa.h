@@ -27,8 +27,9 @@
  *    reads key/value head floor(h / (Hq / Hkv)) (contiguous head groups).
  *  - Pointers q, k, v, o, lse, mask, sinks and workspace are DEVICE pointers
  *    owned by the caller; the library never allocates, frees or retains them.
- *    Base pointers of q, k, v, o and mask must be 16-byte aligned; lse, sinks
- *    4-byte aligned; workspace 256-byte aligned.
+ *    Base pointers of q, k, v and o must be 16-byte aligned; mask aligned to
+ *    its element size; lse, sinks 4-byte aligned; workspace 256-byte
+ *    aligned.
  *  - sdpa_forward is asynchronous on `stream` (a cudaStream_t, passed as
  *    void* so that this header needs no CUDA include; NULL = legacy default
  *    stream).  It never synchronises the host.
@@ -48,7 +49,7 @@
 extern "C" {
 #endif
 
-#define SDPA_ABI_VERSION 4
+#define SDPA_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define SDPA_API __attribute__((visibility("default")))
@@ -236,6 +237,53 @@ SDPA_API sdpa_status_t sdpa_backward(const sdpa_params_t* params, const void* q,
                                      const float* lse, void* dq, void* dk, void* dv,
                                      void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * sdpa_host_staging_size — bytes of device staging memory that
+ * sdpa_forward_host needs for this problem cut into `pieces` pieces (device
+ * copies of q, k, v, o and lse, and two workspaces); 0 for a problem that
+ * sdpa_forward_host rejects.  Pure host function.
+ */
+SDPA_API size_t sdpa_host_staging_size(const sdpa_params_t* params, int pieces);
+
+/*
+ * sdpa_forward_host — sdpa_forward for callers whose q, k, v and results
+ * live in host memory: the whole trip of the mlx page's call (mlx 0.30.7
+ * scaled_dot_product_attention.cpp, eval_gpu: the framework's arrays brought
+ * to the device, the fused graph run, the output handed back), with the
+ * transfers of one piece overlapping the kernels of another.
+ *  q_host, k_host, v_host: inputs in HOST memory, dense [B, H, L, D] in
+ *      params->dtype (page-locked memory, cudaMallocHost or
+ *      cudaHostRegister, lets the copies overlap; pageable memory works, with
+ *      each copy waiting for the host).
+ *  o_host, lse_host: outputs in host memory, dense (lse_host may be NULL).
+ *  params: as for sdpa_forward; mask and sinks, if any, are DEVICE pointers.
+ *      Dense layouts only: SDPA_FLAG_STRIDES, a kv_capacity other than 0 or
+ *      seq_len_kv, or per-batch length arrays give SDPA_ERR_UNSUPPORTED.
+ *  staging / staging_bytes: caller-owned device memory of at least
+ *      sdpa_host_staging_size(params, pieces) bytes, 256-byte aligned; two
+ *      calls whose work overlaps must not share it.
+ *  pieces: the (batch, kv-head) pairs are cut into about this many pieces,
+ *      each within one batch.  Piece i's host-to-device copies run on two
+ *      copy streams, its kernels (those of sdpa_forward, with
+ *      SDPA_FLAG_SHARED_GPU) on one of two compute streams, its
+ *      device-to-host copies on a fifth: one cudaMemcpyAsync per piece and
+ *      tensor.
+ *  stream: the caller's stream.  The work starts after what is already
+ *      enqueued on it, and what the caller enqueues on it afterwards runs
+ *      after this call's copies have landed in o_host and lse_host (e.g. a
+ *      cudaStreamSynchronize(stream) makes them readable).
+ * The five streams and their events belong to the library: created on the
+ * first call on a device (with that device current) and kept until exit;
+ * calls from several threads are serialised while they enqueue.  Nothing is
+ * allocated on the device.  sdpa_last_launch_count counts the kernels of
+ * every piece.  Errors as for sdpa_forward; SDPA_ERR_WORKSPACE_TOO_SMALL for
+ * too small a staging area.
+ */
+SDPA_API sdpa_status_t sdpa_forward_host(const sdpa_params_t* params, const void* q_host,
+                                         const void* k_host, const void* v_host, void* o_host,
+                                         float* lse_host, void* staging, size_t staging_bytes,
+                                         int pieces, void* stream);
+
 /* sdpa_status_string — static, NUL-terminated text for a status code. */
 SDPA_API const char* sdpa_status_string(sdpa_status_t status);
 
@@ -253,6 +301,29 @@ SDPA_API sdpa_status_t sdpa_device_status(void* stream);
  * restores the default.  Returns the previous value.
  */
 SDPA_API uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * sdpa_debug_set_option — test hooks that override a launch decision of
+ * later calls, process-wide (they exist so that tests reach paths that the
+ * planner would not pick for the test's sizes).  Returns the previous value;
+ * an unknown option returns -1 and changes nothing.
+ *  SDPA_DEBUG_DECODE_SPLITS   split count of the vector path (0: the plan's)
+ *  SDPA_DEBUG_DECODE_CLUSTER  0: never merge the splits inside a cluster
+ *                             (two passes); 1: as planned (default)
+ *  SDPA_DEBUG_DECODE_DROP_LAST 1: the vector path's producer skips its last
+ *                             copy, so that a bounded wait runs out and the
+ *                             call reports SDPA_ERR_TIMEOUT (default 0)
+ *  SDPA_DEBUG_PREFILL_SPLIT   -1: the plan's (default); 0: never split the
+ *                             last wave; 2, 4: every unit shared by that
+ *                             many CTAs of a cluster
+ */
+typedef enum {
+  SDPA_DEBUG_DECODE_SPLITS = 0,
+  SDPA_DEBUG_DECODE_CLUSTER = 1,
+  SDPA_DEBUG_DECODE_DROP_LAST = 2,
+  SDPA_DEBUG_PREFILL_SPLIT = 3
+} sdpa_debug_option_t;
+SDPA_API int sdpa_debug_set_option(int option, int value);
 
 /* sdpa_abi_version — SDPA_ABI_VERSION of the built library. */
 SDPA_API int sdpa_abi_version(void);

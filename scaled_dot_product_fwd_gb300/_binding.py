@@ -30,7 +30,12 @@ KERNELS = {0: "none", 1: "prefill_tc", 2: "prefill_f32", 3: "decode_splitkv", 4:
 EXPORTS = ("sdpa_workspace_size", "sdpa_select_kernel", "sdpa_forward", "sdpa_status_string",
            "sdpa_device_status", "sdpa_debug_set_wait_limit_ns", "sdpa_abi_version",
            "sdpa_forward_decode_noalloc", "sdpa_last_launch_count",
-           "sdpa_backward_workspace_size", "sdpa_backward")
+           "sdpa_backward_workspace_size", "sdpa_backward", "sdpa_debug_set_option",
+           "sdpa_host_staging_size", "sdpa_forward_host")
+
+# sdpa_debug_option_t
+DEBUG_OPTIONS = {"decode_splits": 0, "decode_cluster": 1, "decode_drop_last": 2,
+                 "prefill_split": 3}
 
 
 class SdpaParams(ctypes.Structure):
@@ -82,7 +87,14 @@ def load_library(path: str = LIB_PATH):
             lib.sdpa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             lib.sdpa_debug_set_wait_limit_ns.restype = ctypes.c_uint64
             lib.sdpa_abi_version.restype = ctypes.c_int
+            lib.sdpa_debug_set_option.argtypes = [ctypes.c_int, ctypes.c_int]
+            lib.sdpa_debug_set_option.restype = ctypes.c_int
             lib.sdpa_last_launch_count.restype = ctypes.c_int
+            lib.sdpa_host_staging_size.argtypes = [P, ctypes.c_int]
+            lib.sdpa_host_staging_size.restype = ctypes.c_size_t
+            lib.sdpa_forward_host.argtypes = [P] + [ctypes.c_void_p] * 6 + [
+                ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+            lib.sdpa_forward_host.restype = ctypes.c_int
             lib.sdpa_forward_decode_noalloc.argtypes = [P] + [ctypes.c_void_p] * 6
             lib.sdpa_forward_decode_noalloc.restype = ctypes.c_int
             lib.sdpa_backward_workspace_size.argtypes = [P]
@@ -242,6 +254,16 @@ def sdpa_debug_set_wait_limit_ns(ns: int) -> int:
     return int(load_library().sdpa_debug_set_wait_limit_ns(int(ns)))
 
 
+def sdpa_debug_set_option(option, value: int) -> int:
+    """Set a test hook of the library (a DEBUG_OPTIONS name or its number);
+    returns the previous value."""
+    code = DEBUG_OPTIONS[option] if isinstance(option, str) else int(option)
+    prev = int(load_library().sdpa_debug_set_option(code, int(value)))
+    if prev == -1 and not 0 <= code < len(DEBUG_OPTIONS):
+        raise ValueError("unknown debug option %r" % (option,))
+    return prev
+
+
 def sdpa_abi_version() -> int:
     return int(load_library().sdpa_abi_version())
 
@@ -375,43 +397,29 @@ def sdpa_forward(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=N
 _host_cache = {}
 
 
-def _host_chunks(B, Hkv, chunks):
-    """(b, kv-head range) pieces: every batch split into about chunks / B
-    contiguous kv-head ranges (a piece never crosses a batch)."""
-    per_b = max(1, min(Hkv, -(-chunks // max(B, 1))))
-    out = []
-    for b in range(B):
-        for i in range(per_b):
-            h0, h1 = (Hkv * i) // per_b, (Hkv * (i + 1)) // per_b
-            if h1 > h0:
-                out.append((b, h0, h1))
-    return out
+def sdpa_host_staging_size(params, pieces: int) -> int:
+    return int(load_library().sdpa_host_staging_size(ctypes.byref(params), int(pieces)))
 
 
 def sdpa_forward_host(q, k, v, scale=None, causal=False, mask=None, sinks=None, out=None,
-                      lse=None, chunks=8, device=None, graph=True):
-    """sdpa_forward on pinned host tensors, with the transfers overlapped.
+                      lse=None, chunks=8, device=None):
+    """sdpa_forward on host tensors through the C call sdpa_forward_host.
 
-    q [B, Hq, Lq, D] and k/v [B, Hkv, Lk, D] are contiguous pinned CPU tensors
-    of one dtype; mask and sinks, if given, are CUDA tensors as for
-    sdpa_forward.  The (batch, kv-head) pairs are cut into about `chunks`
-    pieces (within one batch each).  Piece c's host-to-device copies (two
-    copy streams), its sdpa_forward call (the library's kernels, on device
-    buffers cached per shape; two compute streams taken in turn, each with its
-    own workspace) and the device-to-host copies of its output and LSE run on
-    separate streams, so the transfers of one piece overlap the kernels of
-    others.  With graph=True the first call for a given set of buffers and
-    arguments runs eagerly and records the whole pipeline as a CUDA graph;
-    later calls with the same buffers replay it (one launch).  The calling
-    thread's current stream forks the work and joins it: the pinned host
-    results (`out`, `lse` or new pinned tensors, returned) are complete once
-    that stream reaches the end of the call, e.g. after
-    torch.cuda.synchronize().
+    q [B, Hq, Lq, D] and k/v [B, Hkv, Lk, D] are contiguous CPU tensors of one
+    dtype (pinned, so that the copies overlap the kernels); mask and sinks,
+    if given, are CUDA tensors as for sdpa_forward.  The library cuts the
+    (batch, kv-head) pairs into about `chunks` pieces and overlaps each
+    piece's copies with the others' kernels on its own streams, forked from
+    and joined back to the current stream of `device`; the results (`out`,
+    `lse` or new pinned tensors, returned) are complete once that stream
+    reaches the end of the call, e.g. after torch.cuda.synchronize().  This
+    function only allocates the device staging area (cached per device,
+    size and stream: calls on different streams never share one).
     """
     torch = _torch()
     for t in (q, k, v):
-        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous pinned host tensors")
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous host tensors")
     if q.dtype != k.dtype or q.dtype != v.dtype:
         raise TypeError("q, k, v must share a dtype")
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -420,8 +428,6 @@ def sdpa_forward_host(q, k, v, scale=None, causal=False, mask=None, sinks=None, 
         device = torch.device("cuda", torch.cuda.current_device())
     B, Hq, Lq, D = q.shape
     _, Hkv, Lk, _ = k.shape
-    if Hkv < 1 or Hq % Hkv != 0:
-        raise ValueError("Hq must be a multiple of Hkv")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -429,90 +435,39 @@ def sdpa_forward_host(q, k, v, scale=None, causal=False, mask=None, sinks=None, 
     if lse is None:
         lse = torch.empty((B, Hq, Lq), dtype=torch.float32, pin_memory=True)
     for t in (out, lse):
-        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
-            raise ValueError("out and lse must be contiguous pinned host tensors")
-    key = (device.index, q.dtype, tuple(q.shape), tuple(k.shape), threading.get_ident())
-    c = _host_cache.get(key)
-    if c is None:
-        c = dict(q=torch.empty(q.shape, dtype=q.dtype, device=device),
-                 k=torch.empty(k.shape, dtype=k.dtype, device=device),
-                 v=torch.empty(v.shape, dtype=v.dtype, device=device),
-                 o=torch.empty(q.shape, dtype=q.dtype, device=device),
-                 l=torch.empty((B, Hq, Lq), dtype=torch.float32, device=device),
-                 streams=[torch.cuda.Stream(device) for _ in range(5)], ws={}, graphs={})
-        _host_cache[key] = c
-    args = (q, k, v, scale, causal, mask, sinks, out, lse, max(1, int(chunks)), device)
-    if not graph:
-        _host_pipeline(torch, c, *args)
-        return out, lse
-    gkey = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-            float(scale), bool(causal), max(1, int(chunks)),
-            None if mask is None else (mask.data_ptr(), tuple(mask.shape), tuple(mask.stride())),
-            None if sinks is None else sinks.data_ptr())
-    g = c["graphs"].get(gkey)
-    if g is not None:
-        g.replay()
-        return out, lse
-    _host_pipeline(torch, c, *args)  # this call's results, and everything warmed up
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        _host_pipeline(torch, c, *args)
-    if len(c["graphs"]) >= 8:  # keep the latest few buffer sets
-        c["graphs"].pop(next(iter(c["graphs"])))
-    c["graphs"][gkey] = g
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("out and lse must be contiguous host tensors")
+    mask_ptr, mstride, flags = None, (0, 0, 0, 1), 0
+    if mask is not None:
+        if (mask.dtype != q.dtype and mask.dtype != torch.bool) or not mask.is_cuda:
+            raise TypeError("mask must have q's dtype (or bool) and live on the GPU")
+        if mask.dtype == torch.bool:
+            flags |= SDPA_FLAG_BOOL_MASK
+        mexp = mask.expand(B, Hq, Lq, Lk)
+        if mexp.stride(3) != 1:
+            raise ValueError("mask must be contiguous along the key dimension")
+        mask_ptr, mstride = mexp.data_ptr(), tuple(mexp.stride())
+    sinks_ptr = None
+    if sinks is not None:
+        if sinks.dtype != torch.float32 or not sinks.is_cuda or sinks.numel() != Hq:
+            raise TypeError("sinks must be a float32 CUDA tensor of Hq values")
+        sinks_ptr = sinks.data_ptr()
+    params = make_params(B, Hq, Hkv, Lq, Lk, D, dtype_code(q.dtype), scale, causal, mask_ptr,
+                         mstride, sinks_ptr)
+    params.flags |= flags
+    pieces = max(1, int(chunks))
+    nbytes = sdpa_host_staging_size(params, pieces)
+    if nbytes == 0:
+        raise SdpaError(2, "problem not supported by sdpa_forward_host")
+    stream = torch.cuda.current_stream(device)
+    key = (device.index, nbytes, stream.cuda_stream)
+    buf = _host_cache.get(key)
+    if buf is None:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _host_cache[key] = buf
+    st = load_library().sdpa_forward_host(ctypes.byref(params), q.data_ptr(), k.data_ptr(),
+                                          v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                          buf.data_ptr(), nbytes, pieces, stream.cuda_stream)
+    if st != 0:
+        raise SdpaError(st, sdpa_status_string(st))
     return out, lse
-
-
-def _host_pipeline(torch, c, q, k, v, scale, causal, mask, sinks, out, lse, chunks, device):
-    B, Hq, Lq, D = q.shape
-    _, Hkv, Lk, _ = k.shape
-    G = Hq // Hkv
-    s_in0, s_in1, s_c0, s_c1, s_out = c["streams"]
-    cur = torch.cuda.current_stream(device)
-    fork = torch.cuda.Event()
-    fork.record(cur)
-    for st in c["streams"]:
-        st.wait_event(fork)
-    mexp = mask.expand(B, Hq, Lq, Lk) if mask is not None else None
-    pieces = _host_chunks(B, Hkv, chunks)
-    # one workspace per compute stream (pieces on the two streams run at once)
-    widest = max(h1 - h0 for _, h0, h1 in pieces)
-    nbytes = sdpa_workspace_size(make_params(1, widest * G, widest, Lq, Lk, D, dtype_code(q.dtype),
-                                             scale, causal, 1 if mask is not None else None,
-                                             (0, 0, 0, 1), 1 if sinks is not None else None))
-    ws = []
-    for j in range(2):
-        buf = c["ws"].get(j)
-        if nbytes > 0 and (buf is None or buf.numel() < nbytes):
-            buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
-            c["ws"][j] = buf
-        ws.append(buf if nbytes > 0 else None)
-    for i, (b, h0, h1) in enumerate(pieces):
-        g0, g1 = h0 * G, h1 * G
-        with torch.cuda.stream(s_in0):
-            c["q"][b, g0:g1].copy_(q[b, g0:g1], non_blocking=True)
-            e_q = torch.cuda.Event()
-            e_q.record(s_in0)
-        with torch.cuda.stream(s_in1):
-            c["k"][b, h0:h1].copy_(k[b, h0:h1], non_blocking=True)
-            c["v"][b, h0:h1].copy_(v[b, h0:h1], non_blocking=True)
-            e_kv = torch.cuda.Event()
-            e_kv.record(s_in1)
-        s_c = s_c0 if i % 2 == 0 else s_c1
-        s_c.wait_event(e_q)
-        s_c.wait_event(e_kv)
-        with torch.cuda.stream(s_c):
-            sdpa_forward(c["q"][b:b + 1, g0:g1], c["k"][b:b + 1, h0:h1], c["v"][b:b + 1, h0:h1],
-                         scale=scale, causal=causal,
-                         mask=None if mexp is None else mexp[b:b + 1, g0:g1],
-                         sinks=None if sinks is None else sinks[g0:g1],
-                         out=c["o"][b:b + 1, g0:g1], lse=c["l"][b:b + 1, g0:g1],
-                         workspace=ws[i % 2], shared_gpu=True)
-            e_c = torch.cuda.Event()
-            e_c.record(s_c)
-        s_out.wait_event(e_c)
-        with torch.cuda.stream(s_out):
-            out[b, g0:g1].copy_(c["o"][b, g0:g1], non_blocking=True)
-            lse[b, g0:g1].copy_(c["l"][b, g0:g1], non_blocking=True)
-    for st in c["streams"]:
-        cur.wait_stream(st)

@@ -173,8 +173,8 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
       cluster = true;
     }
   }
-  if (const char* env = getenv("GB300_SDPA_DECODE_SPLITS")) {  // test override
-    const int f = atoi(env);
+  {  // test hook
+    const int f = debug_option(SDPA_DEBUG_DECODE_SPLITS);
     if (f >= 1) {
       best = f < max_s ? f : max_s;
       cluster = best >= 2 && best <= 16 && (best & (best - 1)) == 0 && D % best == 0;
@@ -243,12 +243,11 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   a.lse = lse;
   a.sinks = p.sinks;
   a.cluster = 0;
-  const char* clu = getenv("GB300_SDPA_DECODE_CLUSTER");  // test override: 0 = two passes
-  a.cluster_ok = (plan.cluster && !(clu && clu[0] == '0')) ? 1 : 0;
+  // (test hook: 0 = two passes)
+  a.cluster_ok = (plan.cluster && debug_option(SDPA_DEBUG_DECODE_CLUSTER) != 0) ? 1 : 0;
   a.status = env.status;
   a.wait_ns = env.wait_limit_ns;
-  const char* drop = getenv("GB300_SDPA_DEBUG_DROP_LAST_TILE");
-  a.debug_drop_last = (drop && drop[0] == '1') ? 1 : 0;
+  a.debug_drop_last = debug_option(SDPA_DEBUG_DECODE_DROP_LAST) == 1 ? 1 : 0;
   sdpa_status_t st;
   bool merged = false;
   const int D = p.head_dim, hg = plan.head_group;

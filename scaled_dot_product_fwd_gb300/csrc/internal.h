@@ -38,6 +38,8 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);
 // and the current bound on device-side waits; both owned by sdpa_api.cu.
 int* status_word_current_device();
 uint64_t current_wait_limit_ns();
+// Current value of a test hook (sdpa_debug_set_option; sdpa_debug_option_t).
+int debug_option(int option);
 // Kernels enqueued by the calling thread's last call (sdpa_last_launch_count).
 void set_last_launches(int n);
 // The problem with SDPA_FLAG_STRIDES set and every tensor's strides filled

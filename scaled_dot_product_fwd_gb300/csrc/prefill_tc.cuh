@@ -227,39 +227,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// 2^x for a pair x in [-125, 128) on the FMA pipe.  x = n + f with n the
-// nearest integer (added to 1.5 * 2^23, whose low mantissa bits then hold n)
-// and f in [-1/2, 1/2]; 2^f from a degree-3 polynomial fitted for this
-// kernel (minimax in relative error on [-1/2, 1/2], max 7.5e-5, below the
-// rounding of the fp16/bf16 P it feeds); 2^n enters as n << 23 added to the
-// exponent field.  The caller clamps x below at -125 so the field stays >= 1.
-__device__ __forceinline__ void exp2_poly_pair(uint64_t X, float& r0, float& r1) {
-  constexpr uint64_t kMagic = 0x4b4000004b400000ull;     // 1.5 * 2^23 (pair)
-  constexpr uint64_t kNegMagic = 0xcb400000cb400000ull;  // -1.5 * 2^23
-  constexpr uint64_t kNeg1 = 0xbf800000bf800000ull;      // -1
-  constexpr uint64_t kC0 = 0x3f7ffb493f7ffb49ull;        // 0.99992806
-  constexpr uint64_t kC1 = 0x3f31798d3f31798dull;        // 0.69326097
-  constexpr uint64_t kC2 = 0x3e786f0d3e786f0dull;        // 0.24261113
-  constexpr uint64_t kC3 = 0x3d61fbb03d61fbb0ull;        // 0.05517167
-  const uint64_t NP = f2_add(X, kMagic);
-  const uint64_t N = f2_add(NP, kNegMagic);
-  const uint64_t F = f2_fma(N, kNeg1, X);
-  uint64_t P = f2_fma(kC3, F, kC2);
-  P = f2_fma(P, F, kC1);
-  P = f2_fma(P, F, kC0);
-  float p0, p1, n0, n1;
-  f2_unpack(P, p0, p1);
-  f2_unpack(NP, n0, n1);
-  r0 = __int_as_float(__float_as_int(p0) + (__float_as_int(n0) << 23));
-  r1 = __int_as_float(__float_as_int(p1) + (__float_as_int(n1) << 23));
-}
-
-// Pairs (bit i of the mask = pair index mod 8) whose exponentials go to the
-// FMA pipe instead of the MUFU unit.
-#ifndef SDPA_POLY_PAIRS_MASK
-#define SDPA_POLY_PAIRS_MASK 0x00
-#endif
-
 // p_i = 2^(s_i * sl2 - m) for one row of raw scores, packed to fp16/bf16
 // pairs; rs receives the fp32 sum of the p_i.
 // With X3, pk2 receives the bf16 residuals p - bf16(p) (P_lo).
@@ -274,14 +241,10 @@ __device__ __forceinline__ void softmax_pairs(const uint32_t (&s)[N], float sl2,
   for (int i = 0; i < N / 2; ++i) {
     const uint64_t X = f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
                               SL, NM);
-    float x0, x1, p0, p1;
+    float x0, x1;
     f2_unpack(X, x0, x1);
-    if ((SDPA_POLY_PAIRS_MASK >> (i & 7)) & 1) {
-      exp2_poly_pair(f2_pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f)), p0, p1);
-    } else {
-      p0 = ex2(x0);
-      p1 = ex2(x1);
-    }
+    const float p0 = ex2(x0);
+    const float p1 = ex2(x1);
     acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
     pk[i] = Elem<BF16>::pack(p0, p1);
     if constexpr (X3) {
@@ -1444,8 +1407,8 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   const int U = static_cast<int>(units);
   const int nkv = (p.seq_len_kv + BN - 1) / BN;
   int ksplit = 1, tail = 0;
-  const char* force = getenv("GB300_SDPA_PREFILL_SPLIT");  // test override
-  const int forced = force ? atoi(force) : -1;             // 0: never; 2, 4: every unit
+  // test hook: -1 the plan's; 0 never; 2, 4 every unit
+  const int forced = debug_option(SDPA_DEBUG_PREFILL_SPLIT);
   // (not for a call that shares the GPU: its last wave is not idle SMs)
   if (!p.causal && forced != 0 && (forced > 0 || !(p.flags & SDPA_FLAG_SHARED_GPU))) {
     static int active[2] = {0, 0};  // clusters of 2, 4 that can be resident (-1: none)

@@ -33,6 +33,9 @@ constexpr int kMaxDecodeRows = 8;     // query rows per head of the vector path,
 constexpr int kMaxDecodeRowsTc = 2;   // the same where a tensor-core prefill exists
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+// test hooks (sdpa_debug_set_option), indexed by sdpa_debug_option_t
+constexpr int kDebugOptions = 4;
+std::atomic<int> g_debug[kDebugOptions] = {{0}, {1}, {0}, {-1}};
 thread_local int g_last_launches = 0;
 std::mutex g_dev_mutex;
 int* g_status_ptr[kMaxDevices] = {};
@@ -78,6 +81,12 @@ sdpa_status_t validate_problem(const sdpa_params_t* p) {
   // head_dim 512 is served by the vector path only (up to 8 query rows).
   if (p->head_dim == 512 && p->seq_len_q > kMaxDecodeRows) return SDPA_ERR_UNSUPPORTED;
   return SDPA_OK;
+}
+
+// Bytes of one mask element: 1 for a boolean mask, else the dtype's size.
+size_t mask_elem_size(const sdpa_params_t& p) {
+  if (p.flags & SDPA_FLAG_BOOL_MASK) return 1;
+  return p.dtype == SDPA_F32 ? 4 : 2;
 }
 
 // The dense layout (and kv_capacity) written out as strides, so that every
@@ -156,6 +165,9 @@ int* status_word_current_device() {
 }
 
 uint64_t current_wait_limit_ns() { return g_wait_ns.load(); }
+int debug_option(int option) {
+  return (option >= 0 && option < kDebugOptions) ? g_debug[option].load() : 0;
+}
 
 void set_last_launches(int n) { g_last_launches = n; }
 
@@ -201,6 +213,11 @@ uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns) {
   return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns);
 }
 
+int sdpa_debug_set_option(int option, int value) {
+  if (option < 0 || option >= kDebugOptions) return -1;
+  return g_debug[option].exchange(value);
+}
+
 sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k, const void* v,
                            void* o, float* lse, void* workspace, size_t workspace_bytes,
                            void* stream) {
@@ -212,7 +229,9 @@ sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k,
   if (!q || !o || (p->seq_len_kv > 0 && (!k || !v))) return SDPA_ERR_INVALID_ARGUMENT;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
     return SDPA_ERR_MISALIGNED;
-  if (p->mask && !aligned(p->mask, 16)) return SDPA_ERR_MISALIGNED;
+  // the mask is read element by element where its rows are not 16-byte
+  // aligned (the kernels check each row), so its own element size will do
+  if (p->mask && !aligned(p->mask, mask_elem_size(*p))) return SDPA_ERR_MISALIGNED;
   if (lse && !aligned(lse, 4)) return SDPA_ERR_MISALIGNED;
   if (p->sinks && !aligned(p->sinks, 4)) return SDPA_ERR_MISALIGNED;
   if ((p->seq_lens_q && !aligned(p->seq_lens_q, 4)) ||
@@ -292,9 +311,10 @@ sdpa_status_t sdpa_backward(const sdpa_params_t* p, const void* q, const void* k
   if (!has_q && !has_k) return SDPA_OK;
   if (has_q && (!q || !o || !d_o || !lse || !dq)) return SDPA_ERR_INVALID_ARGUMENT;
   if (has_k && (!k || !v || !dk || !dv)) return SDPA_ERR_INVALID_ARGUMENT;
-  const void* p16[] = {q, k, v, o, d_o, dq, dk, dv, p->mask};
+  const void* p16[] = {q, k, v, o, d_o, dq, dk, dv};
   for (const void* ptr : p16)
     if (ptr && !aligned(ptr, 16)) return SDPA_ERR_MISALIGNED;
+  if (p->mask && !aligned(p->mask, mask_elem_size(*p))) return SDPA_ERR_MISALIGNED;
   if (lse && !aligned(lse, 4)) return SDPA_ERR_MISALIGNED;
   const size_t need = gb300::backward_workspace(*p);
   if (need > 0) {

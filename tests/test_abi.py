@@ -56,7 +56,7 @@ def test_launch_count_is_zero_after_a_rejected_call(sdpa_lib):
 
 
 def test_abi_version_and_status_strings(sdpa_lib):
-    assert S.sdpa_abi_version() == 4
+    assert S.sdpa_abi_version() == 5
     assert S.sdpa_status_string(0) == "ok"
     assert S.sdpa_status_string(2) == "unsupported problem"
     assert S.sdpa_status_string(99) == "unknown status"
@@ -127,7 +127,7 @@ def test_null_and_misaligned_pointers_rejected(sdpa_lib):
     assert S.sdpa_forward_raw(p, 264, 256, 256, 256, None, None, 0, None) == 3
     assert S.sdpa_forward_raw(p, 256, 256, 256, 258, None, None, 0, None) == 3
     assert S.sdpa_forward_raw(p, 256, 256, 256, 256, 258, None, 0, None) == 3
-    pm = P(mask=8)
+    pm = P(mask=9)  # a mask must be aligned to its element size (2 bytes here)
     assert S.sdpa_forward_raw(pm, 256, 256, 256, 256, None, None, 0, None) == 3
     ps = P(sinks=2)
     assert S.sdpa_forward_raw(ps, 256, 256, 256, 256, None, None, 0, None) == 3
@@ -162,21 +162,42 @@ def test_python_binding_rejects_cpu_tensors(sdpa_lib):
         S.sdpa_forward(q, q, q)
 
 
-def test_host_entry_rejects_unpinned_inputs(sdpa_lib):
+def test_host_entry_rejects_bad_tensors(sdpa_lib):
     torch = pytest.importorskip("torch")
     q = torch.zeros(1, 2, 4, 64, dtype=torch.float16)
     with pytest.raises(ValueError):
-        S.sdpa_forward_host(q, q, q)
+        S.sdpa_forward_host(q[0], q[0], q[0])  # not 4-D
+    with pytest.raises(ValueError):
+        S.sdpa_forward_host(q.transpose(1, 2), q, q)  # not contiguous
 
 
-@pytest.mark.parametrize("nb,hkv,chunks", [(1, 1, 8), (2, 38, 8), (2, 38, 3), (3, 4, 1), (1, 5, 64)])
-def test_host_entry_pieces_cover_every_head_once(nb, hkv, chunks):
-    pieces = B._host_chunks(nb, hkv, chunks)
-    seen = [(b, h) for b, h0, h1 in pieces for h in range(h0, h1)]
-    assert sorted(seen) == [(b, h) for b in range(nb) for h in range(hkv)]
-    assert all(0 <= h0 < h1 <= hkv for _, h0, h1 in pieces)
-    # every batch in about chunks / nb pieces
-    assert len(pieces) == nb * min(hkv, -(-chunks // nb))
+def _align(n):
+    return (n + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("pieces", [1, 3, 8, 64])
+def test_host_staging_size(sdpa_lib, pieces):
+    # prefill (no workspace): device copies of q, k, v, o and lse, each
+    # 256-byte aligned, whatever the number of pieces
+    B_, Hq, Hkv, Lq, Lk, D = 2, 6, 3, 300, 333, 64
+    p = S.make_params(B_, Hq, Hkv, Lq, Lk, D, S.SDPA_F16, 0.125)
+    q = B_ * Hq * Lq * D * 2
+    kv = B_ * Hkv * Lk * D * 2
+    want = 2 * _align(q) + 2 * _align(kv) + _align(B_ * Hq * Lq * 4)
+    assert S.sdpa_host_staging_size(p, pieces) == want
+    # decode: plus two workspaces of the widest piece, which shrink as the
+    # pieces get narrower
+    d1 = S.sdpa_host_staging_size(S.make_params(2, 32, 8, 1, 32768, 128, S.SDPA_BF16, 0.088), 1)
+    d8 = S.sdpa_host_staging_size(S.make_params(2, 32, 8, 1, 32768, 128, S.SDPA_BF16, 0.088), 8)
+    assert d1 > d8 > 0
+
+
+def test_host_entry_rejects_strided_problems(sdpa_lib):
+    p = S.make_params(1, 4, 2, 300, 300, 64, S.SDPA_F16, 0.125, kv_capacity=512)
+    assert S.sdpa_host_staging_size(p, 4) == 0
+    lib = sdpa_lib
+    assert lib.sdpa_forward_host(ctypes.byref(p), 256, 256, 256, 256, None, 256, 1 << 30, 4,
+                                 None) == 2  # SDPA_ERR_UNSUPPORTED, before any CUDA call
 
 
 def test_flags_are_checked(sdpa_lib):

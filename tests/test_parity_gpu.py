@@ -90,6 +90,22 @@ def sample_rows(w, n_random=400, tail=160, seed=7):
     return np.unique(np.array(picks, dtype=np.int64))
 
 
+@pytest.fixture
+def hooks():
+    """Set library test hooks (sdpa_debug_set_option by name); each hook the
+    test touches gets its previous value back afterwards."""
+    import scaled_dot_product_fwd_gb300 as S
+    saved = {}
+
+    def set_hook(name, value):
+        prev = S.sdpa_debug_set_option(name, int(value))
+        saved.setdefault(name, prev)
+
+    yield set_hook
+    for name, prev in saved.items():
+        S.sdpa_debug_set_option(name, prev)
+
+
 def wl(B, Hq, Hkv, Lq, Lk, D, dtype, **kw):
     name = "case_%d_%d_%d_%d_%d_%d_%s" % (B, Hq, Hkv, Lq, Lk, D, dtype)
     return W.Workload(name, B, Hq, Hkv, Lq, Lk, D, dtype, **kw)
@@ -201,28 +217,28 @@ def test_decode_sweep(cuda, dtype, D, G, Lk):
     check(cuda, wl(2, Hkv * G, Hkv, 1, Lk, D, dtype, sinks=(Lk % 2 == 1)))
 
 
-@pytest.mark.parametrize("cluster", ["1", "0"])
+@pytest.mark.parametrize("cluster", [1, 0])
 @pytest.mark.parametrize("splits", [1, 2, 4, 5, 8, 16, 64])
-def test_decode_forced_splits(cuda, splits, cluster, monkeypatch):
+def test_decode_forced_splits(cuda, splits, cluster, hooks):
     """Split counts that a thread-block cluster merges (2, 4, 8, 16) and ones
     that go through the combine kernel; cluster "0" forces the two-pass form."""
-    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", str(splits))
-    monkeypatch.setenv("GB300_SDPA_DECODE_CLUSTER", cluster)
+    hooks("decode_splits", splits)
+    hooks("decode_cluster", cluster)
     check(cuda, wl(1, 8, 1, 1, 3001, 128, "bfloat16", sinks=True))
 
 
 @pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
 @pytest.mark.parametrize("splits", [2, 16])
-def test_decode_d512_cluster_merge_matches_two_pass(cuda, dtype, splits, monkeypatch):
+def test_decode_d512_cluster_merge_matches_two_pass(cuda, dtype, splits, hooks):
     """The in-cluster merge and the combine kernel give the same result on the
     head_dim 512 GQA-8 shape with sinks (both against the oracle too)."""
     import torch
-    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", str(splits))
+    hooks("decode_splits", splits)
     w = wl(2, 32, 4, 1, 1024, 512, dtype, sinks=True)
     inp = W.make_inputs(w)
     outs = []
-    for cl in ("1", "0"):
-        monkeypatch.setenv("GB300_SDPA_DECODE_CLUSTER", cl)
+    for cl in (1, 0):
+        hooks("decode_cluster", cl)
         outs.append(run_gpu(torch, w, inp))
     o_ref, lse_ref = oracle_rows(w, inp, None)
     for o_gpu, lse_gpu in outs:
@@ -273,7 +289,7 @@ def test_bottom_right_causal_lq_lt_lk(cuda):
     check(cuda, wl(1, 4, 2, 200, 1000, 128, "bfloat16", causal=True))
 
 
-def test_wait_timeout_reports_status(cuda, monkeypatch):
+def test_wait_timeout_reports_status(cuda, hooks):
     """A device wait that runs out sets the status word; the context stays
     usable.  The failure is made on the host: the decode producer is told to
     drop its last copy, so the consumers' bounded wait on it expires."""
@@ -282,15 +298,15 @@ def test_wait_timeout_reports_status(cuda, monkeypatch):
     w = wl(1, 4, 1, 1, 640, 128, "bfloat16")
     inp = W.make_inputs(w)
     q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
-    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", "1")
-    monkeypatch.setenv("GB300_SDPA_DEBUG_DROP_LAST_TILE", "1")
+    hooks("decode_splits", 1)
+    hooks("decode_drop_last", 1)
     old = S.sdpa_debug_set_wait_limit_ns(50_000_000)
     try:
         S.sdpa_forward(q, k, v)
         assert S.sdpa_device_status() == 6  # SDPA_ERR_TIMEOUT
     finally:
         S.sdpa_debug_set_wait_limit_ns(old)
-        monkeypatch.delenv("GB300_SDPA_DEBUG_DROP_LAST_TILE")
+        hooks("decode_drop_last", 0)
     assert S.sdpa_device_status() == 0  # cleared by the read
     check(torch, w)  # the context still works
 
@@ -298,10 +314,11 @@ def test_wait_timeout_reports_status(cuda, monkeypatch):
 # ------------------------------------------------------ host-buffer entry point
 @pytest.mark.parametrize("case", ["f16_mha", "bf16_gqa_causal_sinks", "f32_hilo"])
 def test_host_entry_matches_device_entry(cuda, case):
-    """sdpa_forward_host (pinned host buffers, pieces on several streams) gives
-    the same bytes as sdpa_forward on device buffers: every (b, h) is computed
-    by the same kernel either way (the fp32 case also checks that the two
-    compute streams do not share a workspace)."""
+    """sdpa_forward_host (the C call: pinned host buffers, pieces on the
+    library's streams) gives the same bytes as sdpa_forward on device
+    buffers: every (b, h) is computed by the same kernel either way (the fp32
+    case also checks that the two compute streams do not share a
+    workspace)."""
     import torch
     import scaled_dot_product_fwd_gb300 as S
     w = {"f16_mha": wl(2, 6, 6, 300, 300, 64, "float16"),
@@ -314,12 +331,12 @@ def test_host_entry_matches_device_entry(cuda, case):
     torch.cuda.synchronize()
     o_h = torch.empty_like(q).pin_memory()
     l_h = torch.empty(q.shape[:3], dtype=torch.float32).pin_memory()
-    # first call: eager run plus graph capture; second: graph replay; third: no graph
-    for graph in (True, True, False):
+    # the C call sdpa_forward_host (through ctypes), twice on the same buffers
+    for _ in range(2):
         o_h.zero_()
         l_h.zero_()
         S.sdpa_forward_host(q, k, v, scale=w.scale, causal=w.causal, sinks=s, out=o_h, lse=l_h,
-                            chunks=5, graph=graph)
+                            chunks=5)
         torch.cuda.synchronize()
         assert S.sdpa_device_status() == 0
         assert torch.equal(o_h, o_d.cpu())
@@ -333,6 +350,24 @@ def test_host_entry_decode_against_oracle(cuda):
     inp = W.make_inputs(w)
     q, k, v = (inp[x].pin_memory() for x in ("q", "k", "v"))
     o_h, l_h = S.sdpa_forward_host(q, k, v, scale=w.scale, sinks=inp["sinks"].cuda(), chunks=4)
+    torch.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    o_ref, lse_ref = oracle_rows(w, inp, None)
+    compare(w, o_h, l_h, o_ref, lse_ref, None)
+
+
+@pytest.mark.parametrize("mask", ["key", "full", "bool_key"])
+def test_host_entry_masks_against_oracle(cuda, mask):
+    """The C host-buffer call with masks: each piece reads the mask from its
+    own (batch, head) offset (element-aligned, not 16-byte aligned for 333
+    keys)."""
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    w = wl(2, 8, 4, 150, 333, 64, "float16", mask=mask, causal=True)
+    inp = W.make_inputs(w)
+    q, k, v = (inp[x].pin_memory() for x in ("q", "k", "v"))
+    o_h, l_h = S.sdpa_forward_host(q, k, v, scale=w.scale, causal=True, mask=inp["mask"].cuda(),
+                                   chunks=6)
     torch.cuda.synchronize()
     assert S.sdpa_device_status() == 0
     o_ref, lse_ref = oracle_rows(w, inp, None)
@@ -372,13 +407,13 @@ def test_multi_query_fully_masked_rows(cuda):
 
 
 @pytest.mark.parametrize("splits", [2, 16])
-def test_multi_query_forced_splits(cuda, splits, monkeypatch):
-    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", str(splits))
+def test_multi_query_forced_splits(cuda, splits, hooks):
+    hooks("decode_splits", splits)
     check(cuda, wl(1, 16, 2, 2, 3001, 128, "bfloat16", causal=True, sinks=True))
     check(cuda, wl(1, 8, 1, 6, 3001, 512, "bfloat16", causal=True, sinks=True))
 
 
-def test_launch_count_reports_kernels_per_call(cuda, monkeypatch):
+def test_launch_count_reports_kernels_per_call(cuda, hooks):
     """sdpa_last_launch_count: 1 for prefill, 2 for the fp32 hi/lo prefill
     (split + prefill), 1 or 2 for decode (in-cluster merge or combine pass),
     1 for no keys, 0 after an error or an empty problem."""
@@ -394,12 +429,12 @@ def test_launch_count_reports_kernels_per_call(cuda, monkeypatch):
 
     assert run(wl(1, 2, 2, 300, 300, 64, "float16")) == 1
     assert run(wl(1, 2, 2, 300, 300, 64, "float32")) == 2
-    monkeypatch.setenv("GB300_SDPA_DECODE_SPLITS", "4")
+    hooks("decode_splits", 4)
     assert run(wl(1, 8, 1, 1, 4096, 128, "bfloat16")) == 1  # 4 CTAs per cluster
-    monkeypatch.setenv("GB300_SDPA_DECODE_CLUSTER", "0")
+    hooks("decode_cluster", 0)
     assert run(wl(1, 8, 1, 1, 4096, 128, "bfloat16")) == 2
-    monkeypatch.delenv("GB300_SDPA_DECODE_CLUSTER")
-    monkeypatch.delenv("GB300_SDPA_DECODE_SPLITS")
+    hooks("decode_cluster", 1)
+    hooks("decode_splits", 0)
     q = torch.zeros(1, 2, 4, 64, device="cuda", dtype=torch.float16)
     kk = torch.zeros(1, 2, 0, 64, device="cuda", dtype=torch.float16)
     S.sdpa_forward(q, kk, kk)
@@ -500,21 +535,21 @@ SPLIT_CASES = {
 }
 
 
-@pytest.mark.parametrize("ksplit", ["2", "4"])
+@pytest.mark.parametrize("ksplit", [2, 4])
 @pytest.mark.parametrize("case", sorted(SPLIT_CASES))
-def test_prefill_forced_split(cuda, ksplit, case, monkeypatch):
+def test_prefill_forced_split(cuda, ksplit, case, hooks):
     """Every query-block unit split over its key tiles among the 2 or 4 CTAs
     of a cluster, the partial results merged through distributed shared
     memory (the form the last partial wave of units takes)."""
-    monkeypatch.setenv("GB300_SDPA_PREFILL_SPLIT", ksplit)
+    hooks("prefill_split", ksplit)
     check(cuda, SPLIT_CASES[case])
 
 
-@pytest.mark.parametrize("ksplit", ["2", "4"])
-def test_prefill_forced_split_kv_view(cuda, ksplit, monkeypatch):
+@pytest.mark.parametrize("ksplit", [2, 4])
+def test_prefill_forced_split_kv_view(cuda, ksplit, hooks):
     """Split units with per-batch key lengths (some batches shorter than the
     split count in key tiles, one with no key at all)."""
-    monkeypatch.setenv("GB300_SDPA_PREFILL_SPLIT", ksplit)
+    hooks("prefill_split", ksplit)
     _kv_view_check(3, 4, 2, 260, 600, 700, 64, "float16", False, sinks=True,
                    lens_q=[260, 150, 0], lens_kv=[600, 100, 0])
 
@@ -675,11 +710,11 @@ def _bshd(t):
     return t.transpose(1, 2).contiguous().transpose(1, 2)
 
 
-def _strided_check(w, layout, monkeypatch=None, split=None):
+def _strided_check(w, layout, hooks=None, split=None):
     import torch
     import scaled_dot_product_fwd_gb300 as S
     if split is not None:
-        monkeypatch.setenv("GB300_SDPA_PREFILL_SPLIT", split)
+        hooks("prefill_split", split)
     inp = W.make_inputs(w)
     q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
     mask = None if inp["mask"] is None else inp["mask"].cuda()
@@ -731,11 +766,11 @@ def test_strided_layouts(cuda, case, layout):
     _strided_check(STRIDE_CASES[case], layout)
 
 
-@pytest.mark.parametrize("split", ["2", "4"])
-def test_strided_output_split_units(cuda, split, monkeypatch):
+@pytest.mark.parametrize("split", [2, 4])
+def test_strided_output_split_units(cuda, split, hooks):
     """Split units (partial results merged in the cluster) writing a strided
     output."""
-    _strided_check(wl(1, 4, 2, 300, 1000, 64, "float16"), "kv_cache_bshd", monkeypatch, split)
+    _strided_check(wl(1, 4, 2, 300, 1000, 64, "float16"), "kv_cache_bshd", hooks, split)
 
 
 def test_strided_no_keys(cuda):
