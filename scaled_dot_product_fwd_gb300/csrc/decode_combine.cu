@@ -126,6 +126,8 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   int hg = 1;
   while (hg < G && hg < hg_max) hg <<= 1;
   const int groups = (G + hg - 1) / hg;
+  // the grid's y dimension holds (kv head, head group) pairs, z the batch
+  if (static_cast<long long>(p.num_kv_heads) * groups > 65535 || p.batch > 65535) return false;
   const int kb = dec::keys_per_warp(es, D, hg);
   const int tk = dec::kConsumerWarps * kb;
   const int stage_bytes = 2 * tk * D * es;

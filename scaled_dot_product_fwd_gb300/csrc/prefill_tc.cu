@@ -58,6 +58,7 @@ sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const voi
   sdpa_status_t st = SDPA_ERR_UNSUPPORTED;
   if (p.head_dim == 64) st = launch_prefill_tc_d64(p, q, k, v, o, lse, env, &g);
   if (p.head_dim == 128) st = launch_prefill_tc_d128(p, q, k, v, o, lse, env, &g);
+  if (p.head_dim == 512) st = launch_prefill_tc_d512(p, q, k, v, o, lse, env, &g);
   if (st == SDPA_OK) set_last_launches(g);
   return st;
 }

@@ -1517,5 +1517,9 @@ sdpa_status_t launch_prefill_tc_d64(const sdpa_params_t& p, const void* q, const
 sdpa_status_t launch_prefill_tc_d128(const sdpa_params_t& p, const void* q, const void* k,
                                      const void* v, void* o, float* lse, const LaunchEnv& env,
                                      int* grids);
+// head_dim 512, fp16/bf16 (prefill_d512.cu)
+sdpa_status_t launch_prefill_tc_d512(const sdpa_params_t& p, const void* q, const void* k,
+                                     const void* v, void* o, float* lse, const LaunchEnv& env,
+                                     int* grids);
 
 }  // namespace gb300

@@ -7,11 +7,12 @@
 // chooses between a fused graph and the sdpa_vector kernel) without any
 // fallback: a single query row (Lq = 1), or a few (the rows of a kv head then
 // share its K/V stream: up to 2 at D = 64/128, where the tensor-core tiles
-// are ahead from 4 rows on, measured on GB300; up to 8 at D = 512, which has
-// no prefill kernel), takes the split-KV vector path of MLX PR #4459, every
-// other shape takes the fused prefill kernel for its dtype, and anything else
-// is reported as unsupported (the force_fused admission check of the same PR
-// raises instead of falling back).
+// are ahead from 4 rows on, measured on GB300; up to 8 at D = 512), takes the
+// split-KV vector path of MLX PR #4459, every other shape takes the fused
+// prefill kernel for its dtype (fp32 at D = 512: the vector path with its
+// rows grouped, fp32 products and sums), and anything else is reported as
+// unsupported (the force_fused admission check of the same PR raises instead
+// of falling back).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stddef.h>
@@ -78,8 +79,14 @@ sdpa_status_t validate_problem(const sdpa_params_t* p) {
   // cuDNN's bottom-right causal mask is undefined for Tq > Tkv (mlx 0.30.7
   // supports_sdpa_cudnn); the same rule holds here.
   if (p->causal && p->seq_len_q > p->seq_len_kv) return SDPA_ERR_UNSUPPORTED;
-  // head_dim 512 is served by the vector path only (up to 8 query rows).
-  if (p->head_dim == 512 && p->seq_len_q > kMaxDecodeRows) return SDPA_ERR_UNSUPPORTED;
+  // fp32 at head_dim 512 with many rows runs on the vector path, whose grid
+  // holds (kv head, group of 4 rows) pairs in its y dimension (<= 65535)
+  if (p->dtype == SDPA_F32 && p->head_dim == 512 && p->seq_len_q > kMaxDecodeRows &&
+      p->num_kv_heads > 0) {
+    const int64_t rows = static_cast<int64_t>(p->num_q_heads / p->num_kv_heads) * p->seq_len_q;
+    if (static_cast<int64_t>(p->num_kv_heads) * ((rows + 3) / 4) > 65535)
+      return SDPA_ERR_UNSUPPORTED;
+  }
   return SDPA_OK;
 }
 
@@ -121,6 +128,9 @@ sdpa_kernel_t pick(const sdpa_params_t* p) {
   if (p->seq_len_kv == 0) return SDPA_KERNEL_NO_KEYS;
   if (p->seq_len_q <= (p->head_dim == 512 ? kMaxDecodeRows : kMaxDecodeRowsTc))
     return SDPA_KERNEL_DECODE_SPLITKV;
+  // fp32 at head_dim 512: the vector path for any number of rows (fp32
+  // products and sums); fp16/bf16: the head-dim-512 tensor-core prefill
+  if (p->dtype == SDPA_F32 && p->head_dim == 512) return SDPA_KERNEL_DECODE_SPLITKV;
   if (p->dtype == SDPA_F32)
     return p->head_dim == 64 ? SDPA_KERNEL_PREFILL_TC_F32 : SDPA_KERNEL_PREFILL_F32;
   return SDPA_KERNEL_PREFILL_TC;

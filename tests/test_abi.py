@@ -81,6 +81,9 @@ def P(**kw):
     (dict(Lq=2), "decode_splitkv"),
     (dict(Lq=3), "prefill_tc"),
     (dict(Lq=8, D=512, causal=True), "decode_splitkv"),
+    (dict(Lq=9, D=512), "prefill_tc"),
+    (dict(Lq=4096, Lk=4096, D=512, dtype=S.SDPA_BF16, causal=True), "prefill_tc"),
+    (dict(Lq=9, D=512, dtype=S.SDPA_F32), "decode_splitkv"),
     (dict(Lq=3, dtype=S.SDPA_F32), "prefill_tc_f32"),
     (dict(Lk=0), "no_keys"),
     (dict(Lq=1, Lk=0, D=512), "no_keys"),
@@ -103,7 +106,9 @@ def test_select_kernel(sdpa_lib, kw, kernel):
     (dict(scale=float("inf")), 1),
     (dict(D=96), 2),
     (dict(D=256), 2),
-    (dict(D=512, Lq=9), 2),
+    # fp32 at head_dim 512 on the vector path: (kv head, row group) pairs
+    # past the grid's 65535
+    (dict(D=512, Lq=1 << 17, Lk=1 << 17, Hq=4, Hkv=2, dtype=S.SDPA_F32), 2),
     (dict(Lq=64, Lk=32, causal=True), 2),
     (dict(Lq=(1 << 30) + 1), 2),
     (dict(mask=16, ms=(0, 0, 32, 2)), 1),

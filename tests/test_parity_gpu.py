@@ -844,3 +844,49 @@ def test_lowest_finite_mask(cuda, dtype, D, kind, Lq, Lk):
     assert np.all(np.abs(lg[mid] - lse_ref[mid]) <= 1e-6 * np.abs(lse_ref[mid]))
     hug = big & ~mid
     assert np.allclose(lg[hug], -(2.0 ** 100) * w.scale, rtol=1e-5, atol=0)
+
+
+# ------------------------------------------------ head_dim 512 with many query rows
+D512_CASES = [(9, 300), (129, 333), (1024, 1024)]
+
+
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16", "float32"])
+@pytest.mark.parametrize("Lq,Lk", D512_CASES, ids=lambda c: str(c))
+@pytest.mark.parametrize("causal", [False, True])
+def test_d512_prefill(cuda, dtype, Lq, Lk, causal):
+    """head_dim 512 beyond the vector path's 8 rows: the tensor-core kernel
+    (fp16/bf16; two CTAs per query tile, one per half of O) or the vector
+    path with grouped rows (fp32); GQA-8 with sinks, every row compared."""
+    w = wl(1, 8, 1, Lq, Lk, 512, dtype, causal=causal, sinks=True)
+    check(cuda, w)
+
+
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16"])
+@pytest.mark.parametrize("mask", ["key", "full", "bool_key", "bool_full"])
+def test_d512_prefill_masks(cuda, dtype, mask):
+    check(cuda, wl(2, 4, 2, 150, 333, 512, dtype, mask=mask, causal=True))
+
+
+def test_d512_prefill_strided_and_lengths(cuda):
+    """[B, L, H, D] q, k, v (strides) and per-batch lengths at head_dim 512."""
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    B, Hq, Hkv, Lq, Lk, D = 2, 4, 2, 200, 300, 512
+    w = wl(B, Hq, Hkv, Lq, Lk, D, "bfloat16", causal=True)
+    inp = W.make_inputs(w)
+    q, k, v = (_bshd(inp[x].cuda()) for x in ("q", "k", "v"))
+    lq = torch.tensor([200, 131], dtype=torch.int32, device="cuda")
+    lk = torch.tensor([300, 190], dtype=torch.int32, device="cuda")
+    o, lse = S.sdpa_forward(q, k, v, scale=w.scale, causal=True, seq_lens_q=lq, seq_lens_kv=lk)
+    torch.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    f = W.as_float64
+    for b in range(B):
+        nq, nk = int(lq[b]), int(lk[b])
+        o_ref, lse_ref = O.sdpa(f(inp["q"][b:b + 1, :, :nq]), f(inp["k"][b:b + 1, :, :nk]),
+                                f(inp["v"][b:b + 1, :, :nk]), w.scale, True, None, None)
+        og = f(o[b:b + 1, :, :nq].cpu())
+        assert np.abs(og - o_ref).max() <= TOL["bfloat16"]
+        assert np.abs(lse[b:b + 1, :, :nq].cpu().double().numpy() - lse_ref).max() <= LSE_TOL
+        # rows past the batch's query length see no key
+        assert torch.all(o[b, :, nq:] == 0) and torch.all(torch.isneginf(lse[b, :, nq:]))
