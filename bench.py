@@ -88,7 +88,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -162,22 +162,33 @@ def gpu_inputs(torch, w, copies, device):
     return base, sets
 
 
-def time_device(torch, fn, nsets, steps, warmup, stream):
-    """fn(i) launches step i (input set i % nsets); seconds of `steps` calls."""
+def time_device(torch, fn, nsets, steps, warmup, stream, windows=None):
+    """fn(i) launches step i (input set i % nsets); seconds of `steps` calls.
+
+    With `windows` (a list), events recorded between groups of steps (up to
+    10 groups) append each group's milliseconds per step to it; the total
+    stays the time of exactly `steps` back-to-back calls."""
     for i in range(warmup):
         fn(i % nsets)
     torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(steps):
-        fn(i % nsets)
-    stop.record(stream)
+    nwin = min(10, steps) if windows is not None else 1
+    bounds = [steps * g // nwin for g in range(nwin + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nwin + 1)]
+    evs[0].record(stream)
+    for g in range(nwin):
+        for i in range(bounds[g], bounds[g + 1]):
+            fn(i % nsets)
+        evs[g + 1].record(stream)
     torch.cuda.synchronize()
-    return start.elapsed_time(stop) / 1e3  # seconds
+    if windows is not None:
+        for g in range(nwin):
+            n = bounds[g + 1] - bounds[g]
+            if n > 0:
+                windows.append(evs[g].elapsed_time(evs[g + 1]) / n)
+    return evs[0].elapsed_time(evs[-1]) / 1e3  # seconds
 
 
-def run_workload(torch, S, w, steps, warmup, device, stream, copies=None):
+def run_workload(torch, S, w, steps, warmup, device, stream, copies=None, windows=None):
     """Device-timed seconds for `steps` calls on rotating input copies."""
     es = 4 if w.dtype == "float32" else 2
     per = (w.B * w.Hq * w.Lq * w.D + 2 * w.B * w.Hkv * w.Lk * w.D) * es
@@ -193,7 +204,7 @@ def run_workload(torch, S, w, steps, warmup, device, stream, copies=None):
         S.sdpa_forward(s["q"], s["k"], s["v"], scale=w.scale, causal=w.causal,
                        sinks=s["sinks"], out=outs[i], lse=lses[i])
 
-    secs = time_device(torch, fn, len(sets), steps, warmup, stream)
+    secs = time_device(torch, fn, len(sets), steps, warmup, stream, windows)
     launches = S.sdpa_last_launch_count()  # kernels per call, from the library
     if S.sdpa_device_status() != 0:
         raise RuntimeError("device status set during %s" % w.name)
@@ -274,8 +285,31 @@ def work_per_row(w, total_rows):
     return w.flops() / total_rows, 1e12, "TFLOP/s"
 
 
+def cpu_model():
+    """The host CPU's model name (x86 /proc/cpuinfo 'model name', or the Arm
+    implementer/part fields), else the platform's processor string."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model"):
+            for ln in info.splitlines():
+                if ln.split(":")[0].strip() == key:
+                    return ln.split(":", 1)[1].strip()
+        impl = [ln.split(":", 1)[1].strip() for ln in info.splitlines()
+                if ln.startswith("CPU implementer")]
+        part = [ln.split(":", 1)[1].strip() for ln in info.splitlines()
+                if ln.startswith("CPU part")]
+        if impl and part:
+            return "Arm implementer %s part %s" % (impl[0], part[0])
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w, target_s=12.0):
-    """The float64 oracle on this host's cores over a bounded row sample."""
+    """The float64 oracle on this host's cores over a bounded row sample,
+    plus one thread on a smaller sample (rows per second per core)."""
     import numpy as np
 
     from oracle import oracle as orc
@@ -296,16 +330,30 @@ def cpu_baseline(w, target_s=12.0):
         elapsed += dt
         n = min(total, int(n * max(2.0, 1.5 * (target_s - elapsed) / max(dt, 1e-3))))
     rate = done * work_row / elapsed
-    return {"value": rate / scale, "unit": unit, "cores": orc.num_threads(),
-            "kind": "oracle",
-            "sample": "%d random query rows of %s (all keys each), %.1f s" % (done, w.name, elapsed)}
+    cores = orc.num_threads()
+    # one thread, about 2 s
+    orc.set_num_threads(1)
+    try:
+        rows1 = max(8, min(total, int(2.0 * done / elapsed / max(cores, 1))))
+        t0 = time.perf_counter()
+        orc.sdpa(q, k, v, w.scale, w.causal, rows=rng.integers(0, total, size=rows1))
+        t1 = time.perf_counter() - t0
+    finally:
+        orc.set_num_threads(cores)
+    return {"value": rate / scale, "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": "%d random query rows of %s (all keys each), %.1f s" % (done, w.name, elapsed),
+            "cpu_model": cpu_model(),
+            "single_thread": {"rows_per_s": round(rows1 / t1, 2),
+                              "value": rows1 * work_row / t1 / scale, "unit": unit,
+                              "sample": "%d random rows, %.1f s" % (rows1, t1)},
+            "timer": "time.perf_counter around the oracle's C call"}
 
 
 def secondary(torch, S, device, stream, peaks):
     """Other workloads, device-timed (for context; not the headline)."""
     from scaled_dot_product_fwd_gb300 import workloads as W
     out = {}
-    for w, steps in ((W.CAUSAL_GQA, 100), (W.DIT_F32, 20)):
+    for w, steps in ((W.CAUSAL_GQA, 100), (W.DIT_F32, 20), (W.PREFILL_D512, 20)):
         secs, copies, _, _ = run_workload(torch, S, w, steps, 3, device, stream)
         t = w.flops() * steps / secs / 1e12
         out[w.name] = {"value": round(t, 2), "unit": "TFLOP/s", "ms_per_call": secs / steps * 1e3,
@@ -534,9 +582,10 @@ def gb300_arm(args):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    windows = []
     with ClockSampler(local) as clk:
         secs, copies, per, per_call_launches = run_workload(torch, S, w, args.steps, args.warmup,
-                                                            device, stream)
+                                                            device, stream, windows=windows)
     secs = max_over_ranks(dist, secs, device)
     if dist is not None:
         dist.barrier()
@@ -579,6 +628,11 @@ def gb300_arm(args):
                        copies, copies * per // 10**6),
                    "parallelism": "replicas" if world > 1 else "single"},
         "gpu_launches": launches,
+        "step_ms_spread": {"windows": len(windows),
+                           "median": round(statistics.median(windows), 5),
+                           "min": round(min(windows), 5), "max": round(max(windows), 5),
+                           "note": "ms per step of each of up to 10 consecutive groups of "
+                                   "the K timed steps (same run as value)"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2),
                      "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4),

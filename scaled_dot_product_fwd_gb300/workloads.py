@@ -71,8 +71,12 @@ DECODE_D512 = {
     for b in (1, 2) for dt in ("bfloat16", "float16", "float32") for s in (False, True)
 }
 DECODE_LONG = Workload("decode_long_b8_kl32768_d128_bf16", 8, 32, 8, 1, 32768, 128, "bfloat16")
+# The D512 decode workload's heads (32 query heads over 4 KV heads, head_dim
+# 512) over a 4096-token prompt: the prefill that precedes that decode.
+PREFILL_D512 = Workload("prefill_d512_b1_h32_kv4_l4096_bf16_causal", 1, 32, 4, 4096, 4096, 512,
+                        "bfloat16", causal=True)
 
-NAMED = {w.name: w for w in [TINY, DIT_F16, DIT_F32, CAUSAL_GQA, DECODE_LONG,
+NAMED = {w.name: w for w in [TINY, DIT_F16, DIT_F32, CAUSAL_GQA, DECODE_LONG, PREFILL_D512,
                              *DECODE_D512.values()]}
 
 
