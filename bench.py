@@ -607,6 +607,8 @@ def gb300_arm(args):
         sustained = peaks["bf16_tflops_sustained"]
         if w.dtype == "float32" and w.D != 64:  # fp32 FMA tiles
             traffic = profile_traffic("prefill_f32_" + w.name, ["prefill_f32.cu"])
+        elif w.D == 512:  # two CTAs per query tile, each half of O
+            traffic = profile_traffic("prefill_d512_" + w.name, ["prefill_d512.cu", "ptx.cuh"])
         else:  # tensor-core kernel (fp32 at D = 64 as bf16 hi/lo parts)
             tu = "prefill_tc.cu" if w.dtype == "float32" else "prefill_tc_d%d.cu" % w.D
             traffic = profile_traffic("prefill_tc_" + w.name, ["prefill_tc.cuh", tu, "ptx.cuh"])

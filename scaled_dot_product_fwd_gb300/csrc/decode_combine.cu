@@ -118,6 +118,8 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
 bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
+  if (decode_tc_plan(p, num_sms, out)) return true;
+  out->tc = false;
   const int es = elem_bytes(p.dtype);
   const int D = p.head_dim;
   // rows per kv head: its G query heads times Lq query rows
@@ -197,14 +199,11 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   return true;
 }
 
-sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
-                            const void* k, const void* v, void* o, float* lse, void* workspace,
-                            const LaunchEnv& env) {
-  const size_t rows =
-      static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * plan.num_splits;
-  float* ws_o = static_cast<float*>(workspace);
-  float* ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                          align256(rows * p.head_dim * sizeof(float)));
+// The vector split pass (any head_dim, dtype and head group).
+static sdpa_status_t launch_vector(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
+                                   const void* k, const void* v, void* o, float* lse,
+                                   float* ws_o, float* ws_ml, const LaunchEnv& env,
+                                   bool* merged) {
   dec::SplitArgs a;
   a.q = q;
   a.k = k;
@@ -250,14 +249,29 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   a.status = env.status;
   a.wait_ns = env.wait_limit_ns;
   a.debug_drop_last = debug_option(SDPA_DEBUG_DECODE_DROP_LAST) == 1 ? 1 : 0;
-  sdpa_status_t st;
-  bool merged = false;
   const int D = p.head_dim, hg = plan.head_group;
   switch (p.dtype) {
-    case SDPA_F32: st = dec::launch_split_f32(a, D, hg, p.batch, env.stream, &merged); break;
-    case SDPA_F16: st = dec::launch_split_f16(a, D, hg, p.batch, env.stream, &merged); break;
-    case SDPA_BF16: st = dec::launch_split_bf16(a, D, hg, p.batch, env.stream, &merged); break;
+    case SDPA_F32: return dec::launch_split_f32(a, D, hg, p.batch, env.stream, merged);
+    case SDPA_F16: return dec::launch_split_f16(a, D, hg, p.batch, env.stream, merged);
+    case SDPA_BF16: return dec::launch_split_bf16(a, D, hg, p.batch, env.stream, merged);
     default: return SDPA_ERR_UNSUPPORTED;
+  }
+}
+
+sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
+                            const void* k, const void* v, void* o, float* lse, void* workspace,
+                            const LaunchEnv& env) {
+  const size_t rows =
+      static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * plan.num_splits;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                          align256(rows * p.head_dim * sizeof(float)));
+  sdpa_status_t st;
+  bool merged = false;
+  if (plan.tc) {
+    st = launch_decode_tc(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, &merged);
+  } else {
+    st = launch_vector(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, &merged);
   }
   if (st != SDPA_OK) return st;
   if (merged) {

@@ -30,9 +30,17 @@ struct DecodePlan {
   bool cluster;     // merge the splits inside a thread-block cluster when it
                     // can be resident (else the combine pass does)
   size_t workspace; // bytes of partial results (also reserved for clusters)
+  bool tc = false;  // head_dim 512, fp16/bf16, up to 16 rows per kv head: the
+                    // tensor-core pass (head_group = rows, tile_keys = 128)
 };
 
 bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);
+// The tensor-core head_dim-512 part of the plan (false: not such a problem)
+// and its launch; *merged is false when the combine pass must follow.
+bool decode_tc_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);
+sdpa_status_t launch_decode_tc(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
+                               const void* k, const void* v, void* o, float* lse, float* ws_o,
+                               float* ws_ml, const LaunchEnv& env, bool* merged);
 
 // Device status word of the current device (nullptr if there is no device)
 // and the current bound on device-side waits; both owned by sdpa_api.cu.

@@ -27,4 +27,12 @@ bool encode_tiled_4d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ba
                      uint64_t row_stride, uint64_t head_stride, uint64_t batch_stride,
                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
+// The same with a box of box_heads heads (128-byte swizzle): the box lands
+// as box_heads x box_rows rows of box_inner elements, heads outermost.
+bool encode_tiled_4d_box(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                         uint64_t inner, uint64_t rows, uint64_t heads, uint64_t batches,
+                         uint32_t elem_bytes, uint32_t box_inner, uint32_t box_rows,
+                         uint32_t box_heads, uint64_t row_stride, uint64_t head_stride,
+                         uint64_t batch_stride);
+
 }  // namespace gb300

@@ -121,6 +121,18 @@ def test_dit_sampled(cuda, w):
     check(cuda, w, sample_rows(w))
 
 
+def test_dit_f32_accuracy_margin(cuda, capsys):
+    """fp32 DiT through the tensor cores (bf16 hi/lo parts, three products per
+    score, P split the same way against V's parts): the largest |dO| against
+    the fp64 oracle on the sampled rows, printed so that the margin to the fp32
+    tolerance is on record, and held to a quarter of that tolerance."""
+    w = W.DIT_F32
+    err = check(cuda, w, sample_rows(w))
+    with capsys.disabled():
+        print("\n%s: max |dO| %.3g (tolerance %.3g)" % (w.name, err, TOL[w.dtype]))
+    assert err <= TOL[w.dtype] / 4
+
+
 def test_causal_gqa_sampled(cuda):
     check(cuda, W.CAUSAL_GQA, sample_rows(W.CAUSAL_GQA, n_random=300, tail=130))
 
