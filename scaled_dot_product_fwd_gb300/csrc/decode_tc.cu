@@ -31,11 +31,12 @@
 // tile as the B operand of the value product, and finally read O^T; since
 // the max is known before any probability is formed, O is never rescaled.
 // The splits' normalised partial outputs and (m, l) of one (half, kv head,
-// batch) merge inside a thread-block cluster when the splits fit one: each
-// split sends its partial with one bulk copy into the shared memory of an
-// extra CTA of the cluster, which waits for them on an mbarrier and merges;
-// else they merge through the workspace and the combine kernel.  A call with
-// one split writes O directly.
+// batch) merge inside a thread-block cluster of the S splits when it can be
+// resident: split r sends column slice q of its partial (with the rows'
+// (m, l)) by bulk copy into CTA q's inbox, and CTA q merges slice q of every
+// row, so the exchange is spread over all S SMs; else they merge through the
+// workspace and the combine kernel.  A call with one split writes O
+// directly.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -54,7 +55,7 @@ constexpr int kN = 16;                   // query rows of a kv head, padded
 constexpr int kMaxTiles = 4;             // key tiles per split (score tiles in TMEM)
 constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 columns of 2 bytes
 constexpr int kSlotBytes = 2 * kChunkBytes;
-constexpr int kRing = 6;                 // one tile's 4 K slots and 2 V slots
+constexpr int kRing = 5;                 // a tile's 4 K slots and its first V slot
 constexpr int kQChunkBytes = kN * 128;   // Q: 8 chunks of kN rows x 64 columns
 constexpr int kQBytes = 8 * kQChunkBytes;
 constexpr int kPChunkBytes = kN * 128;   // P^T of a tile: 2 chunks of kN rows x 64 keys
@@ -67,19 +68,25 @@ constexpr uint32_t kOCol = kMaxTiles * kN;  // O^T blocks after the score tiles
 constexpr int kQOff = 0;
 constexpr int kPOff = kQOff + kQBytes;
 constexpr int kRingOff = kPOff + kMaxTiles * kPBytes;
-constexpr int kBarOff = kRingOff + kRing * kSlotBytes;
-// q_full, full[kRing], empty[kRing], s_full[kMaxTiles], p_ready[kMaxTiles], o_done, drain
-constexpr int kNBars = 1 + 2 * kRing + 2 * kMaxTiles + 2;
+constexpr int kInboxOff = kRingOff + kRing * kSlotBytes;
+constexpr int kInboxBytes = 32 * 1024;   // the cluster merge's incoming slices
+constexpr int kBarOff = kInboxOff + kInboxBytes;
+// q_full, full[kRing], empty[kRing], s_full[kMaxTiles], p_ready[kMaxTiles], o_done,
+// drain, inbox
+constexpr int kNBars = 1 + 2 * kRing + 2 * kMaxTiles + 3;
 constexpr int kMiscOff = kBarOff + kNBars * 8;
 constexpr int kRedOff = kMiscOff + 16;  // two [4 warps][kN] reduction buffers
 constexpr int kSmem = kRedOff + 2 * 4 * kN * 4 + 1024;  // + alignment slack
 static_assert(kSmem <= 232448, "shared memory budget");
 static_assert(kOCol + 2 * kN <= kTmemCols, "TMEM budget");
 static_assert((kPOff % 1024) == 0 && (kRingOff % 1024) == 0, "swizzle atoms 1024-aligned");
-constexpr int kMaxClusterSplits = 8;       // splits merged in a cluster (+1 merging CTA)
-constexpr int kPartBytes = kN * kDH * 4 + 2 * kN * 4;  // a split's partial: [kN][kDH], (m, l)[kN]
-static_assert(kMaxClusterSplits * kPartBytes <= kRing * kSlotBytes, "merge slots");
-static_assert(kPartBytes % 16 == 0, "bulk copy granularity");
+constexpr int kMaxCluster = 16;  // splits merged in a cluster (a power of two)
+// a slice record: R rows x kDH / S columns of a split's partial output, then
+// (m, l) of the kN rows; S records leave and S arrive per CTA
+__host__ __device__ constexpr int slice_bytes(int R, int S) { return R * (kDH / S) * 4 + 2 * kN * 4; }
+static_assert(2 * slice_bytes(kN, 2) <= kInboxBytes && 16 * slice_bytes(kN, 16) <= kInboxBytes,
+              "inbox");
+static_assert(2 * slice_bytes(kN, 2) <= kRing * kSlotBytes, "staging");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -239,8 +246,10 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <bool BF16, int S>
-__device__ __forceinline__ void merge_cta(const Args& a, uint8_t* smem, int kvh, int half, int b);
+template <bool BF16, int NR, int S>
+__device__ __forceinline__ void cluster_merge(const Args& a, uint8_t* smem, int split, int kvh,
+                                              int half, int b, bool ok, const float (&Mr)[NR],
+                                              const float (&Lr)[NR], const float (&ov)[2][NR]);
 
 // NR: rows of a kv head the softmax handles (8 or 16; R <= NR); the products
 // always carry kN = 16 columns.
@@ -265,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_ready = s_full + kMaxTiles;
   uint64_t* o_done = p_ready + kMaxTiles;
   uint64_t* drain = o_done + 1;
+  uint64_t* inbox_full = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
   float* red_m = reinterpret_cast<float*>(smem + kRedOff);  // [4][kN]
@@ -277,18 +287,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int half = blockIdx.y & 1;
   const int b = blockIdx.z;
   const bool clustered = a.mode == kCluster;
-  if (clustered && split == a.num_splits) {
-    switch (a.num_splits) {
-      case 2: merge_cta<BF16, 2>(a, smem, kvh, half, b); break;
-      case 3: merge_cta<BF16, 3>(a, smem, kvh, half, b); break;
-      case 4: merge_cta<BF16, 4>(a, smem, kvh, half, b); break;
-      case 5: merge_cta<BF16, 5>(a, smem, kvh, half, b); break;
-      case 6: merge_cta<BF16, 6>(a, smem, kvh, half, b); break;
-      case 7: merge_cta<BF16, 7>(a, smem, kvh, half, b); break;
-      default: merge_cta<BF16, 8>(a, smem, kvh, half, b); break;
-    }
-    return;
-  }
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -302,6 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(inbox_full, 1);
+    if (clustered)  // every split of the cluster sends this CTA one slice
+      mbar_arrive_expect_tx(inbox_full, static_cast<uint32_t>(
+                                            a.num_splits * slice_bytes(a.R, a.num_splits)));
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -318,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // (nothing of this CTA's needs publishing by this arrive: the merging
-  // CTA's barrier set-up is ordered by its own release)
+  // (the inbox barrier's set-up is ordered by the mbarrier-init fence; the
+  // matching wait comes before the first copy into a peer)
   if (clustered) cluster_arrive_relaxed();
   // Launched with programmatic stream serialization: the next call's CTAs
   // may start their set-up on idle SMs now; global memory is touched only
@@ -646,22 +648,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (a.mode != kCluster) return;
 
-  // ---- splits merged inside the cluster: stage this split's partial output
-  // and (m, l) in the (now idle) ring, then one bulk copy into its slot of
-  // the merging CTA.  The second cluster barrier keeps every CTA alive until
-  // the merging CTA has received all copies (their sources are read until
-  // then).  Every thread meets both barriers, also after a failed wait.
-  float* part = reinterpret_cast<float*>(sRing);  // [R][kDH], then (m, l)[kN]
-  float* pml = part + a.R * kDH;
-  __syncthreads();  // the producer's drain precedes the writes below
+  __syncthreads();  // the producer's drain precedes the staging below
+  switch (a.num_splits) {
+    case 2: cluster_merge<BF16, NR, 2>(a, smem, split, kvh, half, b, ok, Mr, Lr, ov); break;
+    case 4: cluster_merge<BF16, NR, 4>(a, smem, split, kvh, half, b, ok, Mr, Lr, ov); break;
+    case 8: cluster_merge<BF16, NR, 8>(a, smem, split, kvh, half, b, ok, Mr, Lr, ov); break;
+    default: cluster_merge<BF16, NR, 16>(a, smem, split, kvh, half, b, ok, Mr, Lr, ov); break;
+  }
+}
+
+// Splits merged inside the cluster (CTA rank = split r of S).  Each CTA
+// stages its normalised partial output as S slice records (R rows x 256/S
+// columns, then (m, l) of the rows) in its idle ring, sends record q to CTA
+// q's inbox slot r, waits for its own S incoming records and merges column
+// slice r of the half for every row: M = max of the m's (and the sink
+// logit), weights l_s 2^(m_s - M), O = sum of weight x partial / (sum of
+// weights + the sink's), LSE = (M + log2 L) ln 2.  The second cluster
+// barrier keeps every CTA alive until all copies have landed (their sources
+// are read until then).  Every thread meets both cluster barriers, also
+// after a failed wait.
+template <bool BF16, int NR, int S>
+__device__ __forceinline__ void cluster_merge(const Args& a, uint8_t* smem, int split, int kvh,
+                                              int half, int b, bool ok, const float (&Mr)[NR],
+                                              const float (&Lr)[NR], const float (&ov)[2][NR]) {
+  using E = Elem<BF16>;
+  using T = typename E::T;
+  constexpr int W = kDH / S;  // columns of a slice
+  const int RB = slice_bytes(a.R, S);
+  uint8_t* stage = smem + kRingOff;
+  uint8_t* inbox = smem + kInboxOff;
+  uint64_t* inbox_full = reinterpret_cast<uint64_t*>(smem + kBarOff) + 1 + 2 * kRing +
+                         2 * kMaxTiles + 2;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+  const int warp = threadIdx.x >> 5;
   if (warp < 4) {
     const int i = threadIdx.x;
 #pragma unroll
-    for (int c = 0; c < NR; ++c) {
-      if (c < a.R) {
-        part[c * kDH + i] = ok ? ov[0][c] : 0.f;
-        part[c * kDH + 128 + i] = ok ? ov[1][c] : 0.f;
-      }
+    for (int j = 0; j < 2; ++j) {
+      const int d = 128 * j + i;  // column of the half
+      float* rec = reinterpret_cast<float*>(stage + (d / W) * RB) + (d % W);
+#pragma unroll
+      for (int c = 0; c < NR; ++c)
+        if (c < a.R) rec[c * W] = ok ? ov[j][c] : 0.f;
     }
     if (i < kN) {
       float m = -INFINITY, l = 0.f;
@@ -671,64 +699,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = (ok && Lr[c] > 0.f) ? Mr[c] : -INFINITY;
           l = ok ? Lr[c] : 0.f;
         }
-      pml[2 * i] = m;
-      pml[2 * i + 1] = l;
+#pragma unroll
+      for (int q = 0; q < S; ++q) {
+        float* ml = reinterpret_cast<float*>(stage + q * RB + a.R * W * 4);
+        ml[2 * i] = m;
+        ml[2 * i + 1] = l;
+      }
     }
     fence_proxy_async_shared();
   }
   __syncthreads();
-  cluster_wait();
-  if (threadIdx.x == 0) {
-    const uint32_t dst = static_cast<uint32_t>(a.num_splits);
-    const uint32_t bytes = static_cast<uint32_t>(a.R * kDH * 4 + 2 * kN * 4);
-    bulk_copy_to_cluster(cluster_map(sRing + split * kPartBytes, dst), smem_addr(part), bytes,
-                         cluster_map(bars, dst));
+  cluster_wait();  // every inbox barrier of the cluster is set up
+  if (threadIdx.x < S) {
+    const uint32_t q = threadIdx.x;
+    bulk_copy_to_cluster(cluster_map(inbox + split * RB, q), smem_addr(stage + q * RB),
+                         static_cast<uint32_t>(RB), cluster_map(inbox_full, q));
   }
-  __syncwarp();
-  cluster_arrive();
-  cluster_wait();
-}
-
-// The merging CTA of a cluster (block x = S): receives the S splits' partial
-// results of one (half, kv head, batch) and merges them, four head
-// dimensions per task: M = max of the m's (and the sink logit), weights
-// l_s 2^(m_s - M), O = sum of weight x partial / sum of weights (the sink
-// joins the denominator only), LSE = (M + log2 L) ln 2.
-template <bool BF16, int S>
-__device__ __forceinline__ void merge_cta(const Args& a, uint8_t* smem, int kvh, int half, int b) {
-  using E = Elem<BF16>;
-  using T = typename E::T;
-  uint8_t* slots = smem + kRingOff;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
-  const uint32_t bytes = static_cast<uint32_t>(a.R * kDH * 4 + 2 * kN * 4);
-  if (threadIdx.x == 0) {
-    *abort_flag = 0;
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(S) * bytes);
-  }
-  __syncthreads();
-  cluster_arrive();
-  cluster_wait();
-  griddep_launch_dependents();
-  griddep_wait();
   const WaitCtl wc{a.wait_ns, abort_flag, a.status};
   // bounded by the limit only: copies into this CTA must land before it leaves
-  const bool ok = __syncthreads_and(mbar_wait_cluster(bar, 0, wc));
-  cluster_arrive();  // every copy has landed: the splits may leave
-  if (ok) {
-    constexpr int kQ4 = kDH / 4;
+  const bool got = __syncthreads_and(mbar_wait_cluster(inbox_full, 0, wc));
+  cluster_arrive();  // every copy into this CTA has landed
+  const bool aborted = *abort_flag != 0;
+  if (got && !aborted) {
+    constexpr int kQ4 = W / 4;
     for (int task = threadIdx.x; task < a.R * kQ4; task += kThreads) {
       const int c = task / kQ4;
-      const int d = 4 * (task % kQ4);
+      const int w = 4 * (task % kQ4);
       const int hq = kvh * a.G + a.row_h[c];
       float mq[S], lq[S];
       float M = -INFINITY;
 #pragma unroll
       for (int q = 0; q < S; ++q) {
-        const float2 ml = reinterpret_cast<const float2*>(
-            reinterpret_cast<const float*>(slots + q * kPartBytes) + a.R * kDH)[c];
+        const float2 ml =
+            reinterpret_cast<const float2*>(inbox + q * RB + a.R * W * 4)[c];
         mq[q] = ml.x;
         lq[q] = ml.y;
         M = fmaxf(M, mq[q]);
@@ -742,22 +745,21 @@ __device__ __forceinline__ void merge_cta(const Args& a, uint8_t* smem, int kvh,
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < S; ++q) {
-        const float w = (lq[q] > 0.f) ? lq[q] * ex2(mq[q] - M) : 0.f;
-        const float4 v =
-            *reinterpret_cast<const float4*>(slots + q * kPartBytes + (c * kDH + d) * 4);
-        L += w;
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+        const float wq = (lq[q] > 0.f) ? lq[q] * ex2(mq[q] - M) : 0.f;
+        const float4 v = *reinterpret_cast<const float4*>(inbox + q * RB + (c * W + w) * 4);
+        L += wq;
+        acc.x = fmaf(wq, v.x, acc.x);
+        acc.y = fmaf(wq, v.y, acc.y);
+        acc.z = fmaf(wq, v.z, acc.z);
+        acc.w = fmaf(wq, v.w, acc.w);
       }
       if (a.sinks && M != -INFINITY) L += ex2(sk - M);
       const float inv = (L > 0.f) ? rcp(L) : 0.f;
       T* orow = static_cast<T*>(a.o) + b * a.os0 + hq * a.os1 + a.row_q[c] * a.os2 +
-                half * kDH + d;
+                half * kDH + split * W + w;
       *reinterpret_cast<uint2*>(orow) =
           make_uint2(E::pack(acc.x * inv, acc.y * inv), E::pack(acc.z * inv, acc.w * inv));
-      if (half == 0 && d == 0 && a.lse) {
+      if (split == 0 && half == 0 && w == 0 && a.lse) {
         const size_t row = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq + a.row_q[c];
         a.lse[row] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
       }
@@ -772,8 +774,8 @@ namespace {
 // Clusters of `size` CTAs of the kernel that can be resident at once (cached
 // per size; a large number when it cannot be asked, e.g. without a device).
 int max_active_clusters(int size) {
-  static int cache[dtc::kMaxClusterSplits + 2] = {};
-  if (size < 2 || size > dtc::kMaxClusterSplits + 1) return 0;
+  static int cache[dtc::kMaxCluster + 1] = {};
+  if (size < 2 || size > dtc::kMaxCluster) return 0;
   if (cache[size] != 0) return cache[size];
   auto kern = dtc::decode_tc_kernel<true, 8>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dtc::kSmem);
@@ -820,20 +822,25 @@ bool decode_tc_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   if (tiles_per > dtc::kMaxTiles) tiles_per = dtc::kMaxTiles;
   S = (ntiles + tiles_per - 1) / tiles_per;
   if (S < 1) S = 1;
-  // The S splits of one (half, kv head, batch) and a merging CTA form a
-  // cluster when all the plan's clusters can be resident at once; else
-  // fewer, longer splits if that makes them fit (not for a forced count).
+  // The splits of one (half, kv head, batch) form a cluster (2, 4, 8 or 16
+  // CTAs; empty splits past the keys) when all the plan's clusters can be
+  // resident at once: the smallest power of two >= S if that fits, else the
+  // largest smaller one whose splits stay within kMaxTiles tiles (not for a
+  // forced count).
   bool cluster = false;
-  for (int c = S; c >= 2 && c <= dtc::kMaxClusterSplits; --c) {
-    const int tp = (ntiles + c - 1) / c;
-    if (tp > dtc::kMaxTiles) break;
-    if (units <= max_active_clusters(c + 1)) {
-      cluster = true;
-      tiles_per = tp;
-      S = (ntiles + tp - 1) / tp;
-      break;
+  if (S > 1 && S <= dtc::kMaxCluster) {
+    int c = 2;
+    while (c < S) c <<= 1;
+    for (; c >= 2; c >>= 1) {
+      const int tp = (ntiles + c - 1) / c;
+      if (tp <= dtc::kMaxTiles && units <= max_active_clusters(c)) {
+        cluster = true;
+        S = c;
+        tiles_per = tp;
+        break;
+      }
+      if (forced >= 1) break;
     }
-    if (forced >= 1) break;
   }
   out->head_group = R;
   out->num_groups = 1;
@@ -922,8 +929,9 @@ static sdpa_status_t launch_tc(const sdpa_params_t& p, const DecodePlan& plan, c
   // splits and a merging CTA are all resident at once
   const long long nclusters = 2LL * p.num_kv_heads * p.batch;
   const bool clustered = S > 1 && plan.cluster && debug_option(SDPA_DEBUG_DECODE_CLUSTER) != 0 &&
-                         S <= kMaxClusterSplits && nclusters <= max_active_clusters(S + 1);
-  const dim3 grid(static_cast<unsigned>(clustered ? S + 1 : S),
+                         S <= kMaxCluster && (S & (S - 1)) == 0 &&
+                         nclusters <= max_active_clusters(S);
+  const dim3 grid(static_cast<unsigned>(S),
                   static_cast<unsigned>(2 * p.num_kv_heads), static_cast<unsigned>(p.batch));
   // programmatic stream serialization (the kernel waits for the previous
   // grid before it touches global memory), plus the cluster when merging
@@ -931,7 +939,7 @@ static sdpa_status_t launch_tc(const sdpa_params_t& p, const DecodePlan& plan, c
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = static_cast<unsigned>(S + 1);
+  attr[1].val.clusterDim.x = static_cast<unsigned>(S);
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
