@@ -718,7 +718,9 @@ __device__ __forceinline__ void cluster_merge(const Args& a, uint8_t* smem, int 
   const WaitCtl wc{a.wait_ns, abort_flag, a.status};
   // bounded by the limit only: copies into this CTA must land before it leaves
   const bool got = __syncthreads_and(mbar_wait_cluster(inbox_full, 0, wc));
-  cluster_arrive();  // every copy into this CTA has landed
+  // every copy into this CTA has landed (the peers only learn that their
+  // sources are no longer read: no data of this CTA's to publish)
+  cluster_arrive_relaxed();
   const bool aborted = *abort_flag != 0;
   if (got && !aborted) {
     constexpr int kQ4 = W / 4;
