@@ -599,8 +599,12 @@ def gb300_arm(args):
         work, unit, scale = w.kv_bytes(), "GB/s", 1e9
         bound, peak, peak_name = "hbm", peaks["hbm_gbs"], " (HBM copy)"
         sustained = peaks["hbm_gbs"]
-        traffic = profile_traffic("decode_split_" + w.name,
-                                  ["decode.cuh", "decode_combine.cu", "ptx.cuh"])
+        if w.D == 512 and w.dtype != "float32" and w.Hq // w.Hkv * w.Lq <= 16:
+            # the tensor-core pass (head_dim 512, fp16/bf16, up to 16 rows per kv head)
+            traffic = profile_traffic("decode_tc_" + w.name, ["decode_tc.cu", "ptx.cuh"])
+        else:
+            traffic = profile_traffic("decode_split_" + w.name,
+                                      ["decode.cuh", "decode_combine.cu", "ptx.cuh"])
     else:
         work, unit, scale = flops, "TFLOP/s", 1e12
         bound, peak, peak_name = "tensor", peaks["bf16_tflops"], " (bf16 dense, burst)"
