@@ -90,7 +90,52 @@ struct SplitArgs {
   // the driver accepts both maps.
   int use_tma;
   CUtensorMap tmK, tmV;
+  // Ragged plan (per-batch key lengths on the device): the grid is one
+  // linear range of work items and every CTA derives the split size from
+  // seq_lens_kv itself (ragged_tiles_per_split), so that the items of the
+  // call's real keys fill whole waves of the GPU.  num_splits is then the
+  // workspace's split capacity per row.
+  int ragged;
+  int batch;        // B
+  int slots;        // CTAs resident at once
+  int tiles_base;   // tiles per split of the plan for rows of Lk keys
 };
+
+// Ragged plan: tiles per split for the batches' real key counts.  W = the
+// real tiles of all (batch, unit) pairs; the splits of the plan for full
+// rows (tiles_base tiles) would fill `waves` waves of `slots` CTAs; the split
+// size is the smallest that keeps the items (every pair's real tiles cut
+// into splits) within those waves, and at least the size that keeps each
+// row within `max_splits` splits.
+__host__ __device__ inline int ragged_tiles_per_split(const int* lens, int B, int Lk, int tk,
+                                                      int units, int slots, int tiles_base,
+                                                      int max_splits) {
+  long long W = 0;
+  for (int b = 0; b < B; ++b) {
+    const int L = lens[b] < 0 ? 0 : (lens[b] > Lk ? Lk : lens[b]);
+    W += (L + tk - 1) / tk;
+  }
+  W *= units;
+  const int tiles_cap = (Lk + tk - 1) / tk;
+  int tp_min = (tiles_cap + max_splits - 1) / max_splits;
+  if (tp_min < 1) tp_min = 1;
+  if (W == 0) return tp_min;
+  const long long per_wave = static_cast<long long>(slots) * (tiles_base > 0 ? tiles_base : 1);
+  long long waves = (W + per_wave / 2) / per_wave;  // nearest whole number of waves
+  if (waves < 1) waves = 1;
+  const long long cap = waves * slots;
+  int tp = static_cast<int>((W + cap - 1) / cap);
+  if (tp < tp_min) tp = tp_min;
+  for (int it = 0; it < 64; ++it, ++tp) {  // per-pair rounding adds items
+    long long items = 0;
+    for (int b = 0; b < B; ++b) {
+      const int L = lens[b] < 0 ? 0 : (lens[b] > Lk ? Lk : lens[b]);
+      items += (((L + tk - 1) / tk) + tp - 1) / tp;
+    }
+    if (items * units <= cap) break;
+  }
+  return tp;
+}
 
 template <typename T>
 struct Ld;
@@ -265,15 +310,37 @@ __global__ void __launch_bounds__(kThreads, (D <= 128 && HG <= 4) ? 2 : 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / a.num_groups;
-  const int grp = blockIdx.y % a.num_groups;
-  const int b = blockIdx.z;
+  int split = blockIdx.x;
+  int kvh = blockIdx.y / a.num_groups;
+  int grp = blockIdx.y % a.num_groups;
+  int b = blockIdx.z;
+  int split_keys = a.split_keys;
+  if (a.ragged) {
+    // item blockIdx.x of the ragged plan: (batch, unit, split) in that order
+    const int units = a.Hkv * a.num_groups;
+    split_keys = C::TK * ragged_tiles_per_split(a.seq_lens_kv, a.batch, a.Lk, C::TK, units,
+                                                a.slots, a.tiles_base, a.num_splits);
+    int item = blockIdx.x;
+    b = -1;
+    for (int bb = 0; bb < a.batch; ++bb) {
+      const int L = min(max(a.seq_lens_kv[bb], 0), a.Lk);
+      const int sb = (L + split_keys - 1) / split_keys;
+      if (item < units * sb) {
+        b = bb;
+        split = item % sb;
+        kvh = (item / sb) / a.num_groups;
+        grp = (item / sb) % a.num_groups;
+        break;
+      }
+      item -= units * sb;
+    }
+    if (b < 0) return;  // past the call's last item (the whole CTA)
+  }
   // this batch's lengths (padding masks), clamped to the call's maxima
   const int Lkb = a.seq_lens_kv ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
   const int Lqb = a.seq_lens_q ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
-  const int key_begin = split * a.split_keys;
-  const int key_end = min(Lkb, key_begin + a.split_keys);
+  const int key_begin = split * split_keys;
+  const int key_end = min(Lkb, key_begin + split_keys);
   const int nkeys = max(0, key_end - key_begin);
   const int ntiles = (nkeys + C::TK - 1) / C::TK;
 
@@ -681,6 +748,19 @@ sdpa_status_t launch_split(SplitArgs a, int batch, cudaStream_t stream, bool* me
                            static_cast<int>(smem)) != cudaSuccess)
     return SDPA_ERR_CUDA;
   dim3 grid(a.num_splits, a.Hkv * a.num_groups, batch);
+  if (a.ragged) {
+    // at most the plan's waves plus one partial split per (batch, unit) pair
+    const long long units = static_cast<long long>(a.Hkv) * a.num_groups;
+    long long items = static_cast<long long>(a.num_splits) * units * batch;
+    const long long bound = static_cast<long long>(a.slots) *
+                                ((units * batch * ((a.Lk + C::TK - 1) / C::TK) +
+                                  static_cast<long long>(a.slots) * a.tiles_base - 1) /
+                                 (static_cast<long long>(a.slots) * a.tiles_base) + 1) +
+                            units * batch;
+    if (bound < items) items = bound;
+    grid = dim3(static_cast<unsigned>(items), 1, 1);
+    a.cluster_ok = 0;
+  }
   *merged = false;
   const int S = a.num_splits;
   if (a.cluster_ok && S >= 2 && S <= kMaxClusterSplits && (S & (S - 1)) == 0 && D % S == 0) {

@@ -13,6 +13,8 @@
 #include <cuda_fp16.h>
 #include <stdlib.h>
 
+#include <algorithm>
+
 #include "decode.cuh"
 #include "internal.h"
 
@@ -31,6 +33,10 @@ struct CombineArgs {
   int Hq, num_splits, D;
   int rows_per_head;  // query rows per (batch, head): 1 for decode
   long long os0, os1, os2;  // element strides of o (batch, head, row)
+  // ragged plan: a row of batch b merges only that batch's splits (the
+  // split kernel's plan, derived the same way); num_splits is the row stride
+  const int* seq_lens_kv;
+  int ragged, batch, Lk, tile_keys, units, slots, tiles_base;
 };
 
 constexpr int kMaxSplits = 1024;  // upper bound of the split plan
@@ -60,8 +66,16 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
   __shared__ float red[kCombineThreads / 32];
   const size_t row = blockIdx.x;  // (b * Hq + hq) * rows_per_head + i
   const int hq = static_cast<int>((row / a.rows_per_head) % a.Hq);
-  const int S = a.num_splits;
-  const float* ml = a.ws_ml + row * S * 2;
+  int S = a.num_splits;
+  if (a.ragged) {
+    const int b = static_cast<int>(row / (static_cast<size_t>(a.rows_per_head) * a.Hq));
+    const int sk = a.tile_keys * ragged_tiles_per_split(a.seq_lens_kv, a.batch, a.Lk, a.tile_keys,
+                                                        a.units, a.slots, a.tiles_base,
+                                                        a.num_splits);
+    const int L = min(max(a.seq_lens_kv[b], 0), a.Lk);
+    S = (L + sk - 1) / sk;
+  }
+  const float* ml = a.ws_ml + row * a.num_splits * 2;
   float M = -INFINITY;
   for (int s = threadIdx.x; s < S; s += kCombineThreads) M = fmaxf(M, ml[2 * s]);
   M = block_reduce(M, true, red);
@@ -84,7 +98,7 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
   T* orow = static_cast<T*>(a.o) + static_cast<long long>(bh / a.Hq) * a.os0 +
             static_cast<long long>(hq) * a.os1 +
             static_cast<long long>(row - bh * a.rows_per_head) * a.os2;
-  const float4* wo = reinterpret_cast<const float4*>(a.ws_o + row * S * a.D);
+  const float4* wo = reinterpret_cast<const float4*>(a.ws_o + row * a.num_splits * a.D);
   const int D4 = a.D / 4;
   for (int c = threadIdx.x; c < D4; c += kCombineThreads) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -186,7 +200,20 @@ bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   }
   const int tiles_per = (ntiles + best - 1) / best;
   const int split_keys = tiles_per * tk;
-  const int splits = (p.seq_len_kv + split_keys - 1) / split_keys;
+  int splits = (p.seq_len_kv + split_keys - 1) / split_keys;
+  // Per-batch key lengths on the device: the ragged plan, whose split size
+  // the kernels derive from the lengths (room for twice the splits of a
+  // full row, so that shorter rows can be cut finer); not with a forced
+  // split count (test hook) and not for very large batches (every CTA reads
+  // the B lengths).
+  out->ragged = false;
+  out->slots = static_cast<int>(slots);
+  out->tiles_base = tiles_per;
+  if (p.seq_lens_kv && p.batch <= 256 && debug_option(SDPA_DEBUG_DECODE_SPLITS) < 1) {
+    out->ragged = true;
+    cluster = false;
+    splits = std::min(std::min(2 * splits, 1024), std::max(ntiles, 1));
+  }
   out->head_group = hg;
   out->num_groups = groups;
   out->tile_keys = tk;
@@ -249,6 +276,10 @@ static sdpa_status_t launch_vector(const sdpa_params_t& p, const DecodePlan& pla
   a.status = env.status;
   a.wait_ns = env.wait_limit_ns;
   a.debug_drop_last = debug_option(SDPA_DEBUG_DECODE_DROP_LAST) == 1 ? 1 : 0;
+  a.ragged = plan.ragged ? 1 : 0;
+  a.batch = p.batch;
+  a.slots = plan.slots;
+  a.tiles_base = plan.tiles_base;
   const int D = p.head_dim, hg = plan.head_group;
   switch (p.dtype) {
     case SDPA_F32: return dec::launch_split_f32(a, D, hg, p.batch, env.stream, merged);
@@ -291,6 +322,14 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   c.os0 = p.o_stride[0];
   c.os1 = p.o_stride[1];
   c.os2 = p.o_stride[2];
+  c.seq_lens_kv = p.seq_lens_kv;
+  c.ragged = plan.ragged ? 1 : 0;
+  c.batch = p.batch;
+  c.Lk = p.seq_len_kv;
+  c.tile_keys = plan.tile_keys;
+  c.units = p.num_kv_heads * plan.num_groups;
+  c.slots = plan.slots;
+  c.tiles_base = plan.tiles_base;
   st = launch_combine(p.dtype, c, static_cast<unsigned>(p.batch) * p.num_q_heads * p.seq_len_q,
                       env.stream);
   if (st == SDPA_OK) set_last_launches(2);
@@ -311,6 +350,8 @@ sdpa_status_t launch_no_keys(const sdpa_params_t& p, void* o, float* lse, const 
   c.os0 = p.o_stride[0];
   c.os1 = p.o_stride[1];
   c.os2 = p.o_stride[2];
+  c.seq_lens_kv = nullptr;
+  c.ragged = 0;
   const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q;
   if (rows > 0x7fffffffu) return SDPA_ERR_UNSUPPORTED;
   return launch_combine(p.dtype, c, static_cast<unsigned>(rows), env.stream);

@@ -30,6 +30,9 @@ struct DecodePlan {
   bool cluster;     // merge the splits inside a thread-block cluster when it
                     // can be resident (else the combine pass does)
   size_t workspace; // bytes of partial results (also reserved for clusters)
+  bool ragged = false;  // per-batch lengths: split size derived on the device
+  int slots = 0;        // CTAs resident at once (the ragged plan's wave)
+  int tiles_base = 0;   // tiles per split for rows of the full length
   bool tc = false;  // head_dim 512, fp16/bf16, up to 16 rows per kv head: the
                     // tensor-core pass (head_group = rows, tile_keys = 128)
 };

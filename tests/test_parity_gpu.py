@@ -530,6 +530,18 @@ def test_kv_view_long_decode_and_few_queries(cuda):
                    lens_q=[2, 1], lens_kv=[777, 300])
 
 
+@pytest.mark.parametrize("lens_kv", [[4096, 3584, 3072, 2560, 2048, 1536, 1024, 512],
+                                     [4095, 1, 0, 2049, 17, 4096, 1000, 3]],
+                         ids=["descending", "odd_and_empty"])
+def test_kv_view_ragged_plan(cuda, lens_kv):
+    """Decode over a KV cache with ragged per-batch lengths at the long
+    decode's head shape: the split size comes from the device lengths (every
+    CTA derives it, and the combine derives each row's split count), so the
+    items of the real keys fill whole waves."""
+    _kv_view_check(8, 32, 8, 1, 4096, 4096, 128, "bfloat16", False, sinks=True,
+                   lens_q=[1] * 8, lens_kv=lens_kv)
+
+
 def test_kv_view_noalloc(cuda):
     _kv_view_check(2, 32, 4, 1, 1024, 1100, 512, "bfloat16", False, sinks=True,
                    lens_q=[1, 1], lens_kv=[1000, 3], noalloc=True)
