@@ -175,9 +175,13 @@ typedef struct {
 /*
  * sdpa_workspace_size — bytes of device workspace that sdpa_forward needs for
  * this problem (split-KV partial outputs of the decode path; the bf16 hi/lo
- * copies of q, k and v of the fp32 tensor-core prefill; 0 when the chosen
- * path needs none).  Pure host function; returns 0 for an invalid
- * problem as well (sdpa_forward then reports the error).
+ * copies of q, k and v of the fp32 tensor-core prefill; for an fp16/bf16
+ * prefill whose mask has a row per query, room for a copy of the mask laid
+ * out in the kernel's 128 x 128 score tiles — optional: with a smaller or
+ * NULL workspace that call reads the mask where it lies, slower where a
+ * warp's rows are far apart; 0 when the chosen path needs none).  Pure host
+ * function; returns 0 for an invalid problem as well (sdpa_forward then
+ * reports the error).
  */
 SDPA_API size_t sdpa_workspace_size(const sdpa_params_t* params);
 

@@ -17,6 +17,8 @@ struct LaunchEnv {
   uint64_t wait_limit_ns;
   int num_sms;
   cudaStream_t stream;
+  // prefill: the mask re-laid in score tiles (mask_tiles.cu), or nullptr
+  const void* mask_tiles = nullptr;
 };
 
 // Split-KV decode plan (pure function of the problem and the SM count).
@@ -63,6 +65,10 @@ sdpa_status_t launch_prefill_tc(const sdpa_params_t& p, const void* q, const voi
 // fp32 inputs, D = 64: split into bf16 hi/lo parts in the workspace, then the
 // tensor-core kernel with three products per MMA step.
 size_t prefill_x3_workspace(const sdpa_params_t& p);
+// A mask with a row per query, copied into the prefill's score-tile layout:
+// bytes of the copy (0 when the call takes none) and the copy itself.
+size_t prefill_mask_tiles_bytes(const sdpa_params_t& p);
+sdpa_status_t launch_mask_tiles(const sdpa_params_t& p, void* out, cudaStream_t stream);
 sdpa_status_t launch_prefill_x3(const sdpa_params_t& p, const void* q, const void* k,
                                 const void* v, void* o, float* lse, void* workspace,
                                 const LaunchEnv& env);

@@ -169,7 +169,11 @@ struct PrefillArgs {
   // boolean mask, 1/scale as hi + lo for an additive one.
   int kbias;
   uint32_t qbias;
-
+  // EXT: a mask with a row per query copied into score tiles (mask_tiles.cu),
+  // or nullptr.  Tile (plane, query tile, key tile) of 128 x 128 holds
+  // [key group][128 rows][16 bytes]; plane = b * tm_bmul + h * tm_hmul.
+  const uint8_t* tmask;
+  int tm_nqt, tm_nkt, tm_bmul, tm_hmul;
 };
 
 template <bool BF16>
@@ -805,8 +809,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A mask row shared by every query row (boolean or additive) reaches the
     // fused path through S itself (kbias); a mask with a row per query takes
     // 16-byte loads where the row is 16-byte aligned.
-    const bool mrow16 = EXT && mrowb && !kbias && (reinterpret_cast<uintptr_t>(mrowb) & 15u) == 0;
-    const bool mrowa16 = EXT && mrow && !kbias && (reinterpret_cast<uintptr_t>(mrow) & 15u) == 0;
+    // With the mask's score-tile copy, this row's 16 bytes of key group 0 of
+    // key tile jb; group g of tile jb + j is g * 2048 (additive) or g * 2048
+    // (boolean: 16 keys a group) further, tile j at j tile-bytes.
+    const uint8_t* mt = nullptr;
+    if (EXT && a.tmask && row_ok) {
+      const long long plane = static_cast<long long>(b) * a.tm_bmul + h * a.tm_hmul;
+      mt = a.tmask +
+           ((plane * a.tm_nqt + qi / BM) * a.tm_nkt + jb) * (a.mask_bool ? 16384 : 32768) +
+           (qi % BM) * 16;
+    }
+    const bool mrow16 =
+        EXT && mrowb && !kbias && (mt || (reinterpret_cast<uintptr_t>(mrowb) & 15u) == 0);
+    const bool mrowa16 =
+        EXT && mrow && !kbias && (mt || (reinterpret_cast<uintptr_t>(mrow) & 15u) == 0);
     // keys are counted from this CTA's first key tile from here on
     limit -= jb * BN;
     float m = -INFINITY;  // reference max (log2 units)
@@ -1019,7 +1035,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the loop)
         if constexpr (EXT) {
           const int kv0 = j * BN;
-          if (kv0 + BN - 1 <= limit) {
+          if (mt) {
+            // the warp's 32 rows of a key group are 512 contiguous bytes (4
+            // lines): lanes l, l + 8, l + 16, l + 24 cover a group's lines
+            const int g = r & 7;
+            if (a.mask_bool) {
+              prefetch_l1(mt + j * 16384 + g * 2048);
+            } else {
+              prefetch_l1(mt + j * 32768 + (2 * g) * 2048);
+              prefetch_l1(mt + j * 32768 + (2 * g + 1) * 2048);
+            }
+          } else if (kv0 + BN - 1 <= limit) {
             if (mrow16) {
               prefetch_l1(mrowb + kv0);
               prefetch_l1(mrowb + kv0 + BN - 1);
@@ -1107,8 +1133,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!__any_sync(0xffffffffu, redo)) break;
               need_max = redo;
             }
-          } else if (kFusedPartial ? fused_ok && !(mrow && !kbias && kv0 + BN - 1 > limit)
-                                   : fast) {
+          } else if (kFusedPartial
+                         ? fused_ok && !(mrow && !kbias && !(EXT && mt) && kv0 + BN - 1 > limit)
+                         : fast) {
             // Positive scale, no additive mask: p = 2^(s * scale*log2e - m)
             // with the scale folded into one packed FMA per pair, taken
             // against the current reference max m without looking for the
@@ -1134,11 +1161,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (EXT) {
                 if (kbias) {
                   // nothing to apply
-                } else if (mrow16 && kv0 + BN - 1 <= limit) {
-                  const uint4* src = reinterpret_cast<const uint4*>(mrowb + kv0);
+                } else if (mrow16 && (mt || kv0 + BN - 1 <= limit)) {
+                  // 16 keys a load: the row's own bytes, or its group rows of
+                  // the score-tile copy (keys past the row's limit are -inf
+                  // already; the copy is in bounds for every key of the tile)
+                  const uint4* src = mt ? reinterpret_cast<const uint4*>(mt + j * 16384)
+                                        : reinterpret_cast<const uint4*>(mrowb + kv0);
+                  const int cstep = mt ? 128 : 1;
 #pragma unroll
                   for (int c = 0; c < BN / 16; ++c) {
-                    const uint4 q4 = src[c];
+                    const uint4 q4 = src[c * cstep];
                     const uint32_t wd[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
@@ -1149,12 +1181,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                   for (int i = 0; i < BN; ++i)
                     if (kv0 + i <= limit && !mrowb[kv0 + i]) s[i] = 0xff800000u;
-                } else if (mrow && mrowa16 && kv0 + BN - 1 <= limit) {
-                  // additive row, 16-byte aligned: 8 values per load
-                  const uint4* src = reinterpret_cast<const uint4*>(mrow + kv0);
+                } else if (mrow && mrowa16 && (mt || kv0 + BN - 1 <= limit)) {
+                  // additive row, 8 values a load: the row where it is 16-byte
+                  // aligned, else its group rows of the score-tile copy
+                  const uint4* src = mt ? reinterpret_cast<const uint4*>(mt + j * 32768)
+                                        : reinterpret_cast<const uint4*>(mrow + kv0);
+                  const int cstep = mt ? 128 : 1;
 #pragma unroll
                   for (int c = 0; c < BN / 8; ++c) {
-                    const uint4 q4 = src[c];
+                    const uint4 q4 = src[c * cstep];
                     const uint32_t wd[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -1340,6 +1375,11 @@ sdpa_status_t launch_impl(const sdpa_params_t& p, const void* q, const void* k, 
   a.seq_lens_q = p.seq_lens_q;
   a.seq_lens_kv = p.seq_lens_kv;
   a.mask_bool = (p.flags & SDPA_FLAG_BOOL_MASK) ? 1 : 0;
+  a.tmask = EXT ? static_cast<const uint8_t*>(env.mask_tiles) : nullptr;
+  a.tm_nqt = (p.seq_len_q + 127) / 128;
+  a.tm_nkt = (p.seq_len_kv + 127) / 128;
+  a.tm_bmul = p.mask_stride[0] ? (p.mask_stride[1] ? p.num_q_heads : 1) : 0;
+  a.tm_hmul = p.mask_stride[1] ? 1 : 0;
   a.os0 = p.o_stride[0];
   a.os1 = p.o_stride[1];
   a.os2 = p.o_stride[2];

@@ -14,7 +14,7 @@ sdpa_status_t launch_prefill_tc_d128(const sdpa_params_t& p, const void* q, cons
     st.k[i] = p.k_stride[i];
     st.v[i] = p.v_stride[i];
   }
-  if (prefill_needs_ext(p))
+  if (prefill_needs_ext(p) || env.mask_tiles)
     return bf16 ? launch_impl<128, true, false, true>(p, q, k, v, q, k, v, o, lse, st, env, grids)
                 : launch_impl<128, false, false, true>(p, q, k, v, q, k, v, o, lse, st, env, grids);
   return bf16 ? launch_impl<128, true, false, false>(p, q, k, v, q, k, v, o, lse, st, env, grids)

@@ -211,6 +211,9 @@ sdpa_kernel_t sdpa_select_kernel(const sdpa_params_t* params, sdpa_status_t* sta
 size_t sdpa_workspace_size(const sdpa_params_t* params) {
   if (validate_problem(params) != SDPA_OK) return 0;
   if (pick(params) == SDPA_KERNEL_PREFILL_TC_F32) return gb300::prefill_x3_workspace(*params);
+  // a mask with a row per query: room for its score-tile copy (optional:
+  // without it the prefill reads the mask where it lies)
+  if (pick(params) == SDPA_KERNEL_PREFILL_TC) return gb300::prefill_mask_tiles_bytes(*params);
   if (pick(params) != SDPA_KERNEL_DECODE_SPLITKV) return 0;
   gb300::DecodePlan plan;
   if (!gb300::decode_plan(*params, current_num_sms(), &plan)) return 0;
@@ -273,8 +276,17 @@ sdpa_status_t sdpa_forward(const sdpa_params_t* p, const void* q, const void* k,
   // every launcher reads the layout from the stride fields
   const sdpa_params_t n = normalized(p);
   switch (kern) {
-    case SDPA_KERNEL_PREFILL_TC:  // sets the count itself (1 or 2 grids)
-      return gb300::launch_prefill_tc(n, q, k, v, o, lse, env);
+    case SDPA_KERNEL_PREFILL_TC: {  // sets the count itself (1 or 2 grids)
+      const size_t mt = gb300::prefill_mask_tiles_bytes(n);
+      if (mt > 0 && workspace && workspace_bytes >= mt && aligned(workspace, 256)) {
+        st = gb300::launch_mask_tiles(n, workspace, env.stream);
+        if (st != SDPA_OK) return st;
+        env.mask_tiles = workspace;
+      }
+      st = gb300::launch_prefill_tc(n, q, k, v, o, lse, env);
+      if (st == SDPA_OK && env.mask_tiles) g_last_launches += 1;
+      return st;
+    }
     case SDPA_KERNEL_PREFILL_F32:
       st = gb300::launch_prefill_f32(n, q, k, v, o, lse, env);
       if (st == SDPA_OK) g_last_launches = 1;

@@ -695,6 +695,43 @@ def test_additive_row_mask(cuda, dtype, D, Lk, causal):
     check(cuda, wl(2, 8, 2, 300, Lk, D, dtype, mask="full", causal=causal, sinks=causal))
 
 
+@pytest.mark.parametrize("kind", ["full", "bool_full"])
+@pytest.mark.parametrize("Lk", [512, 333])
+@pytest.mark.parametrize("workspace", [False, True])
+def test_row_mask_workspace_forms(cuda, kind, Lk, workspace):
+    """A mask with a row per query through the C call: with the workspace
+    that sdpa_workspace_size reports the call first copies the mask into
+    score tiles; with none it reads the mask where it lies (16-byte loads
+    where rows are aligned, else per element).  Both against the oracle,
+    causal with a ragged tail, GQA."""
+    import torch
+    import scaled_dot_product_fwd_gb300 as S
+    w = wl(2, 8, 2, 300, Lk, 64, "float16", mask=kind, causal=True, sinks=True)
+    inp = W.make_inputs(w)
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    m, sk = inp["mask"].cuda(), inp["sinks"].cuda()
+    mexp = m.expand(w.B, w.Hq, w.Lq, w.Lk)
+    flags = S._binding.SDPA_FLAG_BOOL_MASK if m.dtype == torch.bool else 0
+    p = S.make_params(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D, S.dtype_code(q.dtype), w.scale, True,
+                      mexp.data_ptr(), tuple(int(x) for x in mexp.stride()), sk.data_ptr(),
+                      flags=flags)
+    need = S._binding.sdpa_workspace_size(p)
+    assert need > 0  # the tiled copy is offered for a row-per-query mask
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda") if workspace else None
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    st = S._binding.sdpa_forward_raw(p, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), None if ws is None else ws.data_ptr(),
+                                     0 if ws is None else need,
+                                     torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    assert S.sdpa_last_launch_count() == (2 if workspace else 1)
+    torch.cuda.synchronize()
+    assert S.sdpa_device_status() == 0
+    o_ref, lse_ref = oracle_rows(w, inp, None)
+    compare(w, o.cpu(), lse.cpu(), o_ref, lse_ref, None)
+
+
 @pytest.mark.parametrize("D,dtype,kind,causal", [(64, "float16", "bool_key", False),
                                                  (64, "bfloat16", "bool_full", True),
                                                  (128, "bfloat16", "bool_key", True)])
