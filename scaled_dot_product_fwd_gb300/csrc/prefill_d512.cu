@@ -47,13 +47,14 @@ constexpr int kThreads = 192;
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 512;      // allocation (power of two)
-constexpr uint32_t kSCol = 0;            // S, and P over its first 64 columns
-constexpr uint32_t kOCol = kBN;          // the half of O
+constexpr uint32_t kSCol = 0;            // S of tile j in buffer j % 2 (columns
+                                         // 128 (j % 2) ...), P over its first 64
+constexpr uint32_t kOCol = 2 * kBN;      // the half of O
 constexpr int kQOff = 0;
 constexpr int kRingOff = kQChunks * kChunkBytes;
 constexpr int kBarOff = kRingOff + kRing * kChunkBytes;
-// q_full, full[kRing], empty[kRing], s_full, p_ready, o_done, drain
-constexpr int kNBars = 1 + 2 * kRing + 4;
+// q_full, full[kRing], empty[kRing], s_full[2], p_ready[2], o_done, drain, pv_done
+constexpr int kNBars = 1 + 2 * kRing + 7;
 constexpr int kMiscOff = kBarOff + kNBars * 8;
 constexpr int kSmem = kMiscOff + 16 + 1024;  // + alignment slack
 static_assert(kSmem <= 232448, "shared memory budget");
@@ -123,10 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars;
   uint64_t* full = bars + 1;
   uint64_t* empty = full + kRing;
-  uint64_t* s_full = empty + kRing;
-  uint64_t* p_ready = s_full + 1;
-  uint64_t* o_done = p_ready + 1;
+  uint64_t* s_full = empty + kRing;  // [2]: S of a buffer complete
+  uint64_t* p_ready = s_full + 2;    // [2]: P of a buffer written
+  uint64_t* o_done = p_ready + 2;
   uint64_t* drain = o_done + 1;
+  uint64_t* pv_done = drain + 1;     // one phase per tile: its PV products complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -162,10 +164,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_ready, kBM);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_ready[i], kBM);
+    }
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(pv_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -191,11 +196,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(q_full, kQChunks * kChunkBytes);
       for (int c = 0; c < kQChunks; ++c)
         tma_load_4d(sQ + c * kChunkBytes, &tmQ, q_full, c * kChunkCols, m0, h, b);
+      // the MMA issuer's order: K_0, then per step j >= 1 K_j and V_{j-1}
+      // (S_j is computed while the softmax warps work on S_{j-1}), then the
+      // last V
       int seq = 0;
       bool pok = true;
-      for (int j = 0; j < nkv && pok; ++j) {
-        const int key0 = j * kBN;
-        for (int c = 0; c < kStepChunks; ++c, ++seq) {
+      for (int j = 0; j <= nkv && pok; ++j) {
+        for (int c = 0; c < kStepChunks; ++c) {
+          const bool is_k = c < kQChunks;
+          const int tile = is_k ? j : j - 1;
+          if (tile < 0 || tile >= nkv) continue;
           const int s = seq % kRing;
           const int use = seq / kRing;
           if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, wc)) {
@@ -204,21 +214,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&full[s], kChunkBytes);
           uint8_t* dst = sRing + s * kChunkBytes;
-          if (c < kQChunks)
-            tma_load_4d(dst, &tmK, &full[s], c * kChunkCols, key0, kvh, b);
+          if (is_k)
+            tma_load_4d(dst, &tmK, &full[s], c * kChunkCols, tile * kBN, kvh, b);
           else
-            tma_load_4d(dst, &tmV, &full[s], half * kDH + (c - kQChunks) * kChunkCols, key0,
-                        kvh, b);
+            tma_load_4d(dst, &tmV, &full[s], half * kDH + (c - kQChunks) * kChunkCols,
+                        tile * kBN, kvh, b);
           last_use[s] = use;
+          ++seq;
         }
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    // One thread issues: per key tile the eight K chunks' products into S,
-    // a commit that hands S to the softmax warps, then after they have
-    // written P the half's four V chunks' products into O.  Each chunk's
-    // slot is released by a commit once its products complete.
+    // One thread issues, per step j: S_j = sum over the eight K chunks into
+    // S buffer j % 2 and a commit that hands it to the softmax warps; then,
+    // once they have written P_{j-1}, the half's four V chunks' products
+    // O += P_{j-1} V_{j-1} and a commit (pv_done) for a rescale of O.  S_j
+    // thus runs while the softmax warps work on S_{j-1}; S_{j+2} overwrites
+    // buffer j % 2 only after PV_j, issued before it, has read P_j (the MMAs
+    // run in issue order).  Each chunk's slot is released by a commit once
+    // its products complete.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_f16(BF16, kBM, kBN, false, false);
       constexpr uint32_t idO = idesc_f16(BF16, kBM, kChunkCols, false, true);
@@ -227,31 +242,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t v_desc = sdesc(smem_addr(sRing), kBN * 128, 1024, kSwizzle128B);
       bool ok = mbar_wait(q_full, 0, wc);
       int seq = 0;
-      for (int j = 0; j < nkv; ++j) {
-        // S_j = sum over the eight column chunks c of Q_c K_c^T; a K step of
-        // 16 elements is 32 bytes inside the 128-byte swizzled rows
-        for (int c = 0; c < kQChunks; ++c, ++seq) {
-          const int s = seq % kRing;
-          ok = ok && mbar_wait(&full[s], static_cast<uint32_t>((seq / kRing) & 1), wc);
-          if (ok) {
-            tc_fence_after();
+      for (int j = 0; j <= nkv; ++j) {
+        if (j < nkv) {
+          // S_j = sum over the eight column chunks c of Q_c K_c^T; a K step
+          // of 16 elements is 32 bytes inside the 128-byte swizzled rows
+          const uint32_t dS = tmem + kSCol + (j & 1) * kBN;
+          for (int c = 0; c < kQChunks; ++c, ++seq) {
+            const int s = seq % kRing;
+            ok = ok && mbar_wait(&full[s], static_cast<uint32_t>((seq / kRing) & 1), wc);
+            if (ok) {
+              tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kChunkCols / 16; ++kk) {
-              const uint64_t qd = q_desc + static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4);
-              const uint64_t kd = k_desc + static_cast<uint64_t>((s * kChunkBytes + kk * 32) >> 4);
-              mma_f16_ss(tmem + kSCol, qd, kd, idS, (c > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kChunkCols / 16; ++kk) {
+                const uint64_t qd =
+                    q_desc + static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4);
+                const uint64_t kd =
+                    k_desc + static_cast<uint64_t>((s * kChunkBytes + kk * 32) >> 4);
+                mma_f16_ss(dS, qd, kd, idS, (c > 0 || kk > 0) ? 1u : 0u);
+              }
             }
+            mma_commit(&empty[s]);
           }
-          mma_commit(&empty[s]);
+          mma_commit(&s_full[j & 1]);
         }
-        // S_j complete (and every earlier product: O holds the sum through
-        // P_{j-1} V_{j-1}); the softmax warps take it
-        mma_commit(s_full);
-        ok = ok && mbar_wait(p_ready, static_cast<uint32_t>(j & 1), wc);
+        if (j == 0) continue;
+        // O_half += P_{j-1} V_{j-1}: P (128 x 128, K-major) from TMEM, 2
+        // elements per column; V chunk c (64 columns of the half) MN-major,
+        // 16 keys per K step (2048 bytes)
+        const int pj = j - 1;
+        ok = ok && mbar_wait(&p_ready[pj & 1], static_cast<uint32_t>((pj >> 1) & 1), wc);
         if (ok) tc_fence_after();
-        // O_half += P_j V_j: P (128 x 128, K-major) from TMEM, 2 elements per
-        // column; V chunk c (64 columns of the half) MN-major, 16 keys per
-        // K step (2048 bytes)
+        const uint32_t aP = tmem + kSCol + (pj & 1) * kBN;
         for (int c = 0; c < kVChunks; ++c, ++seq) {
           const int s = seq % kRing;
           ok = ok && mbar_wait(&full[s], static_cast<uint32_t>((seq / kRing) & 1), wc);
@@ -261,12 +282,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < kBN / 16; ++kk) {
               const uint64_t vd =
                   v_desc + static_cast<uint64_t>((s * kChunkBytes + kk * 16 * 128) >> 4);
-              mma_f16_ts(tmem + kOCol + c * kChunkCols, tmem + kSCol + kk * 8, vd, idO,
-                         (j > 0 || kk > 0) ? 1u : 0u);
+              mma_f16_ts(tmem + kOCol + c * kChunkCols, aP + kk * 8, vd, idO,
+                         (pj > 0 || kk > 0) ? 1u : 0u);
             }
           }
           mma_commit(&empty[s]);
         }
+        mma_commit(pv_done);
       }
       mma_commit(o_done);
       // every product completes before TMEM is freed
@@ -280,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qi = m0 + r;
     const bool row_ok = qi < a.Lq;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_off + kSCol;
     const uint32_t tO = tmem + lane_off + kOCol;
     int limit = Lkb - 1;  // last key visible to this row
     if (a.causal) limit = min(limit, qi + (Lkb - Lqb));
@@ -299,7 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = 0.f;        // running sum relative to m
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      ok = __all_sync(0xffffffffu, ok && mbar_wait(s_full, static_cast<uint32_t>(j & 1), wc));
+      const uint32_t tS = tmem + lane_off + kSCol + (j & 1) * kBN;  // S_j, then P_j
+      ok = __all_sync(0xffffffffu,
+                      ok && mbar_wait(&s_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), wc));
       if (ok) {
         tc_fence_after();
         uint32_t s[kBN];
@@ -362,9 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[i] = H::pack(p0, p1);
         }
         l = l * alpha + ((rp[0] + rp[1]) + (rp[2] + rp[3]));
-        // O holds the sum through P_{j-1} V_{j-1} (the commit behind s_full
-        // tracks every earlier product); rescale rows whose max moved
+        // Rescale rows whose max moved, once O holds the sum through
+        // P_{j-1} V_{j-1}: PV_{j-1} runs beside this step (issued after
+        // S_j), PV_{j-2} has completed (issued before S_j, whose commit this
+        // step waited for), so phase j-1 of pv_done is the next to complete
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          ok = __all_sync(0xffffffffu,
+                          ok && mbar_wait(pv_done, static_cast<uint32_t>((j - 1) & 1), wc));
+          tc_fence_after();
           __syncwarp();
 #pragma unroll 1
           for (int c = 0; c < kDH / 32; ++c) {
@@ -382,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
       }
       // P_j is in TMEM: every thread arrives every step, also after a failed wait
-      mbar_arrive(p_ready);
+      mbar_arrive(&p_ready[j & 1]);
     }
     ok = __all_sync(0xffffffffu, ok && mbar_wait(o_done, 0, wc));
     if (ok) {
