@@ -13,15 +13,18 @@
 //
 // GB300 design: a 128 x 512 fp32 output tile alone would fill the 512 TMEM
 // columns, so each CTA owns one D-half: (query tile of 128 rows, half, head,
-// batch).  TMEM holds S (128 columns) and the CTA's half of O (256 columns);
-// both halves of a query tile compute the same S and softmax (the price of
-// the split is S computed twice: 1.5x the MMA work of the definition).
+// batch).  TMEM holds two S buffers (128 columns each) and the CTA's half
+// of O (256 columns); both halves of a query tile compute the same S and
+// softmax (the price of the split is S computed twice: 1.5x the MMA work of
+// the definition).
 // Q (128 rows x 512, 128 KB) stays in shared memory as eight 128-byte
-// swizzled chunks of 64 columns; for each key tile the producer streams the
-// eight K chunks and the half's four V chunks through a ring of six chunk
-// slots.  Warps: 0-3 softmax (one query row per thread = TMEM lane), 4 TMA
-// producer, 5 MMA issuer (one thread): S = sum_c Q_c K_c^T (M128 N128 K16),
-// then O_half += P V_half (P from TMEM, four N64 column blocks).
+// swizzled chunks of 64 columns; the producer streams K_j (eight chunks)
+// before V_{j-1} (the half's four chunks) through a ring of three 32 KB
+// slots, two chunks a slot.  Warps: 0-3 softmax (one query row per thread =
+// TMEM lane), 4 TMA producer, 5 MMA issuer (one thread): S_j = sum_c Q_c K_c^T
+// (M128 N128 K16) into TMEM buffer j % 2, then O_half += P_{j-1} V_{j-1}
+// (P from TMEM, four N64 column blocks), so that S_j runs while the softmax
+// warps work on S_{j-1}.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,8 +44,15 @@ constexpr int kChunkCols = 64;           // columns of one 128-byte swizzled chu
 constexpr int kChunkBytes = 128 * 128;   // 128 rows x 128 bytes
 constexpr int kQChunks = kD / kChunkCols;    // 8
 constexpr int kVChunks = kDH / kChunkCols;   // 4
-constexpr int kStepChunks = kQChunks + kVChunks;  // per key tile: K chunks, then V chunks
-constexpr int kRing = 6;
+// The ring moves chunks in pairs (a slot holds two chunks of one operand):
+// the issuing thread's wait on a slot costs it hundreds of clk of issue while
+// products are in flight, so fewer, larger slots (same 96 KB) halve those
+// waits.
+constexpr int kSlotBytes = 2 * kChunkBytes;
+constexpr int kKSlots = kQChunks / 2;                 // 4
+constexpr int kVSlots = kVChunks / 2;                 // 2
+constexpr int kStepSlots = kKSlots + kVSlots;         // per key tile: K slots, then V slots
+constexpr int kRing = 3;
 constexpr int kThreads = 192;
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -52,7 +62,7 @@ constexpr uint32_t kSCol = 0;            // S of tile j in buffer j % 2 (columns
 constexpr uint32_t kOCol = 2 * kBN;      // the half of O
 constexpr int kQOff = 0;
 constexpr int kRingOff = kQChunks * kChunkBytes;
-constexpr int kBarOff = kRingOff + kRing * kChunkBytes;
+constexpr int kBarOff = kRingOff + kRing * kSlotBytes;
 // q_full, full[kRing], empty[kRing], s_full[2], p_ready[2], o_done, drain, pv_done
 constexpr int kNBars = 1 + 2 * kRing + 7;
 constexpr int kMiscOff = kBarOff + kNBars * 8;
@@ -202,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int seq = 0;
       bool pok = true;
       for (int j = 0; j <= nkv && pok; ++j) {
-        for (int c = 0; c < kStepChunks; ++c) {
-          const bool is_k = c < kQChunks;
+        for (int i = 0; i < kStepSlots; ++i) {
+          const bool is_k = i < kKSlots;
           const int tile = is_k ? j : j - 1;
           if (tile < 0 || tile >= nkv) continue;
           const int s = seq % kRing;
@@ -212,13 +222,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             pok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], kChunkBytes);
-          uint8_t* dst = sRing + s * kChunkBytes;
-          if (is_k)
-            tma_load_4d(dst, &tmK, &full[s], c * kChunkCols, tile * kBN, kvh, b);
-          else
-            tma_load_4d(dst, &tmV, &full[s], half * kDH + (c - kQChunks) * kChunkCols,
-                        tile * kBN, kvh, b);
+          mbar_arrive_expect_tx(&full[s], kSlotBytes);
+          uint8_t* dst = sRing + s * kSlotBytes;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            if (is_k)
+              tma_load_4d(dst + hh * kChunkBytes, &tmK, &full[s], (2 * i + hh) * kChunkCols,
+                          tile * kBN, kvh, b);
+            else
+              tma_load_4d(dst + hh * kChunkBytes, &tmV, &full[s],
+                          half * kDH + (2 * (i - kKSlots) + hh) * kChunkCols, tile * kBN, kvh, b);
+          }
           last_use[s] = use;
           ++seq;
         }
@@ -247,18 +261,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S_j = sum over the eight column chunks c of Q_c K_c^T; a K step
           // of 16 elements is 32 bytes inside the 128-byte swizzled rows
           const uint32_t dS = tmem + kSCol + (j & 1) * kBN;
-          for (int c = 0; c < kQChunks; ++c, ++seq) {
+          for (int i = 0; i < kKSlots; ++i, ++seq) {
             const int s = seq % kRing;
             ok = ok && mbar_wait(&full[s], static_cast<uint32_t>((seq / kRing) & 1), wc);
             if (ok) {
               tc_fence_after();
 #pragma unroll
-              for (int kk = 0; kk < kChunkCols / 16; ++kk) {
-                const uint64_t qd =
-                    q_desc + static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4);
-                const uint64_t kd =
-                    k_desc + static_cast<uint64_t>((s * kChunkBytes + kk * 32) >> 4);
-                mma_f16_ss(dS, qd, kd, idS, (c > 0 || kk > 0) ? 1u : 0u);
+              for (int hh = 0; hh < 2; ++hh) {
+                const int c = 2 * i + hh;
+#pragma unroll
+                for (int kk = 0; kk < kChunkCols / 16; ++kk) {
+                  const uint64_t qd =
+                      q_desc + static_cast<uint64_t>((c * kChunkBytes + kk * 32) >> 4);
+                  const uint64_t kd = k_desc + static_cast<uint64_t>(
+                                                   (s * kSlotBytes + hh * kChunkBytes + kk * 32) >> 4);
+                  mma_f16_ss(dS, qd, kd, idS, (c > 0 || kk > 0) ? 1u : 0u);
+                }
               }
             }
             mma_commit(&empty[s]);
@@ -273,17 +291,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = ok && mbar_wait(&p_ready[pj & 1], static_cast<uint32_t>((pj >> 1) & 1), wc);
         if (ok) tc_fence_after();
         const uint32_t aP = tmem + kSCol + (pj & 1) * kBN;
-        for (int c = 0; c < kVChunks; ++c, ++seq) {
+        for (int i = 0; i < kVSlots; ++i, ++seq) {
           const int s = seq % kRing;
           ok = ok && mbar_wait(&full[s], static_cast<uint32_t>((seq / kRing) & 1), wc);
           if (ok) {
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              const uint64_t vd =
-                  v_desc + static_cast<uint64_t>((s * kChunkBytes + kk * 16 * 128) >> 4);
-              mma_f16_ts(tmem + kOCol + c * kChunkCols, aP + kk * 8, vd, idO,
-                         (pj > 0 || kk > 0) ? 1u : 0u);
+            for (int hh = 0; hh < 2; ++hh) {
+              const int c = 2 * i + hh;
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk) {
+                const uint64_t vd = v_desc + static_cast<uint64_t>(
+                                                 (s * kSlotBytes + hh * kChunkBytes + kk * 16 * 128) >> 4);
+                mma_f16_ts(tmem + kOCol + c * kChunkCols, aP + kk * 8, vd, idO,
+                           (pj > 0 || kk > 0) ? 1u : 0u);
+              }
             }
           }
           mma_commit(&empty[s]);
