@@ -848,11 +848,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Huge mask values (magnitude 2^64 or more) exist only in bfloat16 and
     // float masks.  Key masks (one row shared by the query rows) give them
     // their exact form: on the key-mask MMA step (bfloat16) and, in the fp32
-    // hi/lo kernel, on the extended instantiation's general path.  Masks with
-    // a row per query keep the plain product, whose unrolled code is a third
-    // of the size (carried by the boundary tiles' general path, its size
-    // alone measured 3.5 % of the unmasked DiT loop): there a finite value
-    // whose scaled product overflows fp32 acts as -inf.
+    // hi/lo kernel, on the extended instantiation's general path; so do the
+    // fused path's bfloat16 rows (masks with a row per query, read from the
+    // score-tile copy or aligned rows).  The general path keeps the plain
+    // product, whose unrolled code is a third of the size (carried by the
+    // boundary tiles' general path, its size alone measured 3.5 % of the
+    // unmasked DiT loop): there a finite value whose scaled product overflows
+    // fp32 acts as -inf.
     constexpr bool kHugeMask = EXT && X3;
     const float mhuge = mask_huge_log2(a.sl2);  // a huge mask value in log2 units
     auto mlog2 = [&](float mv) { return kHugeMask ? mask_log2(mv, mhuge) : mv * kLog2e; };
@@ -1194,8 +1196,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                       const float mv = E::bits_to_f((wd[e >> 1] >> (16 * (e & 1))) & 0xffffu);
-                      s[8 * c + e] =
-                          __float_as_uint(fmaf(mv, rscale, __uint_as_float(s[8 * c + e])));
+                      // a bfloat16 value of magnitude 2^64 or more enters as
+                      // +-2^100 raw-score units (exact; fp16 has none)
+                      const bool huge = BF16 && fabsf(mv) >= kMaskBig;
+                      s[8 * c + e] = __float_as_uint(fmaf(huge ? copysignf(kMaskHugeRaw, mv) : mv,
+                                                          huge ? 1.f : rscale,
+                                                          __uint_as_float(s[8 * c + e])));
                     }
                   }
                 }

@@ -863,12 +863,14 @@ def test_lowest_finite_mask(cuda, dtype, D, kind, Lq, Lk):
     by it in other rows weigh nothing.  Key masks (one row shared by the
     query rows), the single-query path and the fp32 head-dim-128 kernel give
     such rows that result, with LSE -2^100 * scale (a mask value of magnitude
-    2^64 or more enters as 2^100 in raw-score units); fp16's lowest value
-    (-65504) is an ordinary value everywhere (LSE within 1e-6 relative).  On
-    the tensor-core paths for masks with a row per query, a bfloat16/float
-    value whose scaled product overflows fp32 acts as -inf: a row masked by
-    it throughout sees no key (O = 0, LSE = -inf).  Every other row matches
-    the oracle at the usual bars.
+    2^64 or more enters as 2^100 in raw-score units), and so do bfloat16
+    masks with a row per query on the tensor-core prefill (read from their
+    score-tile copy); fp16's lowest value (-65504) is an ordinary value
+    everywhere (LSE within 1e-6 relative).  On the fp32 tensor-core path
+    (head_dim 64) for masks with a row per query, a value whose scaled
+    product overflows fp32 acts as -inf: a row masked by it throughout sees
+    no key (O = 0, LSE = -inf).  Every other row matches the oracle at the
+    usual bars.
     """
     torch = cuda
     w = wl(2, 4, 2, Lq, Lk, D, dtype, mask=kind, causal=False)
@@ -888,7 +890,7 @@ def test_lowest_finite_mask(cuda, dtype, D, kind, Lq, Lk):
     lg = lse_gpu.double().numpy().reshape(-1)
     o_ref, lse_ref = o_ref.reshape(-1, D), lse_ref.reshape(-1)
     assert np.all(np.isfinite(og))
-    per_query_tc = kind != "key" and Lq > 2 and (dtype == "bfloat16" or (dtype == "float32" and D == 64))
+    per_query_tc = kind != "key" and Lq > 2 and dtype == "float32" and D == 64
     gone = (lse_ref < -1e30) if per_query_tc else np.zeros_like(lse_ref, dtype=bool)
     if gone.any():          # rows that see no key on the per-query tensor-core paths
         assert np.all(np.isneginf(lg[gone])) and np.all(og[gone] == 0)
