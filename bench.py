@@ -602,6 +602,9 @@ def gb300_arm(args):
         if w.D == 512 and w.dtype != "float32" and w.Hq // w.Hkv * w.Lq <= 16:
             # the tensor-core pass (head_dim 512, fp16/bf16, up to 16 rows per kv head)
             traffic = profile_traffic("decode_tc_" + w.name, ["decode_tc.cu", "ptx.cuh"])
+        elif w.D == 128 and w.dtype != "float32" and w.Hq // w.Hkv * w.Lq <= 16:
+            # the streaming tensor-core pass at head_dim 128
+            traffic = profile_traffic("decode_tc128_" + w.name, ["decode_tc128.cu", "ptx.cuh"])
         else:
             traffic = profile_traffic("decode_split_" + w.name,
                                       ["decode.cuh", "decode_combine.cu", "ptx.cuh"])

@@ -124,10 +124,10 @@ typedef enum {
  *      (o = 0, lse = -inf or the sink), and the bottom-right causal rule
  *      uses the batch's own lengths: key j visible to query i iff
  *      j <= i + (seq_lens_kv[b] - seq_lens_q[b]).  Both arrays must stay
- *      valid until the call's kernels have run.  The prefill kernels load
- *      whole key tiles, so v rows [seq_lens_kv[b], seq_len_kv) meet zero
- *      weights there and must hold finite values (rows past seq_len_kv are
- *      never read).
+ *      valid until the call's kernels have run.  The prefill kernels and
+ *      the fp16/bf16 decode passes at head_dim 128 and 512 load whole key
+ *      tiles, so v rows [seq_lens_kv[b], seq_len_kv) meet zero weights there
+ *      and must hold finite values (rows past seq_len_kv are never read).
  *  flags: an OR of the SDPA_FLAG_* bits below (other bits must be 0, else
  *      SDPA_ERR_INVALID_ARGUMENT).
  *  q_stride, k_stride, v_stride, o_stride (ABI 4): read only with
@@ -311,7 +311,7 @@ SDPA_API uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns);
  * later calls, process-wide (they exist so that tests reach paths that the
  * planner would not pick for the test's sizes).  Returns the previous value;
  * an unknown option returns -1 and changes nothing.
- *  SDPA_DEBUG_DECODE_SPLITS   split count of the vector path (0: the plan's)
+ *  SDPA_DEBUG_DECODE_SPLITS   split count of the decode passes (0: the plan's)
  *  SDPA_DEBUG_DECODE_CLUSTER  0: never merge the splits inside a cluster
  *                             (two passes); 1: as planned (default)
  *  SDPA_DEBUG_DECODE_DROP_LAST 1: the vector path's producer skips its last
@@ -320,12 +320,15 @@ SDPA_API uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns);
  *  SDPA_DEBUG_PREFILL_SPLIT   -1: the plan's (default); 0: never split the
  *                             last wave; 2, 4: every unit shared by that
  *                             many CTAs of a cluster
+ *  SDPA_DEBUG_DECODE_VECTOR   1: head_dim-128 fp16/bf16 decode on the vector
+ *                             path instead of the tensor-core pass (default 0)
  */
 typedef enum {
   SDPA_DEBUG_DECODE_SPLITS = 0,
   SDPA_DEBUG_DECODE_CLUSTER = 1,
   SDPA_DEBUG_DECODE_DROP_LAST = 2,
-  SDPA_DEBUG_PREFILL_SPLIT = 3
+  SDPA_DEBUG_PREFILL_SPLIT = 3,
+  SDPA_DEBUG_DECODE_VECTOR = 4
 } sdpa_debug_option_t;
 SDPA_API int sdpa_debug_set_option(int option, int value);
 

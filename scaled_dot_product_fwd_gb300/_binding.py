@@ -35,7 +35,7 @@ EXPORTS = ("sdpa_workspace_size", "sdpa_select_kernel", "sdpa_forward", "sdpa_st
 
 # sdpa_debug_option_t
 DEBUG_OPTIONS = {"decode_splits": 0, "decode_cluster": 1, "decode_drop_last": 2,
-                 "prefill_split": 3}
+                 "prefill_split": 3, "decode_vector": 4}
 
 
 class SdpaParams(ctypes.Structure):

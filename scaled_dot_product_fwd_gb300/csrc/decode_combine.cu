@@ -57,13 +57,22 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
   return v;
 }
 
-// One block per output row: the split weights 2^(lse_s - M) go to shared
-// memory once, then each thread sums its float4 columns over the splits with
-// the loads of several splits in flight.
+// One block per output row.  Thread t owns float4 column t % (D/4) of the
+// splits t / (D/4), t / (D/4) + ng, ... (ng = 128 / (D/4) groups of splits),
+// and loads its first kPrefetch partials before the weights are known, so
+// that the partial outputs and the (m, l) pairs share one memory round trip;
+// the weights 2^(lse_s - M) go to shared memory once, and the groups' sums
+// meet in shared memory at the end.
 template <typename T>
 __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const CombineArgs a) {
+  constexpr int kPrefetch = 8;
   __shared__ float w[kMaxSplits];
   __shared__ float red[kCombineThreads / 32];
+  __shared__ float4 part[kCombineThreads];
+  // Launched with programmatic stream serialization: the split pass's
+  // partial results are complete and visible after this wait.
+  griddep_wait();
+  griddep_launch_dependents();
   const size_t row = blockIdx.x;  // (b * Hq + hq) * rows_per_head + i
   const int hq = static_cast<int>((row / a.rows_per_head) % a.Hq);
   int S = a.num_splits;
@@ -74,6 +83,19 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
                                                         a.num_splits);
     const int L = min(max(a.seq_lens_kv[b], 0), a.Lk);
     S = (L + sk - 1) / sk;
+  }
+  const int D4 = a.D / 4;
+  const int ng = D4 >= kCombineThreads ? 1 : kCombineThreads / D4;  // groups of splits
+  const int c = static_cast<int>(threadIdx.x) % D4;
+  const int g = static_cast<int>(threadIdx.x) / D4;
+  const bool col_ok = g < ng;
+  const float4* wo = reinterpret_cast<const float4*>(a.ws_o + row * a.num_splits * a.D);
+  float4 pre[kPrefetch];
+#pragma unroll
+  for (int j = 0; j < kPrefetch; ++j) {
+    const int s = g + j * ng;
+    pre[j] = (col_ok && s < S) ? wo[static_cast<size_t>(s) * D4 + c]
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const float* ml = a.ws_ml + row * a.num_splits * 2;
   float M = -INFINITY;
@@ -94,29 +116,46 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const C
   L = block_reduce(L, false, red);  // its barriers also publish w[]
   if (a.sinks && M != -INFINITY) L += ex2(sk - M);
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  const size_t bh = row / a.rows_per_head;
-  T* orow = static_cast<T*>(a.o) + static_cast<long long>(bh / a.Hq) * a.os0 +
-            static_cast<long long>(hq) * a.os1 +
-            static_cast<long long>(row - bh * a.rows_per_head) * a.os2;
-  const float4* wo = reinterpret_cast<const float4*>(a.ws_o + row * a.num_splits * a.D);
-  const int D4 = a.D / 4;
-  for (int c = threadIdx.x; c < D4; c += kCombineThreads) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (L > 0.f) {
-#pragma unroll 8
-      for (int s = 0; s < S; ++s) {
-        const float4 v = wo[static_cast<size_t>(s) * D4 + c];
-        const float ws = w[s];
-        acc.x = fmaf(ws, v.x, acc.x);
-        acc.y = fmaf(ws, v.y, acc.y);
-        acc.z = fmaf(ws, v.z, acc.z);
-        acc.w = fmaf(ws, v.w, acc.w);
-      }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col_ok && L > 0.f) {
+#pragma unroll
+    for (int j = 0; j < kPrefetch; ++j) {
+      const int s = g + j * ng;
+      const float ws = s < S ? w[s] : 0.f;
+      acc.x = fmaf(ws, pre[j].x, acc.x);
+      acc.y = fmaf(ws, pre[j].y, acc.y);
+      acc.z = fmaf(ws, pre[j].z, acc.z);
+      acc.w = fmaf(ws, pre[j].w, acc.w);
     }
-    orow[4 * c + 0] = StoreAs<T>::c(acc.x * inv);
-    orow[4 * c + 1] = StoreAs<T>::c(acc.y * inv);
-    orow[4 * c + 2] = StoreAs<T>::c(acc.z * inv);
-    orow[4 * c + 3] = StoreAs<T>::c(acc.w * inv);
+#pragma unroll 4
+    for (int s = g + kPrefetch * ng; s < S; s += ng) {
+      const float4 v = wo[static_cast<size_t>(s) * D4 + c];
+      const float ws = w[s];
+      acc.x = fmaf(ws, v.x, acc.x);
+      acc.y = fmaf(ws, v.y, acc.y);
+      acc.z = fmaf(ws, v.z, acc.z);
+      acc.w = fmaf(ws, v.w, acc.w);
+    }
+  }
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  if (g == 0) {
+    float4 t = part[c];
+    for (int gg = 1; gg < ng; ++gg) {
+      const float4 u = part[gg * D4 + c];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    const size_t bh = row / a.rows_per_head;
+    T* orow = static_cast<T*>(a.o) + static_cast<long long>(bh / a.Hq) * a.os0 +
+              static_cast<long long>(hq) * a.os1 +
+              static_cast<long long>(row - bh * a.rows_per_head) * a.os2;
+    orow[4 * c + 0] = StoreAs<T>::c(t.x * inv);
+    orow[4 * c + 1] = StoreAs<T>::c(t.y * inv);
+    orow[4 * c + 2] = StoreAs<T>::c(t.z * inv);
+    orow[4 * c + 3] = StoreAs<T>::c(t.w * inv);
   }
   if (threadIdx.x == 0 && a.lse) a.lse[row] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
@@ -133,7 +172,9 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   if (decode_tc_plan(p, num_sms, out)) return true;
+  if (decode_tc128_plan(p, num_sms, out)) return true;
   out->tc = false;
+  out->tc128 = false;
   const int es = elem_bytes(p.dtype);
   const int D = p.head_dim;
   // rows per kv head: its G query heads times Lq query rows
@@ -301,6 +342,8 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
   bool merged = false;
   if (plan.tc) {
     st = launch_decode_tc(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, &merged);
+  } else if (plan.tc128) {
+    st = launch_decode_tc128(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, &merged);
   } else {
     st = launch_vector(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, &merged);
   }
@@ -372,12 +415,25 @@ static sdpa_status_t launch_combine(int dtype, const dec::CombineArgs& c, unsign
                          cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     carveout_set = true;
   }
+  // programmatic stream serialization: the blocks may become resident while
+  // the split pass drains; each waits for it before its first global read
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(dec::kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   switch (dtype) {
-    case SDPA_F32: dec::decode_combine_kernel<float><<<grid, dec::kCombineThreads, 0, stream>>>(c); break;
-    case SDPA_F16: dec::decode_combine_kernel<__half><<<grid, dec::kCombineThreads, 0, stream>>>(c); break;
-    default: dec::decode_combine_kernel<__nv_bfloat16><<<grid, dec::kCombineThreads, 0, stream>>>(c); break;
+    case SDPA_F32: e = cudaLaunchKernelEx(&cfg, dec::decode_combine_kernel<float>, c); break;
+    case SDPA_F16: e = cudaLaunchKernelEx(&cfg, dec::decode_combine_kernel<__half>, c); break;
+    default: e = cudaLaunchKernelEx(&cfg, dec::decode_combine_kernel<__nv_bfloat16>, c); break;
   }
-  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 }  // namespace gb300

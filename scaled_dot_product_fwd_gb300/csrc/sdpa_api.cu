@@ -35,8 +35,8 @@ constexpr int kMaxDecodeRowsTc = 2;   // the same where a tensor-core prefill ex
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 // test hooks (sdpa_debug_set_option), indexed by sdpa_debug_option_t
-constexpr int kDebugOptions = 4;
-std::atomic<int> g_debug[kDebugOptions] = {{0}, {1}, {0}, {-1}};
+constexpr int kDebugOptions = 5;
+std::atomic<int> g_debug[kDebugOptions] = {{0}, {1}, {0}, {-1}, {0}};
 thread_local int g_last_launches = 0;
 std::mutex g_dev_mutex;
 int* g_status_ptr[kMaxDevices] = {};

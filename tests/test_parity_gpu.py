@@ -229,11 +229,18 @@ def test_decode_sweep(cuda, dtype, D, G, Lk):
     check(cuda, wl(2, Hkv * G, Hkv, 1, Lk, D, dtype, sinks=(Lk % 2 == 1)))
 
 
+@pytest.mark.parametrize("path", ["tc", "vector"])
 @pytest.mark.parametrize("cluster", [1, 0])
 @pytest.mark.parametrize("splits", [1, 2, 4, 5, 8, 16, 64])
-def test_decode_forced_splits(cuda, splits, cluster, hooks):
-    """Split counts that a thread-block cluster merges (2, 4, 8, 16) and ones
-    that go through the combine kernel; cluster "0" forces the two-pass form."""
+def test_decode_forced_splits(cuda, splits, cluster, path, hooks):
+    """Split counts on both head_dim-128 decode passes.  The vector pass
+    merges 2, 4, 8 or 16 splits inside a thread-block cluster (cluster "0"
+    forces its two-pass form); the tensor-core pass always merges through the
+    combine kernel, and holds at most 14 tiles of 128 keys per split (1 forced
+    split of 3001 keys runs as 2 splits of 12 tiles)."""
+    if path == "tc" and cluster == 0:
+        pytest.skip("the tensor-core pass has no cluster merge")
+    hooks("decode_vector", 1 if path == "vector" else 0)
     hooks("decode_splits", splits)
     hooks("decode_cluster", cluster)
     check(cuda, wl(1, 8, 1, 1, 3001, 128, "bfloat16", sinks=True))
@@ -301,15 +308,18 @@ def test_bottom_right_causal_lq_lt_lk(cuda):
     check(cuda, wl(1, 4, 2, 200, 1000, 128, "bfloat16", causal=True))
 
 
-def test_wait_timeout_reports_status(cuda, hooks):
+@pytest.mark.parametrize("path", ["tc", "vector"])
+def test_wait_timeout_reports_status(cuda, path, hooks):
     """A device wait that runs out sets the status word; the context stays
     usable.  The failure is made on the host: the decode producer is told to
-    drop its last copy, so the consumers' bounded wait on it expires."""
+    drop its last copy, so the consumers' bounded wait on it expires (on the
+    tensor-core pass, the MMA thread's wait on the last V tile)."""
     import torch
     import scaled_dot_product_fwd_gb300 as S
     w = wl(1, 4, 1, 1, 640, 128, "bfloat16")
     inp = W.make_inputs(w)
     q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    hooks("decode_vector", 1 if path == "vector" else 0)
     hooks("decode_splits", 1)
     hooks("decode_drop_last", 1)
     old = S.sdpa_debug_set_wait_limit_ns(50_000_000)
@@ -442,9 +452,15 @@ def test_launch_count_reports_kernels_per_call(cuda, hooks):
     assert run(wl(1, 2, 2, 300, 300, 64, "float16")) == 1
     assert run(wl(1, 2, 2, 300, 300, 64, "float32")) == 2
     hooks("decode_splits", 4)
+    assert run(wl(1, 8, 1, 1, 4096, 128, "bfloat16")) == 2  # tensor-core pass + combine
+    hooks("decode_splits", 1)
+    assert run(wl(1, 8, 1, 1, 1000, 128, "bfloat16")) == 1  # one split writes O
+    hooks("decode_splits", 4)
+    hooks("decode_vector", 1)
     assert run(wl(1, 8, 1, 1, 4096, 128, "bfloat16")) == 1  # 4 CTAs per cluster
     hooks("decode_cluster", 0)
     assert run(wl(1, 8, 1, 1, 4096, 128, "bfloat16")) == 2
+    hooks("decode_vector", 0)
     hooks("decode_cluster", 1)
     hooks("decode_splits", 0)
     q = torch.zeros(1, 2, 4, 64, device="cuda", dtype=torch.float16)
@@ -530,16 +546,30 @@ def test_kv_view_long_decode_and_few_queries(cuda):
                    lens_q=[2, 1], lens_kv=[777, 300])
 
 
+@pytest.mark.parametrize("path", ["tc", "vector"])
 @pytest.mark.parametrize("lens_kv", [[4096, 3584, 3072, 2560, 2048, 1536, 1024, 512],
                                      [4095, 1, 0, 2049, 17, 4096, 1000, 3]],
                          ids=["descending", "odd_and_empty"])
-def test_kv_view_ragged_plan(cuda, lens_kv):
+def test_kv_view_ragged_plan(cuda, lens_kv, path, hooks):
     """Decode over a KV cache with ragged per-batch lengths at the long
-    decode's head shape: the split size comes from the device lengths (every
-    CTA derives it, and the combine derives each row's split count), so the
-    items of the real keys fill whole waves."""
+    decode's head shape.  Vector pass: the split size comes from the device
+    lengths (every CTA derives it, and the combine derives each row's split
+    count), so the items of the real keys fill whole waves.  Tensor-core
+    pass: splits past a batch's length leave empty partial results."""
+    hooks("decode_vector", 1 if path == "vector" else 0)
     _kv_view_check(8, 32, 8, 1, 4096, 4096, 128, "bfloat16", False, sinks=True,
                    lens_q=[1] * 8, lens_kv=lens_kv)
+
+
+@pytest.mark.parametrize("dtype", ["float16", "bfloat16"])
+def test_kv_view_tc128_multi_tile_splits(cuda, dtype):
+    """The head_dim-128 tensor-core pass with splits of 14 tiles of 128 keys
+    (all score tiles of a split in TMEM, the K/V ring wrapping many times):
+    two query rows per batch (16 rows per kv head with G = 8), the causal rule,
+    sinks, ragged query and key lengths including empty and one-key rows."""
+    _kv_view_check(8, 64, 8, 2, 9000, 9100, 128, dtype, True, sinks=True,
+                   lens_q=[2, 1, 2, 0, 2, 2, 1, 2],
+                   lens_kv=[9000, 1, 4000, 0, 8999, 1793, 128, 129])
 
 
 def test_kv_view_noalloc(cuda):
