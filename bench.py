@@ -380,16 +380,17 @@ def secondary(torch, S, device, stream, peaks):
 
 
 def run_backward(torch, S, device, peaks):
-    """Backward pass (sdpa_backward: pre, main and post kernels) on the DiT
-    fp16 and causal GQA bf16 shapes; TFLOP/s counts 2.5 x the forward's
+    """Backward pass (sdpa_backward: pre, main and post kernels; fp32: pre,
+    dK/dV and dQ kernels) on the DiT fp16, causal GQA bf16 and DiT fp32
+    shapes; TFLOP/s counts 2.5 x the forward's
     algorithmic FLOPs (S recomputed, dP, dV, dK, dQ: five products of the
     forward's two).  Synthetic N(0, 1) q, k, v, dO drawn on the device; o and
     lse from the forward."""
     from scaled_dot_product_fwd_gb300 import workloads as W
     g = torch.Generator(device=device).manual_seed(1)
     res = {}
-    for w in (W.DIT_F16, W.CAUSAL_GQA):
-        dt = torch.float16 if w.dtype == "float16" else torch.bfloat16
+    for w in (W.DIT_F16, W.CAUSAL_GQA, W.DIT_F32):
+        dt = {"float16": torch.float16, "bfloat16": torch.bfloat16}.get(w.dtype, torch.float32)
         q = torch.randn(w.B, w.Hq, w.Lq, w.D, device=device, dtype=dt, generator=g)
         k = torch.randn(w.B, w.Hkv, w.Lk, w.D, device=device, dtype=dt, generator=g)
         v = torch.randn(w.B, w.Hkv, w.Lk, w.D, device=device, dtype=dt, generator=g)

@@ -224,8 +224,12 @@ SDPA_API size_t sdpa_backward_workspace_size(const sdpa_params_t* params);
  * dS = P (dO V^T - D), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO; with
  * the options of the mlx cuDNN backward graph: scale, bottom-right causal
  * mask, additive or boolean mask, sink token).  The problem description is
- * the forward's (same params); supported: dtype fp16 or bf16, head_dim 64 or
- * 128, no per-batch length arrays (else SDPA_ERR_UNSUPPORTED).
+ * the forward's (same params), per-batch length arrays included: rows and
+ * keys past a batch's lengths get zero gradients.  Supported: head_dim 64 or
+ * 128 (else SDPA_ERR_UNSUPPORTED); fp16/bf16 on the tensor cores, fp32 on
+ * fp32 CUDA-core kernels.  Rows of q, k, v and d_o inside seq_len_q /
+ * seq_len_kv but past a batch's lengths must hold finite values (whole tiles
+ * are read; their weights are zero).
  *  q, k, v, o, lse: the forward's inputs, output and log-sum-exp (lse is
  *      required: the forward must have been asked for it).
  *  d_o: gradient of the loss with respect to o, in o's layout.

@@ -177,14 +177,18 @@ def sdpa_backward_workspace_size(params: SdpaParams) -> int:
 
 
 def sdpa_backward(q, k, v, o, lse, d_o, scale=None, causal=False, mask=None, sinks=None,
-                  dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dQ, dK, dV of sdpa_forward on the GPU (fp16/bf16, head_dim 64 or 128).
+                  dq=None, dk=None, dv=None, workspace=None, stream=None, seq_lens_q=None,
+                  seq_lens_kv=None):
+    """dQ, dK, dV of sdpa_forward on the GPU (fp32/fp16/bf16, head_dim 64 or
+    128).
 
-    q, k, v, mask, sinks, scale and causal as given to sdpa_forward; o and
-    lse its outputs; d_o the gradient of the loss with respect to o (o's
-    shape and dtype).  Tensors need a contiguous last dimension; dq, dk, dv
-    default to the layouts of q, k, v.  dk and dv sum over the query heads of
-    each kv head.  Returns (dq, dk, dv).
+    q, k, v, mask, sinks, scale, causal and the per-batch lengths
+    (seq_lens_q, seq_lens_kv: int32 CUDA tensors of B elements) as given to
+    sdpa_forward; o and lse its outputs; d_o the gradient of the loss with
+    respect to o (o's shape and dtype).  Tensors need a contiguous last
+    dimension; dq, dk, dv default to the layouts of q, k, v.  dk and dv sum
+    over the query heads of each kv head; rows past a batch's lengths get
+    zero gradients.  Returns (dq, dk, dv).
     """
     torch = _torch()
     for t in (q, k, v, o, d_o):
@@ -228,9 +232,18 @@ def sdpa_backward(q, k, v, o, lse, d_o, scale=None, causal=False, mask=None, sin
     for g, t in ((dq, q), (dk, k), (dv, v)):
         if g.shape != t.shape or g.dtype != t.dtype or g.stride() != t.stride():
             raise ValueError("dq, dk, dv must have the shapes, dtype and layouts of q, k, v")
+    lens = []
+    for t in (seq_lens_q, seq_lens_kv):
+        if t is not None:
+            if t.dtype != torch.int32 or not t.is_cuda or t.numel() != B:
+                raise TypeError("seq_lens_q / seq_lens_kv must be int32 CUDA tensors of B elements")
+            t = t.contiguous()
+        lens.append(t)
     strides = tuple(tuple(int(s) for s in t.stride()[:3]) for t in (q, k, v, o))
     params = make_params(B, Hq, Hkv, Lq, Lk, D, dtype_code(q.dtype), scale, causal, mask_ptr,
-                         mstride, sinks_ptr, flags=flags, strides=strides)
+                         mstride, sinks_ptr, flags=flags, strides=strides,
+                         seq_lens_q_ptr=None if lens[0] is None else lens[0].data_ptr(),
+                         seq_lens_kv_ptr=None if lens[1] is None else lens[1].data_ptr())
     nbytes = sdpa_backward_workspace_size(params)
     if workspace is None and nbytes > 0:
         workspace = _workspace(nbytes, q.device)

@@ -107,6 +107,8 @@ struct BwdArgs {
   int mask_bool;
   const float* lse2;  // [B, Hq, Lq]: LSE in log2 units (+inf: the row sees nothing)
   const float* dvec;  // [B, Hq, Lq]: D_i = dO_i . O_i
+  const int* seq_lens_q;   // NULL or [B]: query rows [0, len) of batch b take part
+  const int* seq_lens_kv;  // NULL or [B]: keys [0, len) of batch b are visible
   float* dq_acc;      // [B, Hq, Lq, D] fp32, cleared before the pass
   void* dk;
   void* dv;
@@ -179,8 +181,8 @@ __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c
 
 // ---------------------------------------------------------------- pre / post
 // Per query row (b, h, i): D_i = dO_i . O_i, LSE in log2 units (+inf for a
-// row that saw nothing, so that every P of it is 0), and a cleared dQ row.
-// One warp per row.
+// row that saw nothing, or lies past its batch's query length, so that every
+// P of it is 0), and a cleared dQ row.  One warp per row.
 struct PreArgs {
   const void* o;
   const void* d_o;
@@ -188,6 +190,7 @@ struct PreArgs {
   float* lse2;
   float* dvec;
   float* dq_acc;
+  const int* seq_lens_q;  // NULL or [B]: rows at or past a batch's length take no part
   int Hq, Lq, D;
   long long os0, os1, os2;  // strides of o and dO (dO has o's layout)
   long long rows;
@@ -199,6 +202,8 @@ template <>
 __device__ __forceinline__ float ld_f(const __half* p) { return __half2float(*p); }
 template <>
 __device__ __forceinline__ float ld_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+template <>
+__device__ __forceinline__ float ld_f(const float* p) { return *p; }
 
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
@@ -215,11 +220,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreArgs a) {
   for (int d = lane; d < a.D; d += 32) s = fmaf(ld_f(o + d), ld_f(g + d), s);
 #pragma unroll
   for (int w = 16; w >= 1; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
-  float* dq = a.dq_acc + row * a.D;
-  for (int d = lane; d < a.D; d += 32) dq[d] = 0.f;
+  if (a.dq_acc) {
+    float* dq = a.dq_acc + row * a.D;
+    for (int d = lane; d < a.D; d += 32) dq[d] = 0.f;
+  }
   if (lane == 0) {
     a.dvec[row] = s;
-    const float l = a.lse[row];
+    const bool live = !a.seq_lens_q || i < min(max(a.seq_lens_q[b], 0), a.Lq);
+    const float l = live ? a.lse[row] : -INFINITY;
     // A row that saw no key, or only keys whose mask values were huge (LSE
     // -2^100 * scale, beside which its scores vanish), takes no part: P = 0
     // there.  For the latter that is exact for dQ and dK (the scores do not
@@ -305,12 +313,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int j0 = blockIdx.x * kBT;  // first key of the tile
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
-  const int off = a.Lk - a.Lq;      // bottom-right causal: key j visible to row i iff j <= i + off
-  // query tiles of each head that hold a row seeing a key of this tile
-  const int nqt = (a.Lq + kBT - 1) / kBT;
+  // this batch's lengths (padding masks), clamped to the call's
+  const int Lkb = a.seq_lens_kv ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
+  const int Lqb = a.seq_lens_q ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
+  const int off = Lkb - Lqb;  // bottom-right causal: key j visible to row i iff j <= i + off
+  // query tiles of each head that hold a row seeing a key of this tile (none
+  // when the tile lies past the batch's keys)
+  const int nqt = (Lqb + kBT - 1) / kBT;
   int qt0 = 0;
   if (a.causal && j0 - off > 0) qt0 = (j0 - off) / kBT;
-  const int per_head = nqt > qt0 ? nqt - qt0 : 0;
+  const int per_head = (nqt > qt0 && j0 < Lkb) ? nqt - qt0 : 0;
   const int nsteps = a.G * per_head;  // (query head of the group, query tile) pairs
 
   if (threadIdx.x == 0) {
@@ -490,8 +502,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int hq = kvh * a.G + s / per_head;
       const int i = (qt0 + s % per_head) * kBT + (threadIdx.x & (kBT - 1));
       const size_t row = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq + i;
-      if (threadIdx.x < kBT) return i < a.Lq ? -a.lse2[row] : -INFINITY;
-      return i < a.Lq ? -a.dvec[row] : 0.f;
+      if (threadIdx.x < kBT) return i < Lqb ? -a.lse2[row] : -INFINITY;
+      return i < Lqb ? -a.dvec[row] : 0.f;
     };
     float stat = nsteps > 0 ? row_stat(0) : 0.f;
     // dQ tile of step s (TMEM lane r = query row q0 + r) added into the fp32
@@ -507,7 +519,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t v[32];
         __syncwarp();  // .aligned TMEM access after per-lane stores
         tmem_ld32_sync(tmem + lane_off + C::dq_col(s) + hf * (D / 2) + c * 32, v);
-        if (i < a.Lq) {
+        if (i < Lqb) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
@@ -547,14 +559,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       named_bar_sync(kBarPair + quarter, 64);
       if (ok) {
         // visible query columns of this key: [clo, chi) of the tile
-        int clo = 0, chi = min(kBT, a.Lq - q0);
-        if (jr >= a.Lk) chi = 0;
+        int clo = 0, chi = min(kBT, Lqb - q0);
+        if (jr >= Lkb) chi = 0;
         if (a.causal) clo = min(max(jr - off - q0, 0), kBT);
         // mask entries of this key for the tile's rows (ms2 apart): additive
         // (mrow) or boolean (mrowb)
         const T* mrow = nullptr;
         const uint8_t* mrowb = nullptr;
-        if (a.mask && jr < a.Lk) {
+        if (a.mask && jr < Lkb) {
           const long long moff = b * a.ms0 + hq * a.ms1 + q0 * a.ms2 + jr;
           if (a.mask_bool)
             mrowb = static_cast<const uint8_t*>(a.mask) + moff;
@@ -713,6 +725,41 @@ size_t backward_workspace(const sdpa_params_t& p) {
   return align256b(rows * p.head_dim * 4) + 2 * align256b(rows * 4);
 }
 
+void backward_stats_slots(const sdpa_params_t& p, void* workspace, float** lse2, float** dvec) {
+  const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  *lse2 = reinterpret_cast<float*>(w + align256b(rows * p.head_dim * 4));
+  *dvec = reinterpret_cast<float*>(w + align256b(rows * p.head_dim * 4) + align256b(rows * 4));
+}
+
+sdpa_status_t launch_backward_pre(const sdpa_params_t& p, const void* o, const void* d_o,
+                                  const float* lse, float* lse2, float* dvec, float* dq_acc,
+                                  cudaStream_t stream) {
+  PreArgs pa;
+  pa.o = o;
+  pa.d_o = d_o;
+  pa.lse = lse;
+  pa.lse2 = lse2;
+  pa.dvec = dvec;
+  pa.dq_acc = dq_acc;
+  pa.seq_lens_q = p.seq_lens_q;
+  pa.Hq = p.num_q_heads;
+  pa.Lq = p.seq_len_q;
+  pa.D = p.head_dim;
+  pa.os0 = p.o_stride[0];
+  pa.os1 = p.o_stride[1];
+  pa.os2 = p.o_stride[2];
+  pa.rows = static_cast<long long>(p.batch) * p.num_q_heads * p.seq_len_q;
+  if (pa.rows <= 0) return SDPA_OK;
+  const unsigned blocks = static_cast<unsigned>((pa.rows * 32 + 255) / 256);
+  switch (p.dtype) {
+    case SDPA_F32: bwd_pre_kernel<float><<<blocks, 256, 0, stream>>>(pa); break;
+    case SDPA_F16: bwd_pre_kernel<__half><<<blocks, 256, 0, stream>>>(pa); break;
+    default: bwd_pre_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(pa); break;
+  }
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
 namespace {
 
 template <int D, bool BF16>
@@ -728,25 +775,10 @@ sdpa_status_t launch_bwd_impl(const sdpa_params_t& p, const void* q, const void*
   float* lse2 = reinterpret_cast<float*>(w + align256b(rows * D * 4));
   float* dvec = reinterpret_cast<float*>(w + align256b(rows * D * 4) + align256b(rows * 4));
   // D_i, LSE in log2 units, cleared dQ accumulator
-  PreArgs pa;
-  pa.o = o;
-  pa.d_o = d_o;
-  pa.lse = lse;
-  pa.lse2 = lse2;
-  pa.dvec = dvec;
-  pa.dq_acc = dq_acc;
-  pa.Hq = p.num_q_heads;
-  pa.Lq = p.seq_len_q;
-  pa.D = D;
-  pa.os0 = p.o_stride[0];
-  pa.os1 = p.o_stride[1];
-  pa.os2 = p.o_stride[2];
-  pa.rows = rows;
-  const unsigned row_blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
   int launched = 0;
   if (rows > 0) {
-    bwd_pre_kernel<T><<<row_blocks, 256, 0, env.stream>>>(pa);
-    if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
+    const sdpa_status_t st = launch_backward_pre(p, o, d_o, lse, lse2, dvec, dq_acc, env.stream);
+    if (st != SDPA_OK) return st;
     ++launched;
   }
   if (p.seq_len_kv > 0) {
@@ -783,6 +815,8 @@ sdpa_status_t launch_bwd_impl(const sdpa_params_t& p, const void* q, const void*
     a.mask_bool = (p.flags & SDPA_FLAG_BOOL_MASK) ? 1 : 0;
     a.lse2 = lse2;
     a.dvec = dvec;
+    a.seq_lens_q = p.seq_lens_q;
+    a.seq_lens_kv = p.seq_lens_kv;
     a.dq_acc = dq_acc;
     a.dk = dk;
     a.dv = dv;
@@ -827,6 +861,7 @@ sdpa_status_t launch_bwd_impl(const sdpa_params_t& p, const void* q, const void*
   qa.qs2 = p.q_stride[2];
   qa.rows = rows;
   if (rows > 0) {
+    const unsigned row_blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
     bwd_post_kernel<T><<<row_blocks, 256, 0, env.stream>>>(qa);
     if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
     ++launched;
@@ -841,6 +876,8 @@ sdpa_status_t launch_backward(const sdpa_params_t& p, const void* q, const void*
                               const void* v, const void* o, const void* d_o, const float* lse,
                               void* dq, void* dk, void* dv, void* workspace,
                               const LaunchEnv& env) {
+  if (p.dtype == SDPA_F32)
+    return launch_backward_f32(p, q, k, v, o, d_o, lse, dq, dk, dv, workspace, env);
   const bool bf16 = p.dtype == SDPA_BF16;
   if (p.head_dim == 64)
     return bf16 ? launch_bwd_impl<64, true>(p, q, k, v, o, d_o, lse, dq, dk, dv, workspace, env)

@@ -93,6 +93,19 @@ sdpa_status_t launch_decode(const sdpa_params_t& p, const DecodePlan& plan, cons
 // layouts of q, k, v; dO in o's layout; lse the forward's.  Workspace:
 // backward_workspace(p) bytes (fp32 dQ accumulator, LSE in log2 units, D).
 size_t backward_workspace(const sdpa_params_t& p);
+// Addresses of the LSE (log2 units) and D arrays inside that workspace.
+void backward_stats_slots(const sdpa_params_t& p, void* workspace, float** lse2, float** dvec);
+// The backward's pre pass: D_i = dO_i . O_i and LSE in log2 units per query
+// row (+inf where the row takes no part), and a cleared dQ accumulator
+// (dq_acc may be NULL).
+sdpa_status_t launch_backward_pre(const sdpa_params_t& p, const void* o, const void* d_o,
+                                  const float* lse, float* lse2, float* dvec, float* dq_acc,
+                                  cudaStream_t stream);
+// The fp32 backward (CUDA-core kernels; backward_f32.cu).
+sdpa_status_t launch_backward_f32(const sdpa_params_t& p, const void* q, const void* k,
+                                  const void* v, const void* o, const void* d_o,
+                                  const float* lse, void* dq, void* dk, void* dv,
+                                  void* workspace, const LaunchEnv& env);
 sdpa_status_t launch_backward(const sdpa_params_t& p, const void* q, const void* k,
                               const void* v, const void* o, const void* d_o, const float* lse,
                               void* dq, void* dk, void* dv, void* workspace,

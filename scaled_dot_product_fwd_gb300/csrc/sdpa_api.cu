@@ -309,9 +309,7 @@ namespace {
 sdpa_status_t validate_backward(const sdpa_params_t* p) {
   const sdpa_status_t st = validate_problem(p);
   if (st != SDPA_OK) return st;
-  if (p->dtype != SDPA_F16 && p->dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128) return SDPA_ERR_UNSUPPORTED;
-  if (p->seq_lens_q || p->seq_lens_kv) return SDPA_ERR_UNSUPPORTED;
   return SDPA_OK;
 }
 }  // namespace
