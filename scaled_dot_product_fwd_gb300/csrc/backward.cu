@@ -278,7 +278,9 @@ __device__ __forceinline__ void bwd_drain_wait(uint64_t* bar, uint32_t parity, u
 }
 
 // ---------------------------------------------------------------- main pass
-template <int D, bool BF16>
+// LENS: the call has per-batch length arrays (without them the lengths stay
+// the call's own, read from the kernel parameters where they are used).
+template <int D, bool BF16, bool LENS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -314,8 +316,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int kvh = blockIdx.y;
   const int b = blockIdx.z;
   // this batch's lengths (padding masks), clamped to the call's
-  const int Lkb = a.seq_lens_kv ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
-  const int Lqb = a.seq_lens_q ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
+  const int Lkb = (LENS && a.seq_lens_kv) ? min(max(a.seq_lens_kv[b], 0), a.Lk) : a.Lk;
+  const int Lqb = (LENS && a.seq_lens_q) ? min(max(a.seq_lens_q[b], 0), a.Lq) : a.Lq;
   const int off = Lkb - Lqb;  // bottom-right causal: key j visible to row i iff j <= i + off
   // query tiles of each head that hold a row seeing a key of this tile (none
   // when the tile lies past the batch's keys)
@@ -828,19 +830,20 @@ sdpa_status_t launch_bwd_impl(const sdpa_params_t& p, const void* q, const void*
     a.dvs2 = p.v_stride[2];
     a.status = env.status;
     a.wait_ns = env.wait_limit_ns;
-    auto kern = bwd_kernel<D, BF16>;
+    const bool lens = p.seq_lens_q || p.seq_lens_kv;
+    auto kern = lens ? bwd_kernel<D, BF16, true> : bwd_kernel<D, BF16, false>;
     // The setmaxnreg split must fit the registers the kernel is launched with
-    // (an increase beyond them would wait forever): check once.
-    static int regs_ok = 0;  // 0 unknown, 1 fits, -1 does not
-    if (regs_ok == 0) {
+    // (an increase beyond them would wait forever): check once per kernel.
+    static int regs_ok[2] = {0, 0};  // 0 unknown, 1 fits, -1 does not
+    if (regs_ok[lens] == 0) {
       cudaFuncAttributes fa;
       if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SDPA_ERR_CUDA;
       const long alloc = static_cast<long>((fa.numRegs + 7) & ~7) * kBwdThreads;
       const long need = static_cast<long>(kComputeThreads) * kComputeRegs +
                         static_cast<long>(kBwdThreads - kComputeThreads) * kControlRegs;
-      regs_ok = alloc >= need ? 1 : -1;
+      regs_ok[lens] = alloc >= need ? 1 : -1;
     }
-    if (regs_ok < 0) return SDPA_ERR_UNSUPPORTED;
+    if (regs_ok[lens] < 0) return SDPA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
         cudaSuccess)
       return SDPA_ERR_CUDA;
