@@ -379,7 +379,7 @@ def secondary(torch, S, device, stream, peaks):
     return out
 
 
-def run_backward(torch, S, device, peaks):
+def run_backward(torch, S, device, peaks, names=None):
     """Backward pass (sdpa_backward: pre, main and post kernels; fp32: pre,
     dK/dV and dQ kernels) on the DiT fp16, causal GQA bf16 and DiT fp32
     shapes; TFLOP/s counts 2.5 x the forward's
@@ -390,6 +390,8 @@ def run_backward(torch, S, device, peaks):
     g = torch.Generator(device=device).manual_seed(1)
     res = {}
     for w in (W.DIT_F16, W.CAUSAL_GQA, W.DIT_F32):
+        if names and w.name not in names:
+            continue
         dt = {"float16": torch.float16, "bfloat16": torch.bfloat16}.get(w.dtype, torch.float32)
         q = torch.randn(w.B, w.Hq, w.Lq, w.D, device=device, dtype=dt, generator=g)
         k = torch.randn(w.B, w.Hkv, w.Lk, w.D, device=device, dtype=dt, generator=g)
@@ -721,6 +723,8 @@ def main():
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the backward pass workloads and print them (a profiling "
                          "target; not the benchmark line)")
+    ap.add_argument("--backward-workloads", default="",
+                    help="with --backward-only: comma-separated workload names (default: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -729,7 +733,8 @@ def main():
         import scaled_dot_product_fwd_gb300 as S
         torch.cuda.set_device(0)
         peaks, _ = load_peaks()
-        print(json.dumps(run_backward(torch, S, "cuda", peaks)), flush=True)
+        names = [n for n in args.backward_workloads.split(",") if n]
+        print(json.dumps(run_backward(torch, S, "cuda", peaks, names)), flush=True)
         return
     if args.impl == "reference":
         reference_arm(args)
