@@ -160,6 +160,49 @@ def test_decode_workspace_size_and_check(sdpa_lib):
     assert S.sdpa_forward_raw(pf, 256, 256, 256, 256, None, None, 0, None) == 4
 
 
+def _ws(rows, splits, D):
+    """Workspace of a two-pass decode plan: rows x splits partial outputs of D
+    floats, then rows x splits (m, l) pairs, each part 256-byte aligned."""
+    a = lambda x: (x + 255) // 256 * 256
+    return a(rows * splits * D * 4) + a(rows * splits * 2 * 4)
+
+
+def test_tc128_decode_plan(sdpa_lib):
+    """The head_dim-128 tensor-core decode plan, through the workspace it
+    asks for (pure host logic; 152 SMs when no device is visible): splits of
+    at most 14 tiles of 128 keys, as many per (kv head, batch) as one wave of
+    two CTAs per SM holds, the tiles spread evenly over them."""
+    # long decode: 64 (kv head, batch) units, 256 tiles: 4 splits a unit
+    # would exceed 14 tiles, so 19 splits of 14 (the last one 4)
+    p = P(Lq=1, Lk=32768, B=8, Hq=32, Hkv=8, D=128)
+    assert S.sdpa_workspace_size(p) == _ws(8 * 32, 19, 128)
+    # one tile: one split, O written directly, no workspace
+    assert S.sdpa_workspace_size(P(Lq=1, Lk=128, B=1, Hq=8, Hkv=1, D=128)) == 0
+    # a single kv head of 3001 keys (24 tiles): 24 one-tile splits fill the wave
+    p1 = P(Lq=1, Lk=3001, B=1, Hq=8, Hkv=1, D=128, dtype=S.SDPA_F16)
+    assert S.sdpa_workspace_size(p1) == _ws(8, 24, 128)
+    prev = S.sdpa_debug_set_option("decode_splits", 1)
+    try:
+        # one forced split exceeds 14 tiles: two splits of 12
+        assert S.sdpa_workspace_size(p1) == _ws(8, 2, 128)
+    finally:
+        S.sdpa_debug_set_option("decode_splits", prev)
+    # one kv head of 131072 keys (1024 tiles): 304 splits would hold 3.4
+    # tiles, so 256 splits of 4
+    assert S.sdpa_workspace_size(P(Lq=1, Lk=131072, B=1, Hq=16, Hkv=1, D=128)) == \
+        _ws(16, 256, 128)
+    prev = S.sdpa_debug_set_option("decode_vector", 1)
+    try:
+        # the vector path's own plan (a different split count)
+        ws_vec = S.sdpa_workspace_size(p1)
+        assert ws_vec > 0 and ws_vec != _ws(8, 24, 128)
+    finally:
+        S.sdpa_debug_set_option("decode_vector", prev)
+    # fp32 and more than 16 rows per kv head stay on the vector path
+    assert S.sdpa_workspace_size(P(Lq=1, Lk=32768, B=8, Hq=32, Hkv=8, D=128,
+                                   dtype=S.SDPA_F32)) != _ws(8 * 32, 19, 128)
+
+
 def test_python_binding_rejects_cpu_tensors(sdpa_lib):
     torch = pytest.importorskip("torch")
     q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
