@@ -125,7 +125,7 @@ typedef enum {
  *      uses the batch's own lengths: key j visible to query i iff
  *      j <= i + (seq_lens_kv[b] - seq_lens_q[b]).  Both arrays must stay
  *      valid until the call's kernels have run.  The prefill kernels and
- *      the fp16/bf16 decode passes at head_dim 128 and 512 load whole key
+ *      the fp16/bf16 decode passes load whole key
  *      tiles, so v rows [seq_lens_kv[b], seq_len_kv) meet zero weights there
  *      and must hold finite values (rows past seq_len_kv are never read).
  *  flags: an OR of the SDPA_FLAG_* bits below (other bits must be 0, else
@@ -324,8 +324,9 @@ SDPA_API uint64_t sdpa_debug_set_wait_limit_ns(uint64_t ns);
  *  SDPA_DEBUG_PREFILL_SPLIT   -1: the plan's (default); 0: never split the
  *                             last wave; 2, 4: every unit shared by that
  *                             many CTAs of a cluster
- *  SDPA_DEBUG_DECODE_VECTOR   1: head_dim-128 fp16/bf16 decode on the vector
- *                             path instead of the tensor-core pass (default 0)
+ *  SDPA_DEBUG_DECODE_VECTOR   1: head_dim-64/128 fp16/bf16 decode on the
+ *                             vector path instead of the tensor-core pass
+ *                             (default 0)
  */
 typedef enum {
   SDPA_DEBUG_DECODE_SPLITS = 0,

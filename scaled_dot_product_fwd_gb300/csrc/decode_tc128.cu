@@ -1,7 +1,7 @@
-// decode_tc128.cu — single- and few-query attention at head_dim 128 for
-// fp16/bf16 on the 5th-generation tensor cores: the split-KV first pass of
-// long key ranges (KV-cache decode), with the query rows of one kv head (its
-// G heads x Lq rows, up to 16) on the narrow side of both products.
+// decode_tc128.cu — single- and few-query attention at head_dim 128 (and
+// 64) for fp16/bf16 on the 5th-generation tensor cores: the split-KV first
+// pass of long key ranges (KV-cache decode), with the query rows of one kv
+// head (its G heads x Lq rows, up to 16) on the narrow side of both products.
 //
 // The method is the two-pass split-KV attention of MLX PR #4459 ("Add D512
 // support to Metal vector attention"): a first pass over chunks of the key
@@ -9,8 +9,10 @@
 // second pass that merges the chunks by their log-sum-exp (the combine
 // kernel).  With G query heads per kv head, a split's per-key dot products
 // and its value accumulation are two skinny matrix products,
-//     S^T  = K Q^T     M = 128 keys,       N = 16 rows, K = 128
+//     S^T  = K Q^T     M = 128 keys,       N = 16 rows, K = D
 //     O^T += V^T P^T   M = 128 head dims,  N = 16 rows, K = 128 keys
+// (at D = 64 the second 64 rows of V^T are the slot's unused half: those
+// rows of O^T are never read)
 // which leave the CUDA cores nothing per key but the exponential: a vector
 // kernel spends about 250 FMAs of dot products and accumulation per (key,
 // head) and cannot stream K and V faster than its arithmetic, while here the
@@ -19,8 +21,8 @@
 // One CTA per (split of at most kMaxTiles tiles of 128 keys, kv head,
 // batch), two CTAs per SM (256 TMEM columns and 110 KB of shared memory
 // each).  Warp 4 loads Q (one box per 64 columns), then the split's K tiles,
-// then its V tiles, through a 3-slot ring of 32 KB (a tile: two 64-column
-// chunks of 128 rows, 128-byte swizzle); warp 5 (one thread) issues the
+// then its V tiles, through a 3-slot ring of 32 KB (a tile: D / 64 chunks of
+// 64 columns and 128 rows, 128-byte swizzle); warp 5 (one thread) issues the
 // MMAs.  Every score tile of the split stays in TMEM (16 columns each), so
 // warps 0-3 (thread = TMEM lane: a key of the tile, later a head dimension of
 // O^T) take the exact row max over the whole split before any probability is
@@ -39,14 +41,13 @@
 namespace gb300 {
 namespace dtc128 {
 
-constexpr int kD = 128;
 constexpr int kTK = 128;                 // keys per tile (rows of S^T)
 constexpr int kN = 16;                   // query rows of a kv head, padded
 constexpr int kMaxTiles = 14;            // key tiles per split (score tiles in TMEM)
 constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 columns of 2 bytes
-constexpr int kSlotBytes = 2 * kChunkBytes;  // a K or V tile, all 128 columns
+constexpr int kSlotBytes = 2 * kChunkBytes;  // a K or V tile (two chunks at D = 128)
 constexpr int kRing = 3;
-constexpr int kQChunkBytes = kN * 128;   // Q: 2 chunks of kN rows x 64 columns
+constexpr int kQChunkBytes = kN * 128;   // Q: D / 64 chunks of kN rows x 64 columns
 constexpr int kQBytes = 2 * kQChunkBytes;
 constexpr int kPChunkBytes = kN * 128;   // P^T of a tile: 2 chunks of kN rows x 64 keys
 constexpr int kPBytes = 2 * kPChunkBytes;
@@ -172,9 +173,9 @@ __device__ __forceinline__ float rcp(float x) {
   return y;
 }
 
-// NR: rows of a kv head the softmax handles (8 or 16; R <= NR); the products
-// always carry kN = 16 columns.
-template <bool BF16, int NR>
+// D: head_dim (64 or 128).  NR: rows of a kv head the softmax handles (8 or
+// 16; R <= NR); the products always carry kN = 16 columns.
+template <int D, bool BF16, int NR>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_tc128_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
@@ -258,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       // Q: per 64 columns one box of the kv head's G heads x Lq rows, which
       // lands as rows (head, query row) = c of the chunk (rows past R are
       // not written: they only reach score columns that are never read)
-      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(2 * a.R * 128));
-      for (int c = 0; c < 2; ++c)
+      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>((D / 64) * a.R * 128));
+      for (int c = 0; c < D / 64; ++c)
         tma_load_4d(sQ + c * kQChunkBytes, &tmQ, q_full, 64 * c, 0, kvh * a.G, b);
       // the split's K tiles, then its V tiles; keys past Lk read as zero
       int seq = 0;
@@ -277,11 +278,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             pok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], kSlotBytes);
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>((D / 64) * kChunkBytes));
           uint8_t* dst = sRing + s * kSlotBytes;
           const int key = key_begin + t * kTK;
-          tma_load_4d(dst, map, &full[s], 0, key, kvh, b);
-          tma_load_4d(dst + kChunkBytes, map, &full[s], 64, key, kvh, b);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(dst + c * kChunkBytes, map, &full[s], 64 * c, key, kvh, b);
           last_use[s] = use;
         }
       }
@@ -296,20 +297,20 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint64_t k_desc = sdesc(smem_addr(sRing), 16, 1024, kSwizzle128B);
       const uint64_t q_desc = sdesc(smem_addr(sQ), 16, 1024, kSwizzle128B);
       // V^T (A, MN-major: the two 64-column atoms 16 KB apart, 8-key groups
-      // 1024 bytes apart; a K step of 16 keys is 2048 bytes) and P^T (B,
-      // K-major)
+      // 1024 bytes apart; a K step of 16 keys is 2048 bytes; at D = 64 the
+      // second atom is the slot's unused half) and P^T (B, K-major)
       const uint64_t v_desc = sdesc(smem_addr(sRing), kChunkBytes, 1024, kSwizzle128B);
       const uint64_t p_desc = sdesc(smem_addr(sP), 16, 1024, kSwizzle128B);
       bool mok = ntile == 0 || mbar_wait(q_full, 0, wc);
       int seq = 0;
       for (int t = 0; t < ntile; ++t, ++seq) {
-        // S^T_t = K_t Q^T over the 8 column steps
+        // S^T_t = K_t Q^T over the D / 16 column steps
         const int s = seq % kRing;
         mok = mok && mbar_wait(&full[s], static_cast<uint32_t>((seq / kRing) & 1), wc);
         if (mok) {
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ko = s * kSlotBytes + (kk >> 2) * kChunkBytes + (kk & 3) * 32;
             const uint32_t qo = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
             mma_f16_ss(tmem + t * kN, k_desc + (ko >> 4), q_desc + (qo >> 4), idS,
@@ -459,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int c = 0; c < NR; ++c)
       Lr[c] = (red_l[c] + red_l[NR + c]) + (red_l[2 * NR + c] + red_l[3 * NR + c]);
 
-    // O^T: thread i holds head dimension i of the NR rows
+    // O^T: thread i holds head dimension i of the NR rows (i < D)
     ok = __all_sync(0xffffffffu, ok && (ntile == 0 || mbar_wait(o_done, 0, wc)));
     float ov[NR];
 #pragma unroll
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           const float w = (L > 0.f && Lr[c] > 0.f) ? Lr[c] * f * rcp(L) : 0.f;
           T* orow = static_cast<T*>(a.o) + b * a.os0 + hq * a.os1 + a.row_q[c] * a.os2 + i;
-          orow[0] = E::c(ov[c] * w);
+          if (i < D) orow[0] = E::c(ov[c] * w);
           if (i == c && a.lse) {
             const size_t row = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq + a.row_q[c];
             a.lse[row] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
@@ -511,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int hq = kvh * a.G + a.row_h[c];
           const size_t row = (static_cast<size_t>(b) * a.Hq + hq) * a.Lq + a.row_q[c];
           const size_t slot = row * a.num_splits + split;
-          a.ws_o[slot * kD + i] = ov[c];
+          if (i < D) a.ws_o[slot * D + i] = ov[c];
           if (i == c) {
             a.ws_ml[2 * slot] = Lr[c] > 0.f ? Mr[c] : -INFINITY;
             a.ws_ml[2 * slot + 1] = Lr[c];
@@ -540,12 +541,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 }  // namespace dtc128
 
-// Whether the head_dim-128 tensor-core pass takes a decode problem: fp16 or
-// bf16, up to 16 rows per kv head, and q, k, v strides that a tensor map
+// Whether the tensor-core pass takes a decode problem: head_dim 64 or 128,
+// fp16 or bf16, up to 16 rows per kv head, and q, k, v strides that a tensor map
 // takes (positive multiples of 16 bytes, the dense layout when the caller
 // gave none).
 static bool tc128_fits(const sdpa_params_t& p) {
-  if (p.head_dim != dtc128::kD || p.dtype == SDPA_F32) return false;
+  if ((p.head_dim != 64 && p.head_dim != 128) || p.dtype == SDPA_F32) return false;
   const int R = p.num_q_heads / p.num_kv_heads * p.seq_len_q;
   if (R > dtc128::kN || p.num_kv_heads > 65535 || p.batch > 65535) return false;
   if (debug_option(SDPA_DEBUG_DECODE_VECTOR) == 1) return false;  // test hook
@@ -557,7 +558,7 @@ static bool tc128_fits(const sdpa_params_t& p) {
   return true;
 }
 
-// Plan of the head_dim-128 tensor-core decode: as many splits per (kv head,
+// Plan of the tensor-core decode at head_dim 64/128: as many splits per (kv head,
 // batch) as one wave of two CTAs per SM holds, each at most kMaxTiles tiles
 // (more splits, in further waves, where that bound requires), the tiles
 // spread evenly over the splits.  Returns false when the problem is not one
@@ -593,13 +594,13 @@ bool decode_tc128_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out) {
   out->workspace = 0;
   if (S > 1) {
     const size_t rows = static_cast<size_t>(p.batch) * p.num_q_heads * p.seq_len_q * S;
-    out->workspace = ((rows * dtc128::kD * sizeof(float) + 255) & ~static_cast<size_t>(255)) +
+    out->workspace = ((rows * p.head_dim * sizeof(float) + 255) & ~static_cast<size_t>(255)) +
                      ((rows * 2 * sizeof(float) + 255) & ~static_cast<size_t>(255));
   }
   return true;
 }
 
-template <bool BF16>
+template <int D, bool BF16>
 static sdpa_status_t launch_tc128(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
                                   const void* k, const void* v, void* o, float* lse,
                                   float* ws_o, float* ws_ml, const LaunchEnv& env,
@@ -609,15 +610,15 @@ static sdpa_status_t launch_tc128(const sdpa_params_t& p, const DecodePlan& plan
       BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const int G = p.num_q_heads / p.num_kv_heads;
   CUtensorMap tq, tk, tv;
-  // q as [B, Hq, Lq, 128], box 64 x Lq rows x G heads; k, v as
-  // [B, Hkv, Lk, 128], box 64 x 128 rows (rows past Lk read as zero); all
+  // q as [B, Hq, Lq, D], box 64 x Lq rows x G heads; k, v as
+  // [B, Hkv, Lk, D], box 64 x 128 rows (rows past Lk read as zero); all
   // with the given strides, innermost first, 128-byte swizzle
-  if (!encode_tiled_4d_box(&tq, dt, q, kD, p.seq_len_q, p.num_q_heads, p.batch, 2, 64,
+  if (!encode_tiled_4d_box(&tq, dt, q, D, p.seq_len_q, p.num_q_heads, p.batch, 2, 64,
                            static_cast<uint32_t>(p.seq_len_q), static_cast<uint32_t>(G),
                            p.q_stride[2], p.q_stride[1], p.q_stride[0]) ||
-      !encode_tiled_4d(&tk, dt, k, kD, p.seq_len_kv, p.num_kv_heads, p.batch, 2, 64, kTK,
+      !encode_tiled_4d(&tk, dt, k, D, p.seq_len_kv, p.num_kv_heads, p.batch, 2, 64, kTK,
                        p.k_stride[2], p.k_stride[1], p.k_stride[0]) ||
-      !encode_tiled_4d(&tv, dt, v, kD, p.seq_len_kv, p.num_kv_heads, p.batch, 2, 64, kTK,
+      !encode_tiled_4d(&tv, dt, v, D, p.seq_len_kv, p.num_kv_heads, p.batch, 2, 64, kTK,
                        p.v_stride[2], p.v_stride[1], p.v_stride[0]))
     return SDPA_ERR_CUDA;
   Args a;
@@ -656,7 +657,7 @@ static sdpa_status_t launch_tc128(const sdpa_params_t& p, const DecodePlan& plan
   a.status = env.status;
   a.wait_ns = env.wait_limit_ns;
   a.debug_drop_last = debug_option(SDPA_DEBUG_DECODE_DROP_LAST) == 1 ? 1 : 0;
-  auto kern = a.R <= 8 ? decode_tc128_kernel<BF16, 8> : decode_tc128_kernel<BF16, 16>;
+  auto kern = a.R <= 8 ? decode_tc128_kernel<D, BF16, 8> : decode_tc128_kernel<D, BF16, 16>;
   static bool attr_set[2] = {false, false};
   if (!attr_set[a.R <= 8]) {
     cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -686,10 +687,14 @@ sdpa_status_t launch_decode_tc128(const sdpa_params_t& p, const DecodePlan& plan
                                   const void* k, const void* v, void* o, float* lse,
                                   float* ws_o, float* ws_ml, const LaunchEnv& env,
                                   bool* merged) {
-  if (p.dtype == SDPA_BF16)
-    return launch_tc128<true>(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, merged);
-  if (p.dtype == SDPA_F16)
-    return launch_tc128<false>(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, merged);
+  const bool bf16 = p.dtype == SDPA_BF16;
+  if (p.dtype != SDPA_BF16 && p.dtype != SDPA_F16) return SDPA_ERR_UNSUPPORTED;
+  if (p.head_dim == 128)
+    return bf16 ? launch_tc128<128, true>(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, merged)
+                : launch_tc128<128, false>(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, merged);
+  if (p.head_dim == 64)
+    return bf16 ? launch_tc128<64, true>(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, merged)
+                : launch_tc128<64, false>(p, plan, q, k, v, o, lse, ws_o, ws_ml, env, merged);
   return SDPA_ERR_UNSUPPORTED;
 }
 

@@ -37,8 +37,8 @@ struct DecodePlan {
   int tiles_base = 0;   // tiles per split for rows of the full length
   bool tc = false;  // head_dim 512, fp16/bf16, up to 16 rows per kv head: the
                     // tensor-core pass (head_group = rows, tile_keys = 128)
-  bool tc128 = false;  // head_dim 128, fp16/bf16, up to 16 rows per kv head:
-                       // the streaming tensor-core pass (two-pass merge)
+  bool tc128 = false;  // head_dim 64/128, fp16/bf16, up to 16 rows per kv
+                       // head: the streaming tensor-core pass (two-pass merge)
 };
 
 bool decode_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);
@@ -48,7 +48,7 @@ bool decode_tc_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);
 sdpa_status_t launch_decode_tc(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
                                const void* k, const void* v, void* o, float* lse, float* ws_o,
                                float* ws_ml, const LaunchEnv& env, bool* merged);
-// The head_dim-128 tensor-core pass: its plan (false: not such a problem)
+// The head_dim-64/128 tensor-core pass: its plan (false: not such a problem)
 // and its launch; *merged is false when the combine pass must follow.
 bool decode_tc128_plan(const sdpa_params_t& p, int num_sms, DecodePlan* out);
 sdpa_status_t launch_decode_tc128(const sdpa_params_t& p, const DecodePlan& plan, const void* q,
