@@ -203,6 +203,24 @@ def test_tc128_decode_plan(sdpa_lib):
                                    dtype=S.SDPA_F32)) != _ws(8 * 32, 19, 128)
 
 
+def test_backward_workspace_size(sdpa_lib):
+    """sdpa_backward_workspace_size (pure host): an fp32 dQ accumulator
+    [B, Hq, Lq, D] and two fp32 [B, Hq, Lq] arrays, each 256-byte aligned, for
+    fp32, fp16 and bf16 at head_dim 64 and 128, with or without per-batch
+    length arrays; 0 for head_dim 512."""
+    a = lambda x: (x + 255) // 256 * 256
+    for dtype in (S.SDPA_F32, S.SDPA_F16, S.SDPA_BF16):
+        for D in (64, 128):
+            p = P(dtype=dtype, D=D, B=2, Hq=4, Hkv=2, Lq=33, Lk=70)
+            rows = 2 * 4 * 33
+            assert S.sdpa_backward_workspace_size(p) == a(rows * D * 4) + 2 * a(rows * 4)
+    # per-batch lengths are accepted (only the pointers are looked at here)
+    pl = S.make_params(2, 4, 2, 33, 70, 64, S.SDPA_BF16, 0.125, True, None, (0, 0, 0, 1), None,
+                       seq_lens_q_ptr=256, seq_lens_kv_ptr=512)
+    assert S.sdpa_backward_workspace_size(pl) == a(264 * 64 * 4) + 2 * a(264 * 4)
+    assert S.sdpa_backward_workspace_size(P(D=512, Lq=4, Lk=9)) == 0
+
+
 def test_python_binding_rejects_cpu_tensors(sdpa_lib):
     torch = pytest.importorskip("torch")
     q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
